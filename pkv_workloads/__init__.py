@@ -1,0 +1,293 @@
+"""Seeded synthetic workloads for paged decode attention.
+
+This package only draws random inputs and describes the five workloads; it holds
+none of the method's arithmetic (no allocator, append, quantisation or attention
+code).  Both the CUDA path and the CPU oracle consume what it produces, so the
+two always see the same bytes.
+
+Shapes follow the head shapes and batch mixes that the TensorRT-LLM pages use
+("TensorRT-LLM 推理加速实战", §8 KV Cache 深入 / §8.1 KV Cache 显存估算: Llama-3.1-70B
+with 8 KV heads and head_dim 128; "TensorRT-LLM 深度实战", §3.1 Paged KV Cache with
+page_size 16; the 200-concurrent-request FP8 scenario of the aiqz.cc page,
+KV缓存管理 section).  No dataset is involved; every input is drawn here.
+
+Random numbers: splitmix64 (counter-based, see gen.c).  Each workload has a base
+seed 266*1000 + index; each independent stream (context lengths, free-list
+permutation, churn script, history K, history V, new K, new V, Q) uses as its
+seed the tag-th output of the base stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libpkvgen.so")
+_lib = None
+
+TAG_LENS, TAG_PERM, TAG_CHURN, TAG_K_HIST, TAG_V_HIST, TAG_K_NEW, TAG_V_NEW, TAG_Q = range(1, 9)
+TEMP_SEQ_BASE = 1_000_000
+MASK64 = (1 << 64) - 1
+GAMMA = 0x9E3779B97F4A7C15
+
+
+def build_native(force: bool = False) -> str:
+    """Compile gen.c into an in-tree shared library (gcc, portable flags)."""
+    if os.path.exists(_LIB_PATH) and not force:
+        src_m = os.path.getmtime(os.path.join(_HERE, "gen.c"))
+        if os.path.getmtime(_LIB_PATH) >= src_m:
+            return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off",
+                           os.path.join(_HERE, "gen.c"), "-o", tmp, "-lm", "-lpthread"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _native():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build_native())
+        lib.wl_splitmix64_at.restype = ctypes.c_uint64
+        lib.wl_splitmix64_at.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        lib.wl_normal_at.restype = ctypes.c_double
+        lib.wl_normal_at.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        lib.wl_normal_bf16.restype = None
+        lib.wl_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double,
+                                       ctypes.c_double, ctypes.c_void_p, ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+# ----------------------------------------------------------------------------- scalar draws
+def splitmix64_at(seed: int, i: int) -> int:
+    """i-th output (0-based) of the splitmix64 stream with initial state `seed` (pure Python)."""
+    z = (seed + (i + 1) * GAMMA) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+def unit(seed: int, i: int) -> float:
+    """Uniform in [0, 1) from the top 53 bits of draw i."""
+    return (splitmix64_at(seed, i) >> 11) * (1.0 / (1 << 53))
+
+
+def uniform_int(seed: int, i: int, lo: int, hi: int) -> int:
+    """Uniform integer in [lo, hi] (multiply-shift on 53 random bits)."""
+    n = hi - lo + 1
+    return lo + (((splitmix64_at(seed, i) >> 11) * n) >> 53)
+
+
+def normal(seed: int, i: int) -> float:
+    """i-th standard normal of the stream (Box-Muller cosine branch), fp64."""
+    return _native().wl_normal_at(seed & MASK64, i)
+
+
+def stream_seed(base_seed: int, tag: int) -> int:
+    return splitmix64_at(base_seed, tag)
+
+
+def permutation(seed: int, n: int) -> np.ndarray:
+    """Seeded Fisher-Yates (Durstenfeld) shuffle of 0..n-1; draw k picks the k-th swap partner."""
+    a = list(range(n))
+    k = 0
+    for i in range(n - 1, 0, -1):
+        j = uniform_int(seed, k, 0, i)
+        k += 1
+        a[i], a[j] = a[j], a[i]
+    return np.asarray(a, dtype=np.int32)
+
+
+def normal_bf16(seed: int, offset: int, n: int, threads: int | None = None) -> np.ndarray:
+    """bf16 bit patterns (uint16) of N(0,1) draws offset .. offset+n-1."""
+    out = np.empty(n, dtype=np.uint16)
+    if n:
+        t = threads or min(64, os.cpu_count() or 1)
+        _native().wl_normal_bf16(seed & MASK64, offset, n, 0.0, 1.0, out.ctypes.data, t)
+    return out
+
+
+# ----------------------------------------------------------------------------- workloads
+@dataclass
+class Workload:
+    """One synthetic decode step over a paged KV pool.
+
+    lens[b]      tokens already cached for sequence b before the step;
+    append       whether the step writes one new token per sequence at position lens[b];
+    attend_lens  context length the attention covers (lens + append);
+    free_order   initial free-list order handed to the allocator (a permutation);
+    alloc_ops    allocator script: ("reserve", seq_id, total_tokens) / ("release", seq_id);
+    seq_ids      the batch's sequence ids, in batch order.
+    """
+    name: str
+    index: int
+    description: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    block_size: int
+    kv_dtype: str  # "bf16" | "fp8_e4m3"
+    num_blocks: int
+    lens: np.ndarray
+    append: bool
+    free_order: np.ndarray
+    alloc_ops: list = field(default_factory=list)
+    seq_ids: np.ndarray = None
+
+    @property
+    def seed(self) -> int:
+        return 266 * 1000 + self.index
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def attend_lens(self) -> np.ndarray:
+        return (self.lens + (1 if self.append else 0)).astype(np.int32)
+
+    @property
+    def n_hist(self) -> int:
+        return int(self.lens.sum())
+
+    @property
+    def hist_offsets(self) -> np.ndarray:
+        """Start of each sequence's tokens in the concatenated history stream."""
+        return np.concatenate([[0], np.cumsum(self.lens)]).astype(np.int64)
+
+    @property
+    def elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == "fp8_e4m3" else 2
+
+    def kv_read_bytes(self) -> int:
+        """K+V bytes one attention pass must read: 2*D*bytes per (token, kv head)."""
+        return int(self.attend_lens.astype(np.int64).sum()) * self.Hkv * 2 * self.D * self.elem_bytes
+
+    # --- tensors (bf16 bit patterns as uint16) ---
+    def history_k(self, tok_begin: int = 0, tok_end: int | None = None) -> np.ndarray:
+        return self._hist(TAG_K_HIST, tok_begin, tok_end)
+
+    def history_v(self, tok_begin: int = 0, tok_end: int | None = None) -> np.ndarray:
+        return self._hist(TAG_V_HIST, tok_begin, tok_end)
+
+    def _hist(self, tag, tok_begin, tok_end):
+        tok_end = self.n_hist if tok_end is None else tok_end
+        row = self.Hkv * self.D
+        flat = normal_bf16(stream_seed(self.seed, tag), tok_begin * row, (tok_end - tok_begin) * row)
+        return flat.reshape(tok_end - tok_begin, self.Hkv, self.D)
+
+    def new_k(self) -> np.ndarray:
+        return normal_bf16(stream_seed(self.seed, TAG_K_NEW), 0, self.B * self.Hkv * self.D).reshape(
+            self.B, self.Hkv, self.D)
+
+    def new_v(self) -> np.ndarray:
+        return normal_bf16(stream_seed(self.seed, TAG_V_NEW), 0, self.B * self.Hkv * self.D).reshape(
+            self.B, self.Hkv, self.D)
+
+    def query(self) -> np.ndarray:
+        return normal_bf16(stream_seed(self.seed, TAG_Q), 0, self.B * self.Hq * self.D).reshape(
+            self.B, self.Hq, self.D)
+
+    def hist_positions(self, tok_begin: int = 0, tok_end: int | None = None):
+        """(seq_ids, positions) of history tokens [tok_begin, tok_end) of the concatenated stream."""
+        tok_end = self.n_hist if tok_end is None else tok_end
+        off = self.hist_offsets
+        t = np.arange(tok_begin, tok_end, dtype=np.int64)
+        b = np.searchsorted(off, t, side="right") - 1
+        return self.seq_ids[b], (t - off[b]).astype(np.int64)
+
+    def max_blocks(self) -> int:
+        return int(-(-int(self.attend_lens.max()) // self.block_size)) if self.B else 0
+
+
+def _ceil_div(a, b):
+    return -(-a // b)
+
+
+def _simple_ops(lens, append):
+    return [("reserve", b, int(lens[b]) + (1 if append else 0)) for b in range(len(lens))]
+
+
+def make_workload(name: str) -> Workload:
+    """The five workloads: c0 (tiny parity case) .. c4 (churned FP8 pool)."""
+    idx = int(name[1:])
+    seed = 266 * 1000 + idx
+    s_lens = stream_seed(seed, TAG_LENS)
+    s_perm = stream_seed(seed, TAG_PERM)
+    if idx == 0:
+        lens = np.array([5, 17, 33, 64], dtype=np.int64)
+        w = Workload(name, 0, "tiny paged decode, GQA 2:1, head_dim 64, block 16, 32-block pool, permuted blocks",
+                     4, 4, 2, 64, 16, "bf16", 32, lens, True, permutation(s_perm, 32))
+    elif idx == 1:
+        lens = np.array([uniform_int(s_lens, b, 128, 2048) for b in range(32)], dtype=np.int64)
+        need = int(sum(_ceil_div(int(L) + 1, 64) for L in lens))
+        nb = need + _ceil_div(need, 10)
+        w = Workload(name, 1, "Llama-2-7B-shape MHA layer decode, batch 32, contexts U[128,2048], block 64",
+                     32, 32, 32, 128, 64, "bf16", nb, lens, True, permutation(s_perm, nb))
+    elif idx == 2:
+        lens = np.array([min(4096, max(16, int(round(512.0 * math.exp(normal(s_lens, b)))))) for b in range(128)],
+                        dtype=np.int64)
+        nb = (2 * 1 * 8 * 128 * 4096 * 128 * 2) // (64 * 2 * 8 * 128 * 2)  # M_kv(128 seqs x 4096) / block bytes
+        w = Workload(name, 2, "Llama-3-8B-shape GQA in-flight batch, batch 128, lognormal contexts, block 64",
+                     128, 32, 8, 128, 64, "bf16", nb, lens, True, permutation(s_perm, nb))
+    elif idx == 3:
+        k = 1024
+        lens = np.array([32 * k, 48 * k, 64 * k, 80 * k, 96 * k, 112 * k, 128 * k, 128 * k], dtype=np.int64)
+        nb = int(sum(_ceil_div(int(L), 64) for L in lens))
+        w = Workload(name, 3, "70B-shape long context, batch 8, 32k-128k contexts, GQA 8:1, block 64",
+                     8, 64, 8, 128, 64, "bf16", nb, lens, False, permutation(s_perm, nb))
+    elif idx == 4:
+        lens = np.array([uniform_int(s_lens, b, 64, 8192) for b in range(200)], dtype=np.int64)
+        nb = (200 * 8192) // 16
+        w = Workload(name, 4, "200-request churned pool, FP8-e4m3 KV with per-(block,head) scales, block 16",
+                     200, 32, 8, 128, 16, "fp8_e4m3", nb, lens, True, np.arange(nb, dtype=np.int32))
+    else:
+        raise ValueError(name)
+    w.seq_ids = np.arange(w.B, dtype=np.int64)
+    if idx == 4:
+        w.alloc_ops = _churn_ops(w, stream_seed(seed, TAG_CHURN))
+    else:
+        w.alloc_ops = _simple_ops(w.lens, w.append)
+    return w
+
+
+def _churn_ops(w: Workload, s_churn: int):
+    """1000 seeded create/release cycles of temporary sequences, their release, then round-robin
+    growth of the batch block by block.  Temporary sequences hold whole blocks (k * block_size
+    tokens), so the script can count held blocks without modelling the allocator."""
+    ops, live, held, tid = [], [], 0, 0
+    bs = w.block_size
+    for i in range(1000):
+        u = unit(s_churn, 3 * i)
+        if u < 0.5 and w.num_blocks - held >= 64:
+            k = uniform_int(s_churn, 3 * i + 1, 1, 64)
+            seq = TEMP_SEQ_BASE + tid
+            tid += 1
+            ops.append(("reserve", seq, k * bs))
+            live.append((seq, k))
+            held += k
+        elif live:
+            j = uniform_int(s_churn, 3 * i + 2, 0, len(live) - 1)
+            seq, k = live.pop(j)
+            ops.append(("release", seq))
+            held -= k
+    for seq, _ in live:
+        ops.append(("release", seq))
+    total = [int(L) + (1 if w.append else 0) for L in w.lens]
+    need = [_ceil_div(t, bs) for t in total]
+    for r in range(max(need)):
+        for b in range(w.B):
+            if need[b] > r:
+                ops.append(("reserve", b, min((r + 1) * bs, total[b])))
+    return ops
+
+
+WORKLOADS = ("c0", "c1", "c2", "c3", "c4")
