@@ -1,0 +1,190 @@
+/*
+ * pkv — paged KV cache and decode attention for one GB300 (sm_103a).
+ *
+ * Plain C ABI: opaque handles, raw pointers, sizes and status codes.  No C++ or
+ * framework types cross it and no exception leaves it.  Pointers documented as
+ * "device" must be CUDA device (or managed) memory on the pool's device; "host"
+ * pointers are ordinary CPU memory.  The caller owns every buffer it passes; the
+ * pool owns its own device storage.  Kernels run asynchronously on the caller's
+ * stream (NULL = the legacy default stream); argument errors are reported
+ * synchronously and launch nothing.  Faults that only the device can see (a
+ * block id or slot outside the pool, an over-long context) are recorded in the
+ * pool's device error word and read back with pkv_check_device_error(); the
+ * kernels never read or write outside the pool or the caller's buffers.
+ *
+ * Nothing here is thread-safe: serialise calls that touch the same pool or
+ * allocator.
+ *
+ * Problem statement (page title, section):
+ *  - "TensorRT-LLM 深度实战" (chenxutan.com), §3.1 Paged KV Cache: the KV memory is
+ *    cut into fixed pages, handed to sequences on demand from a free-page list
+ *    and returned when a sequence finishes; a per-sequence page table maps a
+ *    sequence to its pages.
+ *  - "TensorRT-LLM 推理加速实战" (socake.github.io), §8 KV Cache 深入: block_size 64
+ *    (vLLM uses 16); FP8 KV cache (fp8_e4m3); §8.1 the KV bytes-per-token formula;
+ *    §7.2 masked_mha, the decode-phase attention of one new token per request.
+ *  - "TensorRT-LLM加速大模型推理实战" (codearts.csdn.net): GQA/MQA, several query
+ *    heads sharing one KV head.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_pool pkv_pool;
+typedef struct pkv_allocator pkv_allocator;
+/* Same handle as cudaStream_t / CUstream. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* bad size, null or misaligned pointer, unsupported shape */
+    PKV_ERR_OOM = 2,         /* not enough free blocks (nothing was changed) or cudaMalloc failed */
+    PKV_ERR_NO_SEQ = 3,      /* unknown sequence id */
+    PKV_ERR_BOUNDS = 4,      /* index outside the pool / table / capacity (host check or device flag) */
+    PKV_ERR_CUDA = 5,        /* a CUDA runtime call failed */
+    PKV_ERR_TIMEOUT = 6      /* a kernel's bounded wait ran out (device flag); results are invalid */
+} pkv_status;
+
+typedef enum {
+    PKV_KV_BF16 = 0,     /* K/V stored as bf16 */
+    PKV_KV_FP8_E4M3 = 1  /* K/V stored as OCP E4M3 codes with one fp32 scale per (block, K|V, head) */
+} pkv_dtype;
+
+/* ------------------------------------------------------------------ block allocator (host)
+ * The pages' PagedKVCache ("TensorRT-LLM 深度实战", §3.1): a free list that starts as
+ * 0..num_blocks-1 and hands out blocks with pop() from its end, a table
+ * seq_id -> [block ids] in the order the blocks were taken, growth by whole
+ * blocks, and release that appends a sequence's blocks back in table order.
+ * Unlike the page's sketch, running out of blocks changes nothing.
+ */
+
+/* num_blocks >= 1; block_size a power of two in [16, 256].  *out is owned by the caller
+ * and freed with pkv_allocator_destroy. */
+pkv_status pkv_allocator_create(int num_blocks, int block_size, pkv_allocator** out);
+pkv_status pkv_allocator_destroy(pkv_allocator* a);
+
+/* Replace the free list by order[0..n) (the last entry is handed out first).  Only while
+ * no sequence holds blocks; order must be a permutation of 0..num_blocks-1. */
+pkv_status pkv_allocator_set_free_order(pkv_allocator* a, const int32_t* order_host, int n);
+
+/* Make seq_id able to hold n_tokens tokens: an unknown seq_id is created with
+ * ceil(n_tokens / block_size) blocks, a known one takes ceil((n_tokens - capacity) /
+ * block_size) more when n_tokens exceeds its capacity.  PKV_ERR_OOM if the free list is
+ * too short; then neither the sequence nor the free list changes. */
+pkv_status pkv_seq_reserve(pkv_allocator* a, int64_t seq_id, int64_t n_tokens);
+
+/* Return all of seq_id's blocks to the free list (appended in table order) and forget it. */
+pkv_status pkv_seq_release(pkv_allocator* a, int64_t seq_id);
+
+/* Number of blocks seq_id holds (PKV_ERR_NO_SEQ if unknown). */
+pkv_status pkv_seq_num_blocks(const pkv_allocator* a, int64_t seq_id, int* out);
+
+pkv_status pkv_num_free_blocks(const pkv_allocator* a, int* out);
+
+/* Copy the free list (index n-1 is handed out next) into out_host[0..capacity); *n gets its
+ * length.  PKV_ERR_BOUNDS if capacity is too small (nothing written). */
+pkv_status pkv_free_list(const pkv_allocator* a, int32_t* out_host, int capacity, int* n);
+
+/* Pack the block tables of seq_ids[0..B) into out_host[B][max_blocks] (int32, row-major),
+ * padding with -1.  PKV_ERR_NO_SEQ for an unknown id, PKV_ERR_BOUNDS if a sequence holds
+ * more than max_blocks blocks. */
+pkv_status pkv_get_block_tables(const pkv_allocator* a, const int64_t* seq_ids_host, int B, int max_blocks,
+                                int32_t* out_host);
+
+/* out_host[i] = table(seq_ids[i])[pos / block_size] * block_size + pos % block_size for
+ * pos = positions[i]; a negative position gives -1 (a padding token that pkv_append skips).
+ * PKV_ERR_BOUNDS if a position is beyond the sequence's capacity. */
+pkv_status pkv_slot_mapping(const pkv_allocator* a, const int64_t* seq_ids_host, const int64_t* positions_host,
+                            int64_t N, int64_t* out_host);
+
+/* ------------------------------------------------------------------ pool (device)
+ * Device layout ("block pool"): block b, K (kv=0) or V (kv=1), KV head h form one
+ * contiguous tile of block_size*head_dim elements starting at element
+ * ((b*2 + kv)*n_kv_heads + h) * block_size * head_dim.
+ *   bf16 K and V, fp8 K:  row-major [block_size][head_dim] (token t, dim d at t*D + d).
+ *   fp8 V: block_size/16 panels of [head_dim][16]: (t, d) at (t/16)*D*16 + d*16 + pos(t%16),
+ *   each 16-byte panel row holding its tokens in the order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15
+ *   (so one 4-byte load yields the token pairs one MMA k-step consumes).
+ *   fp8 scales: float[num_blocks][n_kv_heads][4]; [..][0] scales K, [..][1] scales V,
+ *   [..][2..3] are zero padding (one 16-byte record per block and head).
+ * An element's value is bf16(bits) or e4m3(code) * scale.
+ */
+
+/* head_dim 64 or 128; block_size a power of two in [16, 256]; n_kv_heads >= 1.  Allocates
+ * the pool with cudaMalloc on the current device and zero-fills it; the pool embeds an
+ * allocator over the same num_blocks (see pkv_pool_allocator). */
+pkv_status pkv_pool_create(int num_blocks, int block_size, int n_kv_heads, int head_dim, pkv_dtype kv_dtype,
+                           pkv_pool** out);
+pkv_status pkv_pool_destroy(pkv_pool* pool);
+
+/* The pool's own allocator; owned by the pool (do not destroy it). */
+pkv_status pkv_pool_allocator(pkv_pool* pool, pkv_allocator** out);
+
+/* Raw device buffers for inspection: the KV bytes and the fp8 scale array (NULL and 0 for
+ * bf16 pools).  Ownership stays with the pool. */
+pkv_status pkv_pool_raw(const pkv_pool* pool, void** kv_dev, size_t* kv_bytes, float** scales_dev,
+                        size_t* scale_bytes);
+
+/* Synchronise the device, read and clear the pool's device error word.  Returns PKV_OK,
+ * PKV_ERR_BOUNDS (a kernel saw an out-of-range block id, slot or context length and
+ * skipped or clamped it) or PKV_ERR_TIMEOUT (a bounded wait expired). */
+pkv_status pkv_check_device_error(pkv_pool* pool);
+
+/* ------------------------------------------------------------------ append (device)
+ * Write each new token's K and V into its physical slot ("TensorRT-LLM 深度实战", §3.1
+ * append_tokens, whose pages hold the tokens' K/V).
+ *   k_new_dev, v_new_dev: bf16 [N][n_kv_heads][head_dim], 16-byte aligned.
+ *   slot_mapping_dev: int64 [N]; slot = block * block_size + offset; -1 skips the token.
+ * bf16 pools store the bits.  fp8 pools quantise: for every (block, K|V, head) whose offset 0
+ * this call writes, the scale becomes amax/448 over this call's tokens in that block (1 if
+ * the amax is 0); other blocks keep their stored scale; each value is stored as
+ * e4m3_rne_satfinite(x / scale) with an IEEE fp32 division.  A slot beyond the pool is
+ * skipped and flagged (PKV_ERR_BOUNDS via pkv_check_device_error).  Two tokens of one call
+ * must not share a slot.  Calls that overlap in time on one pool race. */
+pkv_status pkv_append(pkv_pool* pool, const void* k_new_dev, const void* v_new_dev, const int64_t* slot_mapping_dev,
+                      int64_t N, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------ decode attention (device)
+ * For each sequence b and query head j, with KV head h = j / (n_q_heads / n_kv_heads):
+ *   out[b][j] = softmax_t(scale * <q[b][j], K_b[t]>) . V_b[t],  t < context_lens[b],
+ * K_b/V_b[t] read from block block_tables[b][t / block_size] at offset t % block_size
+ * ("TensorRT-LLM 推理加速实战", §7.2 masked_mha).  Work is split over the context in 64-token
+ * groups balanced across the GPU; partial softmax states (running max, sum, weighted V)
+ * of a sequence cut between CTAs are merged with the log-sum-exp rule.
+ *   q_dev: bf16 [B][n_q_heads][head_dim], 16-byte aligned.
+ *   block_tables_dev: int32 [B][max_blocks]; context_lens_dev: int32 [B].
+ *   out_dev: bf16 [B][n_q_heads][head_dim], 16-byte aligned (fp32 accumulation, RNE to bf16).
+ *   workspace_dev: >= pkv_decode_workspace_bytes() bytes, 256-byte aligned, zero-filled
+ *   before its first use (pkv_decode_workspace_init); every call leaves it ready for the
+ *   next.  Calls that overlap in time must use different workspaces.
+ * n_q_heads must be a multiple of n_kv_heads with at most 8 query heads per KV head.
+ * context_lens[b] == 0 yields zeros.  A context longer than max_blocks*block_size, or a
+ * block id outside the pool, is clamped/skipped and flagged (PKV_ERR_BOUNDS). */
+pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q_dev, const int32_t* block_tables_dev,
+                                int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads, float scale,
+                                void* out_dev, void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Workspace size for pkv_decode_attention with these B, n_q_heads and max_blocks. */
+pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out);
+
+/* cudaMemsetAsync(workspace, 0, bytes, stream): prepares a fresh workspace. */
+pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------ utilities
+ * KV memory ("TensorRT-LLM 推理加速实战" §8.1; aiqz.cc page, KV缓存管理):
+ *   M_kv = 2 * n_layers * n_kv_heads * head_dim * n_tokens * batch * bytes_per_elem. */
+uint64_t pkv_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, int64_t n_tokens, int64_t batch,
+                      double bytes_per_elem);
+
+const char* pkv_status_str(pkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

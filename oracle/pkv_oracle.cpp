@@ -33,7 +33,8 @@
 //   tile(blk, kv, h) starts at byte ((blk*2 + kv)*Hkv + h) * bs * D * esz,
 //   kv = 0 for K, 1 for V, esz = 2 (bf16) or 1 (fp8).
 //   bf16 K and V, fp8 K: row-major [bs][D].
-//   fp8 V: bs/16 column panels, each [D][16]: (t, d) at (t/16)*D*16 + d*16 + t%16.
+//   fp8 V: bs/16 column panels, each [D][16]: (t, d) at (t/16)*D*16 + d*16 + pos(t%16), where
+//   a panel row stores its 16 tokens in the order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15.
 //   fp8 scales: float[num_blocks][Hkv][4]: [.., 0] K scale, [.., 1] V scale.
 #include <algorithm>
 #include <cmath>
@@ -223,9 +224,13 @@ static int64_t tile_base(int64_t blk, int kv, int h, int Hkv, int bs, int D, int
     return (((blk * 2 + kv) * Hkv + h) * (int64_t)bs * D) * esz;
 }
 
+// Byte position of token u (0..15) inside a 16-byte fp8 V panel row: tokens are stored in
+// the order 0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15.
+static int fp8_v_byte(int u) { return u < 8 ? 4 * (u >> 1) + (u & 1) : 4 * ((u - 8) >> 1) + 2 + (u & 1); }
+
 static int64_t elem_offset(int kv, int t, int d, int bs, int D, int fp8) {
     (void)bs;
-    if (fp8 && kv == 1) return (int64_t)(t / 16) * D * 16 + (int64_t)d * 16 + (t % 16);
+    if (fp8 && kv == 1) return (int64_t)(t / 16) * D * 16 + (int64_t)d * 16 + fp8_v_byte(t % 16);
     return (int64_t)t * D + d;
 }
 

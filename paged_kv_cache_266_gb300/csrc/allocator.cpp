@@ -1,0 +1,186 @@
+// Host block allocator for the paged KV pool.
+//
+// "TensorRT-LLM 深度实战" (chenxutan.com), §3.1 Paged KV Cache: free pages are kept in a
+// list that starts as 0..n-1 and is consumed with pop() from its end; a sequence's page
+// table lists its pages in the order they were taken; growth adds whole pages once the
+// tokens outgrow the capacity; a finished sequence's pages go back to the end of the list
+// in table order.  Out-of-memory is checked before anything is taken, so a failing call
+// changes nothing (the page's sketch leaks pages popped before it runs dry).
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv_internal.h"
+
+struct pkv_allocator {
+    int num_blocks = 0;
+    int block_size = 0;
+    std::vector<int32_t> free_list;  // back() is handed out next
+    std::unordered_map<int64_t, std::vector<int32_t>> tables;
+};
+
+namespace pkv {
+
+bool valid_block_size(int bs) { return bs >= 16 && bs <= 256 && (bs & (bs - 1)) == 0; }
+
+pkv_allocator* allocator_new(int num_blocks, int block_size) {
+    pkv_allocator* a = new (std::nothrow) pkv_allocator();
+    if (!a) return nullptr;
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    try {
+        a->free_list.resize(num_blocks);
+    } catch (...) {
+        delete a;
+        return nullptr;
+    }
+    for (int i = 0; i < num_blocks; ++i) a->free_list[i] = i;
+    return a;
+}
+
+void allocator_delete(pkv_allocator* a) { delete a; }
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_allocator_create(int num_blocks, int block_size, pkv_allocator** out) {
+    if (!out || num_blocks < 1 || !pkv::valid_block_size(block_size)) return PKV_ERR_INVALID_ARG;
+    pkv_allocator* a = pkv::allocator_new(num_blocks, block_size);
+    if (!a) return PKV_ERR_OOM;
+    *out = a;
+    return PKV_OK;
+}
+
+pkv_status pkv_allocator_destroy(pkv_allocator* a) {
+    if (!a) return PKV_ERR_INVALID_ARG;
+    pkv::allocator_delete(a);
+    return PKV_OK;
+}
+
+pkv_status pkv_allocator_set_free_order(pkv_allocator* a, const int32_t* order, int n) {
+    if (!a || !order || n != a->num_blocks || !a->tables.empty()) return PKV_ERR_INVALID_ARG;
+    std::vector<char> seen(n, 0);
+    for (int i = 0; i < n; ++i) {
+        if (order[i] < 0 || order[i] >= n || seen[order[i]]) return PKV_ERR_INVALID_ARG;
+        seen[order[i]] = 1;
+    }
+    std::memcpy(a->free_list.data(), order, sizeof(int32_t) * (size_t)n);
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_reserve(pkv_allocator* a, int64_t seq_id, int64_t n_tokens) {
+    if (!a || n_tokens < 0) return PKV_ERR_INVALID_ARG;
+    auto it = a->tables.find(seq_id);
+    const int64_t held = it == a->tables.end() ? 0 : (int64_t)it->second.size();
+    const int64_t bs = a->block_size;
+    const int64_t want = (n_tokens + bs - 1) / bs;
+    const int64_t extra = want > held ? want - held : 0;
+    if (extra > (int64_t)a->free_list.size()) return PKV_ERR_OOM;
+    std::vector<int32_t>& tbl = it == a->tables.end() ? a->tables[seq_id] : it->second;
+    tbl.reserve((size_t)(held + extra));
+    for (int64_t i = 0; i < extra; ++i) {
+        tbl.push_back(a->free_list.back());
+        a->free_list.pop_back();
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_release(pkv_allocator* a, int64_t seq_id) {
+    if (!a) return PKV_ERR_INVALID_ARG;
+    auto it = a->tables.find(seq_id);
+    if (it == a->tables.end()) return PKV_ERR_NO_SEQ;
+    a->free_list.insert(a->free_list.end(), it->second.begin(), it->second.end());
+    a->tables.erase(it);
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_num_blocks(const pkv_allocator* a, int64_t seq_id, int* out) {
+    if (!a || !out) return PKV_ERR_INVALID_ARG;
+    auto it = a->tables.find(seq_id);
+    if (it == a->tables.end()) return PKV_ERR_NO_SEQ;
+    *out = (int)it->second.size();
+    return PKV_OK;
+}
+
+pkv_status pkv_num_free_blocks(const pkv_allocator* a, int* out) {
+    if (!a || !out) return PKV_ERR_INVALID_ARG;
+    *out = (int)a->free_list.size();
+    return PKV_OK;
+}
+
+pkv_status pkv_free_list(const pkv_allocator* a, int32_t* out, int capacity, int* n) {
+    if (!a || !n || (capacity > 0 && !out) || capacity < 0) return PKV_ERR_INVALID_ARG;
+    *n = (int)a->free_list.size();
+    if (capacity < *n) return PKV_ERR_BOUNDS;
+    if (*n) std::memcpy(out, a->free_list.data(), sizeof(int32_t) * (size_t)*n);
+    return PKV_OK;
+}
+
+pkv_status pkv_get_block_tables(const pkv_allocator* a, const int64_t* seq_ids, int B, int max_blocks,
+                                int32_t* out) {
+    if (!a || B < 0 || max_blocks < 0 || (B > 0 && (!seq_ids || (max_blocks > 0 && !out)))) return PKV_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b) {  // validate everything before writing anything
+        auto it = a->tables.find(seq_ids[b]);
+        if (it == a->tables.end()) return PKV_ERR_NO_SEQ;
+        if ((int64_t)it->second.size() > max_blocks) return PKV_ERR_BOUNDS;
+    }
+    for (int b = 0; b < B; ++b) {
+        const std::vector<int32_t>& tbl = a->tables.find(seq_ids[b])->second;
+        int32_t* row = out + (int64_t)b * max_blocks;
+        const int n = (int)tbl.size();
+        if (n) std::memcpy(row, tbl.data(), sizeof(int32_t) * (size_t)n);
+        for (int k = n; k < max_blocks; ++k) row[k] = -1;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_slot_mapping(const pkv_allocator* a, const int64_t* seq_ids, const int64_t* positions, int64_t N,
+                            int64_t* out) {
+    if (!a || N < 0 || (N > 0 && (!seq_ids || !positions || !out))) return PKV_ERR_INVALID_ARG;
+    const int64_t bs = a->block_size;
+    // Consecutive tokens usually belong to one sequence: remember the last lookup.
+    int64_t last_id = 0;
+    const std::vector<int32_t>* last = nullptr;
+    for (int64_t i = 0; i < N; ++i) {
+        const int64_t pos = positions[i];
+        if (pos < 0) {
+            out[i] = -1;
+            continue;
+        }
+        if (!last || seq_ids[i] != last_id) {
+            auto it = a->tables.find(seq_ids[i]);
+            if (it == a->tables.end()) return PKV_ERR_NO_SEQ;
+            last = &it->second;
+            last_id = seq_ids[i];
+        }
+        const int64_t k = pos / bs;
+        if (k >= (int64_t)last->size()) return PKV_ERR_BOUNDS;
+        out[i] = (int64_t)(*last)[(size_t)k] * bs + pos % bs;
+    }
+    return PKV_OK;
+}
+
+uint64_t pkv_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, int64_t n_tokens, int64_t batch,
+                      double bytes_per_elem) {
+    // Integer product first (exact), then the element size; 2 * ... keeps half-byte sizes whole.
+    const uint64_t elems = 2ull * (uint64_t)n_layers * (uint64_t)n_kv_heads * (uint64_t)head_dim *
+                           (uint64_t)n_tokens * (uint64_t)batch;
+    return (uint64_t)((long double)elems * (long double)bytes_per_elem);
+}
+
+const char* pkv_status_str(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_OOM: return "out of memory (no free blocks or device allocation failed)";
+        case PKV_ERR_NO_SEQ: return "unknown sequence id";
+        case PKV_ERR_BOUNDS: return "index out of bounds";
+        case PKV_ERR_CUDA: return "CUDA runtime error";
+        case PKV_ERR_TIMEOUT: return "kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

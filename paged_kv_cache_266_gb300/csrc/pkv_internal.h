@@ -1,0 +1,53 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// Device error word bits (read and cleared by pkv_check_device_error).
+constexpr int kErrBounds = 1;
+constexpr int kErrTimeout = 2;
+
+bool valid_block_size(int bs);
+pkv_allocator* allocator_new(int num_blocks, int block_size);
+void allocator_delete(pkv_allocator* a);
+
+}  // namespace pkv
+
+struct pkv_pool {
+    int num_blocks = 0;
+    int block_size = 0;
+    int n_kv_heads = 0;
+    int head_dim = 0;
+    pkv_dtype dtype = PKV_KV_BF16;
+    int device = 0;
+    int sm_count = 0;
+    int max_smem_per_sm = 0;    // bytes usable by resident CTAs on one SM
+    int max_smem_per_block = 0;  // opt-in dynamic shared memory limit of one CTA
+
+    void* kv = nullptr;  // the block pool, layout documented in pkv.h
+    size_t kv_bytes = 0;
+    float* scales = nullptr;  // fp8: [num_blocks][n_kv_heads][4]
+    size_t scale_bytes = 0;
+    uint32_t* amax_scratch = nullptr;  // fp8 append: [num_blocks][n_kv_heads][2] fp32 bits, kept zero between calls
+    uint8_t* fresh_scratch = nullptr;  // fp8 append: [num_blocks] "offset 0 written by this call", kept zero
+    int* err = nullptr;               // device error word
+
+    // TMA descriptor over all K/V rows: dim0 = head_dim elements, dim1 = num_blocks*2*Hkv*bs rows.
+    CUtensorMap tmap_rows;
+
+    pkv_allocator* alloc = nullptr;
+};
+
+#define PKV_CUDA_TRY(expr)                       \
+    do {                                         \
+        cudaError_t e_ = (expr);                 \
+        if (e_ != cudaSuccess) return PKV_ERR_CUDA; \
+    } while (0)
