@@ -1,0 +1,364 @@
+"""Benchmark: one decode step (append of one token per sequence + paged decode attention)
+on a synthetic in-flight batch, timed on the GPU.  Prints one JSON line.
+
+Default workload: Llama-2-7B-shape MHA layer decode (32 query / 32 KV heads, head_dim 128,
+bf16, block 64, batch 32, contexts U[128, 2048]).  `--workload c2|c3|c4` selects the other
+shapes (for measurement runs; the default line is the headline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--workload c1]
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the workload
+(independent sequences, no data exchange); the value is the sum over ranks divided by the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import pkv_workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak), decode tokens/s"
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def algorithmic_bytes(w) -> dict:
+    """Bytes the step must move at minimum.  Attention: every cached K/V element of every
+    (sequence, KV head) once, fp8 scale pairs of the pages read, Q in, output out, the used
+    block-table entries and the context lengths.  Append: new K/V in, stored K/V out."""
+    L = w.attend_lens.astype(np.int64)
+    pages = ((L + w.block_size - 1) // w.block_size).sum()
+    kv = int(L.sum()) * w.Hkv * 2 * w.D * w.elem_bytes
+    scales = int(pages) * w.Hkv * 8 if w.kv_dtype == "fp8_e4m3" else 0
+    q_out = 2 * w.B * w.Hq * w.D * 2
+    meta = int(pages) * 4 + w.B * 4
+    attn = kv + scales + q_out + meta
+    app = (w.B * w.Hkv * w.D * 2 * 2 + w.B * w.Hkv * w.D * w.elem_bytes * 2 + w.B * 8) if w.append else 0
+    return {"attention": attn, "append": app, "step": attn + app, "kv": kv}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_266_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    src = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == src:
+            return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.bus = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            self.bus = getattr(props, "pci_bus_id", None)
+        except Exception:
+            pass
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            rows.append(f)
+        os.unlink(self.path)
+        if self.bus is not None:
+            mine = [r for r in rows if r[1].lower().endswith(f"{self.bus:02x}:00.0")]
+            rows = mine or rows
+        idx = sorted({r[0] for r in rows})
+        if idx:
+            rows = [r for r in rows if r[0] == idx[0]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": float(rows[0][3]) if rows else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle runs
+def oracle_rate(w, budget_s: float, threads: int):
+    """Time the oracle's decode attention on a bounded sample of the workload's sequences.
+    Returns (GB/s of KV read, seconds, description)."""
+    import oracle.drive as odrive
+    pool, _, tables = odrive.build(w)
+    order = np.argsort(w.attend_lens)  # start from the shortest to size the sample
+    picked, spent, kv = [], 0.0, 0
+    lens = w.attend_lens.astype(np.int64)
+    # Estimate the per-token cost on one sequence, then take enough sequences for the budget.
+    t0 = time.perf_counter()
+    odrive.attention(w, pool, tables, threads=threads, seqs=[int(order[len(order) // 2])])
+    est = (time.perf_counter() - t0) / max(1, lens[order[len(order) // 2]])
+    want_tokens = max(1, int(budget_s / max(est, 1e-9)))
+    for b in order[len(order) // 2:].tolist() + order[: len(order) // 2].tolist():
+        if sum(lens[picked]) >= want_tokens and picked:
+            break
+        picked.append(int(b))
+    t0 = time.perf_counter()
+    odrive.attention(w, pool, tables, threads=threads, seqs=picked)
+    spent = time.perf_counter() - t0
+    kv = int(lens[picked].sum()) * w.Hkv * 2 * w.D * w.elem_bytes
+    return kv / spent / 1e9, spent, f"{len(picked)} of {w.B} sequences ({int(lens[picked].sum())} tokens), all heads"
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle.drive as odrive
+    w = W.make_workload(args.workload)
+    threads = os.cpu_count() or 1
+    pool, _, tables = odrive.build(w)
+    lens = w.attend_lens.astype(np.int64)
+    b_mid = int(np.argsort(lens)[len(lens) // 2])
+    t0 = time.perf_counter()
+    odrive.attention(w, pool, tables, threads=threads, seqs=[b_mid])
+    per_seq = time.perf_counter() - t0
+    budget_total = 120.0
+    per_step = budget_total / max(1, args.steps + args.warmup)
+    # one step = a contiguous slice of heads of one sequence (or a few sequences), sized to the budget
+    n_seq = max(1, min(w.B, int(per_step / max(per_seq, 1e-9))))
+    seqs = [int(b) for b in np.argsort(lens)[len(lens) // 2:][:n_seq]]
+    for _ in range(args.warmup):
+        odrive.attention(w, pool, tables, threads=threads, seqs=seqs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        odrive.attention(w, pool, tables, threads=threads, seqs=seqs)
+    dt = (time.perf_counter() - t0) / args.steps
+    kv = int(lens[seqs].sum()) * w.Hkv * 2 * w.D * w.elem_bytes
+    value = kv / dt / 1e9
+    sample = f"{len(seqs)} of {w.B} sequences of {w.name} per step ({int(lens[seqs].sum())} tokens, all heads)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main arm
+def run_pkv(args, world, rank, local):
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+    from paged_kv_cache_266_gb300 import pkv_check_device_error
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+
+    torch.cuda.set_device(local)
+    w = W.make_workload(args.workload)
+    step = DecodeStep(w, device=f"cuda:{local}")
+    nbytes = algorithmic_bytes(w)
+    stream = torch.cuda.current_stream()
+    launches_per_step = (0 if not w.append else (1 if w.kv_dtype == "bf16" else 3)) + 1
+
+    for _ in range(args.warmup):
+        step.step()
+    torch.cuda.synchronize()
+    if pkv_check_device_error(step.pool.handle) != 0:
+        raise RuntimeError("device error flag set after warm-up")
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for k in range(K):
+        ev_a[k].record(stream)
+        step.append()
+        ev_b[k].record(stream)
+        step.attention()
+        ev_c[k].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    dist_barrier(world)
+    clocks = sampler.stop()
+    total_ms = ev_a[0].elapsed_time(ev_c[-1])
+    attn_ms = [ev_b[k].elapsed_time(ev_c[k]) for k in range(K)]
+    app_ms = [ev_a[k].elapsed_time(ev_b[k]) for k in range(K)]
+    ms_per_step = dist_max(total_ms / K, world)
+    if pkv_check_device_error(step.pool.handle) != 0:
+        raise RuntimeError("device error flag set in the timed region")
+
+    value = world * nbytes["step"] / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    attn_mean = statistics.mean(attn_ms)
+    achieved = nbytes["attention"] / (attn_mean * 1e-3) / 1e9
+    traffic = ncu_traffic(w.name)
+
+    # end to end from host buffers through the public API
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step.step_host()
+    t0 = time.perf_counter()
+    h2d = d2h = 0
+    for _ in range(e2e_steps):
+        h2d, d2h = step.step_host()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = dist_max(e2e_s, world)
+    e2e_value = world * nbytes["step"] / e2e_s / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        threads = os.cpu_count() or 1
+        rate, spent, sample = oracle_rate(w, args.cpu_budget, threads)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{sample}; {spent:.1f} s"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32-accumulate on bf16 KV" if w.kv_dtype == "bf16" else "f32-accumulate on fp8 KV",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "batch": w.B, "q_heads": w.Hq,
+                   "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+                   "context_tokens": int(w.attend_lens.sum()), "kv_bytes_per_step": nbytes["kv"],
+                   "step_bytes": nbytes["step"], "l2": "inputs larger than L2 (KV read per step "
+                   f"{nbytes['kv'] / 2**20:.0f} MiB > {L2_BYTES // 2**20} MiB)", "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
+        "kernel_us": {"attention": round(attn_mean * 1e3, 2), "attention_median": round(statistics.median(attn_ms) * 1e3, 2),
+                      "append": round(statistics.mean(app_ms) * 1e3, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel", "algorithmic_bytes_per_launch": nbytes["attention"]},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    step.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="c1", choices=list(W.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_pkv(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,44 @@
+"""Run the oracle over a workload — TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
+
+Builds the oracle's own allocator replica and host pool from the workload's seeded
+inputs (replaying the same allocation script and the same append calls as the
+device path) and evaluates the decode step in fp64.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+from . import Allocator, Pool
+
+
+def build(w, with_new_token: bool = True):
+    """(pool, allocator, block_tables) after the history and (optionally) the step's append."""
+    alloc = Allocator(w.num_blocks, w.block_size)
+    if alloc.set_free_order(w.free_order):
+        raise RuntimeError("oracle: bad free order")
+    alloc.replay(w.alloc_ops)
+    tables = alloc.block_tables(w.seq_ids, max(1, w.max_blocks()))
+    pool = Pool(w.num_blocks, w.block_size, w.Hkv, w.D, w.kv_dtype == "fp8_e4m3")
+    for t0, t1 in w.hist_chunks():
+        seqs, pos = w.hist_positions(t0, t1)
+        rc = pool.append(w.history_k(t0, t1), w.history_v(t0, t1), alloc.slot_mapping(seqs, pos))
+        if rc:
+            raise RuntimeError(f"oracle append rc={rc}")
+    if w.append and with_new_token:
+        rc = pool.append(w.new_k(), w.new_v(), alloc.slot_mapping(w.seq_ids, w.lens))
+        if rc:
+            raise RuntimeError(f"oracle append rc={rc}")
+    return pool, alloc, tables
+
+
+def attention(w, pool, tables, threads: int | None = None, seqs=None) -> np.ndarray:
+    """fp64 decode attention of the step, [B, Hq, D]; `seqs` limits it to some sequences."""
+    q = w.query()
+    lens = w.attend_lens
+    if seqs is not None:
+        seqs = np.asarray(seqs)
+        q, tables, lens = q[seqs], tables[seqs], lens[seqs]
+    return pool.attention(q, tables, lens, w.Hq, 1.0 / math.sqrt(w.D), threads=threads or os.cpu_count() or 1)

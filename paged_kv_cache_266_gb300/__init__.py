@@ -1,0 +1,263 @@
+"""Paged KV cache and decode attention for one GB300 — Python binding.
+
+Argument marshalling only: every call goes straight to the C ABI declared in
+``include/pkv.h`` (libpkv.so, built in-tree by ``build.py``).  Host arrays are
+numpy; device buffers are torch CUDA tensors (torch provides device memory and
+streams, nothing else).  There is no fallback: if libpkv.so is missing the
+import of any entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = [
+    "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "library_path",
+    "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
+    "pkv_seq_release", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
+    "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
+    "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_workspace_bytes",
+    "pkv_decode_workspace_init", "pkv_kv_bytes", "pkv_status_str", "KVPool",
+]
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OOM, PKV_ERR_NO_SEQ, PKV_ERR_BOUNDS, PKV_ERR_CUDA, PKV_ERR_TIMEOUT = range(7)
+PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+class PKVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {pkv_status_str(status)} (status {status})")
+        self.status = status
+
+
+def _L():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"libpkv.so is not built ({_build.LIB}); run __graft_entry__.build() or "
+                           "python -m paged_kv_cache_266_gb300.build")
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "pkv_allocator_create": (i32, [i32, i32, P(vp)]),
+        "pkv_allocator_destroy": (i32, [vp]),
+        "pkv_allocator_set_free_order": (i32, [vp, vp, i32]),
+        "pkv_seq_reserve": (i32, [vp, i64, i64]),
+        "pkv_seq_release": (i32, [vp, i64]),
+        "pkv_seq_num_blocks": (i32, [vp, i64, P(i32)]),
+        "pkv_num_free_blocks": (i32, [vp, P(i32)]),
+        "pkv_free_list": (i32, [vp, vp, i32, P(i32)]),
+        "pkv_get_block_tables": (i32, [vp, vp, i32, i32, vp]),
+        "pkv_slot_mapping": (i32, [vp, vp, vp, i64, vp]),
+        "pkv_pool_create": (i32, [i32, i32, i32, i32, i32, P(vp)]),
+        "pkv_pool_destroy": (i32, [vp]),
+        "pkv_pool_allocator": (i32, [vp, P(vp)]),
+        "pkv_pool_raw": (i32, [vp, P(vp), P(sz), P(vp), P(sz)]),
+        "pkv_check_device_error": (i32, [vp]),
+        "pkv_append": (i32, [vp, vp, vp, vp, i64, vp]),
+        "pkv_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, sz, vp]),
+        "pkv_decode_workspace_bytes": (i32, [vp, i32, i32, i32, P(sz)]),
+        "pkv_decode_workspace_init": (i32, [vp, sz, vp]),
+        "pkv_kv_bytes": (ctypes.c_uint64, [i64, i64, i64, i64, i64, ctypes.c_double]),
+        "pkv_status_str": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != PKV_OK:
+        raise PKVError(rc, what)
+
+
+def _np(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _dev(t, dtype_name: str, what: str) -> int:
+    """Device pointer of a contiguous torch CUDA tensor of the expected dtype."""
+    import torch
+    want = {"bf16": torch.bfloat16, "i32": torch.int32, "i64": torch.int64, "u8": torch.uint8}[dtype_name]
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what}: expected a CUDA tensor")
+    if t.dtype != want:
+        raise TypeError(f"{what}: expected dtype {want}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+# ----------------------------------------------------------------------------- allocator
+def pkv_allocator_create(num_blocks: int, block_size: int) -> int:
+    h = ctypes.c_void_p()
+    _check(_L().pkv_allocator_create(num_blocks, block_size, ctypes.byref(h)), "pkv_allocator_create")
+    return h.value
+
+
+def pkv_allocator_destroy(a: int) -> None:
+    _check(_L().pkv_allocator_destroy(a), "pkv_allocator_destroy")
+
+
+def pkv_allocator_set_free_order(a: int, order) -> None:
+    o = _np(order, np.int32)
+    _check(_L().pkv_allocator_set_free_order(a, o.ctypes.data, len(o)), "pkv_allocator_set_free_order")
+
+
+def pkv_seq_reserve(a: int, seq_id: int, n_tokens: int) -> None:
+    _check(_L().pkv_seq_reserve(a, seq_id, n_tokens), "pkv_seq_reserve")
+
+
+def pkv_seq_release(a: int, seq_id: int) -> None:
+    _check(_L().pkv_seq_release(a, seq_id), "pkv_seq_release")
+
+
+def pkv_seq_num_blocks(a: int, seq_id: int) -> int:
+    n = ctypes.c_int()
+    _check(_L().pkv_seq_num_blocks(a, seq_id, ctypes.byref(n)), "pkv_seq_num_blocks")
+    return n.value
+
+
+def pkv_num_free_blocks(a: int) -> int:
+    n = ctypes.c_int()
+    _check(_L().pkv_num_free_blocks(a, ctypes.byref(n)), "pkv_num_free_blocks")
+    return n.value
+
+
+def pkv_free_list(a: int) -> np.ndarray:
+    out = np.empty(pkv_num_free_blocks(a), dtype=np.int32)
+    n = ctypes.c_int()
+    _check(_L().pkv_free_list(a, out.ctypes.data, len(out), ctypes.byref(n)), "pkv_free_list")
+    return out[:n.value]
+
+
+def pkv_get_block_tables(a: int, seq_ids, max_blocks: int) -> np.ndarray:
+    s = _np(seq_ids, np.int64)
+    out = np.empty((len(s), max_blocks), dtype=np.int32)
+    _check(_L().pkv_get_block_tables(a, s.ctypes.data, len(s), max_blocks, out.ctypes.data), "pkv_get_block_tables")
+    return out
+
+
+def pkv_slot_mapping(a: int, seq_ids, positions) -> np.ndarray:
+    s, p = _np(seq_ids, np.int64), _np(positions, np.int64)
+    if s.shape != p.shape:
+        raise ValueError("seq_ids and positions must have the same length")
+    out = np.empty(len(s), dtype=np.int64)
+    _check(_L().pkv_slot_mapping(a, s.ctypes.data, p.ctypes.data, len(s), out.ctypes.data), "pkv_slot_mapping")
+    return out
+
+
+# ----------------------------------------------------------------------------- pool
+def pkv_pool_create(num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int, kv_dtype: int) -> int:
+    h = ctypes.c_void_p()
+    _check(_L().pkv_pool_create(num_blocks, block_size, n_kv_heads, head_dim, kv_dtype, ctypes.byref(h)),
+           "pkv_pool_create")
+    return h.value
+
+
+def pkv_pool_destroy(pool: int) -> None:
+    _check(_L().pkv_pool_destroy(pool), "pkv_pool_destroy")
+
+
+def pkv_pool_allocator(pool: int) -> int:
+    h = ctypes.c_void_p()
+    _check(_L().pkv_pool_allocator(pool, ctypes.byref(h)), "pkv_pool_allocator")
+    return h.value
+
+
+def pkv_pool_raw(pool: int):
+    kv, kvb, sc, scb = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_void_p(), ctypes.c_size_t()
+    _check(_L().pkv_pool_raw(pool, ctypes.byref(kv), ctypes.byref(kvb), ctypes.byref(sc), ctypes.byref(scb)),
+           "pkv_pool_raw")
+    return kv.value, kvb.value, sc.value or 0, scb.value
+
+
+def pkv_check_device_error(pool: int) -> int:
+    """Status code of the pool's device error word (read and cleared)."""
+    return _L().pkv_check_device_error(pool)
+
+
+def pkv_append(pool: int, k_new, v_new, slot_mapping, stream=None) -> None:
+    """k_new, v_new: bf16 CUDA tensors [N, Hkv, D]; slot_mapping: int64 CUDA tensor [N]."""
+    N = slot_mapping.shape[0]
+    _check(_L().pkv_append(pool, _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"),
+                           _dev(slot_mapping, "i64", "slot_mapping"), N, _stream(stream)), "pkv_append")
+
+
+def pkv_decode_attention(pool: int, q, block_tables, context_lens, scale: float, out, workspace,
+                         stream=None) -> None:
+    """q/out: bf16 CUDA [B, Hq, D]; block_tables int32 [B, max_blocks]; context_lens int32 [B];
+    workspace: uint8 CUDA tensor of pkv_decode_workspace_bytes() bytes, zeroed before first use."""
+    B, Hq = q.shape[0], q.shape[1]
+    _check(_L().pkv_decode_attention(pool, _dev(q, "bf16", "q"), _dev(block_tables, "i32", "block_tables"),
+                                     block_tables.shape[1], _dev(context_lens, "i32", "context_lens"), B, Hq,
+                                     float(scale), _dev(out, "bf16", "out"), _dev(workspace, "u8", "workspace"),
+                                     workspace.numel(), _stream(stream)), "pkv_decode_attention")
+
+
+def pkv_decode_workspace_bytes(pool: int, B: int, n_q_heads: int, max_blocks: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_L().pkv_decode_workspace_bytes(pool, B, n_q_heads, max_blocks, ctypes.byref(n)),
+           "pkv_decode_workspace_bytes")
+    return n.value
+
+
+def pkv_decode_workspace_init(workspace, stream=None) -> None:
+    _check(_L().pkv_decode_workspace_init(_dev(workspace, "u8", "workspace"), workspace.numel(), _stream(stream)),
+           "pkv_decode_workspace_init")
+
+
+def pkv_kv_bytes(n_layers: int, n_kv_heads: int, head_dim: int, n_tokens: int, batch: int,
+                 bytes_per_elem: float) -> int:
+    return _L().pkv_kv_bytes(n_layers, n_kv_heads, head_dim, n_tokens, batch, bytes_per_elem)
+
+
+def pkv_status_str(s: int) -> str:
+    try:
+        return _L().pkv_status_str(s).decode()
+    except Exception:  # library not loadable: still report the code
+        return f"status {s}"
+
+
+# ----------------------------------------------------------------------------- convenience
+class KVPool:
+    """Owns a pool handle (destroyed with the object) and remembers its geometry."""
+
+    def __init__(self, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
+                 kv_dtype: int = PKV_KV_BF16):
+        self.handle = pkv_pool_create(num_blocks, block_size, n_kv_heads, head_dim, kv_dtype)
+        self.allocator = pkv_pool_allocator(self.handle)
+        self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim = num_blocks, block_size, n_kv_heads, head_dim
+        self.kv_dtype = kv_dtype
+
+    def close(self):
+        if getattr(self, "handle", None):
+            pkv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

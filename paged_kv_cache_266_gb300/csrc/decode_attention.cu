@@ -1,0 +1,781 @@
+// Decode attention over the paged KV pool ("TensorRT-LLM 推理加速实战", §7.2 masked_mha: the
+// decode phase attends one new query token per request to that request's cached K/V; §8:
+// paged blocks of 16/64 tokens, FP8 e4m3 KV).  For sequence b and query head j, with KV head
+// h = j / G (GQA sharing, "TensorRT-LLM加速大模型推理实战"):
+//     out[b][j] = sum_t softmax_t(scale * q[b][j] . K_b[t]) V_b[t].
+//
+// Work decomposition (GB300: 152 SMs, HBM-bound):
+//  * Every (sequence, KV head) pair's context is cut into 64-token groups; the groups of all
+//    pairs, laid end to end (pairs in (b, h) order), are split into gridDim.x contiguous,
+//    equal ranges, one per CTA.  The grid is sized to the resident CTA count, so one wave
+//    streams the whole pool at an even rate whatever the context-length mix.
+//  * A CTA is one producer warp and four consumer warps.  The producer walks its range and,
+//    per group, issues TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzled rows) of the
+//    K and V rows of that group's pages into a ring of shared-memory stages, completion
+//    tracked by mbarriers; plus the query rows at each new pair and, for fp8, the 16-byte
+//    scale records of the pages.  Block ids come from the block table, fetched 32 groups
+//    ahead by the producer's lanes.
+//  * Consumer warp w owns tokens [16w, 16w+16) of every group.  The whole query group of
+//    the KV head (G <= 8 heads) is one MMA N-tile, so each K/V byte is read from HBM once:
+//        S^T[16 tok][8 heads] = K[16 tok][D] . Q^T    (mma.sync m16n8k16, fp32 accumulate)
+//        online softmax on S^T in registers (base-2 exponent, scale*log2 e folded in)
+//        P^T -> B fragment via movmatrix (register transpose, no shared-memory round trip)
+//        O^T[D][8 heads] += V^T[D][16 tok] . P^T       (ldmatrix.trans for bf16 V)
+//    fp8 codes are widened to f16 in registers (exact); the K scale multiplies the scores,
+//    the V scale is folded into the running rescale factor.
+//  * When a pair ends inside the CTA the four warps' (max, sum, O) states are merged through
+//    shared memory and the result is written as bf16.  A pair cut between CTAs leaves one
+//    partial state per CTA in the workspace; the last CTA to finish (atomic ticket, no
+//    waiting) merges them with the log-sum-exp rule in slot order, so results do not depend
+//    on timing.
+//
+// Every mbarrier wait is bounded (2 s of wall time); on expiry the kernel sets the pool's
+// error word and finishes without touching memory outside its buffers.
+#include <algorithm>
+#include <cstdlib>
+
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace attn {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kGroup = 16 * kConsumerWarps;  // tokens per pipeline stage
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMaxG = 8;
+constexpr int kMaxStages = 8;
+constexpr int kMaxBatch = 4096;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kCombineBar = 1;  // named barrier of the consumer warps
+
+struct Params {
+    const uint16_t* q;
+    const int32_t* tables;
+    const int32_t* lens;
+    uint16_t* out;
+    const uint8_t* pool;
+    const float* scales;
+    int* counters;
+    float* partials;
+    int* err;
+    int B, Hq, Hkv, G, max_blocks, bs, num_blocks;
+    int box_rows;  // rows per TMA box: min(bs, kGroup)
+    int ppg;       // page parts per group: kGroup / box_rows
+    int stages;
+    uint32_t stage_bytes, off_v, off_q, off_s;       // within a stage
+    uint32_t off_bar, off_misc, off_cmb, off_lens;  // within the shared-memory block
+    float scale_log2;
+};
+
+// misc words in shared memory
+constexpr int kMiscAbort = 0;
+constexpr int kMiscMergeParts = 1;
+constexpr int kMiscMergeFirst = 2;
+
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* misc) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (misc[kMiscAbort]) return false;
+            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void flag_abort(const Params& p, volatile int* misc) {
+    misc[kMiscAbort] = 1;
+    atomicOr(p.err, kErrTimeout);
+}
+
+// Largest b with Hkv * cumg[b] <= e (pairs of empty sequences have no groups and are skipped).
+__device__ __forceinline__ int find_seq(const int32_t* cumg, int B, int Hkv, int64_t e) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)Hkv * cumg[mid] <= e) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ------------------------------------------------------------------ producer warp
+struct GroupDesc {
+    int b, h, g;
+    int32_t id[4];
+};
+
+template <bool FP8, int D>
+__device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t* cumg, const int32_t* lens_s,
+                         int64_t R0, int64_t R1, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
+                         volatile int* misc) {
+    constexpr int kEsz = FP8 ? 1 : 2;
+    constexpr int kRowBytes = D * kEsz;
+    constexpr int kPanelBytes = FP8 ? D : 128;  // bytes of a row inside one TMA box
+    constexpr int kPanels = kRowBytes / kPanelBytes;
+    const int lane = threadIdx.x & 31;
+
+    auto describe = [&](int64_t e, GroupDesc& d) {
+        d.b = -1;
+        if (e >= R1) return;
+        const int b = find_seq(cumg, p.B, p.Hkv, e);
+        const int ng = cumg[b + 1] - cumg[b];
+        const int64_t r = e - (int64_t)p.Hkv * cumg[b];
+        d.b = b;
+        d.h = (int)(r / ng);
+        d.g = (int)(r - (int64_t)d.h * ng);
+        const int npages = (lens_s[b] + p.bs - 1) / p.bs;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = p.ppg > 1 ? d.g * p.ppg + i : (d.g * kGroup) / p.bs;
+            d.id[i] = (i < p.ppg && k < npages) ? __ldg(p.tables + (int64_t)b * p.max_blocks + k) : -1;
+        }
+    };
+
+    GroupDesc cur, nxt;
+    describe(R0 + lane, cur);
+    int s = 0;
+    uint32_t round = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t e0 = R0; e0 < R1 && ok; e0 += 32) {
+        describe(e0 + 32 + lane, nxt);  // table loads for the next 32 groups are in flight meanwhile
+        const int n = (int)(R1 - e0 < 32 ? R1 - e0 : 32);
+        for (int j = 0; j < n; ++j) {
+            const int b = __shfl_sync(0xffffffffu, cur.b, j);
+            const int h = __shfl_sync(0xffffffffu, cur.h, j);
+            const int g = __shfl_sync(0xffffffffu, cur.g, j);
+            int32_t ids[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ids[i] = __shfl_sync(0xffffffffu, cur.id[i], j);
+            if (lane == 0) {
+                ok = ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, kWaitLimitNs);
+                if (!ok) {
+                    flag_abort(p, misc);
+                } else {
+                    const int64_t e = e0 + j;
+                    const bool first = (e == R0) || (g == 0);
+                    const int L = lens_s[b];
+                    int nparts = 1;
+                    if (p.ppg > 1) nparts = min(p.ppg, (L + p.bs - 1) / p.bs - g * p.ppg);
+                    const uint32_t part_bytes = (uint32_t)p.box_rows * kRowBytes;
+                    const uint32_t bytes = (uint32_t)nparts * part_bytes * 2 + (FP8 ? 16u * nparts : 0u) +
+                                           (first ? (uint32_t)(p.G * D * 2) : 0u);
+                    const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+                    const uint32_t fb = bar_full + 8 * s;
+                    ptx::mbar_arrive_expect_tx(fb, bytes);
+                    const int row_off = p.ppg > 1 ? 0 : (g * kGroup) % p.bs;
+                    for (int i = 0; i < nparts; ++i) {
+                        int blk = ids[i];
+                        if (blk < 0 || blk >= p.num_blocks) {  // keep the byte count exact, read block 0
+                            atomicOr(p.err, kErrBounds);
+                            blk = 0;
+                        }
+                        const int64_t rowK = ((int64_t)(2 * blk) * p.Hkv + h) * p.bs + row_off;
+                        const int64_t rowV = ((int64_t)(2 * blk + 1) * p.Hkv + h) * p.bs + row_off;
+                        const uint32_t dst_rows = (uint32_t)(i * p.box_rows) * kPanelBytes;
+#pragma unroll
+                        for (int q = 0; q < kPanels; ++q)
+                            ptx::tma_load_2d(st + q * (kGroup * kPanelBytes) + dst_rows, tmap, q * (kPanelBytes / kEsz),
+                                             (int32_t)rowK, fb);
+                        if (FP8) {
+                            // V panels ([D][16] per 16 tokens) are contiguous: one bulk copy per part
+                            const uint8_t* src = p.pool + rowV / p.bs * (int64_t)p.bs * D + (int64_t)row_off * D;
+                            ptx::bulk_load(st + p.off_v + (uint32_t)(i * p.box_rows * D), src, part_bytes, fb);
+                            ptx::bulk_load(st + p.off_s + 16 * i, p.scales + ((int64_t)blk * p.Hkv + h) * 4, 16, fb);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < kPanels; ++q)
+                                ptx::tma_load_2d(st + p.off_v + q * (kGroup * kPanelBytes) + dst_rows, tmap,
+                                                 q * (kPanelBytes / kEsz), (int32_t)rowV, fb);
+                        }
+                    }
+                    if (first)
+                        ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D,
+                                       (uint32_t)(p.G * D * 2), fb);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ++issued;
+            if (++s == p.stages) {
+                s = 0;
+                ++round;
+            }
+        }
+        cur = nxt;
+    }
+    // Do not leave while copies into this CTA's shared memory may still be landing.
+    if (lane == 0) {
+        const int64_t lo = issued > p.stages ? issued - p.stages : 0;
+        for (int64_t qq = issued - 1; qq >= lo; --qq)
+            if (!ptx::mbar_wait(bar_full + 8 * (int)(qq % p.stages), (uint32_t)((qq / p.stages) & 1), kWaitLimitNs)) {
+                flag_abort(p, misc);
+                break;
+            }
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ consumer math
+struct SoftmaxState {
+    float m[2];  // running max (base-2 units) of heads 2c, 2c+1
+    float l[2];  // per-lane partial sums of exp2(z - m)
+};
+
+// Online-softmax step on one 16-token S^T tile.  acc: (t=g, j=2c), (g, 2c+1), (g+8, 2c),
+// (g+8, 2c+1).  Returns the rescale factors of the two heads and the probabilities.
+__device__ __forceinline__ void softmax_step(const float (&acc)[4], float sl, int nvalid, int g8, SoftmaxState& st,
+                                             float (&pr)[4], float& a0, float& a1) {
+    float z0 = acc[0] * sl, z1 = acc[1] * sl, z2 = acc[2] * sl, z3 = acc[3] * sl;
+    if (nvalid < 16) {
+        if (g8 >= nvalid) z0 = z1 = -INFINITY;
+        if (g8 + 8 >= nvalid) z2 = z3 = -INFINITY;
+    }
+    float t0 = fmaxf(z0, z2), t1 = fmaxf(z1, z3);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+        t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+        t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+    }
+    const float m0 = fmaxf(st.m[0], t0), m1 = fmaxf(st.m[1], t1);
+    a0 = ptx::exp2_approx(st.m[0] - m0);
+    a1 = ptx::exp2_approx(st.m[1] - m1);
+    st.m[0] = m0;
+    st.m[1] = m1;
+    pr[0] = ptx::exp2_approx(z0 - m0);
+    pr[1] = ptx::exp2_approx(z1 - m1);
+    pr[2] = ptx::exp2_approx(z2 - m0);
+    pr[3] = ptx::exp2_approx(z3 - m1);
+}
+
+template <int D>
+__device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, int nvalid,
+                                          const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], SoftmaxState& st,
+                                          float sl, int lane) {
+    constexpr int KS = D / 16;
+    const int rr = lane & 7, mat = lane >> 3, g8 = lane >> 2, c4 = lane & 3;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int krow = row0 + rr + ((mat & 1) << 3);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int chunk = 2 * ks + (mat >> 1);
+        const uint32_t addr = kst + (chunk >> 3) * (kGroup * 128) + krow * 128 + (((chunk & 7) ^ rr) << 4);
+        uint32_t a0, a1, a2, a3;
+        ptx::ldsm_x4(addr, a0, a1, a2, a3);
+        ptx::mma_bf16(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+    }
+    float pr[4], f0, f1;
+    softmax_step(acc, sl, nvalid, g8, st, pr, f0, f1);
+    const uint32_t p01 = ptx::pack_bf16x2(pr[0], pr[1]), p23 = ptx::pack_bf16x2(pr[2], pr[3]);
+    // the sums use the rounded probabilities the MMA multiplies with
+    st.l[0] = st.l[0] * f0 + ptx::bf16lo_to_f32(p01) + ptx::bf16lo_to_f32(p23);
+    st.l[1] = st.l[1] * f1 + ptx::bf16hi_to_f32(p01) + ptx::bf16hi_to_f32(p23);
+    const uint32_t pb0 = ptx::movmatrix_trans(p01), pb1 = ptx::movmatrix_trans(p23);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= f0;
+        o[mt][1] *= f1;
+        o[mt][2] *= f0;
+        o[mt][3] *= f1;
+    }
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (nvalid < 16) {  // V rows past the context may hold stale bits: zero them
+        mlo = (2 * c4 < nvalid ? 0x0000ffffu : 0u) | (2 * c4 + 1 < nvalid ? 0xffff0000u : 0u);
+        mhi = (2 * c4 + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c4 + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+    const int vrow = row0 + rr + ((mat >> 1) << 3);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        const int chunk = 2 * mt + (mat & 1);
+        const uint32_t addr = vst + (chunk >> 3) * (kGroup * 128) + vrow * 128 + (((chunk & 7) ^ rr) << 4);
+        uint32_t v0, v1, v2, v3;
+        ptx::ldsm_x4_trans(addr, v0, v1, v2, v3);
+        ptx::mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, pb0, pb1);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ uint32_t fp8_k_addr(uint32_t kst, int row, int chunk) {
+    if (D == 128) return kst + row * 128 + ((chunk ^ (row & 7)) << 4);
+    return kst + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+}
+
+template <int D>
+__device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, int nvalid,
+                                         const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], SoftmaxState& st,
+                                         float sl, float sk, float sv, float& sv_prev, int lane) {
+    constexpr int KS = D / 16;
+    const int rr = lane & 7, mat = lane >> 3, g8 = lane >> 2, c4 = lane & 3;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int krow = row0 + rr + ((mat & 1) << 3);
+#pragma unroll
+    for (int kk = 0; kk < KS / 2; ++kk) {
+        uint32_t r0, r1, r2, r3;
+        ptx::ldsm_x4(fp8_k_addr<D>(kst, krow, 2 * kk + (mat >> 1)), r0, r1, r2, r3);
+        ptx::mma_f16(acc, ptx::e4m3x2_to_f16x2(r0), ptx::e4m3x2_to_f16x2(r1), ptx::e4m3x2_to_f16x2(r0 >> 16),
+                     ptx::e4m3x2_to_f16x2(r1 >> 16), qf[2 * kk][0], qf[2 * kk][1]);
+        ptx::mma_f16(acc, ptx::e4m3x2_to_f16x2(r2), ptx::e4m3x2_to_f16x2(r3), ptx::e4m3x2_to_f16x2(r2 >> 16),
+                     ptx::e4m3x2_to_f16x2(r3 >> 16), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+    }
+    float pr[4], f0, f1;
+    softmax_step(acc, sl * sk, nvalid, g8, st, pr, f0, f1);
+    const uint32_t p01 = ptx::pack_f16x2(pr[0], pr[1]), p23 = ptx::pack_f16x2(pr[2], pr[3]);
+    const float2 q01 = ptx::f16x2_to_f32x2(p01), q23 = ptx::f16x2_to_f32x2(p23);
+    st.l[0] = st.l[0] * f0 + q01.x + q23.x;
+    st.l[1] = st.l[1] * f1 + q01.y + q23.y;
+    const uint32_t pb0 = ptx::movmatrix_trans(p01), pb1 = ptx::movmatrix_trans(p23);
+    // O is kept in units of the current tile's V scale: rescale by alpha * s_prev / s_cur
+    const float ratio = __fdividef(sv_prev, sv);
+    sv_prev = sv;
+    f0 *= ratio;
+    f1 *= ratio;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= f0;
+        o[mt][1] *= f1;
+        o[mt][2] *= f0;
+        o[mt][3] *= f1;
+    }
+    // V panel row d holds tokens 2c,2c+1,2c+8,2c+9 in this lane's 4 bytes
+    uint32_t bm = 0xffffffffu;
+    if (nvalid < 16)
+        bm = (2 * c4 < nvalid ? 0x000000ffu : 0u) | (2 * c4 + 1 < nvalid ? 0x0000ff00u : 0u) |
+             (2 * c4 + 8 < nvalid ? 0x00ff0000u : 0u) | (2 * c4 + 9 < nvalid ? 0xff000000u : 0u);
+#pragma unroll
+    for (int mm = 0; mm < KS / 2; ++mm) {
+        uint32_t r0, r1, r2, r3;
+        ptx::ldsm_x4(vst + (uint32_t)(32 * mm + lane) * 16, r0, r1, r2, r3);
+        r0 &= bm;
+        r1 &= bm;
+        r2 &= bm;
+        r3 &= bm;
+        ptx::mma_f16(o[2 * mm], ptx::e4m3x2_to_f16x2(r0), ptx::e4m3x2_to_f16x2(r1), ptx::e4m3x2_to_f16x2(r0 >> 16),
+                     ptx::e4m3x2_to_f16x2(r1 >> 16), pb0, pb1);
+        ptx::mma_f16(o[2 * mm + 1], ptx::e4m3x2_to_f16x2(r2), ptx::e4m3x2_to_f16x2(r3),
+                     ptx::e4m3x2_to_f16x2(r2 >> 16), ptx::e4m3x2_to_f16x2(r3 >> 16), pb0, pb1);
+    }
+}
+
+// Query B-fragments of the group's G heads (rows >= G are zero).
+template <bool FP8, int D>
+__device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const uint8_t* qs, int G, int lane) {
+    const int g8 = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        if (g8 >= G) {
+            qf[ks][0] = qf[ks][1] = 0u;
+        } else if (!FP8) {
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(qs + (size_t)g8 * D * 2);
+            qf[ks][0] = row[(16 * ks + 2 * c4) >> 1];
+            qf[ks][1] = row[(16 * ks + 8 + 2 * c4) >> 1];
+        } else {  // logical k 2c,2c+1 | 2c+8,2c+9 <-> physical d 4c..4c+3 (matches the fp8 K fragment)
+            const uint2 v = *reinterpret_cast<const uint2*>(qs + ((size_t)g8 * D + 16 * ks + 4 * c4) * 2);
+            qf[ks][0] = ptx::pack_f16x2(ptx::bf16lo_to_f32(v.x), ptx::bf16hi_to_f32(v.x));
+            qf[ks][1] = ptx::pack_f16x2(ptx::bf16lo_to_f32(v.y), ptx::bf16hi_to_f32(v.y));
+        }
+    }
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+    return static_cast<uint16_t>(ptx::pack_bf16x2(x, 0.f) & 0xffffu);
+}
+
+// Merge the four warps' states of pair (b, h) and write the output (pair complete in this CTA)
+// or a partial state plus a ticket (pair cut between CTAs; the last one merges all parts).
+template <int D>
+__device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const SoftmaxState& st, float osc, int b,
+                            int h, bool complete, int64_t Ng, int64_t C, const int32_t* cumg, uint8_t* smem,
+                            volatile int* misc) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, c4 = lane & 3;
+    const int G = p.G;
+    float l0 = st.l[0], l1 = st.l[1];
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    constexpr int kStride = D + 4;
+    float* cO = reinterpret_cast<float*>(smem + p.off_cmb);
+    float* cM = cO + kConsumerWarps * G * kStride;
+    float* cL = cM + kConsumerWarps * G;
+    const int j0 = 2 * c4, j1 = 2 * c4 + 1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        const int d = 16 * mt + g8;
+        if (j0 < G) {
+            cO[(warp * G + j0) * kStride + d] = o[mt][0] * osc;
+            cO[(warp * G + j0) * kStride + d + 8] = o[mt][2] * osc;
+        }
+        if (j1 < G) {
+            cO[(warp * G + j1) * kStride + d] = o[mt][1] * osc;
+            cO[(warp * G + j1) * kStride + d + 8] = o[mt][3] * osc;
+        }
+    }
+    if (g8 == 0) {
+        if (j0 < G) {
+            cM[warp * G + j0] = st.m[0];
+            cL[warp * G + j0] = l0;
+        }
+        if (j1 < G) {
+            cM[warp * G + j1] = st.m[1];
+            cL[warp * G + j1] = l1;
+        }
+    }
+    ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+    const int pair = b * p.Hkv + h;
+    uint16_t* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
+    float* part = p.partials + ((int64_t)pair + blockIdx.x) * G * (D + 2);
+    for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+        const int j = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cM[w * G + j]);
+        float acc = 0.f, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = ptx::exp2_approx(cM[w * G + j] - M);
+            acc += f * cO[(w * G + j) * kStride + d];
+            l += f * cL[w * G + j];
+        }
+        if (complete) {
+            out[j * D + d] = f32_to_bf16_bits(acc / l);
+        } else {
+            part[j * (D + 2) + d] = acc;
+            if (d == 0) {
+                part[j * (D + 2) + D] = M;
+                part[j * (D + 2) + D + 1] = l;
+            }
+        }
+    }
+    if (!complete) {
+        __threadfence();
+        ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+        if (tid == 0) {
+            const int ng = cumg[b + 1] - cumg[b];
+            const int64_t e_first = (int64_t)p.Hkv * cumg[b] + (int64_t)h * ng;
+            const int64_t e_last = e_first + ng - 1;
+            const int c1 = (int)(((e_first + 1) * C - 1) / Ng);
+            const int c2 = (int)(((e_last + 1) * C - 1) / Ng);
+            const int ticket = atomicAdd(p.counters + pair, 1);
+            misc[kMiscMergeParts] = ticket == c2 - c1 ? c2 - c1 + 1 : 0;
+            misc[kMiscMergeFirst] = c1;
+        }
+        ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+        const int nparts = misc[kMiscMergeParts];
+        if (nparts) {
+            __threadfence();
+            const float* base = p.partials + ((int64_t)pair + misc[kMiscMergeFirst]) * G * (D + 2);
+            for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+                const int j = e / D, d = e % D;
+                float M = -INFINITY;
+                for (int s = 0; s < nparts; ++s) M = fmaxf(M, __ldcg(base + ((int64_t)s * G + j) * (D + 2) + D));
+                float acc = 0.f, l = 0.f;
+                for (int s = 0; s < nparts; ++s) {
+                    const float* ps = base + ((int64_t)s * G + j) * (D + 2);
+                    const float f = ptx::exp2_approx(__ldcg(ps + D) - M);
+                    acc += f * __ldcg(ps + d);
+                    l += f * __ldcg(ps + D + 1);
+                }
+                out[j * D + d] = f32_to_bf16_bits(acc / l);
+            }
+            if (tid == 0) p.counters[pair] = 0;
+        }
+    }
+    ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+}
+
+template <bool FP8, int D>
+__device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* lens_s, int64_t R0, int64_t R1,
+                         int64_t Ng, int64_t C, uint8_t* smem, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
+                         volatile int* misc) {
+    constexpr int KS = D / 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t qf[KS][2];
+    float o[KS][4];
+    SoftmaxState st;
+    float sv_prev = 1.f;
+    int b = find_seq(cumg, p.B, p.Hkv, R0);
+    int ng = cumg[b + 1] - cumg[b];
+    const int64_t r = R0 - (int64_t)p.Hkv * cumg[b];
+    int h = (int)(r / ng);
+    int g = (int)(r - (int64_t)h * ng);
+    int g_first = g;
+    int s = 0;
+    uint32_t round = 0;
+    bool alive = true;
+    for (int64_t e = R0; e < R1; ++e) {
+        const bool first = (e == R0) || (g == 0);
+        const bool last = (e == R1 - 1) || (g == ng - 1);
+        const uint32_t st_addr = sbase + (uint32_t)s * p.stage_bytes;
+        if (alive && !wait_full(bar_full + 8 * s, round & 1, misc)) {
+            alive = false;
+            flag_abort(p, misc);
+        }
+        if (first) {
+            load_q<FP8, D>(qf, smem + (st_addr - sbase) + p.off_q, p.G, lane);
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            st.m[0] = st.m[1] = -INFINITY;
+            st.l[0] = st.l[1] = 0.f;
+            sv_prev = 1.f;
+            g_first = g;
+        }
+        const int nvalid = min(16, lens_s[b] - g * kGroup - 16 * warp);
+        if (alive && nvalid > 0) {
+            if (FP8) {
+                const int pidx = (16 * warp) / p.box_rows;
+                const float* sc = reinterpret_cast<const float*>(smem + (st_addr - sbase) + p.off_s + 16 * pidx);
+                tile_fp8<D>(st_addr, st_addr + p.off_v + (uint32_t)(warp * D * 16), 16 * warp, nvalid, qf, o, st,
+                            p.scale_log2, sc[0], sc[1], sv_prev, lane);
+            } else {
+                tile_bf16<D>(st_addr, st_addr + p.off_v, 16 * warp, nvalid, qf, o, st, p.scale_log2, lane);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
+        if (last) finish_pair<D>(p, o, st, FP8 ? sv_prev : 1.f, b, h, g_first == 0 && g == ng - 1, Ng, C, cumg, smem,
+                                 misc);
+        if (++s == p.stages) {
+            s = 0;
+            ++round;
+        }
+        if (++g == ng) {
+            g = 0;
+            if (++h == p.Hkv) {
+                h = 0;
+                do {
+                    ++b;
+                } while (b < p.B && cumg[b + 1] == cumg[b]);
+                if (b < p.B) ng = cumg[b + 1] - cumg[b];
+            }
+        }
+    }
+}
+
+template <bool FP8, int D>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t* cumg = reinterpret_cast<int32_t*>(smem + p.off_lens);
+    int32_t* lens_s = cumg + p.B + 1;
+    volatile int* misc = reinterpret_cast<volatile int*>(smem + p.off_misc);
+    const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * p.stages;
+
+    // Context lengths (clamped to the table's capacity) and per-sequence group prefix sums.
+    if (warp == 0) {
+        const int cap = p.max_blocks * p.bs;
+        const int per = (p.B + 31) >> 5;
+        const int b0 = min(p.B, lane * per), b1 = min(p.B, b0 + per);
+        int sum = 0;
+        bool bad = false;
+        for (int bb = b0; bb < b1; ++bb) {
+            int L = __ldg(p.lens + bb);
+            if (L < 0 || L > cap) {
+                bad = true;
+                L = min(max(L, 0), cap);
+            }
+            lens_s[bb] = L;
+            sum += (L + kGroup - 1) / kGroup;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int run = incl - sum;
+        for (int bb = b0; bb < b1; ++bb) {
+            cumg[bb] = run;
+            run += (lens_s[bb] + kGroup - 1) / kGroup;
+        }
+        if (lane == 31) cumg[p.B] = incl;
+        if (bad && blockIdx.x == 0) atomicOr(p.err, kErrBounds);
+        if (lane == 0) {
+            misc[kMiscAbort] = 0;
+            misc[kMiscMergeParts] = 0;
+        }
+    }
+    if (tid == 32) {
+        for (int s = 0; s < p.stages; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, kConsumerWarps);
+        }
+        ptx::fence_barrier_init();
+    }
+    if (tid == 64) ptx::prefetch_tensormap(&tmap);
+    __syncthreads();
+
+    // Groups are split over C = min(grid, groups) CTAs, so every participating CTA owns at
+    // least one group and a pair cut between CTAs has exactly one part per CTA in between.
+    const int64_t Ng = (int64_t)p.Hkv * cumg[p.B];
+    const int64_t C = Ng < (int64_t)gridDim.x ? Ng : (int64_t)gridDim.x;
+    int64_t R0 = 0, R1 = 0;
+    if ((int64_t)blockIdx.x < C) {
+        R0 = (int64_t)blockIdx.x * Ng / C;
+        R1 = ((int64_t)blockIdx.x + 1) * Ng / C;
+    }
+
+    if (warp == kConsumerWarps) {
+        if (R0 < R1) producer<FP8, D>(&tmap, p, cumg, lens_s, R0, R1, sbase, bar_full, bar_empty, misc);
+        return;
+    }
+    // Sequences with an empty context get zeros (no group covers them).
+    for (int bb = blockIdx.x; bb < p.B; bb += gridDim.x) {
+        if (lens_s[bb] != 0) continue;
+        uint4* row = reinterpret_cast<uint4*>(p.out + (int64_t)bb * p.Hq * D);
+        for (int i = tid; i < p.Hq * D / 8; i += kConsumerWarps * 32) row[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (R0 < R1) consumer<FP8, D>(p, cumg, lens_s, R0, R1, Ng, C, smem, sbase, bar_full, bar_empty, misc);
+}
+
+// ------------------------------------------------------------------ host side
+struct Plan {
+    int stages = 0, ctas_per_sm = 0, grid = 0;
+    uint32_t stage_bytes = 0, off_v = 0, off_q = 0, off_s = 0;
+    uint32_t off_bar = 0, off_misc = 0, off_cmb = 0, off_lens = 0, smem_bytes = 0;
+    size_t counters_bytes = 0, ws_bytes = 0;
+};
+
+inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+const void* kernel_for(const pkv_pool* pool) {
+    const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
+    if (pool->head_dim == 128)
+        return fp8 ? (const void*)decode_kernel<true, 128> : (const void*)decode_kernel<false, 128>;
+    return fp8 ? (const void*)decode_kernel<true, 64> : (const void*)decode_kernel<false, 64>;
+}
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return v && *v ? std::atoi(v) : dflt;
+}
+
+bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
+    const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
+    const uint32_t D = (uint32_t)pool->head_dim, esz = fp8 ? 1 : 2;
+    const uint32_t region = kGroup * D * esz;
+    pl.off_v = region;
+    pl.off_q = 2 * region;
+    pl.off_s = pl.off_q + align_up((uint32_t)G * D * 2, 128);
+    pl.stage_bytes = align_up(pl.off_s + (fp8 ? 16u * 4 : 0u), 1024);
+    const uint32_t cmb = align_up((kConsumerWarps * G * (D + 4) + 2 * kConsumerWarps * G) * 4, 16);
+    const uint32_t lens = align_up((2u * B + 1) * 4, 16);
+    const uint32_t fixed = 1024 + 32 + cmb + lens;
+    const int pref = env_int("PKV_ATTN_CTAS_PER_SM", 2);
+    const int max_stages = std::max(2, std::min(kMaxStages, env_int("PKV_ATTN_MAX_STAGES", kMaxStages)));
+    pl.stages = 0;
+    for (int ctas = std::max(1, pref); ctas >= 1; --ctas) {
+        const int budget = std::min(pool->max_smem_per_block, pool->max_smem_per_sm / ctas - 1024);
+        if (budget <= (int)fixed) continue;
+        int S = (int)((budget - fixed) / (pl.stage_bytes + 16));
+        S = std::min(S, max_stages);
+        if (S >= 2) {
+            pl.stages = S;
+            pl.ctas_per_sm = ctas;
+            break;
+        }
+    }
+    if (!pl.stages) return false;
+    pl.off_bar = (uint32_t)pl.stages * pl.stage_bytes;
+    pl.off_misc = pl.off_bar + 16u * pl.stages;
+    pl.off_cmb = align_up(pl.off_misc + 32, 16);
+    pl.off_lens = pl.off_cmb + cmb;
+    pl.smem_bytes = pl.off_lens + lens + 1024;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel_for(pool), kThreads, pl.smem_bytes) != cudaSuccess ||
+        occ < 1)
+        return false;
+    pl.ctas_per_sm = std::min(pl.ctas_per_sm, occ);
+    pl.grid = pl.ctas_per_sm * pool->sm_count;
+    const size_t pairs = (size_t)B * pool->n_kv_heads;
+    pl.counters_bytes = (pairs * sizeof(int) + 255) / 256 * 256;
+    pl.ws_bytes = pl.counters_bytes + (pairs + (size_t)pl.grid) * G * (D + 2) * sizeof(float);
+    return true;
+}
+
+}  // namespace attn
+
+void attention_configure(pkv_pool* pool) {
+    cudaFuncSetAttribute(attn::kernel_for(pool), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         pool->max_smem_per_block);
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out) {
+    (void)max_blocks;
+    if (!pool || !out || B < 0 || B > pkv::attn::kMaxBatch || n_q_heads < 1 || n_q_heads % pool->n_kv_heads)
+        return PKV_ERR_INVALID_ARG;
+    const int G = n_q_heads / pool->n_kv_heads;
+    if (G > pkv::attn::kMaxG) return PKV_ERR_INVALID_ARG;
+    pkv::attn::Plan pl;
+    if (!pkv::attn::make_plan(pool, B, G, pl)) return PKV_ERR_CUDA;
+    *out = pl.ws_bytes;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32_t* block_tables, int max_blocks,
+                                const int32_t* context_lens, int B, int n_q_heads, float scale, void* out,
+                                void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    using namespace pkv::attn;
+    if (!pool || B < 0 || B > kMaxBatch || n_q_heads < 1 || n_q_heads % pool->n_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    const int G = n_q_heads / pool->n_kv_heads;
+    if (G > kMaxG || max_blocks < 1 || (int64_t)max_blocks * pool->block_size >= (1ll << 31))
+        return PKV_ERR_INVALID_ARG;
+    if (!q || !block_tables || !context_lens || !out || !workspace) return PKV_ERR_INVALID_ARG;
+    if (((uintptr_t)q | (uintptr_t)out) & 15u || (uintptr_t)workspace & 255u ||
+        ((uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
+        return PKV_ERR_INVALID_ARG;
+    Plan pl;
+    if (!make_plan(pool, B, G, pl)) return PKV_ERR_CUDA;
+    if (workspace_bytes < pl.ws_bytes) return PKV_ERR_INVALID_ARG;
+    Params p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.tables = block_tables;
+    p.lens = context_lens;
+    p.out = static_cast<uint16_t*>(out);
+    p.pool = static_cast<const uint8_t*>(pool->kv);
+    p.scales = pool->scales;
+    p.counters = static_cast<int*>(workspace);
+    p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
+    p.err = pool->err;
+    p.B = B;
+    p.Hq = n_q_heads;
+    p.Hkv = pool->n_kv_heads;
+    p.G = G;
+    p.max_blocks = max_blocks;
+    p.bs = pool->block_size;
+    p.num_blocks = pool->num_blocks;
+    p.box_rows = std::min(pool->block_size, kGroup);
+    p.ppg = kGroup / p.box_rows;
+    p.stages = pl.stages;
+    p.stage_bytes = pl.stage_bytes;
+    p.off_v = pl.off_v;
+    p.off_q = pl.off_q;
+    p.off_s = pl.off_s;
+    p.off_bar = pl.off_bar;
+    p.off_misc = pl.off_misc;
+    p.off_cmb = pl.off_cmb;
+    p.off_lens = pl.off_lens;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
+    if (pool->head_dim == 128) {
+        if (fp8) decode_kernel<true, 128><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
+        else decode_kernel<false, 128><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
+    } else {
+        if (fp8) decode_kernel<true, 64><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
+        else decode_kernel<false, 64><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

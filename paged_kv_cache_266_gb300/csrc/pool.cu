@@ -1,0 +1,189 @@
+// Paged KV block pool: device storage, its TMA descriptor and the device error word.
+//
+// One pool holds num_blocks blocks of block_size tokens for n_kv_heads heads of K and V
+// ("TensorRT-LLM 深度实战", §3.1: fixed-size pages handed out on demand;
+// "TensorRT-LLM 推理加速实战", §8: block_size 64 by default, 16 in vLLM; FP8 e4m3 KV).
+// Each (block, K|V, head) tile is contiguous, so one page of one head is a single
+// bulk/TMA copy.  The layout is documented in include/pkv.h.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+void attention_configure(pkv_pool* pool);  // decode_attention.cu
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Rows of head_dim elements over the whole pool: row r = ((blk*2 + kv)*Hkv + h)*bs + t.
+// Box: 128 bytes of a row (64 bf16 or 128 fp8 elements; 64 bytes for fp8 head_dim 64) by
+// min(bs, 64) rows, swizzled so that 8 rows of one 16-byte column land in 8 different bank
+// groups for ldmatrix.
+bool encode_rows_map(pkv_pool* p) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const bool fp8 = p->dtype == PKV_KV_FP8_E4M3;
+    const uint64_t esz = fp8 ? 1 : 2;
+    const uint64_t rows = (uint64_t)p->num_blocks * 2 * p->n_kv_heads * p->block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)p->head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(p->head_dim * esz)};
+    const uint32_t inner = fp8 ? (uint32_t)p->head_dim : 64u;  // elements per box row
+    const uint32_t box_rows = p->block_size < 64 ? (uint32_t)p->block_size : 64u;
+    cuuint32_t box[2] = {inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz = inner * esz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUresult r = encode(&p->tmap_rows, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        p->kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+void free_pool(pkv_pool* p) {
+    if (!p) return;
+    if (p->kv) cudaFree(p->kv);
+    if (p->scales) cudaFree(p->scales);
+    if (p->amax_scratch) cudaFree(p->amax_scratch);
+    if (p->fresh_scratch) cudaFree(p->fresh_scratch);
+    if (p->err) cudaFree(p->err);
+    if (p->alloc) allocator_delete(p->alloc);
+    delete p;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_pool_create(int num_blocks, int block_size, int n_kv_heads, int head_dim, pkv_dtype kv_dtype,
+                           pkv_pool** out) {
+    if (!out || num_blocks < 1 || n_kv_heads < 1 || !pkv::valid_block_size(block_size) ||
+        (head_dim != 64 && head_dim != 128) || (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3))
+        return PKV_ERR_INVALID_ARG;
+    const uint64_t rows = (uint64_t)num_blocks * 2 * n_kv_heads * block_size;
+    if (rows >= (1ull << 31)) return PKV_ERR_INVALID_ARG;  // TMA row coordinates are int32
+    pkv_pool* p = new (std::nothrow) pkv_pool();
+    if (!p) return PKV_ERR_OOM;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->n_kv_heads = n_kv_heads;
+    p->head_dim = head_dim;
+    p->dtype = kv_dtype;
+    const bool fp8 = kv_dtype == PKV_KV_FP8_E4M3;
+    p->alloc = pkv::allocator_new(num_blocks, block_size);
+    if (!p->alloc) {
+        pkv::free_pool(p);
+        return PKV_ERR_OOM;
+    }
+    pkv_status st = PKV_OK;
+    do {
+        if (cudaGetDevice(&p->device) != cudaSuccess ||
+            cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
+            cudaDeviceGetAttribute(&p->max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&p->max_smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) !=
+                cudaSuccess) {
+            st = PKV_ERR_CUDA;
+            break;
+        }
+        p->kv_bytes = rows * (uint64_t)head_dim * (fp8 ? 1 : 2);
+        if (cudaMalloc(&p->kv, p->kv_bytes) != cudaSuccess) {
+            st = PKV_ERR_OOM;
+            break;
+        }
+        if (cudaMalloc(&p->err, sizeof(int)) != cudaSuccess) {
+            st = PKV_ERR_OOM;
+            break;
+        }
+        if (fp8) {
+            p->scale_bytes = (size_t)num_blocks * n_kv_heads * 4 * sizeof(float);
+            if (cudaMalloc(&p->scales, p->scale_bytes) != cudaSuccess ||
+                cudaMalloc(&p->amax_scratch, (size_t)num_blocks * n_kv_heads * 2 * sizeof(uint32_t)) != cudaSuccess ||
+                cudaMalloc(&p->fresh_scratch, (size_t)num_blocks) != cudaSuccess) {
+                st = PKV_ERR_OOM;
+                break;
+            }
+        }
+        if (cudaMemset(p->kv, 0, p->kv_bytes) != cudaSuccess || cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
+            (fp8 && (cudaMemset(p->scales, 0, p->scale_bytes) != cudaSuccess ||
+                     cudaMemset(p->amax_scratch, 0, (size_t)num_blocks * n_kv_heads * 2 * sizeof(uint32_t)) !=
+                         cudaSuccess ||
+                     cudaMemset(p->fresh_scratch, 0, (size_t)num_blocks) != cudaSuccess)) ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            st = PKV_ERR_CUDA;
+            break;
+        }
+        if (!pkv::encode_rows_map(p)) {
+            st = PKV_ERR_CUDA;
+            break;
+        }
+        pkv::attention_configure(p);
+        if (cudaGetLastError() != cudaSuccess) {
+            st = PKV_ERR_CUDA;
+            break;
+        }
+    } while (0);
+    if (st != PKV_OK) {
+        pkv::free_pool(p);
+        return st;
+    }
+    *out = p;
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_destroy(pkv_pool* pool) {
+    if (!pool) return PKV_ERR_INVALID_ARG;
+    pkv::free_pool(pool);
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_allocator(pkv_pool* pool, pkv_allocator** out) {
+    if (!pool || !out) return PKV_ERR_INVALID_ARG;
+    *out = pool->alloc;
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_raw(const pkv_pool* pool, void** kv_dev, size_t* kv_bytes, float** scales_dev,
+                        size_t* scale_bytes) {
+    if (!pool) return PKV_ERR_INVALID_ARG;
+    if (kv_dev) *kv_dev = pool->kv;
+    if (kv_bytes) *kv_bytes = pool->kv_bytes;
+    if (scales_dev) *scales_dev = pool->scales;
+    if (scale_bytes) *scale_bytes = pool->scale_bytes;
+    return PKV_OK;
+}
+
+pkv_status pkv_check_device_error(pkv_pool* pool) {
+    if (!pool) return PKV_ERR_INVALID_ARG;
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemcpy(&v, pool->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+    if (v && cudaMemset(pool->err, 0, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (v & pkv::kErrTimeout) return PKV_ERR_TIMEOUT;
+    if (v & pkv::kErrBounds) return PKV_ERR_BOUNDS;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_workspace_init(void* workspace, size_t bytes, pkv_stream_t stream) {
+    if (!workspace && bytes) return PKV_ERR_INVALID_ARG;
+    if (!bytes) return PKV_OK;
+    return cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

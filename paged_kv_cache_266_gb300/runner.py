@@ -1,0 +1,139 @@
+"""One in-flight-batching decode step over a paged pool, driven through the C ABI.
+
+``DecodeStep`` takes a workload description (batch, heads, block size, context
+lengths, an allocation script and seeded inputs), builds the pool on the GPU,
+replays the allocation script on the pool's allocator, writes every sequence's
+history K/V with ``pkv_append`` and keeps the step's inputs resident.  ``step()``
+is the hot path: append the new token of every sequence, then decode attention
+over the grown contexts.  ``step_host()`` is the same step starting from host
+buffers (block tables and slot mapping rebuilt by the allocator, inputs copied in
+from pinned memory, the output copied back).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_allocator_set_free_order, pkv_append,
+               pkv_decode_attention, pkv_decode_workspace_bytes, pkv_get_block_tables, pkv_seq_release,
+               pkv_seq_reserve, pkv_slot_mapping)
+
+def replay(allocator: int, ops) -> None:
+    for op in ops:
+        if op[0] == "reserve":
+            pkv_seq_reserve(allocator, op[1], op[2])
+        else:
+            pkv_seq_release(allocator, op[1])
+
+
+def _bf16(torch, arr: np.ndarray, device):
+    return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class DecodeStep:
+    def __init__(self, w, device: str = "cuda"):
+        import torch
+        self.torch, self.w, self.device = torch, w, device
+        fp8 = w.kv_dtype == "fp8_e4m3"
+        self.pool = KVPool(w.num_blocks, w.block_size, w.Hkv, w.D, PKV_KV_FP8_E4M3 if fp8 else PKV_KV_BF16)
+        a = self.pool.allocator
+        pkv_allocator_set_free_order(a, w.free_order)
+        replay(a, w.alloc_ops)
+        self.max_blocks = max(1, w.max_blocks())
+        self.tables_host = pkv_get_block_tables(a, w.seq_ids, self.max_blocks)
+        self.scale = 1.0 / math.sqrt(w.D)
+        for t0, t1 in w.hist_chunks():
+            seqs, pos = w.hist_positions(t0, t1)
+            slots = torch.from_numpy(pkv_slot_mapping(a, seqs, pos)).to(device)
+            pkv_append(self.pool.handle, _bf16(torch, w.history_k(t0, t1), device),
+                       _bf16(torch, w.history_v(t0, t1), device), slots)
+        torch.cuda.synchronize()
+        self.q = _bf16(torch, w.query(), device)
+        self.k_new = _bf16(torch, w.new_k(), device)
+        self.v_new = _bf16(torch, w.new_v(), device)
+        self.slots_new_host = pkv_slot_mapping(a, w.seq_ids, w.lens) if w.append else np.zeros(0, np.int64)
+        self.slots_new = torch.from_numpy(self.slots_new_host).to(device)
+        self.tables = torch.from_numpy(self.tables_host).to(device)
+        self.lens_host = w.attend_lens.astype(np.int32)
+        self.lens = torch.from_numpy(self.lens_host).to(device)
+        self.out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=device)
+        self.ws_bytes = pkv_decode_workspace_bytes(self.pool.handle, w.B, w.Hq, self.max_blocks)
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+        self._host = None
+
+    def append(self, stream=None):
+        if self.w.append:
+            pkv_append(self.pool.handle, self.k_new, self.v_new, self.slots_new, stream)
+
+    def attention(self, stream=None):
+        pkv_decode_attention(self.pool.handle, self.q, self.tables, self.lens, self.scale, self.out, self.workspace,
+                             stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        self.attention(stream)
+        return self.out
+
+    # --- end to end from host buffers
+    def _prepare_host(self):
+        torch, w = self.torch, self.w
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        self._host = {
+            "q": pin(w.query().view(np.int16)),
+            "k": pin(w.new_k().view(np.int16)),
+            "v": pin(w.new_v().view(np.int16)),
+            "lens": pin(self.lens_host),
+            "tables": torch.empty(self.tables_host.shape, dtype=torch.int32).pin_memory(),
+            "slots": torch.empty(self.slots_new_host.shape, dtype=torch.int64).pin_memory(),
+            "out": torch.empty(w.B, w.Hq, w.D, dtype=torch.int16).pin_memory(),
+        }
+
+    def step_host(self, stream=None):
+        """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The allocator rebuilds the block
+        tables and the slot mapping, inputs go up from pinned memory, the output comes back."""
+        torch, w, a = self.torch, self.w, self.pool.allocator
+        if self._host is None:
+            self._prepare_host()
+        H = self._host
+        H["tables"].numpy()[...] = pkv_get_block_tables(a, w.seq_ids, self.max_blocks)
+        if w.append:
+            H["slots"].numpy()[...] = pkv_slot_mapping(a, w.seq_ids, w.lens)
+        self.q.view(torch.int16).copy_(H["q"], non_blocking=True)
+        self.lens.copy_(H["lens"], non_blocking=True)
+        self.tables.copy_(H["tables"], non_blocking=True)
+        h2d = H["q"].numel() * 2 + H["lens"].numel() * 4 + H["tables"].numel() * 4
+        if w.append:
+            self.k_new.view(torch.int16).copy_(H["k"], non_blocking=True)
+            self.v_new.view(torch.int16).copy_(H["v"], non_blocking=True)
+            self.slots_new.copy_(H["slots"], non_blocking=True)
+            h2d += H["k"].numel() * 2 + H["v"].numel() * 2 + H["slots"].numel() * 8
+        self.step(stream)
+        H["out"].copy_(self.out.view(torch.int16), non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return h2d, H["out"].numel() * 2
+
+    def out_host(self) -> np.ndarray:
+        return self.out.view(self.torch.int16).cpu().numpy().view(np.uint16)
+
+    def pool_bytes_host(self):
+        """Copy the device pool bytes (and fp8 scales) to host numpy arrays."""
+        from . import pkv_pool_raw
+        kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv_pool_raw(self.pool.handle)
+        kv = _wrap_device(kv_ptr, kv_bytes).cpu().numpy()
+        sc = _wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32) if sc_bytes else np.zeros(0, np.float32)
+        return kv, sc
+
+    def close(self):
+        self.pool.close()
+
+
+def _wrap_device(ptr: int, nbytes: int):
+    """A torch uint8 CUDA tensor viewing [ptr, ptr + nbytes) (borrowed memory)."""
+    import torch
+
+    class _Arr:
+        __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3,
+                                    "strides": None}
+
+    return torch.as_tensor(_Arr(), device="cuda")

@@ -32,6 +32,7 @@ _lib = None
 
 TAG_LENS, TAG_PERM, TAG_CHURN, TAG_K_HIST, TAG_V_HIST, TAG_K_NEW, TAG_V_NEW, TAG_Q = range(1, 9)
 TEMP_SEQ_BASE = 1_000_000
+HIST_CHUNK_TOKENS = 65536
 MASK64 = (1 << 64) - 1
 GAMMA = 0x9E3779B97F4A7C15
 
@@ -204,6 +205,12 @@ class Workload:
         b = np.searchsorted(off, t, side="right") - 1
         return self.seq_ids[b], (t - off[b]).astype(np.int64)
 
+    def hist_chunks(self, chunk: int = HIST_CHUNK_TOKENS):
+        """Token ranges [t0, t1) of the concatenated history, one append call each (fp8 block
+        scales are fixed by the call that writes a block's first slot, so both sides must use
+        the same call boundaries)."""
+        return [(t, min(self.n_hist, t + chunk)) for t in range(0, self.n_hist, chunk)]
+
     def max_blocks(self) -> int:
         return int(-(-int(self.attend_lens.max()) // self.block_size)) if self.B else 0
 
@@ -291,3 +298,18 @@ def _churn_ops(w: Workload, s_churn: int):
 
 
 WORKLOADS = ("c0", "c1", "c2", "c3", "c4")
+
+
+def custom_workload(index: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, lens, append: bool = True,
+                    kv_dtype: str = "bf16", spare_blocks: int = 3, shuffle: bool = True) -> Workload:
+    """A small workload for edge cases: explicit context lengths, pool sized to fit plus spares,
+    a seeded shuffled free list, every sequence reserved in batch order."""
+    lens = np.asarray(lens, dtype=np.int64)
+    seed = 266 * 1000 + index
+    total = [int(L) + (1 if append else 0) for L in lens]
+    nb = sum(_ceil_div(t, block_size) for t in total) + spare_blocks
+    order = permutation(stream_seed(seed, TAG_PERM), nb) if shuffle else np.arange(nb, dtype=np.int32)
+    w = Workload(f"custom{index}", index, "edge case", B, Hq, Hkv, D, block_size, kv_dtype, nb, lens, append, order)
+    w.seq_ids = np.arange(B, dtype=np.int64)
+    w.alloc_ops = _simple_ops(lens, append)
+    return w

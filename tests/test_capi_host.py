@@ -1,0 +1,166 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every entry point
+declared in include/pkv.h, and its block allocator matches the oracle's replica bit for bit."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import pkv_workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as m
+    m._L()
+    return m
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(pkv_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    import ctypes
+    lib = ctypes.CDLL(pkv.library_path())
+    names = _declared()
+    assert len(names) >= 20
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol(pkv):
+    missing = [n for n in _declared() if not hasattr(pkv, n)]
+    assert not missing, missing
+
+
+def test_kv_bytes_worked_values(pkv):
+    assert pkv.pkv_kv_bytes(80, 8, 128, 1, 1, 2) == 327680
+    assert pkv.pkv_kv_bytes(80, 8, 128, 1, 1, 1) == 163840
+    assert pkv.pkv_kv_bytes(1, 8, 128, 4096, 128, 2) == 2 ** 31
+    assert pkv.pkv_kv_bytes(80, 8, 128, 1, 1, 0.5) == 81920
+
+
+def test_status_strings(pkv):
+    for s in range(7):
+        assert pkv.pkv_status_str(s)
+    assert pkv.pkv_status_str(0) == "ok"
+
+
+def test_invalid_arguments_are_rejected_without_device_work(pkv):
+    L = pkv._L()
+    import ctypes
+    h = ctypes.c_void_p()
+    assert L.pkv_pool_create(16, 16, 2, 96, 0, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG  # head_dim
+    assert L.pkv_pool_create(16, 24, 2, 64, 0, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG  # block size
+    assert L.pkv_pool_create(16, 16, 2, 64, 7, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG  # dtype
+    assert L.pkv_pool_create(0, 16, 2, 64, 0, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_append(None, None, None, None, 1, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(None, None, None, 1, None, 1, 1, 1.0, None, None, 0, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_allocator_create(0, 16, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_allocator_create(4, 48, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG
+
+
+def _both(pkv, nb, bs, order=None):
+    a = pkv.pkv_allocator_create(nb, bs)
+    o = oracle.Allocator(nb, bs)
+    if order is not None:
+        pkv.pkv_allocator_set_free_order(a, order)
+        assert o.set_free_order(order) == 0
+    return a, o
+
+
+def _same_state(pkv, a, o, live):
+    assert pkv.pkv_free_list(a).tolist() == o.free_list().tolist()
+    for s in live:
+        assert pkv.pkv_seq_num_blocks(a, s) == o.num_pages(s)
+    if live:
+        ids = sorted(live)
+        mb = max(o.num_pages(s) for s in ids) + 2
+        assert np.array_equal(pkv.pkv_get_block_tables(a, ids, mb), o.block_tables(ids, mb))
+
+
+def test_allocator_matches_oracle_on_random_scripts(pkv):
+    rng = np.random.default_rng(0)
+    for trial in range(20):
+        nb, bs = int(rng.integers(1, 200)), int(2 ** rng.integers(4, 9))
+        a, o = _both(pkv, nb, bs, rng.permutation(nb).astype(np.int32) if trial % 2 else None)
+        live = set()
+        for _ in range(300):
+            if rng.random() < 0.6 or not live:
+                s = int(rng.integers(0, 40))
+                n = int(rng.integers(0, 6 * bs))
+                rc_o = o.reserve(s, n)
+                try:
+                    pkv.pkv_seq_reserve(a, s, n)
+                    rc = 0
+                except pkv.PKVError as e:
+                    rc = e.status
+                assert rc == {0: 0, 2: pkv.PKV_ERR_OOM}[rc_o]
+                if rc == 0:
+                    live.add(s)
+            else:
+                s = int(rng.choice(sorted(live)))
+                assert o.release(s) == 0
+                pkv.pkv_seq_release(a, s)
+                live.discard(s)
+            _same_state(pkv, a, o, live)
+        # slot mapping over every held position, plus padding
+        for s in live:
+            n = o.num_pages(s) * bs
+            pos = np.arange(-1, n)
+            assert np.array_equal(pkv.pkv_slot_mapping(a, [s] * len(pos), pos), o.slot_mapping([s] * len(pos), pos))
+        pkv.pkv_allocator_destroy(a)
+
+
+def test_allocator_matches_oracle_on_churned_workload(pkv):
+    w = W.make_workload("c4")
+    a, o = _both(pkv, w.num_blocks, w.block_size, w.free_order)
+    from paged_kv_cache_266_gb300.runner import replay
+    replay(a, w.alloc_ops)
+    o.replay(w.alloc_ops)
+    mb = w.max_blocks()
+    assert np.array_equal(pkv.pkv_get_block_tables(a, w.seq_ids, mb), o.block_tables(w.seq_ids, mb))
+    assert pkv.pkv_free_list(a).tolist() == o.free_list().tolist()
+    seqs, pos = w.hist_positions(0, 5000)
+    assert np.array_equal(pkv.pkv_slot_mapping(a, seqs, pos), o.slot_mapping(seqs, pos))
+    pkv.pkv_allocator_destroy(a)
+
+
+def test_allocator_errors(pkv):
+    a = pkv.pkv_allocator_create(4, 16)
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_seq_release(a, 3)
+    assert e.value.status == pkv.PKV_ERR_NO_SEQ
+    pkv.pkv_seq_reserve(a, 1, 40)  # 3 blocks
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_seq_reserve(a, 2, 40)
+    assert e.value.status == pkv.PKV_ERR_OOM
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_seq_num_blocks(a, 2)  # the failed reserve created nothing
+    assert e.value.status == pkv.PKV_ERR_NO_SEQ
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_get_block_tables(a, [1], 2)
+    assert e.value.status == pkv.PKV_ERR_BOUNDS
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_slot_mapping(a, [1], [48])
+    assert e.value.status == pkv.PKV_ERR_BOUNDS
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_allocator_set_free_order(a, [0, 1, 2, 3])  # blocks are held
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    pkv.pkv_seq_release(a, 1)
+    with pytest.raises(pkv.PKVError):
+        pkv.pkv_allocator_set_free_order(a, [0, 1, 1, 3])  # not a permutation
+    pkv.pkv_allocator_destroy(a)

@@ -1,0 +1,227 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the same seeded
+inputs.  Block tables, slot mappings and appended pool bytes (and fp8 scales) must be
+bit-exact; bf16 attention outputs within max |err| 1e-2 and mean |err| 1e-3 of the oracle,
+fp8-KV outputs within 3e-2 (computed by the oracle from the same fp8 bytes and scales)."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.drive as odrive
+import pkv_workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16_MAX, TOL_MEAN, TOL_FP8_MAX = 1e-2, 1e-3, 3e-2
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as m
+    m._L()
+    return m
+
+
+def _run(pkv, w):
+    import torch
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    step = DecodeStep(w)
+    step.step()
+    torch.cuda.synchronize()
+    return step
+
+
+def _errors(step, ref):
+    got = oracle.bf16_bits_to_f64(step.out_host())
+    err = np.abs(got - ref)
+    return got, err
+
+
+def _check_against_oracle(pkv, w, step, check_pool=True):
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_OK
+    pool, alloc, tables = odrive.build(w)
+    assert np.array_equal(step.tables_host, tables), "block tables differ from the oracle allocator"
+    if w.append:
+        assert np.array_equal(step.slots_new_host, alloc.slot_mapping(w.seq_ids, w.lens))
+    if check_pool:
+        kv, sc = step.pool_bytes_host()
+        assert np.array_equal(kv, pool.data), "appended pool bytes differ from the oracle"
+        if w.kv_dtype == "fp8_e4m3":
+            assert np.array_equal(sc, pool.scales), "fp8 block scales differ from the oracle"
+    ref = odrive.attention(w, pool, tables)
+    got, err = _errors(step, ref)
+    tol = TOL_FP8_MAX if w.kv_dtype == "fp8_e4m3" else TOL_BF16_MAX
+    assert np.isfinite(got).all()
+    assert err.max() <= tol, f"max |err| {err.max():.3e}"
+    assert err.mean() <= TOL_MEAN, f"mean |err| {err.mean():.3e}"
+    return got, ref
+
+
+@pytest.mark.parametrize("name", W.WORKLOADS)
+def test_workload_parity(pkv, name):
+    """The five workloads at full size, every output compared."""
+    w = W.make_workload(name)
+    step = _run(pkv, w)
+    _check_against_oracle(pkv, w, step)
+    step.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_shapes(pkv, dtype, D, bs):
+    """Head dims, block sizes, GQA ratios and ragged tails (lengths that end mid-tile)."""
+    rng = np.random.default_rng(bs * 7 + D)
+    for G, Hkv in ((1, 3), (3, 2), (8, 1)):
+        lens = rng.integers(1, 700, size=5)
+        lens[0] = 1
+        w = W.custom_workload(200 + bs + D + G, 5, G * Hkv, Hkv, D, bs, lens, append=True, kv_dtype=dtype)
+        step = _run(pkv, w)
+        _check_against_oracle(pkv, w, step)
+        step.close()
+
+
+def test_empty_and_single_token_contexts(pkv):
+    w = W.custom_workload(300, 6, 8, 2, 128, 64, [0, 1, 0, 17, 64, 65], append=False)
+    step = _run(pkv, w)
+    got, ref = _check_against_oracle(pkv, w, step)
+    out = step.out_host()
+    assert not out[0].any() and not out[2].any(), "empty contexts must give zeros"
+    # one cached token: the softmax weight is exactly 1, the output is that token's V row
+    v = w.history_v(1, 2)[0]  # sequence 1's only token, [Hkv][D]
+    assert np.array_equal(out[1].reshape(2, 4, 128), np.repeat(v[:, None, :], 4, axis=1))
+    step.close()
+
+
+def test_long_context_split_over_every_cta(pkv):
+    """One sequence of 40000 tokens: its 625 groups are spread over all CTAs, so the final
+    output comes from the last-arriving CTA's merge of hundreds of partial states."""
+    w = W.custom_workload(301, 1, 8, 1, 128, 64, [40000], append=True)
+    step = _run(pkv, w)
+    _check_against_oracle(pkv, w, step)
+    step.close()
+
+
+def test_results_are_deterministic_and_workspace_is_reusable(pkv):
+    import torch
+    w = W.make_workload("c2")
+    step = _run(pkv, w)
+    first = step.out_host().copy()
+    for _ in range(3):
+        step.attention()
+    torch.cuda.synchronize()
+    assert np.array_equal(step.out_host(), first)
+    assert not step.workspace[: w.B * w.Hkv * 4].any(), "merge tickets must return to zero"
+    step.close()
+
+
+def test_out_of_range_block_id_is_flagged_not_faulted(pkv):
+    import torch
+    w = W.custom_workload(302, 3, 4, 2, 128, 16, [40, 40, 40], append=False)
+    step = _run(pkv, w)
+    good = step.out_host().copy()
+    bad = step.tables_host.copy()
+    bad[1, 1] = w.num_blocks + 7
+    step.tables.copy_(torch.from_numpy(bad))
+    step.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_BOUNDS
+    out = step.out_host()
+    assert np.array_equal(out[0], good[0]) and np.array_equal(out[2], good[2])
+    step.close()
+
+
+def test_context_longer_than_table_is_clamped_and_flagged(pkv):
+    import torch
+    w = W.custom_workload(303, 2, 4, 1, 64, 16, [30, 20], append=False)
+    step = _run(pkv, w)
+    good = step.out_host().copy()
+    step.lens.copy_(torch.tensor([30, 10_000], dtype=torch.int32))
+    step.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_BOUNDS
+    assert np.array_equal(step.out_host()[0], good[0])
+    step.close()
+
+
+def test_append_slot_out_of_range_is_skipped_and_flagged(pkv):
+    import torch
+    w = W.custom_workload(304, 2, 2, 2, 64, 16, [3, 3], append=True)
+    step = _run(pkv, w)
+    kv_before, _ = step.pool_bytes_host()
+    step.slots_new.copy_(torch.tensor([w.num_blocks * 16 + 1, -1], dtype=torch.int64))
+    step.append()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_BOUNDS
+    kv_after, _ = step.pool_bytes_host()
+    assert np.array_equal(kv_before, kv_after)
+    step.close()
+
+
+def test_fp8_decode_every_code(pkv):
+    """Raw E4M3 codes written into V with unit scales: with one cached token the output is the
+    decoded V row, which bf16 holds exactly — compared against the oracle's decode table."""
+    import torch
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    w = W.custom_workload(305, 2, 1, 1, 128, 16, [1, 1], append=False, kv_dtype="fp8_e4m3")
+    step = _run(pkv, w)
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    codes = np.concatenate([codes, codes[:2]])  # 256 bytes = two V rows of 128
+    pool = oracle.Pool(w.num_blocks, 16, 1, 128, True)
+    kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(step.pool.handle)
+    dev = _wrap_device(kv_ptr, kv_bytes)
+    scd = _wrap_device(sc_ptr, sc_bytes)
+    for b in range(2):
+        blk = int(step.tables_host[b, 0])
+        for d in range(128):
+            dev[pool.elem_byte(blk, 1, 0, 0, d)] = int(codes[b * 128 + d])
+        sc = torch.tensor([1.0, 1.0, 0.0, 0.0], dtype=torch.float32).view(torch.uint8)
+        scd[blk * 16: blk * 16 + 16].copy_(sc)
+    step.attention()
+    torch.cuda.synchronize()
+    got = oracle.bf16_bits_to_f64(step.out_host()).reshape(256)
+    want = np.array([oracle.e4m3_decode(int(c)) for c in codes])
+    assert np.array_equal(got, want)
+    step.close()
+
+
+def test_fp8_encode_matches_oracle_on_ties_and_subnormals(pkv):
+    """Rows whose amax is 448 get scale 1, so stored codes are e4m3(x) directly: a sweep over
+    grid midpoints (ties), subnormals, saturation and random values must match bit for bit."""
+    import torch
+    from paged_kv_cache_266_gb300 import pkv_append
+    vals = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(3)
+    pool_vals = np.concatenate([mids, -mids, vals, rng.standard_normal(500) * 30, [447.9, -447.9, 1e-9, -0.0]])
+    bf = torch.tensor(pool_vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    D = 128
+    n_tok = -(-len(bf) // (D - 1))
+    rows = np.zeros((n_tok, 1, D), dtype=np.uint16)
+    flat = np.zeros(n_tok * (D - 1), dtype=np.uint16)
+    flat[: len(bf)] = bf
+    rows[:, 0, 1:] = flat.reshape(n_tok, D - 1)
+    rows[:, 0, 0] = torch.tensor([448.0]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[0]
+    nb = n_tok
+    handle = pkv.pkv_pool_create(nb, 16, 1, D, pkv.PKV_KV_FP8_E4M3)
+    slots = np.arange(nb, dtype=np.int64) * 16  # each token opens its own block
+    dk = torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16).cuda()
+    pkv_append(handle, dk, dk, torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(handle) == pkv.PKV_OK
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(handle)
+    kv = _wrap_device(kv_ptr, kv_bytes).cpu().numpy()
+    sc = _wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32)
+    ref = oracle.Pool(nb, 16, 1, D, True)
+    assert ref.append(rows, rows, slots) == 0
+    assert np.array_equal(sc, ref.scales)
+    assert np.array_equal(kv, ref.data)
+    pkv.pkv_pool_destroy(handle)
