@@ -172,27 +172,24 @@ def dist_barrier(world: int):
 
 # ----------------------------------------------------------------------------- CPU oracle runs
 def oracle_rate(w, budget_s: float, threads: int):
-    """Time the oracle's decode attention on a bounded sample of the workload's sequences.
-    Returns (GB/s of KV read, seconds, description)."""
+    """Time the oracle's decode attention over the workload's sequences, cycling through them
+    until about `budget_s` seconds of CPU work are done.  Returns (GB/s of KV read, seconds,
+    description of the sample)."""
     import oracle.drive as odrive
     pool, _, tables = odrive.build(w)
-    order = np.argsort(w.attend_lens)  # start from the shortest to size the sample
-    picked, spent, kv = [], 0.0, 0
     lens = w.attend_lens.astype(np.int64)
-    # Estimate the per-token cost on one sequence, then take enough sequences for the budget.
+    done_tokens, passes, spent = 0, 0, 0.0
     t0 = time.perf_counter()
-    odrive.attention(w, pool, tables, threads=threads, seqs=[int(order[len(order) // 2])])
-    est = (time.perf_counter() - t0) / max(1, lens[order[len(order) // 2]])
-    want_tokens = max(1, int(budget_s / max(est, 1e-9)))
-    for b in order[len(order) // 2:].tolist() + order[: len(order) // 2].tolist():
-        if sum(lens[picked]) >= want_tokens and picked:
-            break
-        picked.append(int(b))
-    t0 = time.perf_counter()
-    odrive.attention(w, pool, tables, threads=threads, seqs=picked)
-    spent = time.perf_counter() - t0
-    kv = int(lens[picked].sum()) * w.Hkv * 2 * w.D * w.elem_bytes
-    return kv / spent / 1e9, spent, f"{len(picked)} of {w.B} sequences ({int(lens[picked].sum())} tokens), all heads"
+    while spent < budget_s:
+        for b in range(w.B):
+            odrive.attention(w, pool, tables, threads=threads, seqs=[b])
+            done_tokens += int(lens[b])
+            spent = time.perf_counter() - t0
+            if spent >= budget_s:
+                break
+        passes += 1
+    kv = done_tokens * w.Hkv * 2 * w.D * w.elem_bytes
+    return kv / spent / 1e9, spent, f"{done_tokens} context tokens of {w.name} (all heads), sequences in batch order"
 
 
 def run_reference(args, world, rank):
@@ -245,6 +242,9 @@ def run_pkv(args, world, rank, local):
     torch.cuda.set_device(local)
     w = W.make_workload(args.workload)
     step = DecodeStep(w, device=f"cuda:{local}")
+    if args.seqs:
+        step.limit_batch(args.seqs)
+        w = W.truncated(w, args.seqs)
     nbytes = algorithmic_bytes(w)
     stream = torch.cuda.current_stream()
     launches_per_step = (0 if not w.append else (1 if w.kv_dtype == "bf16" else 3)) + 1
@@ -347,6 +347,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0, help="profiling: step over the first N sequences only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

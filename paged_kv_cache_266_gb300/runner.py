@@ -62,6 +62,18 @@ class DecodeStep:
         self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
         self._host = None
 
+    def limit_batch(self, n: int) -> None:
+        """Run the step on the first n sequences only (same pool); used to size profiling runs."""
+        torch, w = self.torch, self.w
+        n = max(1, min(n, w.B))
+        self.q, self.k_new, self.v_new = self.q[:n], self.k_new[:n], self.v_new[:n]
+        self.slots_new = self.slots_new[:n] if w.append else self.slots_new
+        self.slots_new_host = self.slots_new_host[:n] if w.append else self.slots_new_host
+        self.tables, self.tables_host = self.tables[:n], self.tables_host[:n]
+        self.lens, self.lens_host = self.lens[:n], self.lens_host[:n]
+        self.out = self.out[:n]
+        self.batch = n
+
     def append(self, stream=None):
         if self.w.append:
             pkv_append(self.pool.handle, self.k_new, self.v_new, self.slots_new, stream)
@@ -79,14 +91,15 @@ class DecodeStep:
     def _prepare_host(self):
         torch, w = self.torch, self.w
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        n = self.batch
         self._host = {
-            "q": pin(w.query().view(np.int16)),
-            "k": pin(w.new_k().view(np.int16)),
-            "v": pin(w.new_v().view(np.int16)),
+            "q": pin(w.query()[:n].view(np.int16)),
+            "k": pin(w.new_k()[:n].view(np.int16)),
+            "v": pin(w.new_v()[:n].view(np.int16)),
             "lens": pin(self.lens_host),
             "tables": torch.empty(self.tables_host.shape, dtype=torch.int32).pin_memory(),
             "slots": torch.empty(self.slots_new_host.shape, dtype=torch.int64).pin_memory(),
-            "out": torch.empty(w.B, w.Hq, w.D, dtype=torch.int16).pin_memory(),
+            "out": torch.empty(n, w.Hq, w.D, dtype=torch.int16).pin_memory(),
         }
 
     def step_host(self, stream=None):
@@ -96,9 +109,10 @@ class DecodeStep:
         if self._host is None:
             self._prepare_host()
         H = self._host
-        H["tables"].numpy()[...] = pkv_get_block_tables(a, w.seq_ids, self.max_blocks)
+        n = self.batch
+        H["tables"].numpy()[...] = pkv_get_block_tables(a, w.seq_ids[:n], self.max_blocks)
         if w.append:
-            H["slots"].numpy()[...] = pkv_slot_mapping(a, w.seq_ids, w.lens)
+            H["slots"].numpy()[...] = pkv_slot_mapping(a, w.seq_ids[:n], w.lens[:n])
         self.q.view(torch.int16).copy_(H["q"], non_blocking=True)
         self.lens.copy_(H["lens"], non_blocking=True)
         self.tables.copy_(H["tables"], non_blocking=True)

@@ -313,3 +313,14 @@ def custom_workload(index: int, B: int, Hq: int, Hkv: int, D: int, block_size: i
     w.seq_ids = np.arange(B, dtype=np.int64)
     w.alloc_ops = _simple_ops(lens, append)
     return w
+
+
+def truncated(w: Workload, n: int) -> Workload:
+    """The same workload seen through its first n sequences (for sizing measurements)."""
+    import copy
+    t = copy.copy(w)
+    t.B = n
+    t.lens = w.lens[:n]
+    t.seq_ids = w.seq_ids[:n]
+    t.name = f"{w.name}[:{n}]"
+    return t

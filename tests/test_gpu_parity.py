@@ -95,7 +95,8 @@ def test_empty_and_single_token_contexts(pkv):
     out = step.out_host()
     assert not out[0].any() and not out[2].any(), "empty contexts must give zeros"
     # one cached token: the softmax weight is exactly 1, the output is that token's V row
-    v = w.history_v(1, 2)[0]  # sequence 1's only token, [Hkv][D]
+    t = int(w.hist_offsets[1])  # sequence 1's only token in the concatenated history
+    v = w.history_v(t, t + 1)[0]  # [Hkv][D]
     assert np.array_equal(out[1].reshape(2, 4, 128), np.repeat(v[:, None, :], 4, axis=1))
     step.close()
 
