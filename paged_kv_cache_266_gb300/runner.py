@@ -61,6 +61,7 @@ class DecodeStep:
         self.ws_bytes = pkv_decode_workspace_bytes(self.pool.handle, w.B, w.Hq, self.max_blocks)
         self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
         self._host = None
+        self.batch = w.B
 
     def limit_batch(self, n: int) -> None:
         """Run the step on the first n sequences only (same pool); used to size profiling runs."""
