@@ -122,10 +122,10 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
         if (e >= R1) return;
         const int b = find_seq(cumg, p.B, p.Hkv, e);
         const int ng = cumg[b + 1] - cumg[b];
-        const int64_t r = e - (int64_t)p.Hkv * cumg[b];
+        const int r = (int)(e - (int64_t)p.Hkv * cumg[b]);  // < Hkv * ng
         d.b = b;
-        d.h = (int)(r / ng);
-        d.g = (int)(r - (int64_t)d.h * ng);
+        d.h = r / ng;
+        d.g = r - d.h * ng;
         const int npages = (lens_s[b] + p.bs - 1) / p.bs;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -140,6 +140,8 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
     uint32_t round = 0;
     int64_t issued = 0;
     bool ok = true;
+    const uint32_t part_bytes = (uint32_t)p.box_rows * kRowBytes;
+    const int64_t tile_elems = (int64_t)p.bs * D;  // one (block, K|V, head) tile
     for (int64_t e0 = R0; e0 < R1 && ok; e0 += 32) {
         describe(e0 + 32 + lane, nxt);  // table loads for the next 32 groups are in flight meanwhile
         const int n = (int)(R1 - e0 < 32 ? R1 - e0 : 32);
@@ -147,58 +149,60 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
             const int b = __shfl_sync(0xffffffffu, cur.b, j);
             const int h = __shfl_sync(0xffffffffu, cur.h, j);
             const int g = __shfl_sync(0xffffffffu, cur.g, j);
-            int32_t ids[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ids[i] = __shfl_sync(0xffffffffu, cur.id[i], j);
+            const int id0 = __shfl_sync(0xffffffffu, cur.id[0], j);
+            const int id1 = __shfl_sync(0xffffffffu, cur.id[1], j);
+            const int id2 = __shfl_sync(0xffffffffu, cur.id[2], j);
+            const int id3 = __shfl_sync(0xffffffffu, cur.id[3], j);
+            const int64_t e = e0 + j;
+            const bool first = (e == R0) || (g == 0);
+            int nparts = 1;
+            if (p.ppg > 1) nparts = min(p.ppg, (lens_s[b] + p.bs - 1) / p.bs - g * p.ppg);
+            const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+            const uint32_t fb = bar_full + 8 * s;
             if (lane == 0) {
                 ok = ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, kWaitLimitNs);
-                if (!ok) {
+                if (!ok)
                     flag_abort(p, misc);
-                } else {
-                    const int64_t e = e0 + j;
-                    const bool first = (e == R0) || (g == 0);
-                    const int L = lens_s[b];
-                    int nparts = 1;
-                    if (p.ppg > 1) nparts = min(p.ppg, (L + p.bs - 1) / p.bs - g * p.ppg);
-                    const uint32_t part_bytes = (uint32_t)p.box_rows * kRowBytes;
-                    const uint32_t bytes = (uint32_t)nparts * part_bytes * 2 + (FP8 ? 16u * nparts : 0u) +
-                                           (first ? (uint32_t)(p.G * D * 2) : 0u);
-                    const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
-                    const uint32_t fb = bar_full + 8 * s;
-                    ptx::mbar_arrive_expect_tx(fb, bytes);
-                    const int row_off = p.ppg > 1 ? 0 : (g * kGroup) % p.bs;
-                    for (int i = 0; i < nparts; ++i) {
-                        int blk = ids[i];
-                        if (blk < 0 || blk >= p.num_blocks) {  // keep the byte count exact, read block 0
-                            atomicOr(p.err, kErrBounds);
-                            blk = 0;
-                        }
-                        const int64_t rowK = ((int64_t)(2 * blk) * p.Hkv + h) * p.bs + row_off;
-                        const int64_t rowV = ((int64_t)(2 * blk + 1) * p.Hkv + h) * p.bs + row_off;
-                        const uint32_t dst_rows = (uint32_t)(i * p.box_rows) * kPanelBytes;
-#pragma unroll
-                        for (int q = 0; q < kPanels; ++q)
-                            ptx::tma_load_2d(st + q * (kGroup * kPanelBytes) + dst_rows, tmap, q * (kPanelBytes / kEsz),
-                                             (int32_t)rowK, fb);
-                        if (FP8) {
-                            // V panels ([D][16] per 16 tokens) are contiguous: one bulk copy per part
-                            const uint8_t* src = p.pool + rowV / p.bs * (int64_t)p.bs * D + (int64_t)row_off * D;
-                            ptx::bulk_load(st + p.off_v + (uint32_t)(i * p.box_rows * D), src, part_bytes, fb);
-                            ptx::bulk_load(st + p.off_s + 16 * i, p.scales + ((int64_t)blk * p.Hkv + h) * 4, 16, fb);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < kPanels; ++q)
-                                ptx::tma_load_2d(st + p.off_v + q * (kGroup * kPanelBytes) + dst_rows, tmap,
-                                                 q * (kPanelBytes / kEsz), (int32_t)rowV, fb);
-                        }
-                    }
-                    if (first)
-                        ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D,
-                                       (uint32_t)(p.G * D * 2), fb);
-                }
+                else
+                    ptx::mbar_arrive_expect_tx(fb, (uint32_t)nparts * part_bytes * 2 + (FP8 ? 16u * nparts : 0u) +
+                                                       (first ? (uint32_t)(p.G * D * 2) : 0u));
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = __shfl_sync(0xffffffffu, ok, 0);  // also orders the expect_tx before every lane's copies
             if (!ok) break;
+            // Lanes 0..nparts-1 issue one page part each (K and V), lane 4 the query rows and
+            // lanes 8..8+nparts-1 the fp8 scale records, so a stage's copies go out in parallel.
+            const int part = lane & 7;
+            int blk = part == 0 ? id0 : part == 1 ? id1 : part == 2 ? id2 : id3;
+            if (part < nparts && (blk < 0 || blk >= p.num_blocks)) {  // keep the byte count exact, read block 0
+                if (lane < 8) atomicOr(p.err, kErrBounds);
+                blk = 0;
+            }
+            const int row_off = p.ppg > 1 ? 0 : (g * kGroup) & (p.bs - 1);
+            const int64_t tileK = (int64_t)(2 * blk) * p.Hkv + h;  // tile index of K; V is Hkv tiles further
+            if (lane < nparts) {
+                const uint32_t dst_rows = (uint32_t)(lane * p.box_rows) * kPanelBytes;
+                const int32_t rowK = (int32_t)(tileK * p.bs + row_off);
+                const int32_t rowV = (int32_t)((tileK + p.Hkv) * p.bs + row_off);
+#pragma unroll
+                for (int q = 0; q < kPanels; ++q)
+                    ptx::tma_load_2d(st + q * (kGroup * kPanelBytes) + dst_rows, tmap, q * (kPanelBytes / kEsz), rowK,
+                                     fb);
+                if (FP8) {
+                    // V panels ([D][16] per 16 tokens) are contiguous: one bulk copy per part
+                    const uint8_t* src = p.pool + (tileK + p.Hkv) * tile_elems + (int64_t)row_off * D;
+                    ptx::bulk_load(st + p.off_v + (uint32_t)(lane * p.box_rows * D), src, part_bytes, fb);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kPanels; ++q)
+                        ptx::tma_load_2d(st + p.off_v + q * (kGroup * kPanelBytes) + dst_rows, tmap,
+                                         q * (kPanelBytes / kEsz), rowV, fb);
+                }
+            } else if (lane == 4 && first) {
+                ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D, (uint32_t)(p.G * D * 2),
+                               fb);
+            } else if (FP8 && lane >= 8 && lane < 8 + nparts) {
+                ptx::bulk_load(st + p.off_s + 16 * part, p.scales + ((int64_t)blk * p.Hkv + h) * 4, 16, fb);
+            }
             ++issued;
             if (++s == p.stages) {
                 s = 0;
@@ -499,13 +503,14 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
     float sv_prev = 1.f;
     int b = find_seq(cumg, p.B, p.Hkv, R0);
     int ng = cumg[b + 1] - cumg[b];
-    const int64_t r = R0 - (int64_t)p.Hkv * cumg[b];
-    int h = (int)(r / ng);
-    int g = (int)(r - (int64_t)h * ng);
+    const int r = (int)(R0 - (int64_t)p.Hkv * cumg[b]);
+    int h = r / ng;
+    int g = r - h * ng;
     int g_first = g;
     int s = 0;
     uint32_t round = 0;
     bool alive = true;
+    const int pidx = (16 * warp) / p.box_rows;  // page part holding this warp's tokens
     for (int64_t e = R0; e < R1; ++e) {
         const bool first = (e == R0) || (g == 0);
         const bool last = (e == R1 - 1) || (g == ng - 1);
@@ -526,7 +531,6 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
         const int nvalid = min(16, lens_s[b] - g * kGroup - 16 * warp);
         if (alive && nvalid > 0) {
             if (FP8) {
-                const int pidx = (16 * warp) / p.box_rows;
                 const float* sc = reinterpret_cast<const float*>(smem + (st_addr - sbase) + p.off_s + 16 * pidx);
                 tile_fp8<D>(st_addr, st_addr + p.off_v + (uint32_t)(warp * D * 16), 16 * warp, nvalid, qf, o, st,
                             p.scale_log2, sc[0], sc[1], sv_prev, lane);
