@@ -176,6 +176,29 @@ pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads
 /* cudaMemsetAsync(workspace, 0, bytes, stream): prepares a fresh workspace. */
 pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------ decode attention without allocation
+ * The pages have no counterpart to this call; it exists for callers that cannot allocate
+ * device memory for a workspace: a plugin inside an engine that has already reserved nearly
+ * all free device memory for its own KV pool (the serving stacks the pages describe hand
+ * 85-92% of free memory to the KV cache), or a latency-critical decode loop that must not
+ * call cudaMalloc because it can synchronise the device.
+ *
+ * Same computation, arguments and errors as pkv_decode_attention, minus the workspace: the
+ * scratch is a fixed PKV_STATIC_WORKSPACE_BYTES array compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine); it clears the merge tickets with
+ * cudaMemsetAsync on `stream` and launches the same kernel.
+ *   - Returns PKV_ERR_INVALID_ARG without launching when pkv_decode_workspace_bytes() for
+ *     these B, n_q_heads, max_blocks exceeds PKV_STATIC_WORKSPACE_BYTES.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with the pool's device current; make that first call before any stream capture.
+ *   - All calls share the one array, so calls that overlap on the GPU (other streams, other
+ *     threads) race and corrupt each other's results: serialise them. */
+#define PKV_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
+pkv_status pkv_decode_attention_static(const pkv_pool* pool, const void* q_dev, const int32_t* block_tables_dev,
+                                       int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads,
+                                       float scale, void* out_dev, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------ utilities
  * KV memory ("TensorRT-LLM 推理加速实战" §8.1; aiqz.cc page, KV缓存管理):
  *   M_kv = 2 * n_layers * n_kv_heads * head_dim * n_tokens * batch * bytes_per_elem. */

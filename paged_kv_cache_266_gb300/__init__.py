@@ -21,11 +21,13 @@ __all__ = [
     "pkv_seq_release", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_workspace_bytes",
-    "pkv_decode_workspace_init", "pkv_kv_bytes", "pkv_status_str", "KVPool",
+    "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
+    "pkv_status_str", "KVPool",
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OOM, PKV_ERR_NO_SEQ, PKV_ERR_BOUNDS, PKV_ERR_CUDA, PKV_ERR_TIMEOUT = range(7)
 PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
+PKV_STATIC_WORKSPACE_BYTES = 8 << 20  # include/pkv.h
 
 _lib = None
 
@@ -70,6 +72,7 @@ def _L():
         "pkv_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, sz, vp]),
         "pkv_decode_workspace_bytes": (i32, [vp, i32, i32, i32, P(sz)]),
         "pkv_decode_workspace_init": (i32, [vp, sz, vp]),
+        "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
         "pkv_kv_bytes": (ctypes.c_uint64, [i64, i64, i64, i64, i64, ctypes.c_double]),
         "pkv_status_str": (ctypes.c_char_p, [i32]),
     }
@@ -226,6 +229,21 @@ def pkv_decode_workspace_bytes(pool: int, B: int, n_q_heads: int, max_blocks: in
 def pkv_decode_workspace_init(workspace, stream=None) -> None:
     _check(_L().pkv_decode_workspace_init(_dev(workspace, "u8", "workspace"), workspace.numel(), _stream(stream)),
            "pkv_decode_workspace_init")
+
+
+def pkv_decode_attention_static(pool: int, q, block_tables, context_lens, scale: float, out, stream=None) -> None:
+    """pkv_decode_attention with the library's fixed device scratch instead of a caller workspace
+    (for callers that cannot allocate device memory); no allocation happens in this call."""
+    B, Hq = q.shape[0], q.shape[1]
+    rc = _L().pkv_decode_attention_static(pool, _dev(q, "bf16", "q"), _dev(block_tables, "i32", "block_tables"),
+                                          block_tables.shape[1], _dev(context_lens, "i32", "context_lens"), B, Hq,
+                                          float(scale), _dev(out, "bf16", "out"), _stream(stream))
+    if rc == PKV_ERR_INVALID_ARG:
+        need = pkv_decode_workspace_bytes(pool, B, Hq, block_tables.shape[1])
+        if need > PKV_STATIC_WORKSPACE_BYTES:
+            raise PKVError(rc, f"pkv_decode_attention_static: needs {need} bytes of scratch, the fixed limit is "
+                               f"{PKV_STATIC_WORKSPACE_BYTES}")
+    _check(rc, "pkv_decode_attention_static")
 
 
 def pkv_kv_bytes(n_layers: int, n_kv_heads: int, head_dim: int, n_tokens: int, batch: int,

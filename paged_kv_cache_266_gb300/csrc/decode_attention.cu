@@ -33,6 +33,7 @@
 // error word and finishes without touching memory outside its buffers.
 #include <algorithm>
 #include <cstdlib>
+#include <mutex>
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
@@ -783,3 +784,57 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free variant
+// For callers that cannot allocate a workspace (see pkv_decode_attention_static in pkv.h): the
+// scratch is this fixed array in the library's device image.  Host code must not use the
+// symbol itself as a pointer (on the host it is only a stand-in); the device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+
+namespace pkv {
+namespace attn {
+
+static __device__ __align__(256) unsigned char g_static_workspace[PKV_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_ws_mutex;
+void* g_static_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_static_workspace on `device`, which must be the current device.
+pkv_status static_workspace(int device, void** out) {
+    if (device < 0 || device >= kMaxDevices) return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+    if (!g_static_ws_ptr[device]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return PKV_ERR_CUDA;
+        g_static_ws_ptr[device] = ptr;
+    }
+    *out = g_static_ws_ptr[device];
+    return PKV_OK;
+}
+
+}  // namespace attn
+}  // namespace pkv
+
+extern "C" pkv_status pkv_decode_attention_static(const pkv_pool* pool, const void* q, const int32_t* block_tables,
+                                                  int max_blocks, const int32_t* context_lens, int B, int n_q_heads,
+                                                  float scale, void* out, pkv_stream_t stream) {
+    if (!pool) return PKV_ERR_INVALID_ARG;
+    size_t need = 0;
+    const pkv_status st = pkv_decode_workspace_bytes(pool, B, n_q_heads, max_blocks, &need);
+    if (st != PKV_OK) return st;
+    if (need > PKV_STATIC_WORKSPACE_BYTES) return PKV_ERR_INVALID_ARG;  // beyond the fixed scratch
+    if (B == 0) return PKV_OK;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cur != pool->device) return PKV_ERR_INVALID_ARG;
+    void* ws = nullptr;
+    const pkv_status ws_st = pkv::attn::static_workspace(cur, &ws);
+    if (ws_st != PKV_OK) return ws_st;
+    // the merge tickets at the front of the workspace must start at zero
+    if (cudaMemsetAsync(ws, 0, (size_t)B * pool->n_kv_heads * sizeof(int), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
+    return pkv_decode_attention(pool, q, block_tables, max_blocks, context_lens, B, n_q_heads, scale, out, ws,
+                                PKV_STATIC_WORKSPACE_BYTES, stream);
+}
