@@ -58,7 +58,8 @@ struct Params {
     const uint8_t* pool;
     const float* scales;
     int* counters;
-    float* partials;
+    float* partials;  // O of the partial states [slots][G][D]
+    float* part_ml;   // their (max, sum) [slots][G][2]
     int* err;
     int B, Hq, Hkv, G, max_blocks, bs, num_blocks;
     int box_rows;  // rows per TMA box: min(bs, kGroup)
@@ -384,16 +385,18 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const uint8_t*
     }
 }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
-    return static_cast<uint16_t>(ptx::pack_bf16x2(x, 0.f) & 0xffffu);
-}
-
 // Merge the four warps' states of pair (b, h) and write the output (pair complete in this CTA)
 // or a partial state plus a ticket (pair cut between CTAs; the last one merges all parts).
+//
+// Shared-memory combine area: O [4 warps][G][D+4], m and l [4][G], merge weights [4][G], and the
+// pair's max and sum [G] each.  Partial states in the workspace: O [slot][G][D] and (m, l)
+// [slot][G][2]; slot = pair + CTA index.
 template <int D>
 __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const SoftmaxState& st, float osc, int b,
                             int h, bool complete, int64_t Ng, int64_t C, const int32_t* cumg, uint8_t* smem,
                             volatile int* misc) {
+    constexpr int kCT = kConsumerWarps * 32;
+    constexpr int kStride = D + 4;  // keeps rows 16-byte aligned and spreads the fragment stores over banks
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, c4 = lane & 3;
     const int G = p.G;
     float l0 = st.l[0], l1 = st.l[1];
@@ -402,10 +405,12 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    constexpr int kStride = D + 4;
     float* cO = reinterpret_cast<float*>(smem + p.off_cmb);
     float* cM = cO + kConsumerWarps * G * kStride;
     float* cL = cM + kConsumerWarps * G;
+    float* cW = cL + kConsumerWarps * G;
+    float* cMp = cW + kConsumerWarps * G;  // pair max per head
+    float* cLp = cMp + G;                   // pair sum per head
     const int j0 = 2 * c4, j1 = 2 * c4 + 1;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
@@ -429,67 +434,129 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
             cL[warp * G + j1] = l1;
         }
     }
-    ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
-    const int pair = b * p.Hkv + h;
-    uint16_t* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
-    float* part = p.partials + ((int64_t)pair + blockIdx.x) * G * (D + 2);
-    for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
-        const int j = e / D, d = e % D;
+    ptx::named_barrier_sync(kCombineBar, kCT);
+    if (tid < G) {  // per head: the pair's max, the four warps' weights and the pair's sum
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cM[w * G + j]);
-        float acc = 0.f, l = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cM[w * G + tid]);
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = ptx::exp2_approx(cM[w * G + j] - M);
-            acc += f * cO[(w * G + j) * kStride + d];
-            l += f * cL[w * G + j];
+            const float f = ptx::exp2_approx(cM[w * G + tid] - M);
+            cW[w * G + tid] = f;
+            L += f * cL[w * G + tid];
+        }
+        cMp[tid] = M;
+        cLp[tid] = L;
+    }
+    ptx::named_barrier_sync(kCombineBar, kCT);
+    const int pair = b * p.Hkv + h;
+    uint16_t* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
+    const int64_t slot = (int64_t)pair + blockIdx.x;
+    float* part_o = p.partials + slot * G * D;
+    for (int e = tid; e < G * (D / 4); e += kCT) {
+        const int j = e / (D / 4), d = (e % (D / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = cW[w * G + j];
+            const float4 v = *reinterpret_cast<const float4*>(cO + (w * G + j) * kStride + d);
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
         }
         if (complete) {
-            out[j * D + d] = f32_to_bf16_bits(acc / l);
+            const float inv = 1.f / cLp[j];
+            *reinterpret_cast<uint2*>(out + j * D + d) =
+                make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv), ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
         } else {
-            part[j * (D + 2) + d] = acc;
-            if (d == 0) {
-                part[j * (D + 2) + D] = M;
-                part[j * (D + 2) + D + 1] = l;
-            }
+            *reinterpret_cast<float4*>(part_o + j * D + d) = acc;
         }
     }
     if (!complete) {
-        __threadfence();
-        ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+        if (tid < G) *reinterpret_cast<float2*>(p.part_ml + (slot * G + tid) * 2) = make_float2(cMp[tid], cLp[tid]);
+        // One thread publishes the CTA's partial state (fence after the barrier covers every
+        // thread's stores) and takes the pair's ticket; the last of its parts merges them.
+        ptx::named_barrier_sync(kCombineBar, kCT);
         if (tid == 0) {
             const int ng = cumg[b + 1] - cumg[b];
             const int64_t e_first = (int64_t)p.Hkv * cumg[b] + (int64_t)h * ng;
             const int64_t e_last = e_first + ng - 1;
             const int c1 = (int)(((e_first + 1) * C - 1) / Ng);
             const int c2 = (int)(((e_last + 1) * C - 1) / Ng);
+            __threadfence();
             const int ticket = atomicAdd(p.counters + pair, 1);
-            misc[kMiscMergeParts] = ticket == c2 - c1 ? c2 - c1 + 1 : 0;
+            const bool last_part = ticket == c2 - c1;
+            if (last_part) __threadfence();
+            misc[kMiscMergeParts] = last_part ? c2 - c1 + 1 : 0;
             misc[kMiscMergeFirst] = c1;
         }
-        ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+        ptx::named_barrier_sync(kCombineBar, kCT);
         const int nparts = misc[kMiscMergeParts];
         if (nparts) {
-            __threadfence();
-            const float* base = p.partials + ((int64_t)pair + misc[kMiscMergeFirst]) * G * (D + 2);
-            for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
-                const int j = e / D, d = e % D;
-                float M = -INFINITY;
-                for (int s = 0; s < nparts; ++s) M = fmaxf(M, __ldcg(base + ((int64_t)s * G + j) * (D + 2) + D));
-                float acc = 0.f, l = 0.f;
-                for (int s = 0; s < nparts; ++s) {
-                    const float* ps = base + ((int64_t)s * G + j) * (D + 2);
-                    const float f = ptx::exp2_approx(__ldcg(ps + D) - M);
-                    acc += f * __ldcg(ps + d);
-                    l += f * __ldcg(ps + D + 1);
+            const int64_t s0 = (int64_t)pair + misc[kMiscMergeFirst];
+            // per head: max and sum over the parts, 16 threads per head
+            {
+                const int j = tid >> 4, sl = tid & 15;
+                float M = -INFINITY, L = 0.f;
+                if (j < G) {
+                    for (int s = sl; s < nparts; s += 16) M = fmaxf(M, __ldcg(p.part_ml + ((s0 + s) * G + j) * 2));
                 }
-                out[j * D + d] = f32_to_bf16_bits(acc / l);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                if (j < G) {
+                    for (int s = sl; s < nparts; s += 16) {
+                        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((s0 + s) * G + j) * 2));
+                        L += ptx::exp2_approx(ml.x - M) * ml.y;
+                    }
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+                if (j < G && sl == 0) {
+                    cMp[j] = M;
+                    cLp[j] = L;
+                }
+            }
+            ptx::named_barrier_sync(kCombineBar, kCT);
+            for (int e = tid; e < G * (D / 4); e += kCT) {
+                const int j = e / (D / 4), d = (e % (D / 4)) * 4;
+                const float M = cMp[j];
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                int s = 0;
+                for (; s + 4 <= nparts; s += 4) {  // four independent loads in flight
+                    float f[4];
+                    float4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        f[u] = __ldcg(p.part_ml + ((s0 + s + u) * G + j) * 2);
+                        v[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + ((s0 + s + u) * G + j) * D + d));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float w = ptx::exp2_approx(f[u] - M);
+                        acc.x += w * v[u].x;
+                        acc.y += w * v[u].y;
+                        acc.z += w * v[u].z;
+                        acc.w += w * v[u].w;
+                    }
+                }
+                for (; s < nparts; ++s) {
+                    const float w = ptx::exp2_approx(__ldcg(p.part_ml + ((s0 + s) * G + j) * 2) - M);
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.partials + ((s0 + s) * G + j) * D + d));
+                    acc.x += w * v.x;
+                    acc.y += w * v.y;
+                    acc.z += w * v.z;
+                    acc.w += w * v.w;
+                }
+                const float inv = 1.f / cLp[j];
+                *reinterpret_cast<uint2*>(out + j * D + d) =
+                    make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv), ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
             }
             if (tid == 0) p.counters[pair] = 0;
         }
     }
-    ptx::named_barrier_sync(kCombineBar, kConsumerWarps * 32);
+    ptx::named_barrier_sync(kCombineBar, kCT);
 }
 
 template <bool FP8, int D>
@@ -643,7 +710,7 @@ struct Plan {
     int stages = 0, ctas_per_sm = 0, grid = 0;
     uint32_t stage_bytes = 0, off_v = 0, off_q = 0, off_s = 0;
     uint32_t off_bar = 0, off_misc = 0, off_cmb = 0, off_lens = 0, smem_bytes = 0;
-    size_t counters_bytes = 0, ws_bytes = 0;
+    size_t counters_bytes = 0, slots = 0, ws_bytes = 0;
 };
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -668,7 +735,7 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     pl.off_q = 2 * region;
     pl.off_s = pl.off_q + align_up((uint32_t)G * D * 2, 128);
     pl.stage_bytes = align_up(pl.off_s + (fp8 ? 16u * 4 : 0u), 1024);
-    const uint32_t cmb = align_up((kConsumerWarps * G * (D + 4) + 2 * kConsumerWarps * G) * 4, 16);
+    const uint32_t cmb = align_up((kConsumerWarps * G * (D + 4) + 3 * kConsumerWarps * G + 2 * G) * 4, 16);
     const uint32_t lens = align_up((2u * B + 1) * 4, 16);
     const uint32_t fixed = 1024 + 32 + cmb + lens;
     const int pref = env_int("PKV_ATTN_CTAS_PER_SM", 2);
@@ -699,7 +766,8 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     pl.grid = pl.ctas_per_sm * pool->sm_count;
     const size_t pairs = (size_t)B * pool->n_kv_heads;
     pl.counters_bytes = (pairs * sizeof(int) + 255) / 256 * 256;
-    pl.ws_bytes = pl.counters_bytes + (pairs + (size_t)pl.grid) * G * (D + 2) * sizeof(float);
+    pl.slots = pairs + (size_t)pl.grid;
+    pl.ws_bytes = pl.counters_bytes + pl.slots * G * (D + 2) * sizeof(float);
     return true;
 }
 
@@ -751,6 +819,7 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32
     p.scales = pool->scales;
     p.counters = static_cast<int*>(workspace);
     p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
+    p.part_ml = p.partials + pl.slots * G * pool->head_dim;
     p.err = pool->err;
     p.B = B;
     p.Hq = n_q_heads;
