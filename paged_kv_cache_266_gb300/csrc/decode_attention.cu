@@ -65,7 +65,7 @@ struct Params {
     int box_rows;  // rows per TMA box: min(bs, kGroup)
     int ppg;       // page parts per group: kGroup / box_rows
     int stages;
-    uint32_t stage_bytes, off_v, off_q, off_s;       // within a stage
+    uint32_t stage_bytes, off_q, off_s;  // within a stage: page parts, query rows, fp8 scale pairs
     uint32_t off_bar, off_misc, off_cmb, off_lens;  // within the shared-memory block
     float scale_log2;
 };
@@ -107,6 +107,7 @@ __device__ __forceinline__ int find_seq(const int32_t* cumg, int B, int Hkv, int
 struct GroupDesc {
     int b, h, g;
     int32_t id[4];
+    float sk[4], sv[4];  // fp8 scales of the group's pages (loaded one batch after the ids)
 };
 
 template <bool FP8, int D>
@@ -114,9 +115,6 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
                          int64_t R0, int64_t R1, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
                          volatile int* misc) {
     constexpr int kEsz = FP8 ? 1 : 2;
-    constexpr int kRowBytes = D * kEsz;
-    constexpr int kPanelBytes = FP8 ? D : 128;  // bytes of a row inside one TMA box
-    constexpr int kPanels = kRowBytes / kPanelBytes;
     const int lane = threadIdx.x & 31;
 
     auto describe = [&](int64_t e, GroupDesc& d) {
@@ -135,17 +133,32 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
             d.id[i] = (i < p.ppg && k < npages) ? __ldg(p.tables + (int64_t)b * p.max_blocks + k) : -1;
         }
     };
+    // fp8: the pages' scale pairs, once their block ids have arrived (out-of-range ids read 0)
+    auto fetch_scales = [&](GroupDesc& d) {
+        if (!FP8 || d.b < 0) return;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int blk = (d.id[i] >= 0 && d.id[i] < p.num_blocks) ? d.id[i] : 0;
+            const float2 v = __ldg(reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + d.h) * 4));
+            d.sk[i] = v.x;
+            d.sv[i] = v.y;
+        }
+    };
 
-    GroupDesc cur, nxt;
+    // Three batches of 32 group descriptors in flight: ids of batch +2 and scales of batch +1
+    // load while batch 0 is issued.
+    GroupDesc cur, nxt, nxt2;
     describe(R0 + lane, cur);
+    fetch_scales(cur);
+    describe(R0 + 32 + lane, nxt);
     int s = 0;
     uint32_t round = 0;
     int64_t issued = 0;
     bool ok = true;
-    const uint32_t part_bytes = (uint32_t)p.box_rows * kRowBytes;
-    const int64_t tile_elems = (int64_t)p.bs * D;  // one (block, K|V, head) tile
+    const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * kEsz;  // K rows + V rows of one page part
     for (int64_t e0 = R0; e0 < R1 && ok; e0 += 32) {
-        describe(e0 + 32 + lane, nxt);  // table loads for the next 32 groups are in flight meanwhile
+        describe(e0 + 64 + lane, nxt2);
+        fetch_scales(nxt);
         const int n = (int)(R1 - e0 < 32 ? R1 - e0 : 32);
         for (int j = 0; j < n; ++j) {
             const int b = __shfl_sync(0xffffffffu, cur.b, j);
@@ -163,47 +176,43 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
             const uint32_t fb = bar_full + 8 * s;
             if (lane == 0) {
                 ok = ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, kWaitLimitNs);
-                if (!ok)
-                    flag_abort(p, misc);
-                else
-                    ptx::mbar_arrive_expect_tx(fb, (uint32_t)nparts * part_bytes * 2 + (FP8 ? 16u * nparts : 0u) +
-                                                       (first ? (uint32_t)(p.G * D * 2) : 0u));
+                if (!ok) flag_abort(p, misc);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);  // also orders the expect_tx before every lane's copies
+            ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            // Lanes 0..nparts-1 issue one page part each (K and V), lane 4 the query rows and
-            // lanes 8..8+nparts-1 the fp8 scale records, so a stage's copies go out in parallel.
-            const int part = lane & 7;
+            const int part = lane & 3;
             int blk = part == 0 ? id0 : part == 1 ? id1 : part == 2 ? id2 : id3;
-            if (part < nparts && (blk < 0 || blk >= p.num_blocks)) {  // keep the byte count exact, read block 0
-                if (lane < 8) atomicOr(p.err, kErrBounds);
-                blk = 0;
-            }
-            const int row_off = p.ppg > 1 ? 0 : (g * kGroup) & (p.bs - 1);
-            const int64_t tileK = (int64_t)(2 * blk) * p.Hkv + h;  // tile index of K; V is Hkv tiles further
-            if (lane < nparts) {
-                const uint32_t dst_rows = (uint32_t)(lane * p.box_rows) * kPanelBytes;
-                const int32_t rowK = (int32_t)(tileK * p.bs + row_off);
-                const int32_t rowV = (int32_t)((tileK + p.Hkv) * p.bs + row_off);
-#pragma unroll
-                for (int q = 0; q < kPanels; ++q)
-                    ptx::tma_load_2d(st + q * (kGroup * kPanelBytes) + dst_rows, tmap, q * (kPanelBytes / kEsz), rowK,
-                                     fb);
-                if (FP8) {
-                    // V panels ([D][16] per 16 tokens) are contiguous: one bulk copy per part
-                    const uint8_t* src = p.pool + (tileK + p.Hkv) * tile_elems + (int64_t)row_off * D;
-                    ptx::bulk_load(st + p.off_v + (uint32_t)(lane * p.box_rows * D), src, part_bytes, fb);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < kPanels; ++q)
-                        ptx::tma_load_2d(st + p.off_v + q * (kGroup * kPanelBytes) + dst_rows, tmap,
-                                         q * (kPanelBytes / kEsz), rowV, fb);
+            if (FP8) {  // scale pairs into the (now free) stage before it is published
+                const float sk0 = __shfl_sync(0xffffffffu, cur.sk[0], j), sv0 = __shfl_sync(0xffffffffu, cur.sv[0], j);
+                const float sk1 = __shfl_sync(0xffffffffu, cur.sk[1], j), sv1 = __shfl_sync(0xffffffffu, cur.sv[1], j);
+                const float sk2 = __shfl_sync(0xffffffffu, cur.sk[2], j), sv2 = __shfl_sync(0xffffffffu, cur.sv[2], j);
+                const float sk3 = __shfl_sync(0xffffffffu, cur.sk[3], j), sv3 = __shfl_sync(0xffffffffu, cur.sv[3], j);
+                if (lane < nparts) {
+                    const float sk = part == 0 ? sk0 : part == 1 ? sk1 : part == 2 ? sk2 : sk3;
+                    const float sv = part == 0 ? sv0 : part == 1 ? sv1 : part == 2 ? sv2 : sv3;
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(st + p.off_s + 8 * lane), "f"(sk), "f"(sv)
+                                 : "memory");
                 }
+                __syncwarp();
+            }
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)nparts * part_bytes + (first ? (uint32_t)(p.G * D * 2) : 0u));
+            __syncwarp();  // the expect-tx precedes every lane's copies
+            // Lanes 0..nparts-1 issue one page part each (K and V rows in one tensor copy) and
+            // lane 4 the query rows, so a stage's copies go out in parallel.
+            if (lane < nparts) {
+                if (blk < 0 || blk >= p.num_blocks) {  // keep the byte count exact, read block 0
+                    atomicOr(p.err, kErrBounds);
+                    blk = 0;
+                }
+                const int row_off = p.ppg > 1 ? 0 : (g * kGroup) & (p.bs - 1);
+                const int32_t rowK = (int32_t)(((int64_t)(2 * blk) * p.Hkv + h) * p.bs + row_off);
+                const uint32_t dst = st + (uint32_t)lane * part_bytes;
+                if (!FP8 && D == 128) ptx::tma_load_4d(dst, tmap, 0, rowK, 0, 0, fb);
+                else ptx::tma_load_3d(dst, tmap, 0, rowK, 0, fb);
             } else if (lane == 4 && first) {
                 ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D, (uint32_t)(p.G * D * 2),
                                fb);
-            } else if (FP8 && lane >= 8 && lane < 8 + nparts) {
-                ptx::bulk_load(st + p.off_s + 16 * part, p.scales + ((int64_t)blk * p.Hkv + h) * 4, 16, fb);
             }
             ++issued;
             if (++s == p.stages) {
@@ -212,6 +221,7 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
             }
         }
         cur = nxt;
+        nxt = nxt2;
     }
     // Do not leave while copies into this CTA's shared memory may still be landing.
     if (lane == 0) {
@@ -257,8 +267,10 @@ __device__ __forceinline__ void softmax_step(const float (&acc)[4], float sl, in
     pr[3] = ptx::exp2_approx(z3 - m1);
 }
 
+// kst / vst: the K and V halves of the warp's page part; row0: the warp's first row in it;
+// pstride: bytes between the two 128-byte panels of a row (bf16 head_dim 128).
 template <int D>
-__device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, int nvalid,
+__device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, uint32_t pstride, int nvalid,
                                           const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], SoftmaxState& st,
                                           float sl, int lane) {
     constexpr int KS = D / 16;
@@ -268,7 +280,7 @@ __device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, 
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
         const int chunk = 2 * ks + (mat >> 1);
-        const uint32_t addr = kst + (chunk >> 3) * (kGroup * 128) + krow * 128 + (((chunk & 7) ^ rr) << 4);
+        const uint32_t addr = kst + (chunk >> 3) * pstride + krow * 128 + (((chunk & 7) ^ rr) << 4);
         uint32_t a0, a1, a2, a3;
         ptx::ldsm_x4(addr, a0, a1, a2, a3);
         ptx::mma_bf16(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
@@ -296,7 +308,7 @@ __device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, 
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
         const int chunk = 2 * mt + (mat & 1);
-        const uint32_t addr = vst + (chunk >> 3) * (kGroup * 128) + vrow * 128 + (((chunk & 7) ^ rr) << 4);
+        const uint32_t addr = vst + (chunk >> 3) * pstride + vrow * 128 + (((chunk & 7) ^ rr) << 4);
         uint32_t v0, v1, v2, v3;
         ptx::ldsm_x4_trans(addr, v0, v1, v2, v3);
         ptx::mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, pb0, pb1);
@@ -307,6 +319,18 @@ template <int D>
 __device__ __forceinline__ uint32_t fp8_k_addr(uint32_t kst, int row, int chunk) {
     if (D == 128) return kst + row * 128 + ((chunk ^ (row & 7)) << 4);
     return kst + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+}
+
+// Row d of the warp's [D][16] V panel: the panel's bytes arrive as 16 swizzled lines of D bytes
+// starting at line row0 of the V half.
+template <int D>
+__device__ __forceinline__ uint32_t fp8_v_addr(uint32_t vst, int row0, int d) {
+    if (D == 128) {
+        const int line = row0 + (d >> 3);
+        return vst + line * 128 + (((d & 7) ^ (line & 7)) << 4);
+    }
+    const int line = row0 + (d >> 2);
+    return vst + line * 64 + (((d & 3) ^ ((line >> 1) & 3)) << 4);
 }
 
 template <int D>
@@ -353,7 +377,7 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
 #pragma unroll
     for (int mm = 0; mm < KS / 2; ++mm) {
         uint32_t r0, r1, r2, r3;
-        ptx::ldsm_x4(vst + (uint32_t)(32 * mm + lane) * 16, r0, r1, r2, r3);
+        ptx::ldsm_x4(fp8_v_addr<D>(vst, row0, 32 * mm + lane), r0, r1, r2, r3);
         r0 &= bm;
         r1 &= bm;
         r2 &= bm;
@@ -579,6 +603,8 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
     uint32_t round = 0;
     bool alive = true;
     const int pidx = (16 * warp) / p.box_rows;  // page part holding this warp's tokens
+    const int prow = (16 * warp) % p.box_rows;  // the warp's first row inside that part
+    const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * (FP8 ? 1 : 2);
     for (int64_t e = R0; e < R1; ++e) {
         const bool first = (e == R0) || (g == 0);
         const bool last = (e == R1 - 1) || (g == ng - 1);
@@ -598,12 +624,13 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
         }
         const int nvalid = min(16, lens_s[b] - g * kGroup - 16 * warp);
         if (alive && nvalid > 0) {
+            const uint32_t kst = st_addr + (uint32_t)pidx * part_bytes;  // the warp's page part: K rows, then V rows
+            const uint32_t vst = kst + part_bytes / 2;
             if (FP8) {
-                const float* sc = reinterpret_cast<const float*>(smem + (st_addr - sbase) + p.off_s + 16 * pidx);
-                tile_fp8<D>(st_addr, st_addr + p.off_v + (uint32_t)(warp * D * 16), 16 * warp, nvalid, qf, o, st,
-                            p.scale_log2, sc[0], sc[1], sv_prev, lane);
+                const float2 sc = *reinterpret_cast<const float2*>(smem + (st_addr - sbase) + p.off_s + 8 * pidx);
+                tile_fp8<D>(kst, vst, prow, nvalid, qf, o, st, p.scale_log2, sc.x, sc.y, sv_prev, lane);
             } else {
-                tile_bf16<D>(st_addr, st_addr + p.off_v, 16 * warp, nvalid, qf, o, st, p.scale_log2, lane);
+                tile_bf16<D>(kst, vst, prow, (uint32_t)p.box_rows * 128, nvalid, qf, o, st, p.scale_log2, lane);
             }
         }
         __syncwarp();
@@ -708,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
 // ------------------------------------------------------------------ host side
 struct Plan {
     int stages = 0, ctas_per_sm = 0, grid = 0;
-    uint32_t stage_bytes = 0, off_v = 0, off_q = 0, off_s = 0;
+    uint32_t stage_bytes = 0, off_q = 0, off_s = 0;
     uint32_t off_bar = 0, off_misc = 0, off_cmb = 0, off_lens = 0, smem_bytes = 0;
     size_t counters_bytes = 0, slots = 0, ws_bytes = 0;
 };
@@ -731,10 +758,9 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
     const uint32_t D = (uint32_t)pool->head_dim, esz = fp8 ? 1 : 2;
     const uint32_t region = kGroup * D * esz;
-    pl.off_v = region;
-    pl.off_q = 2 * region;
+    pl.off_q = 2 * region;  // kGroup rows of K and of V, as ppg page parts
     pl.off_s = pl.off_q + align_up((uint32_t)G * D * 2, 128);
-    pl.stage_bytes = align_up(pl.off_s + (fp8 ? 16u * 4 : 0u), 1024);
+    pl.stage_bytes = align_up(pl.off_s + (fp8 ? 8u * 4 : 0u), 1024);
     const uint32_t cmb = align_up((kConsumerWarps * G * (D + 4) + 3 * kConsumerWarps * G + 2 * G) * 4, 16);
     const uint32_t lens = align_up((2u * B + 1) * 4, 16);
     const uint32_t fixed = 1024 + 32 + cmb + lens;
@@ -832,7 +858,6 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32
     p.ppg = kGroup / p.box_rows;
     p.stages = pl.stages;
     p.stage_bytes = pl.stage_bytes;
-    p.off_v = pl.off_v;
     p.off_q = pl.off_q;
     p.off_s = pl.off_s;
     p.off_bar = pl.off_bar;

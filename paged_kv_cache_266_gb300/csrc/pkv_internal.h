@@ -40,7 +40,7 @@ struct pkv_pool {
     uint8_t* fresh_scratch = nullptr;  // fp8 append: [num_blocks] "offset 0 written by this call", kept zero
     int* err = nullptr;               // device error word
 
-    // TMA descriptor over all K/V rows: dim0 = head_dim elements, dim1 = num_blocks*2*Hkv*bs rows.
+    // TMA descriptor reading a page part's K and V rows in one copy (see pool.cu).
     CUtensorMap tmap_rows;
 
     pkv_allocator* alloc = nullptr;

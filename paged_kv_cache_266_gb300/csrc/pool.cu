@@ -32,26 +32,40 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// Rows of head_dim elements over the whole pool: row r = ((blk*2 + kv)*Hkv + h)*bs + t.
-// Box: 128 bytes of a row (64 bf16 or 128 fp8 elements; 64 bytes for fp8 head_dim 64) by
-// min(bs, 64) rows, swizzled so that 8 rows of one 16-byte column land in 8 different bank
-// groups for ldmatrix.
+// One descriptor reads a page part's K rows and V rows together.  The pool is viewed as rows
+// of head_dim elements (row r = ((blk*2 + kv)*Hkv + h)*bs + t); a K tile's V tile starts Hkv*bs
+// rows further, which is the stride of the last dimension.  Box: min(bs, 64) rows of
+// 128 bytes (64 bf16 or 128 fp8 elements; 64 bytes for fp8 head_dim 64), for K and V, and for
+// bf16 head_dim 128 both 128-byte halves of a row (a panel dimension of stride 128 bytes).
+// Shared memory receives [K|V][panel][row][128 bytes], each 128-byte line swizzled so that 8
+// rows of one 16-byte column land in 8 different bank groups for ldmatrix.
 bool encode_rows_map(pkv_pool* p) {
     auto encode = get_encode_fn();
     if (!encode) return false;
     const bool fp8 = p->dtype == PKV_KV_FP8_E4M3;
     const uint64_t esz = fp8 ? 1 : 2;
+    const uint64_t row_bytes = (uint64_t)p->head_dim * esz;
     const uint64_t rows = (uint64_t)p->num_blocks * 2 * p->n_kv_heads * p->block_size;
-    cuuint64_t dims[2] = {(cuuint64_t)p->head_dim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(p->head_dim * esz)};
+    const uint64_t kv_stride = (uint64_t)p->n_kv_heads * p->block_size * row_bytes;
     const uint32_t inner = fp8 ? (uint32_t)p->head_dim : 64u;  // elements per box row
     const uint32_t box_rows = p->block_size < 64 ? (uint32_t)p->block_size : 64u;
-    cuuint32_t box[2] = {inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle swz = inner * esz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUresult r = encode(&p->tmap_rows, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                        p->kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r;
+    if (!fp8 && p->head_dim == 128) {
+        cuuint64_t dims[4] = {64, (cuuint64_t)rows, 2, 2};
+        cuuint64_t strides[3] = {(cuuint64_t)row_bytes, 128, (cuuint64_t)kv_stride};
+        cuuint32_t box[4] = {64, box_rows, 2, 2};
+        r = encode(&p->tmap_rows, dt, 4, p->kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, 2};
+        cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)kv_stride};
+        cuuint32_t box[3] = {inner, box_rows, 2};
+        r = encode(&p->tmap_rows, dt, 3, p->kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 
