@@ -275,7 +275,8 @@ __device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, 
                                           float sl, int lane) {
     constexpr int KS = D / 16;
     const int rr = lane & 7, mat = lane >> 3, g8 = lane >> 2, c4 = lane & 3;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // two independent accumulation chains over the k-steps halve the dependent MMA latency
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
     const int krow = row0 + rr + ((mat & 1) << 3);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -283,8 +284,10 @@ __device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, 
         const uint32_t addr = kst + (chunk >> 3) * pstride + krow * 128 + (((chunk & 7) ^ rr) << 4);
         uint32_t a0, a1, a2, a3;
         ptx::ldsm_x4(addr, a0, a1, a2, a3);
-        ptx::mma_bf16(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        ptx::mma_bf16((ks & 1) ? acc2 : acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
     float pr[4], f0, f1;
     softmax_step(acc, sl, nvalid, g8, st, pr, f0, f1);
     const uint32_t p01 = ptx::pack_bf16x2(pr[0], pr[1]), p23 = ptx::pack_bf16x2(pr[2], pr[3]);
@@ -339,7 +342,7 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
                                          float sl, float sk, float sv, float& sv_prev, int lane) {
     constexpr int KS = D / 16;
     const int rr = lane & 7, mat = lane >> 3, g8 = lane >> 2, c4 = lane & 3;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
     const int krow = row0 + rr + ((mat & 1) << 3);
 #pragma unroll
     for (int kk = 0; kk < KS / 2; ++kk) {
@@ -347,9 +350,11 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
         ptx::ldsm_x4(fp8_k_addr<D>(kst, krow, 2 * kk + (mat >> 1)), r0, r1, r2, r3);
         ptx::mma_f16(acc, ptx::e4m3x2_to_f16x2(r0), ptx::e4m3x2_to_f16x2(r1), ptx::e4m3x2_to_f16x2(r0 >> 16),
                      ptx::e4m3x2_to_f16x2(r1 >> 16), qf[2 * kk][0], qf[2 * kk][1]);
-        ptx::mma_f16(acc, ptx::e4m3x2_to_f16x2(r2), ptx::e4m3x2_to_f16x2(r3), ptx::e4m3x2_to_f16x2(r2 >> 16),
+        ptx::mma_f16(acc2, ptx::e4m3x2_to_f16x2(r2), ptx::e4m3x2_to_f16x2(r3), ptx::e4m3x2_to_f16x2(r2 >> 16),
                      ptx::e4m3x2_to_f16x2(r3 >> 16), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
     float pr[4], f0, f1;
     softmax_step(acc, sl * sk, nvalid, g8, st, pr, f0, f1);
     const uint32_t p01 = ptx::pack_f16x2(pr[0], pr[1]), p23 = ptx::pack_f16x2(pr[2], pr[3]);
@@ -655,7 +660,7 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
 }
 
 template <bool FP8, int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
+__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
@@ -764,7 +769,9 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     const uint32_t cmb = align_up((kConsumerWarps * G * (D + 4) + 3 * kConsumerWarps * G + 2 * G) * 4, 16);
     const uint32_t lens = align_up((2u * B + 1) * 4, 16);
     const uint32_t fixed = 1024 + 32 + cmb + lens;
-    const int pref = env_int("PKV_ATTN_CTAS_PER_SM", 2);
+    // fp8 tiles carry half the bytes of bf16 ones, so fp8 runs three CTAs per SM (its kernel is
+    // compiled for that register budget) to keep enough tiles in flight
+    const int pref = env_int("PKV_ATTN_CTAS_PER_SM", fp8 ? 3 : 2);
     const int max_stages = std::max(2, std::min(kMaxStages, env_int("PKV_ATTN_MAX_STAGES", kMaxStages)));
     pl.stages = 0;
     for (int ctas = std::max(1, pref); ctas >= 1; --ctas) {
