@@ -170,6 +170,22 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q_dev, const i
                                 int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads, float scale,
                                 void* out_dev, void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------ decode step (device)
+ * One step of in-flight batching for one layer ("TensorRT-LLM 深度实战", §3.2: every step the
+ * running batch appends one token per sequence and runs one forward pass): pkv_append of the
+ * step's new K/V followed by pkv_decode_attention over the grown contexts.  Same arguments,
+ * layouts, results and errors as those two calls made in sequence; all arguments are checked
+ * before anything is launched.  The attention kernel is launched as a programmatic dependent
+ * of the append, so its set-up (context lengths, block tables, query rows) overlaps the append
+ * and its first pool read waits for the append to finish — the per-step launch overhead the
+ * pages counter with CUDA graphs ("TensorRT-LLM 推理加速实战", §7.1).  The append must not write
+ * q, block_tables or context_lens (it only writes the pool). */
+pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new_dev, const void* v_new_dev,
+                           const int64_t* slot_mapping_dev, int64_t N, const void* q_dev,
+                           const int32_t* block_tables_dev, int max_blocks, const int32_t* context_lens_dev, int B,
+                           int n_q_heads, float scale, void* out_dev, void* workspace_dev, size_t workspace_bytes,
+                           pkv_stream_t stream);
+
 /* Workspace size for pkv_decode_attention with these B, n_q_heads and max_blocks. */
 pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out);
 

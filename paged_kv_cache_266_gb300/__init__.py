@@ -20,7 +20,7 @@ __all__ = [
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
     "pkv_seq_release", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
-    "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_workspace_bytes",
+    "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
     "pkv_status_str", "KVPool",
 ]
@@ -71,6 +71,7 @@ def _L():
         "pkv_append": (i32, [vp, vp, vp, vp, i64, vp]),
         "pkv_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, sz, vp]),
         "pkv_decode_workspace_bytes": (i32, [vp, i32, i32, i32, P(sz)]),
+        "pkv_decode_step": (i32, [vp, vp, vp, vp, i64, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, sz, vp]),
         "pkv_decode_workspace_init": (i32, [vp, sz, vp]),
         "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
         "pkv_kv_bytes": (ctypes.c_uint64, [i64, i64, i64, i64, i64, ctypes.c_double]),
@@ -217,6 +218,18 @@ def pkv_decode_attention(pool: int, q, block_tables, context_lens, scale: float,
                                      block_tables.shape[1], _dev(context_lens, "i32", "context_lens"), B, Hq,
                                      float(scale), _dev(out, "bf16", "out"), _dev(workspace, "u8", "workspace"),
                                      workspace.numel(), _stream(stream)), "pkv_decode_attention")
+
+
+def pkv_decode_step(pool: int, k_new, v_new, slot_mapping, q, block_tables, context_lens, scale: float, out, workspace,
+                    stream=None) -> None:
+    """pkv_append(k_new, v_new, slot_mapping) then pkv_decode_attention(...), launched back to back."""
+    B, Hq = q.shape[0], q.shape[1]
+    _check(_L().pkv_decode_step(pool, _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"),
+                                _dev(slot_mapping, "i64", "slot_mapping"), slot_mapping.shape[0], _dev(q, "bf16", "q"),
+                                _dev(block_tables, "i32", "block_tables"), block_tables.shape[1],
+                                _dev(context_lens, "i32", "context_lens"), B, Hq, float(scale), _dev(out, "bf16", "out"),
+                                _dev(workspace, "u8", "workspace"), workspace.numel(), _stream(stream)),
+           "pkv_decode_step")
 
 
 def pkv_decode_workspace_bytes(pool: int, B: int, n_q_heads: int, max_blocks: int) -> int:

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_bf16_kernel(uint16_t* _
                                                                       const uint16_t* __restrict__ v_new,
                                                                       const int64_t* __restrict__ slots, int64_t N,
                                                                       int Hkv, int bs, int num_blocks, int* err) {
+    ptx::grid_launch_dependents();  // a following decode step may begin its set-up
     constexpr int TPR = D / 8;
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gt / TPR;
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_amax_kernel(const uint16_t
                                                                    const int64_t* __restrict__ slots, int64_t N,
                                                                    int Hkv, int bs, int num_blocks,
                                                                    uint32_t* amax, uint8_t* fresh, int* err) {
+    ptx::grid_launch_dependents();  // a following decode step may begin its set-up
     constexpr int TPR = D / 8;  // 8 or 16 lanes per row, aligned inside the warp
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gt / TPR;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_quant_kernel(uint8_t* __re
                                                                     int Hkv, int bs, int num_blocks,
                                                                     const uint32_t* __restrict__ amax,
                                                                     const uint8_t* __restrict__ fresh) {
+    ptx::grid_launch_dependents();  // a following decode step may begin its set-up
     constexpr int TPR = D / 8;
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gt / TPR;
@@ -160,6 +163,7 @@ template <int D>
 __global__ void __launch_bounds__(kAppendThreads) fp8_reset_kernel(const int64_t* __restrict__ slots, int64_t N,
                                                                     int Hkv, int bs, int num_blocks,
                                                                     uint32_t* amax, uint8_t* fresh) {
+    ptx::grid_launch_dependents();  // a following decode step may begin its set-up
     constexpr int TPR = D / 8;
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gt / TPR;
@@ -197,16 +201,27 @@ pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, cons
 }  // namespace
 }  // namespace pkv
 
-extern "C" pkv_status pkv_append(pkv_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping,
-                                 int64_t N, pkv_stream_t stream) {
+namespace pkv {
+
+pkv_status append_check(const pkv_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                        int64_t N) {
     if (!pool || N < 0) return PKV_ERR_INVALID_ARG;
     if (N == 0) return PKV_OK;
     if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u) return PKV_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status pkv_append(pkv_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                 int64_t N, pkv_stream_t stream) {
+    const pkv_status st = pkv::append_check(pool, k_new, v_new, slot_mapping, N);
+    if (st != PKV_OK || N == 0) return st;
     const auto* k = static_cast<const uint16_t*>(k_new);
     const auto* v = static_cast<const uint16_t*>(v_new);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return pool->head_dim == 128 ? pkv::launch_append<128>(pool, k, v, slot_mapping, N, st)
-                                 : pkv::launch_append<64>(pool, k, v, slot_mapping, N, st);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    return pool->head_dim == 128 ? pkv::launch_append<128>(pool, k, v, slot_mapping, N, cs)
+                                 : pkv::launch_append<64>(pool, k, v, slot_mapping, N, cs);
 }

@@ -156,6 +156,9 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
     int64_t issued = 0;
     bool ok = true;
     const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * kEsz;  // K rows + V rows of one page part
+    // When launched behind this step's append (programmatic dependent launch), the pool is read
+    // only after that kernel has finished; otherwise this returns at once.
+    ptx::grid_dependency_wait();
     for (int64_t e0 = R0; e0 < R1 && ok; e0 += 32) {
         describe(e0 + 64 + lane, nxt2);
         fetch_scales(nxt);
@@ -804,33 +807,10 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     return true;
 }
 
-}  // namespace attn
-
-void attention_configure(pkv_pool* pool) {
-    cudaFuncSetAttribute(attn::kernel_for(pool), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         pool->max_smem_per_block);
-}
-
-}  // namespace pkv
-
-extern "C" {
-
-pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out) {
-    (void)max_blocks;
-    if (!pool || !out || B < 0 || B > pkv::attn::kMaxBatch || n_q_heads < 1 || n_q_heads % pool->n_kv_heads)
-        return PKV_ERR_INVALID_ARG;
-    const int G = n_q_heads / pool->n_kv_heads;
-    if (G > pkv::attn::kMaxG) return PKV_ERR_INVALID_ARG;
-    pkv::attn::Plan pl;
-    if (!pkv::attn::make_plan(pool, B, G, pl)) return PKV_ERR_CUDA;
-    *out = pl.ws_bytes;
-    return PKV_OK;
-}
-
-pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32_t* block_tables, int max_blocks,
-                                const int32_t* context_lens, int B, int n_q_heads, float scale, void* out,
-                                void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
-    using namespace pkv::attn;
+// Argument checks, launch plan and kernel parameters for one decode-attention call.
+pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tables, int max_blocks,
+                   const int32_t* context_lens, int B, int n_q_heads, float scale, void* out, void* workspace,
+                   size_t workspace_bytes, Plan& pl, Params& p) {
     if (!pool || B < 0 || B > kMaxBatch || n_q_heads < 1 || n_q_heads % pool->n_kv_heads) return PKV_ERR_INVALID_ARG;
     if (B == 0) return PKV_OK;
     const int G = n_q_heads / pool->n_kv_heads;
@@ -840,10 +820,8 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32
     if (((uintptr_t)q | (uintptr_t)out) & 15u || (uintptr_t)workspace & 255u ||
         ((uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
         return PKV_ERR_INVALID_ARG;
-    Plan pl;
     if (!make_plan(pool, B, G, pl)) return PKV_ERR_CUDA;
     if (workspace_bytes < pl.ws_bytes) return PKV_ERR_INVALID_ARG;
-    Params p;
     p.q = static_cast<const uint16_t*>(q);
     p.tables = block_tables;
     p.lens = context_lens;
@@ -872,16 +850,82 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32
     p.off_cmb = pl.off_cmb;
     p.off_lens = pl.off_lens;
     p.scale_log2 = scale * 1.4426950408889634f;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return PKV_OK;
+}
+
+// Launch on `st`.  With `pdl` the kernel may start while the preceding kernel on the stream
+// (an append of this step) is still running: it prepares everything that does not read the
+// pool and waits (griddepcontrol.wait) before its first page copy.
+pkv_status launch(const pkv_pool* pool, const Plan& pl, const Params& p, cudaStream_t st, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
     const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
-    if (pool->head_dim == 128) {
-        if (fp8) decode_kernel<true, 128><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
-        else decode_kernel<false, 128><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
-    } else {
-        if (fp8) decode_kernel<true, 64><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
-        else decode_kernel<false, 64><<<pl.grid, kThreads, pl.smem_bytes, st>>>(pool->tmap_rows, p);
-    }
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    cudaError_t e;
+    if (pool->head_dim == 128)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 128>, pool->tmap_rows, p)
+                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 128>, pool->tmap_rows, p);
+    else
+        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 64>, pool->tmap_rows, p)
+                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 64>, pool->tmap_rows, p);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace attn
+
+void attention_configure(pkv_pool* pool) {
+    cudaFuncSetAttribute(attn::kernel_for(pool), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         pool->max_smem_per_block);
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out) {
+    (void)max_blocks;
+    if (!pool || !out || B < 0 || B > pkv::attn::kMaxBatch || n_q_heads < 1 || n_q_heads % pool->n_kv_heads)
+        return PKV_ERR_INVALID_ARG;
+    const int G = n_q_heads / pool->n_kv_heads;
+    if (G > pkv::attn::kMaxG) return PKV_ERR_INVALID_ARG;
+    pkv::attn::Plan pl;
+    if (!pkv::attn::make_plan(pool, B, G, pl)) return PKV_ERR_CUDA;
+    *out = pl.ws_bytes;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q, const int32_t* block_tables, int max_blocks,
+                                const int32_t* context_lens, int B, int n_q_heads, float scale, void* out,
+                                void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    pkv::attn::Plan pl;
+    pkv::attn::Params p;
+    const pkv_status st = pkv::attn::prepare(pool, q, block_tables, max_blocks, context_lens, B, n_q_heads, scale, out,
+                                             workspace, workspace_bytes, pl, p);
+    if (st != PKV_OK || B == 0) return st;
+    return pkv::attn::launch(pool, pl, p, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t N,
+                           const void* q, const int32_t* block_tables, int max_blocks, const int32_t* context_lens, int B,
+                           int n_q_heads, float scale, void* out, void* workspace, size_t workspace_bytes,
+                           pkv_stream_t stream) {
+    pkv::attn::Plan pl;
+    pkv::attn::Params p;
+    pkv_status st = pkv::append_check(pool, k_new, v_new, slot_mapping, N);
+    if (st != PKV_OK) return st;
+    st = pkv::attn::prepare(pool, q, block_tables, max_blocks, context_lens, B, n_q_heads, scale, out, workspace,
+                            workspace_bytes, pl, p);
+    if (st != PKV_OK) return st;
+    st = pkv_append(pool, k_new, v_new, slot_mapping, N, stream);
+    if (st != PKV_OK || B == 0) return st;
+    return pkv::attn::launch(pool, pl, p, reinterpret_cast<cudaStream_t>(stream), N > 0);
 }
 
 }  // extern "C"

@@ -16,6 +16,8 @@ constexpr int kErrBounds = 1;
 constexpr int kErrTimeout = 2;
 
 bool valid_block_size(int bs);
+pkv_status append_check(const pkv_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                        int64_t N);
 pkv_allocator* allocator_new(int num_blocks, int block_size);
 void allocator_delete(pkv_allocator* a);
 

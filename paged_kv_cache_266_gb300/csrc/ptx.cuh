@@ -190,6 +190,11 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
+// Programmatic dependent launch: wait for the prerequisite grid (no-op without one) / let the
+// dependent grid start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

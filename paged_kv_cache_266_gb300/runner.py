@@ -16,8 +16,8 @@ import math
 import numpy as np
 
 from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_allocator_set_free_order, pkv_append,
-               pkv_decode_attention, pkv_decode_workspace_bytes, pkv_get_block_tables, pkv_seq_release,
-               pkv_seq_reserve, pkv_slot_mapping)
+               pkv_decode_attention, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
+               pkv_seq_release, pkv_seq_reserve, pkv_slot_mapping)
 
 def replay(allocator: int, ops) -> None:
     for op in ops:
@@ -83,9 +83,15 @@ class DecodeStep:
         pkv_decode_attention(self.pool.handle, self.q, self.tables, self.lens, self.scale, self.out, self.workspace,
                              stream)
 
-    def step(self, stream=None):
-        self.append(stream)
-        self.attention(stream)
+    def step(self, stream=None, fused: bool = True):
+        """Append the new tokens, then attend.  fused: one pkv_decode_step call (the attention
+        kernel's set-up overlaps the append); otherwise pkv_append then pkv_decode_attention."""
+        if fused and self.w.append:
+            pkv_decode_step(self.pool.handle, self.k_new, self.v_new, self.slots_new, self.q, self.tables, self.lens,
+                            self.scale, self.out, self.workspace, stream)
+        else:
+            self.append(stream)
+            self.attention(stream)
         return self.out
 
     # --- end to end from host buffers

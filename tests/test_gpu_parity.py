@@ -88,6 +88,26 @@ def test_shapes(pkv, dtype, D, bs):
         step.close()
 
 
+@pytest.mark.parametrize("name", ["c0", "c2", "c4"])
+def test_fused_step_equals_separate_calls(pkv, name):
+    """pkv_decode_step (append, then attention as a programmatic dependent launch) gives the
+    same pool bytes and outputs, bit for bit, as pkv_append followed by pkv_decode_attention."""
+    import torch
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    w = W.make_workload(name)
+    a, b = DecodeStep(w), DecodeStep(w)
+    a.step(fused=True)
+    b.step(fused=False)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(a.pool.handle) == pkv.PKV_OK
+    assert np.array_equal(a.out_host(), b.out_host())
+    ka, sa = a.pool_bytes_host()
+    kb, sb = b.pool_bytes_host()
+    assert np.array_equal(ka, kb) and np.array_equal(sa, sb)
+    a.close()
+    b.close()
+
+
 def test_empty_and_single_token_contexts(pkv):
     w = W.custom_workload(300, 6, 8, 2, 128, 64, [0, 1, 0, 17, 64, 65], append=False)
     step = _run(pkv, w)
