@@ -111,7 +111,7 @@ struct GroupDesc {
 };
 
 template <bool FP8, int D>
-__device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t* cumg, const int32_t* lens_s,
+__device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, const Params& p, const int32_t* cumg, const int32_t* lens_s,
                          int64_t R0, int64_t R1, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
                          volatile int* misc) {
     constexpr int kEsz = FP8 ? 1 : 2;
@@ -175,6 +175,11 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
             const bool first = (e == R0) || (g == 0);
             int nparts = 1;
             if (p.ppg > 1) nparts = min(p.ppg, (lens_s[b] + p.bs - 1) / p.bs - g * p.ppg);
+            // rows of the last part that hold tokens; a partly filled last part is copied in
+            // 16-row boxes up to its last token
+            const int tail_rows = min(p.box_rows, lens_s[b] - g * kGroup - (nparts - 1) * p.box_rows);
+            const int tail16 = (tail_rows + 15) >> 4;
+            const bool tail_short = p.box_rows > 16 && tail_rows <= p.box_rows - 16;  // saves a 16-row box
             const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
             const uint32_t fb = bar_full + 8 * s;
             if (lane == 0) {
@@ -199,7 +204,9 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
                 __syncwarp();
             }
             if (lane == 0)
-                ptx::mbar_arrive_expect_tx(fb, (uint32_t)nparts * part_bytes + (first ? (uint32_t)(p.G * D * 2) : 0u));
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)(nparts - (tail_short ? 1 : 0)) * part_bytes +
+                                                   (tail_short ? (uint32_t)tail16 * 32u * D * kEsz : 0u) +
+                                                   (first ? (uint32_t)(p.G * D * 2) : 0u));
             __syncwarp();  // the expect-tx precedes every lane's copies
             // Lanes 0..nparts-1 issue one page part each (K and V rows in one tensor copy) and
             // lane 4 the query rows, so a stage's copies go out in parallel.
@@ -211,8 +218,22 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, const int32_t
                 const int row_off = p.ppg > 1 ? 0 : (g * kGroup) & (p.bs - 1);
                 const int32_t rowK = (int32_t)(((int64_t)(2 * blk) * p.Hkv + h) * p.bs + row_off);
                 const uint32_t dst = st + (uint32_t)lane * part_bytes;
-                if (!FP8 && D == 128) ptx::tma_load_4d(dst, tmap, 0, rowK, 0, 0, fb);
-                else ptx::tma_load_3d(dst, tmap, 0, rowK, 0, fb);
+                if (tail_short && lane == nparts - 1) {
+                    constexpr int kPanels = FP8 ? 1 : D / 64;
+                    constexpr uint32_t kPanelRowBytes = FP8 ? D : 128;
+                    const int32_t rowV = rowK + p.Hkv * p.bs;
+                    for (int t = 0; t < tail16; ++t)
+#pragma unroll
+                        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+                            for (int q = 0; q < kPanels; ++q)
+                                ptx::tma_load_2d(dst + (uint32_t)((kv * kPanels + q) * p.box_rows + 16 * t) * kPanelRowBytes,
+                                                 tmap_tail, q * 64, (kv ? rowV : rowK) + 16 * t, fb);
+                } else if (!FP8 && D == 128) {
+                    ptx::tma_load_4d(dst, tmap, 0, rowK, 0, 0, fb);
+                } else {
+                    ptx::tma_load_3d(dst, tmap, 0, rowK, 0, fb);
+                }
             } else if (lane == 4 && first) {
                 ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D, (uint32_t)(p.G * D * 2),
                                fb);
@@ -663,7 +684,9 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
 }
 
 template <bool FP8, int D>
-__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
+__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                          const __grid_constant__ CUtensorMap tmap_tail,
+                                                                          const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
@@ -714,7 +737,10 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
         }
         ptx::fence_barrier_init();
     }
-    if (tid == 64) ptx::prefetch_tensormap(&tmap);
+    if (tid == 64) {
+        ptx::prefetch_tensormap(&tmap);
+        ptx::prefetch_tensormap(&tmap_tail);
+    }
     __syncthreads();
 
     // Groups are split over C = min(grid, groups) CTAs, so every participating CTA owns at
@@ -728,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
     }
 
     if (warp == kConsumerWarps) {
-        if (R0 < R1) producer<FP8, D>(&tmap, p, cumg, lens_s, R0, R1, sbase, bar_full, bar_empty, misc);
+        if (R0 < R1) producer<FP8, D>(&tmap, &tmap_tail, p, cumg, lens_s, R0, R1, sbase, bar_full, bar_empty, misc);
         return;
     }
     // Sequences with an empty context get zeros (no group covers them).
@@ -870,11 +896,11 @@ pkv_status launch(const pkv_pool* pool, const Plan& pl, const Params& p, cudaStr
     const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
     cudaError_t e;
     if (pool->head_dim == 128)
-        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 128>, pool->tmap_rows, p)
-                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 128>, pool->tmap_rows, p);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 128>, pool->tmap_rows, pool->tmap_tail, p)
+                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 128>, pool->tmap_rows, pool->tmap_tail, p);
     else
-        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 64>, pool->tmap_rows, p)
-                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 64>, pool->tmap_rows, p);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 64>, pool->tmap_rows, pool->tmap_tail, p)
+                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 64>, pool->tmap_rows, pool->tmap_tail, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

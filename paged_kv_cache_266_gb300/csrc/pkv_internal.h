@@ -44,6 +44,8 @@ struct pkv_pool {
 
     // TMA descriptor reading a page part's K and V rows in one copy (see pool.cu).
     CUtensorMap tmap_rows;
+    // 16 rows of one 128-byte panel (the tail of a sequence's last page part).
+    CUtensorMap tmap_tail;
 
     pkv_allocator* alloc = nullptr;
 };

@@ -66,6 +66,14 @@ bool encode_rows_map(pkv_pool* p) {
         r = encode(&p->tmap_rows, dt, 3, p->kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
+    if (r != CUDA_SUCCESS) return false;
+    // Tail descriptor: 16-row boxes of one 128-byte panel of K or V rows, for the last, partly
+    // filled part of a sequence (only its rows holding tokens are copied).
+    cuuint64_t dims2[2] = {(cuuint64_t)(fp8 ? p->head_dim : p->head_dim), (cuuint64_t)rows};
+    cuuint64_t strides2[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box2[2] = {inner, 16};
+    r = encode(&p->tmap_tail, dt, 2, p->kv, dims2, strides2, box2, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
