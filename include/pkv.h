@@ -165,7 +165,9 @@ pkv_status pkv_append(pkv_pool* pool, const void* k_new_dev, const void* v_new_d
  *   next.  Calls that overlap in time must use different workspaces.
  * n_q_heads must be a multiple of n_kv_heads with at most 8 query heads per KV head.
  * context_lens[b] == 0 yields zeros.  A context longer than max_blocks*block_size, or a
- * block id outside the pool, is clamped/skipped and flagged (PKV_ERR_BOUNDS). */
+ * block id outside the pool, is clamped/skipped and flagged (PKV_ERR_BOUNDS).  Every wait in
+ * the kernel is bounded (2 s); if one runs out the results are invalid, pkv_check_device_error
+ * returns PKV_ERR_TIMEOUT, and the workspace must be re-initialised before its next use. */
 pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q_dev, const int32_t* block_tables_dev,
                                 int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads, float scale,
                                 void* out_dev, void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);

@@ -68,6 +68,8 @@ struct Params {
     uint32_t stage_bytes, off_q, off_s;  // within a stage: page parts, query rows, fp8 scale pairs
     uint32_t off_bar, off_misc, off_cmb, off_lens;  // within the shared-memory block
     float scale_log2;
+    uint64_t wait_ns;   // bound of every mbarrier wait
+    uint32_t stall_tx;  // test hook: bytes each stage expects beyond its copies (0 in normal use)
 };
 
 // misc words in shared memory
@@ -75,14 +77,14 @@ constexpr int kMiscAbort = 0;
 constexpr int kMiscMergeParts = 1;
 constexpr int kMiscMergeFirst = 2;
 
-__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* misc) {
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* misc, uint64_t limit_ns) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (misc[kMiscAbort]) return false;
-            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return false;
+            if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
 }
@@ -183,7 +185,7 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
             const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
             const uint32_t fb = bar_full + 8 * s;
             if (lane == 0) {
-                ok = ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, kWaitLimitNs);
+                ok = !misc[kMiscAbort] && ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, p.wait_ns);
                 if (!ok) flag_abort(p, misc);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -206,7 +208,7 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
             if (lane == 0)
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)(nparts - (tail_short ? 1 : 0)) * part_bytes +
                                                    (tail_short ? (uint32_t)tail16 * 32u * D * kEsz : 0u) +
-                                                   (first ? (uint32_t)(p.G * D * 2) : 0u));
+                                                   (first ? (uint32_t)(p.G * D * 2) : 0u) + p.stall_tx);
             __syncwarp();  // the expect-tx precedes every lane's copies
             // Lanes 0..nparts-1 issue one page part each (K and V rows in one tensor copy) and
             // lane 4 the query rows, so a stage's copies go out in parallel.
@@ -251,7 +253,7 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
     if (lane == 0) {
         const int64_t lo = issued > p.stages ? issued - p.stages : 0;
         for (int64_t qq = issued - 1; qq >= lo; --qq)
-            if (!ptx::mbar_wait(bar_full + 8 * (int)(qq % p.stages), (uint32_t)((qq / p.stages) & 1), kWaitLimitNs)) {
+            if (!ptx::mbar_wait(bar_full + 8 * (int)(qq % p.stages), (uint32_t)((qq / p.stages) & 1), p.wait_ns)) {
                 flag_abort(p, misc);
                 break;
             }
@@ -638,7 +640,7 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
         const bool first = (e == R0) || (g == 0);
         const bool last = (e == R1 - 1) || (g == ng - 1);
         const uint32_t st_addr = sbase + (uint32_t)s * p.stage_bytes;
-        if (alive && !wait_full(bar_full + 8 * s, round & 1, misc)) {
+        if (alive && !wait_full(bar_full + 8 * s, round & 1, misc, p.wait_ns)) {
             alive = false;
             flag_abort(p, misc);
         }
@@ -663,7 +665,9 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
             }
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
+        // A warp that gave up waiting no longer releases stages: the stage's phase is unknown, so
+        // the producer must not reuse it (its own bounded wait then runs out).
+        if (lane == 0 && alive) ptx::mbar_arrive(bar_empty + 8 * s);
         if (last) finish_pair<D>(p, o, st, FP8 ? sv_prev : 1.f, b, h, g_first == 0 && g == ng - 1, Ng, C, cumg, smem,
                                  misc);
         if (++s == p.stages) {
@@ -876,6 +880,12 @@ pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tab
     p.off_cmb = pl.off_cmb;
     p.off_lens = pl.off_lens;
     p.scale_log2 = scale * 1.4426950408889634f;
+    // Test hooks for the bounded waits (failure detection is tested without a GPU fault):
+    // PKV_TEST_WAIT_LIMIT_MS shortens every wait, PKV_TEST_STALL_COPIES makes every stage expect
+    // 16 bytes no copy delivers, so the waits run out and the call reports PKV_ERR_TIMEOUT.
+    const int limit_ms = env_int("PKV_TEST_WAIT_LIMIT_MS", 0);
+    p.wait_ns = limit_ms > 0 ? (uint64_t)limit_ms * 1000000ull : kWaitLimitNs;
+    p.stall_tx = env_int("PKV_TEST_STALL_COPIES", 0) ? 16u : 0u;
     return PKV_OK;
 }
 

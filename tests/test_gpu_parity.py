@@ -159,6 +159,29 @@ def test_out_of_range_block_id_is_flagged_not_faulted(pkv):
     step.close()
 
 
+def test_bounded_waits_report_timeout_and_leave_the_context_usable(pkv, monkeypatch):
+    """Every mbarrier wait in the attention kernel is bounded.  With the test hooks the stages
+    expect bytes no copy delivers and the waits give up after 20 ms: the call reports
+    PKV_ERR_TIMEOUT, no fault, and the next normal call gives the same results as before."""
+    import torch
+    w = W.custom_workload(306, 3, 8, 2, 128, 64, [300, 70, 900], append=False)
+    step = _run(pkv, w)
+    good = step.out_host().copy()
+    monkeypatch.setenv("PKV_TEST_WAIT_LIMIT_MS", "20")
+    monkeypatch.setenv("PKV_TEST_STALL_COPIES", "1")
+    step.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_TIMEOUT
+    monkeypatch.delenv("PKV_TEST_WAIT_LIMIT_MS")
+    monkeypatch.delenv("PKV_TEST_STALL_COPIES")
+    pkv.pkv_decode_workspace_init(step.workspace)  # merge tickets may have been left mid-count
+    step.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_OK
+    assert np.array_equal(step.out_host(), good)
+    step.close()
+
+
 def test_context_longer_than_table_is_clamped_and_flagged(pkv):
     import torch
     w = W.custom_workload(303, 2, 4, 1, 64, 16, [30, 20], append=False)
