@@ -156,18 +156,26 @@ def pkv_free_list(a: int) -> np.ndarray:
     return out[:n.value]
 
 
-def pkv_get_block_tables(a: int, seq_ids, max_blocks: int) -> np.ndarray:
+def _out_array(out, shape, dtype):
+    if out is None:
+        return np.empty(shape, dtype=dtype)
+    if out.shape != tuple(shape) or out.dtype != dtype or not out.flags["C_CONTIGUOUS"]:
+        raise ValueError(f"out must be a contiguous {np.dtype(dtype).name} array of shape {tuple(shape)}")
+    return out
+
+
+def pkv_get_block_tables(a: int, seq_ids, max_blocks: int, out: np.ndarray | None = None) -> np.ndarray:
     s = _np(seq_ids, np.int64)
-    out = np.empty((len(s), max_blocks), dtype=np.int32)
+    out = _out_array(out, (len(s), max_blocks), np.int32)
     _check(_L().pkv_get_block_tables(a, s.ctypes.data, len(s), max_blocks, out.ctypes.data), "pkv_get_block_tables")
     return out
 
 
-def pkv_slot_mapping(a: int, seq_ids, positions) -> np.ndarray:
+def pkv_slot_mapping(a: int, seq_ids, positions, out: np.ndarray | None = None) -> np.ndarray:
     s, p = _np(seq_ids, np.int64), _np(positions, np.int64)
     if s.shape != p.shape:
         raise ValueError("seq_ids and positions must have the same length")
-    out = np.empty(len(s), dtype=np.int64)
+    out = _out_array(out, (len(s),), np.int64)
     _check(_L().pkv_slot_mapping(a, s.ctypes.data, p.ctypes.data, len(s), out.ctypes.data), "pkv_slot_mapping")
     return out
 

@@ -96,43 +96,59 @@ class DecodeStep:
 
     # --- end to end from host buffers
     def _prepare_host(self):
+        """One pinned staging buffer holding every input of a step (q, new K/V, block tables,
+        context lengths, slots) and a device buffer of the same layout whose slices are the
+        kernel arguments, so a step needs one host-to-device copy and one copy back."""
         torch, w = self.torch, self.w
-        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         n = self.batch
-        self._host = {
-            "q": pin(w.query()[:n].view(np.int16)),
-            "k": pin(w.new_k()[:n].view(np.int16)),
-            "v": pin(w.new_v()[:n].view(np.int16)),
-            "lens": pin(self.lens_host),
-            "tables": torch.empty(self.tables_host.shape, dtype=torch.int32).pin_memory(),
-            "slots": torch.empty(self.slots_new_host.shape, dtype=torch.int64).pin_memory(),
-            "out": torch.empty(n, w.Hq, w.D, dtype=torch.int16).pin_memory(),
-        }
+        parts = [("q", (n, w.Hq, w.D), np.int16), ("k", (n, w.Hkv, w.D), np.int16),
+                 ("v", (n, w.Hkv, w.D), np.int16), ("tables", (n, self.max_blocks), np.int32),
+                 ("lens", (n,), np.int32), ("slots", (n if w.append else 0,), np.int64)]
+        offs, total = {}, 0
+        for name, shape, dt in parts:
+            offs[name] = total
+            total += (int(np.prod(shape)) * np.dtype(dt).itemsize + 255) // 256 * 256
+        hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(total, dtype=torch.uint8, device=self.device)
+        hnp = hbuf.numpy()
+        H, Dv = {}, {}
+        tdt = {np.int16: torch.int16, np.int32: torch.int32, np.int64: torch.int64}
+        for name, shape, dt in parts:
+            nbytes = int(np.prod(shape)) * np.dtype(dt).itemsize
+            H[name] = hnp[offs[name]:offs[name] + nbytes].view(dt).reshape(shape)
+            Dv[name] = dbuf[offs[name]:offs[name] + nbytes].view(tdt[dt]).view(shape)
+        H["q"][...] = w.query()[:n].view(np.int16)
+        H["k"][...] = w.new_k()[:n].view(np.int16)
+        H["v"][...] = w.new_v()[:n].view(np.int16)
+        H["lens"][...] = self.lens_host
+        self._host = {"hbuf": hbuf, "dbuf": dbuf, "H": H,
+                      "q": Dv["q"].view(torch.bfloat16), "k": Dv["k"].view(torch.bfloat16),
+                      "v": Dv["v"].view(torch.bfloat16), "tables": Dv["tables"], "lens": Dv["lens"],
+                      "slots": Dv["slots"], "out": torch.empty(n, w.Hq, w.D, dtype=torch.int16).pin_memory()}
 
     def step_host(self, stream=None):
-        """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The allocator rebuilds the block
-        tables and the slot mapping, inputs go up from pinned memory, the output comes back."""
+        """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The allocator writes the block
+        tables and the slot mapping into the pinned staging buffer, one copy takes every input
+        to the device, the fused step runs, and the output comes back."""
         torch, w, a = self.torch, self.w, self.pool.allocator
         if self._host is None:
             self._prepare_host()
-        H = self._host
+        X = self._host
+        H = X["H"]
         n = self.batch
-        H["tables"].numpy()[...] = pkv_get_block_tables(a, w.seq_ids[:n], self.max_blocks)
+        pkv_get_block_tables(a, w.seq_ids[:n], self.max_blocks, out=H["tables"])
         if w.append:
-            H["slots"].numpy()[...] = pkv_slot_mapping(a, w.seq_ids[:n], w.lens[:n])
-        self.q.view(torch.int16).copy_(H["q"], non_blocking=True)
-        self.lens.copy_(H["lens"], non_blocking=True)
-        self.tables.copy_(H["tables"], non_blocking=True)
-        h2d = H["q"].numel() * 2 + H["lens"].numel() * 4 + H["tables"].numel() * 4
+            pkv_slot_mapping(a, w.seq_ids[:n], w.lens[:n], out=H["slots"])
+        X["dbuf"].copy_(X["hbuf"], non_blocking=True)
         if w.append:
-            self.k_new.view(torch.int16).copy_(H["k"], non_blocking=True)
-            self.v_new.view(torch.int16).copy_(H["v"], non_blocking=True)
-            self.slots_new.copy_(H["slots"], non_blocking=True)
-            h2d += H["k"].numel() * 2 + H["v"].numel() * 2 + H["slots"].numel() * 8
-        self.step(stream)
-        H["out"].copy_(self.out.view(torch.int16), non_blocking=True)
+            pkv_decode_step(self.pool.handle, X["k"], X["v"], X["slots"], X["q"], X["tables"], X["lens"], self.scale,
+                            self.out, self.workspace, stream)
+        else:
+            pkv_decode_attention(self.pool.handle, X["q"], X["tables"], X["lens"], self.scale, self.out,
+                                 self.workspace, stream)
+        X["out"].copy_(self.out.view(torch.int16), non_blocking=True)
         torch.cuda.current_stream().synchronize()
-        return h2d, H["out"].numel() * 2
+        return X["hbuf"].numel(), X["out"].numel() * 2
 
     def out_host(self) -> np.ndarray:
         return self.out.view(self.torch.int16).cpu().numpy().view(np.uint16)

@@ -108,6 +108,25 @@ def test_fused_step_equals_separate_calls(pkv, name):
     b.close()
 
 
+@pytest.mark.parametrize("name", ["c0", "c4"])
+def test_host_to_host_step_equals_device_step(pkv, name):
+    """The end-to-end step (allocator tables and slots into a pinned staging buffer, one copy to
+    the device, fused step, output copied back) gives the device-resident step's output."""
+    import torch
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    w = W.make_workload(name)
+    step = DecodeStep(w)
+    step.step()
+    torch.cuda.synchronize()
+    want = step.out_host().copy()
+    for _ in range(2):
+        h2d, d2h = step.step_host()
+        assert h2d > 0 and d2h == want.size * 2
+        got = step._host["out"].numpy().view(np.uint16)
+        assert np.array_equal(got, want)
+    step.close()
+
+
 def test_empty_and_single_token_contexts(pkv):
     w = W.custom_workload(300, 6, 8, 2, 128, 64, [0, 1, 0, 17, 64, 65], append=False)
     step = _run(pkv, w)
