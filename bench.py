@@ -343,6 +343,52 @@ def run_pkv(args, world, rank, local):
     step.close()
 
 
+def run_loop(args, world, rank, local):
+    """In-flight batching decode loop (one layer, Llama-3-8B shapes): sequences finish and join
+    every step, blocks grow on demand, each step is a graph-replayed host-to-host decode step."""
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+    from paged_kv_cache_266_gb300 import pkv_check_device_error
+    from paged_kv_cache_266_gb300.engine import DecodeLoop
+    torch.cuda.set_device(local)
+    n = args.warmup + args.steps
+    sc = W.make_loop_script(index=50, n_steps=n, max_batch=args.loop_batch, Hq=32, Hkv=8, D=128, block_size=64,
+                            kv_dtype="bf16", prompt_lo=128, prompt_hi=2048, p_finish=0.01)
+    inputs = [sc.step_inputs(t, range(sc.max_batch)) for t in range(n)]
+    # joining sequences' prompt K/V staged on the device beforehand (their prefill's output)
+    dev = f"cuda:{local}"
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    prompts = {s: tuple(map(to_dev, sc.prompt_kv(s, m))) for _, joined in sc.steps for s, m in joined if m}
+    loop = DecodeLoop(sc, graphs=True, device=dev, prompts=prompts)
+    for t in range(args.warmup):
+        loop.step(inputs[t])
+    loop.timing = {k: 0.0 for k in loop.timing}
+    kv_bytes, tokens = 0, 0
+    dist_barrier(world)
+    t0 = time.perf_counter()
+    for t in range(args.warmup, n):
+        run, _ = loop.step(inputs[t])
+        tokens += len(run)
+        kv_bytes += sum(loop.lens[s] for s in run) * sc.Hkv * 2 * sc.D * 2
+    dt = dist_max(time.perf_counter() - t0, world)
+    if pkv_check_device_error(loop.pool.handle) != 0:
+        raise RuntimeError("device error flag set in the decode loop")
+    if rank == 0:
+        K = args.steps
+        print(json.dumps({
+            "metric": "in-flight decode loop (one layer): decode tokens/s, KV GB/s", "value": round(world * tokens / dt, 1),
+            "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "kv_gbs": round(world * kv_bytes / dt / 1e9, 1), "data": "synthetic",
+            "config": {"workload": sc.name, "batch": sc.max_batch, "q_heads": sc.Hq, "kv_heads": sc.Hkv, "head_dim": sc.D,
+                       "block_size": sc.block_size, "prompts": "U[128,2048]", "finish_prob_per_step": 0.01,
+                       "joined": sum(len(j) for _, j in sc.steps[args.warmup:]), "graphs": "one per batch bucket"},
+            "host_ms_per_step": {k: round(v / K * 1e3, 4) for k, v in loop.timing.items()},
+        }), flush=True)
+    loop.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -354,12 +400,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--seqs", type=int, default=0, help="profiling: step over the first N sequences only")
+    ap.add_argument("--loop", action="store_true", help="measure the in-flight decode loop instead of one step")
+    ap.add_argument("--loop-batch", type=int, default=128)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.loop:
+        run_loop(args, world, rank, local)
     else:
         run_pkv(args, world, rank, local)
     if world > 1:

@@ -79,6 +79,12 @@ pkv_status pkv_allocator_set_free_order(pkv_allocator* a, const int32_t* order_h
  * too short; then neither the sequence nor the free list changes. */
 pkv_status pkv_seq_reserve(pkv_allocator* a, int64_t seq_id, int64_t n_tokens);
 
+/* pkv_seq_reserve for count sequences in order (one decode step grows every running sequence
+ * by a token).  Stops at the first failure: returns its status and, in *done, how many
+ * reservations succeeded (those stay in place). */
+pkv_status pkv_seq_reserve_many(pkv_allocator* a, const int64_t* seq_ids_host, const int64_t* n_tokens_host,
+                                int64_t count, int64_t* done);
+
 /* Return all of seq_id's blocks to the free list (appended in table order) and forget it. */
 pkv_status pkv_seq_release(pkv_allocator* a, int64_t seq_id);
 

@@ -42,3 +42,44 @@ def attention(w, pool, tables, threads: int | None = None, seqs=None) -> np.ndar
         seqs = np.asarray(seqs)
         q, tables, lens = q[seqs], tables[seqs], lens[seqs]
     return pool.attention(q, tables, lens, w.Hq, 1.0 / math.sqrt(w.D), threads=threads or os.cpu_count() or 1)
+
+
+def run_loop(script, n_steps: int | None = None, threads: int | None = None):
+    """Replay a decode-loop schedule (finished sequences release their pages, joiners get their
+    prompt appended, every running sequence appends one token and attends).  Yields, per step,
+    (running sequence ids, fp64 output [B][Hq][D]); the pool replica is returned last."""
+    from . import Allocator, Pool
+    sc = script
+    alloc = Allocator(sc.num_blocks, sc.block_size)
+    pool = Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, sc.kv_dtype == "fp8_e4m3")
+    max_blocks = -(-sc.max_len // sc.block_size)
+    lens, running = {}, []
+    steps = sc.steps if n_steps is None else sc.steps[:n_steps]
+    outs = []
+    for t, (finished, joined) in enumerate(steps):
+        for s in finished:
+            if alloc.release(s):
+                raise RuntimeError("oracle loop: release failed")
+            running.remove(s)
+            del lens[s]
+        for s, n in joined:
+            if alloc.reserve(s, n):
+                raise RuntimeError("oracle loop: out of pages")
+            if n:
+                k, v = sc.prompt_kv(s, n)
+                pool.append(k, v, alloc.slot_mapping([s] * n, np.arange(n)))
+            lens[s] = n
+            running.append(s)
+        for s in running:
+            if alloc.reserve(s, lens[s] + 1):
+                raise RuntimeError("oracle loop: out of pages")
+        k, v, q = sc.step_inputs(t, running)
+        pos = np.array([lens[s] for s in running], dtype=np.int64)
+        pool.append(k, v, alloc.slot_mapping(running, pos))
+        tables = alloc.block_tables(running, max_blocks)
+        out = pool.attention(q, tables, (pos + 1).astype(np.int32), sc.Hq, 1.0 / math.sqrt(sc.D),
+                             threads=threads or os.cpu_count() or 1)
+        for s in running:
+            lens[s] += 1
+        outs.append((list(running), out))
+    return outs, pool

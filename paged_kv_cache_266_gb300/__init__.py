@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "library_path",
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
-    "pkv_seq_release", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
+    "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
@@ -58,6 +58,7 @@ def _L():
         "pkv_allocator_set_free_order": (i32, [vp, vp, i32]),
         "pkv_seq_reserve": (i32, [vp, i64, i64]),
         "pkv_seq_release": (i32, [vp, i64]),
+        "pkv_seq_reserve_many": (i32, [vp, vp, vp, i64, P(i64)]),
         "pkv_seq_num_blocks": (i32, [vp, i64, P(i32)]),
         "pkv_num_free_blocks": (i32, [vp, P(i32)]),
         "pkv_free_list": (i32, [vp, vp, i32, P(i32)]),
@@ -131,6 +132,15 @@ def pkv_allocator_set_free_order(a: int, order) -> None:
 
 def pkv_seq_reserve(a: int, seq_id: int, n_tokens: int) -> None:
     _check(_L().pkv_seq_reserve(a, seq_id, n_tokens), "pkv_seq_reserve")
+
+
+def pkv_seq_reserve_many(a: int, seq_ids, n_tokens) -> None:
+    s, n = _np(seq_ids, np.int64), _np(n_tokens, np.int64)
+    if s.shape != n.shape:
+        raise ValueError("seq_ids and n_tokens must have the same length")
+    done = ctypes.c_int64()
+    _check(_L().pkv_seq_reserve_many(a, s.ctypes.data, n.ctypes.data, len(s), ctypes.byref(done)),
+           f"pkv_seq_reserve_many (after {done.value} reservations)")
 
 
 def pkv_seq_release(a: int, seq_id: int) -> None:

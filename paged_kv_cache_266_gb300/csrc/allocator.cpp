@@ -87,6 +87,19 @@ pkv_status pkv_seq_reserve(pkv_allocator* a, int64_t seq_id, int64_t n_tokens) {
     return PKV_OK;
 }
 
+pkv_status pkv_seq_reserve_many(pkv_allocator* a, const int64_t* seq_ids, const int64_t* n_tokens, int64_t count,
+                                int64_t* done) {
+    if (!a || count < 0 || (count > 0 && (!seq_ids || !n_tokens))) return PKV_ERR_INVALID_ARG;
+    int64_t i = 0;
+    pkv_status st = PKV_OK;
+    for (; i < count; ++i) {
+        st = pkv_seq_reserve(a, seq_ids[i], n_tokens[i]);
+        if (st != PKV_OK) break;
+    }
+    if (done) *done = i;
+    return st;
+}
+
 pkv_status pkv_seq_release(pkv_allocator* a, int64_t seq_id) {
     if (!a) return PKV_ERR_INVALID_ARG;
     auto it = a->tables.find(seq_id);

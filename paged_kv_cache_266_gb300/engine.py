@@ -1,0 +1,176 @@
+"""In-flight batching decode loop for one attention layer over a paged pool.
+
+"TensorRT-LLM 深度实战" (chenxutan.com), §3.2 (continuous / in-flight batching): every step
+finished sequences leave and release their pages (§3.1 release), waiting ones join, and the
+running batch takes one forward step.  "TensorRT-LLM 推理加速实战" (socake.github.io), §7.1:
+decode steps are launch-bound at small batch and are replayed from CUDA graphs, one graph per
+batch-size bucket because a graph is fixed to its shapes.
+
+Each step here:
+  1. releases the finished sequences' blocks (pkv_seq_release);
+  2. admits joining sequences: blocks for their prompt (pkv_seq_reserve) and the prompt's K/V
+     written with pkv_append (prefill attention itself is not part of this library);
+  3. gives every running sequence room for one more token (pkv_seq_reserve grows by whole
+     blocks), writes block tables, new-token slots and context lengths straight into a pinned
+     staging buffer together with the step's q / new K / new V;
+  4. runs, on the batch padded to its bucket, one host-to-device copy, pkv_decode_step (append +
+     attention) and the copy of the output back — captured once per bucket as a CUDA graph and
+     replayed.  Padding rows have context length 0 and slot -1, so they write nothing and read
+     nothing; their outputs are zeros.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
+               pkv_get_block_tables, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many, pkv_slot_mapping)
+
+DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
+
+
+class _Bucket:
+    """Device buffers, pinned staging and (optionally) the captured graph for one batch size."""
+
+    def __init__(self, torch, loop, Bp: int, device):
+        sc = loop.script
+        self.Bp = Bp
+        parts = [("q", (Bp, sc.Hq, sc.D), np.int16), ("k", (Bp, sc.Hkv, sc.D), np.int16),
+                 ("v", (Bp, sc.Hkv, sc.D), np.int16), ("tables", (Bp, loop.max_blocks), np.int32),
+                 ("lens", (Bp,), np.int32), ("slots", (Bp,), np.int64)]
+        offs, total = {}, 0
+        for name, shape, dt in parts:
+            offs[name] = total
+            total += (int(np.prod(shape)) * np.dtype(dt).itemsize + 255) // 256 * 256
+        self.hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dbuf = torch.empty(total, dtype=torch.uint8, device=device)
+        tdt = {np.int16: torch.int16, np.int32: torch.int32, np.int64: torch.int64}
+        hnp = self.hbuf.numpy()
+        self.H, self.Dv = {}, {}
+        for name, shape, dt in parts:
+            nbytes = int(np.prod(shape)) * np.dtype(dt).itemsize
+            self.H[name] = hnp[offs[name]:offs[name] + nbytes].view(dt).reshape(shape)
+            self.Dv[name] = self.dbuf[offs[name]:offs[name] + nbytes].view(tdt[dt]).view(shape)
+        self.q = self.Dv["q"].view(torch.bfloat16)
+        self.k = self.Dv["k"].view(torch.bfloat16)
+        self.v = self.Dv["v"].view(torch.bfloat16)
+        self.out = torch.zeros(Bp, sc.Hq, sc.D, dtype=torch.bfloat16, device=device)
+        self.out_host = torch.empty(Bp, sc.Hq, sc.D, dtype=torch.int16).pin_memory()
+        ws = pkv_decode_workspace_bytes(loop.pool.handle, Bp, sc.Hq, loop.max_blocks)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+        self.graph = None
+
+    def run(self, torch, loop):
+        """Copy the staged inputs in, run the fused step, copy the output out (no sync)."""
+        self.dbuf.copy_(self.hbuf, non_blocking=True)
+        pkv_decode_step(loop.pool.handle, self.k, self.v, self.Dv["slots"], self.q, self.Dv["tables"],
+                        self.Dv["lens"], loop.scale, self.out, self.workspace)
+        self.out_host.copy_(self.out.view(torch.int16), non_blocking=True)
+
+
+class DecodeLoop:
+    def __init__(self, script, graphs: bool = True, buckets=DEFAULT_BUCKETS, device: str = "cuda",
+                 prompts=None):
+        """prompts: optional {seq_id: (k, v)} of device bf16 tensors [n][Hkv][D] (a joining
+        sequence's prompt K/V as its prefill produced them); else drawn from the script."""
+        import torch
+        self.prompts = prompts or {}
+        self.torch, self.script, self.graphs, self.device = torch, script, graphs, device
+        fp8 = script.kv_dtype == "fp8_e4m3"
+        self.pool = KVPool(script.num_blocks, script.block_size, script.Hkv, script.D,
+                           PKV_KV_FP8_E4M3 if fp8 else PKV_KV_BF16)
+        self.alloc = self.pool.allocator
+        self.max_blocks = -(-script.max_len // script.block_size)
+        self.scale = 1.0 / math.sqrt(script.D)
+        self.buckets = sorted(buckets)
+        self._bk = {}
+        self.lens: dict[int, int] = {}
+        self.running: list[int] = []
+        self.t = 0
+        self.timing = {"admit_s": 0.0, "prepare_s": 0.0, "device_s": 0.0}  # host wall time per phase
+
+    def _bucket(self, B: int) -> _Bucket:
+        Bp = next((b for b in self.buckets if b >= B), None)
+        if Bp is None:
+            raise ValueError(f"batch {B} exceeds the largest bucket {self.buckets[-1]}")
+        if Bp not in self._bk:
+            self._bk[Bp] = _Bucket(self.torch, self, Bp, self.device)
+        return self._bk[Bp]
+
+    def _admit(self, seq: int, n: int):
+        torch = self.torch
+        pkv_seq_reserve(self.alloc, seq, n)
+        if n:
+            slots = pkv_slot_mapping(self.alloc, [seq] * n, np.arange(n, dtype=np.int64))
+            if seq in self.prompts:
+                dk, dv = self.prompts[seq]
+            else:
+                k, v = self.script.prompt_kv(seq, n)
+                dk = torch.from_numpy(np.ascontiguousarray(k).view(np.int16)).view(torch.bfloat16).to(self.device)
+                dv = torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).to(self.device)
+            pkv_append(self.pool.handle, dk, dv, torch.from_numpy(slots).to(self.device, non_blocking=True))
+        self.lens[seq] = n
+        self.running.append(seq)
+
+    def step(self, inputs=None):
+        """Run the next scheduled step; returns (running sequence ids, output [B][Hq][D] bf16 bits).
+        inputs: optional (k_new, v_new, q) for the running sequences (else drawn from the script)."""
+        import time
+        torch, sc = self.torch, self.script
+        t0 = time.perf_counter()
+        finished, joined = sc.steps[self.t]
+        for s in finished:
+            pkv_seq_release(self.alloc, s)
+            self.running.remove(s)
+            del self.lens[s]
+        for s, n in joined:
+            self._admit(s, n)
+        t1 = time.perf_counter()
+        run = list(self.running)
+        B = len(run)
+        pos = np.array([self.lens[s] for s in run], dtype=np.int64)
+        pkv_seq_reserve_many(self.alloc, run, pos + 1)  # room for this step's token
+        bk = self._bucket(B)
+        H = bk.H
+        k, v, q = inputs if inputs is not None else sc.step_inputs(self.t, run)
+        H["q"][:B] = q.view(np.int16)
+        H["k"][:B] = k.view(np.int16)
+        H["v"][:B] = v.view(np.int16)
+        H["q"][B:] = 0
+        H["k"][B:] = 0
+        H["v"][B:] = 0
+        pkv_get_block_tables(self.alloc, run, self.max_blocks, out=H["tables"][:B])
+        H["tables"][B:] = -1
+        pkv_slot_mapping(self.alloc, run, pos, out=H["slots"][:B])
+        H["slots"][B:] = -1
+        H["lens"][:B] = pos + 1
+        H["lens"][B:] = 0
+        t2 = time.perf_counter()
+        if self.graphs:
+            if bk.graph is None:
+                bk.run(torch, self)  # warm-up outside capture (builds plans, loads modules)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        bk.run(torch, self)
+                torch.cuda.current_stream().wait_stream(side)
+                bk.graph = g
+            bk.graph.replay()
+        else:
+            bk.run(torch, self)
+        torch.cuda.current_stream().synchronize()
+        t3 = time.perf_counter()
+        self.timing["admit_s"] += t1 - t0
+        self.timing["prepare_s"] += t2 - t1
+        self.timing["device_s"] += t3 - t2
+        for s in run:
+            self.lens[s] += 1
+        self.t += 1
+        return run, bk.out_host.numpy()[:B].view(np.uint16).copy()
+
+    def close(self):
+        self.pool.close()

@@ -324,3 +324,85 @@ def truncated(w: Workload, n: int) -> Workload:
     t.seq_ids = w.seq_ids[:n]
     t.name = f"{w.name}[:{n}]"
     return t
+
+
+# ----------------------------------------------------------------------------- decode loop
+TAG_LOOP_SCHED, TAG_LOOP_PROMPT_K, TAG_LOOP_PROMPT_V, TAG_LOOP_K, TAG_LOOP_V, TAG_LOOP_Q = range(20, 26)
+
+
+@dataclass
+class LoopScript:
+    """A seeded schedule of in-flight-batching decode steps ("TensorRT-LLM 深度实战", §3.2: each
+    step removes finished sequences, admits waiting ones and runs one forward pass).
+
+    steps[t] = (finished, joined): sequence ids leaving before step t and (seq_id, prompt_len)
+    pairs admitted before step t.  Every running sequence then appends one token and attends.
+    Tensors are drawn per (sequence, position) / (step, row) so both sides read the same bytes."""
+    name: str
+    seed: int
+    Hq: int
+    Hkv: int
+    D: int
+    block_size: int
+    kv_dtype: str
+    num_blocks: int
+    max_batch: int
+    steps: list
+    max_len: int
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    def prompt_kv(self, seq_id: int, n: int):
+        """History K and V ([n][Hkv][D] bf16 bits) of a joining sequence's prompt."""
+        row = self.Hkv * self.D
+        off = seq_id * self.max_len * row
+        k = normal_bf16(stream_seed(self.seed, TAG_LOOP_PROMPT_K), off, n * row).reshape(n, self.Hkv, self.D)
+        v = normal_bf16(stream_seed(self.seed, TAG_LOOP_PROMPT_V), off, n * row).reshape(n, self.Hkv, self.D)
+        return k, v
+
+    def step_inputs(self, t: int, running):
+        """(k_new, v_new, q) of step t for the running sequences, in their order (row i of step t
+        is drawn from the block of the stream reserved for that step and row)."""
+        n = len(running)
+        row_kv, row_q = self.Hkv * self.D, self.Hq * self.D
+        k = normal_bf16(stream_seed(self.seed, TAG_LOOP_K), t * self.max_batch * row_kv, n * row_kv)
+        v = normal_bf16(stream_seed(self.seed, TAG_LOOP_V), t * self.max_batch * row_kv, n * row_kv)
+        q = normal_bf16(stream_seed(self.seed, TAG_LOOP_Q), t * self.max_batch * row_q, n * row_q)
+        return k.reshape(n, self.Hkv, self.D), v.reshape(n, self.Hkv, self.D), q.reshape(n, self.Hq, self.D)
+
+
+def make_loop_script(index: int = 40, n_steps: int = 32, max_batch: int = 24, Hq: int = 8, Hkv: int = 2, D: int = 128,
+                     block_size: int = 16, kv_dtype: str = "bf16", prompt_lo: int = 1, prompt_hi: int = 300,
+                     p_finish: float = 0.12, num_blocks: int | None = None) -> LoopScript:
+    """Seeded churn: each step every running sequence finishes with probability p_finish, then new
+    sequences (prompt lengths U[prompt_lo, prompt_hi]) fill the batch back to max_batch.  The
+    pool is sized so that the script never runs out of blocks."""
+    seed = 266 * 1000 + index
+    s = stream_seed(seed, TAG_LOOP_SCHED)
+    draw = 0
+    running, lens, steps, next_id, peak = [], {}, [], 0, 0
+    for t in range(n_steps):
+        finished = []
+        for sid in list(running):
+            if unit(s, draw) < p_finish:
+                finished.append(sid)
+                running.remove(sid)
+                del lens[sid]
+            draw += 1
+        joined = []
+        while len(running) < max_batch:
+            n = uniform_int(s, draw, prompt_lo, prompt_hi)
+            draw += 1
+            joined.append((next_id, n))
+            running.append(next_id)
+            lens[next_id] = n
+            next_id += 1
+        steps.append((finished, joined))
+        for sid in running:
+            lens[sid] += 1
+        peak = max(peak, sum(_ceil_div(L, block_size) for L in lens.values()))
+    max_len = prompt_hi + n_steps + 1
+    nb = num_blocks or peak + 8
+    return LoopScript(f"loop{index}", seed, Hq, Hkv, D, block_size, kv_dtype, nb, max_batch, steps, max_len)

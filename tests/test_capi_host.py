@@ -164,3 +164,26 @@ def test_allocator_errors(pkv):
     with pytest.raises(pkv.PKVError):
         pkv.pkv_allocator_set_free_order(a, [0, 1, 1, 3])  # not a permutation
     pkv.pkv_allocator_destroy(a)
+
+
+def test_reserve_many_equals_sequential_reserves(pkv):
+    rng = np.random.default_rng(3)
+    a = pkv.pkv_allocator_create(64, 16)
+    o = oracle.Allocator(64, 16)
+    seqs = np.arange(10, dtype=np.int64)
+    toks = rng.integers(0, 60, 10)
+    pkv.pkv_seq_reserve_many(a, seqs, toks)
+    for s, n in zip(seqs, toks):
+        assert o.reserve(int(s), int(n)) == 0
+    _same_state(pkv, a, o, set(seqs.tolist()))
+    # growth for every sequence, then one that cannot fit: earlier ones stay, the call reports OOM
+    grow = toks + 16
+    big = np.array(grow)
+    big[5] = 10_000
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.pkv_seq_reserve_many(a, seqs, big)
+    assert e.value.status == pkv.PKV_ERR_OOM and "after 5 reservations" in str(e.value)
+    for s in range(5):
+        assert o.reserve(int(seqs[s]), int(grow[s])) == 0
+    _same_state(pkv, a, o, set(seqs.tolist()))
+    pkv.pkv_allocator_destroy(a)
