@@ -57,6 +57,9 @@ def _L():
         "oracle_alloc_free_list": (None, [vp, vp]),
         "oracle_alloc_block_tables": (i32, [vp, vp, i32, i32, vp]),
         "oracle_alloc_slot_mapping": (i32, [vp, vp, vp, i64, vp]),
+        "oracle_alloc_share_prefix": (i32, [vp, i64, i64, i64, vp, vp]),
+        "oracle_alloc_holders": (i32, [vp, i32]),
+        "oracle_copy_block": (None, [vp, vp, i32, i32, i32, i32, i64, i64]),
         "oracle_m_kv": (f64, [f64] * 6),
         "oracle_e4m3_decode": (f64, [ctypes.c_uint8]),
         "oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
@@ -137,6 +140,15 @@ class Allocator:
             raise RuntimeError(f"oracle slot_mapping rc={rc}")
         return out
 
+    def share_prefix(self, src: int, dst: int, n_tokens: int):
+        """(status, cow_src, cow_dst); see oracle_alloc_share_prefix."""
+        cs, cd = ctypes.c_int32(), ctypes.c_int32()
+        rc = _L().oracle_alloc_share_prefix(self._h, src, dst, n_tokens, ctypes.byref(cs), ctypes.byref(cd))
+        return rc, cs.value, cd.value
+
+    def holders(self, page: int) -> int:
+        return _L().oracle_alloc_holders(self._h, page)
+
     def replay(self, ops) -> None:
         """Run an allocation script of ("reserve", seq, tokens) / ("release", seq) ops."""
         for op in ops:
@@ -184,6 +196,9 @@ class Pool:
         self.data = np.zeros(_L().oracle_pool_bytes(num_blocks, block_size, n_kv_heads, head_dim, self.fp8),
                              dtype=np.uint8)
         self.scales = np.zeros(_L().oracle_scale_floats(num_blocks, n_kv_heads), dtype=np.float32)
+
+    def copy_block(self, src: int, dst: int) -> None:
+        _L().oracle_copy_block(_p(self.data), _p(self.scales), self.bs, self.Hkv, self.D, self.fp8, src, dst)
 
     def elem_byte(self, blk, kv, h, t, d) -> int:
         return _L().oracle_elem_byte(blk, kv, h, t, d, self.bs, self.Hkv, self.D, self.fp8)

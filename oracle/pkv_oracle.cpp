@@ -51,6 +51,7 @@ struct Allocator {
     int block_size;
     std::vector<int32_t> free_pages;                          // pop() from the back
     std::unordered_map<int64_t, std::vector<int32_t>> table;  // seq -> pages
+    std::vector<int> holders;                                 // sequences holding each page
 };
 
 double bf16_to_double(uint16_t b) {
@@ -70,6 +71,7 @@ void* oracle_alloc_new(int num_blocks, int block_size) {
     a->num_blocks = num_blocks;
     a->block_size = block_size;
     for (int i = 0; i < num_blocks; ++i) a->free_pages.push_back(i);
+    a->holders.assign(num_blocks, 0);
     return a;
 }
 
@@ -102,6 +104,7 @@ int oracle_alloc_reserve(void* p, int64_t seq, int64_t n_tokens) {
     std::vector<int32_t>& pages = a->table[seq];
     for (int64_t i = 0; i < need; ++i) {
         pages.push_back(a->free_pages.back());
+        a->holders[a->free_pages.back()] = 1;
         a->free_pages.pop_back();
     }
     return 0;
@@ -111,10 +114,48 @@ int oracle_alloc_release(void* p, int64_t seq) {
     Allocator* a = (Allocator*)p;
     auto it = a->table.find(seq);
     if (it == a->table.end()) return 3;
-    for (int32_t page : it->second) a->free_pages.push_back(page);
+    // a page goes back to the free list when its last holder lets go (pages in table order)
+    for (int32_t page : it->second) {
+        a->holders[page] -= 1;
+        if (a->holders[page] == 0) a->free_pages.push_back(page);
+    }
     a->table.erase(it);
     return 0;
 }
+
+// Block reuse (pnsm.cn page §3.1 enable_block_reuse; "TensorRT-LLM 推理加速实战" §8 KV cache reuse,
+// like prefix caching), in this reading: dst starts with src's first n tokens; src's full pages
+// among them are shared; a prefix ending inside a page gets a fresh page that the caller fills
+// with a copy of src's page.  Returns 0, 3 (no src), 1 (dst exists), 4 (n beyond src), 2 (no page).
+int oracle_alloc_share_prefix(void* p, int64_t src, int64_t dst, int64_t n, int32_t* cow_src, int32_t* cow_dst) {
+    Allocator* a = (Allocator*)p;
+    auto it = a->table.find(src);
+    if (it == a->table.end()) return 3;
+    if (a->table.count(dst) || src == dst) return 1;
+    if (n < 0 || n > (int64_t)it->second.size() * a->block_size) return 4;
+    int64_t full = n / a->block_size;
+    bool partial = n % a->block_size != 0;
+    if (partial && a->free_pages.empty()) return 2;
+    std::vector<int32_t> pages;
+    for (int64_t k = 0; k < full; ++k) {
+        pages.push_back(it->second[k]);
+        a->holders[it->second[k]] += 1;
+    }
+    *cow_src = -1;
+    *cow_dst = -1;
+    if (partial) {
+        int32_t page = a->free_pages.back();
+        a->free_pages.pop_back();
+        a->holders[page] = 1;
+        *cow_src = it->second[full];
+        *cow_dst = page;
+        pages.push_back(page);
+    }
+    a->table[dst] = pages;
+    return 0;
+}
+
+int oracle_alloc_holders(void* p, int32_t page) { return ((Allocator*)p)->holders[page]; }
 
 int oracle_alloc_num_free(void* p) { return (int)((Allocator*)p)->free_pages.size(); }
 
@@ -460,6 +501,13 @@ int oracle_decode_attention_split(const uint8_t* pool, const float* scales, int 
             }
         }
     return 0;
+}
+
+// Copy page src's K, V (all heads) and fp8 scales onto page dst of the host pool replica.
+void oracle_copy_block(uint8_t* pool, float* scales, int bs, int Hkv, int D, int fp8, int64_t src, int64_t dst) {
+    int64_t block_bytes = (int64_t)2 * Hkv * bs * D * (fp8 ? 1 : 2);
+    std::memcpy(pool + dst * block_bytes, pool + src * block_bytes, (size_t)block_bytes);
+    if (fp8) std::memcpy(scales + dst * Hkv * 4, scales + src * Hkv * 4, sizeof(float) * Hkv * 4);
 }
 
 // Pool geometry helpers for callers that size host replicas.
