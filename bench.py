@@ -389,6 +389,82 @@ def run_loop(args, world, rank, local):
     loop.close()
 
 
+def run_prefix(args, world, rank, local):
+    """Block reuse: 128 children of one 2048-token prompt (Llama-3-8B layer shapes, block 64), each
+    with its own U[128,2048] suffix.  The same decode step is timed over the shared pool and over
+    an unshared pool holding the same logical contexts; L2 is flushed before every timed step."""
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    from paged_kv_cache_266_gb300.runner import PrefixDecode
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    sc = W.make_prefix_script()
+    row = sc.Hkv * 2 * sc.D * 2
+    logical = int(sc.attend_lens.sum()) * row
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    K = max(3, min(args.steps, 500))
+    res = {}
+    sampler = ClockSampler(local)
+    sampler.start()
+    for share in (True, False):
+        st = PrefixDecode(sc, share=share, device=dev)
+        for _ in range(args.warmup):
+            st.step()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush.zero_()
+            e0[k].record(stream)
+            st.step()
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+        if pkv.pkv_check_device_error(st.pool.handle) != 0:
+            raise RuntimeError("device error flag set in the timed region")
+        ms = dist_max(statistics.mean(e0[k].elapsed_time(e1[k]) for k in range(K)), world)
+        res[share] = {"ms_per_step": ms, "blocks": st.blocks_held, "cow_copies": st.cow_copies}
+        st.close()
+    clocks = sampler.stop()
+    # host cost of forking: B shares of the P-token prefix on a fresh allocator
+    a = pkv.pkv_allocator_create(sc.num_blocks, sc.block_size)
+    pkv.pkv_seq_reserve(a, sc.parent, sc.P)
+    t0 = time.perf_counter()
+    for b in range(sc.B):
+        pkv.pkv_seq_share_prefix(a, sc.parent, b, sc.P)
+    fork_us = (time.perf_counter() - t0) / sc.B * 1e6
+    pkv.pkv_allocator_destroy(a)
+    if rank != 0:
+        return
+    sh, un = res[True], res[False]
+    peak, peak_kind = measured_peaks()
+    unique = sh["blocks"] * sc.block_size * row
+    print(json.dumps({
+        "metric": "shared-prefix decode step: logical KV bytes attended per second", "value":
+        round(world * logical / (sh["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(sh["ms_per_step"], 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32-accumulate on bf16 KV", "data": "synthetic",
+        "config": {"workload": sc.name, "description": "128 children of one 2048-token prompt, suffixes U[128,2048], "
+                   "Llama-3-8B layer shapes (32 q / 8 kv heads, head_dim 128), block 64", "batch": sc.B,
+                   "prefix_tokens": sc.P, "context_tokens": int(sc.attend_lens.sum()), "logical_kv_bytes": logical,
+                   "l2": "flushed before every timed step"},
+        "shared": {"blocks_held": sh["blocks"], "pool_bytes_held": unique, "cow_copies": sh["cow_copies"],
+                   "ms_per_step": round(sh["ms_per_step"], 5)},
+        "unshared": {"blocks_held": un["blocks"], "pool_bytes_held": un["blocks"] * sc.block_size * row,
+                     "ms_per_step": round(un["ms_per_step"], 5),
+                     "logical_gbs": round(world * logical / (un["ms_per_step"] * 1e-3) / 1e9, 2)},
+        "speedup_vs_unshared": round(un["ms_per_step"] / sh["ms_per_step"], 4),
+        "pct_of_hbm_peak_logical": round(100 * logical / (sh["ms_per_step"] * 1e-3) / 1e9 / peak, 2),
+        "peak": peak, "peak_kind": peak_kind,
+        "host_fork_us_per_child": round(fork_us, 3),
+        "gpu_launches": K * 2,
+        "clocks": clocks,
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,6 +478,7 @@ def main():
     ap.add_argument("--seqs", type=int, default=0, help="profiling: step over the first N sequences only")
     ap.add_argument("--loop", action="store_true", help="measure the in-flight decode loop instead of one step")
     ap.add_argument("--loop-batch", type=int, default=128)
+    ap.add_argument("--prefix", action="store_true", help="measure decode over children of a shared prompt prefix")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -410,6 +487,8 @@ def main():
         run_reference(args, world, rank)
     elif args.loop:
         run_loop(args, world, rank, local)
+    elif args.prefix:
+        run_prefix(args, world, rank, local)
     else:
         run_pkv(args, world, rank, local)
     if world > 1:

@@ -85,8 +85,24 @@ pkv_status pkv_seq_reserve(pkv_allocator* a, int64_t seq_id, int64_t n_tokens);
 pkv_status pkv_seq_reserve_many(pkv_allocator* a, const int64_t* seq_ids_host, const int64_t* n_tokens_host,
                                 int64_t count, int64_t* done);
 
-/* Return all of seq_id's blocks to the free list (appended in table order) and forget it. */
+/* Drop seq_id: each of its blocks loses one holder, and blocks left with none are appended to
+ * the free list in table order.  Forgets seq_id. */
 pkv_status pkv_seq_release(pkv_allocator* a, int64_t seq_id);
+
+/* Block reuse (the pages' enable_block_reuse / enable_kv_cache_reuse: a new request reuses the
+ * KV blocks of a cached prefix, "TensorRT-LLM 推理加速实战" §8).  New sequence dst_seq starts with
+ * the first n_tokens tokens of src_seq: src's first n_tokens / block_size blocks are shared
+ * (each gains a holder).  If n_tokens ends inside a block, dst gets a fresh block for it and
+ * *cow_src_block / *cow_dst_block name the block to copy (pkv_pool_copy_block) before dst
+ * appends; otherwise both are -1.  Appends to dst must start at position n_tokens, so no
+ * shared block is ever written.  PKV_ERR_NO_SEQ (src unknown), PKV_ERR_INVALID_ARG (dst exists
+ * or equals src), PKV_ERR_BOUNDS (n_tokens beyond src's capacity), PKV_ERR_OOM (no block for the
+ * copy); on error nothing changes. */
+pkv_status pkv_seq_share_prefix(pkv_allocator* a, int64_t src_seq, int64_t dst_seq, int64_t n_tokens,
+                                int32_t* cow_src_block, int32_t* cow_dst_block);
+
+/* Number of sequences holding `block` (0 = on the free list). */
+pkv_status pkv_block_refcount(const pkv_allocator* a, int32_t block, int* out);
 
 /* Number of blocks seq_id holds (PKV_ERR_NO_SEQ if unknown). */
 pkv_status pkv_seq_num_blocks(const pkv_allocator* a, int64_t seq_id, int* out);
@@ -136,6 +152,10 @@ pkv_status pkv_pool_allocator(pkv_pool* pool, pkv_allocator** out);
  * bf16 pools).  Ownership stays with the pool. */
 pkv_status pkv_pool_raw(const pkv_pool* pool, void** kv_dev, size_t* kv_bytes, float** scales_dev,
                         size_t* scale_bytes);
+
+/* Copy block src_block's K and V (every head) and, for fp8 pools, its scale records onto
+ * dst_block, asynchronously on `stream` (the copy-on-write step of pkv_seq_share_prefix). */
+pkv_status pkv_pool_copy_block(pkv_pool* pool, int32_t src_block, int32_t dst_block, pkv_stream_t stream);
 
 /* Synchronise the device, read and clear the pool's device error word.  Returns PKV_OK,
  * PKV_ERR_BOUNDS (a kernel saw an out-of-range block id, slot or context length and

@@ -18,7 +18,8 @@ from . import build as _build
 __all__ = [
     "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "library_path",
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
-    "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
+    "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_share_prefix", "pkv_block_refcount",
+    "pkv_pool_copy_block", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
@@ -59,6 +60,9 @@ def _L():
         "pkv_seq_reserve": (i32, [vp, i64, i64]),
         "pkv_seq_release": (i32, [vp, i64]),
         "pkv_seq_reserve_many": (i32, [vp, vp, vp, i64, P(i64)]),
+        "pkv_seq_share_prefix": (i32, [vp, i64, i64, i64, P(ctypes.c_int32), P(ctypes.c_int32)]),
+        "pkv_block_refcount": (i32, [vp, i32, P(i32)]),
+        "pkv_pool_copy_block": (i32, [vp, i32, i32, vp]),
         "pkv_seq_num_blocks": (i32, [vp, i64, P(i32)]),
         "pkv_num_free_blocks": (i32, [vp, P(i32)]),
         "pkv_free_list": (i32, [vp, vp, i32, P(i32)]),
@@ -143,6 +147,21 @@ def pkv_seq_reserve_many(a: int, seq_ids, n_tokens) -> None:
            f"pkv_seq_reserve_many (after {done.value} reservations)")
 
 
+def pkv_seq_share_prefix(a: int, src_seq: int, dst_seq: int, n_tokens: int):
+    """New sequence dst starts with src's first n_tokens; returns (cow_src_block, cow_dst_block),
+    both -1 when no block has to be copied."""
+    cs, cd = ctypes.c_int32(), ctypes.c_int32()
+    _check(_L().pkv_seq_share_prefix(a, src_seq, dst_seq, n_tokens, ctypes.byref(cs), ctypes.byref(cd)),
+           "pkv_seq_share_prefix")
+    return cs.value, cd.value
+
+
+def pkv_block_refcount(a: int, block: int) -> int:
+    n = ctypes.c_int()
+    _check(_L().pkv_block_refcount(a, block, ctypes.byref(n)), "pkv_block_refcount")
+    return n.value
+
+
 def pkv_seq_release(a: int, seq_id: int) -> None:
     _check(_L().pkv_seq_release(a, seq_id), "pkv_seq_release")
 
@@ -213,6 +232,10 @@ def pkv_pool_raw(pool: int):
     _check(_L().pkv_pool_raw(pool, ctypes.byref(kv), ctypes.byref(kvb), ctypes.byref(sc), ctypes.byref(scb)),
            "pkv_pool_raw")
     return kv.value, kvb.value, sc.value or 0, scb.value
+
+
+def pkv_pool_copy_block(pool: int, src_block: int, dst_block: int, stream=None) -> None:
+    _check(_L().pkv_pool_copy_block(pool, src_block, dst_block, _stream(stream)), "pkv_pool_copy_block")
 
 
 def pkv_check_device_error(pool: int) -> int:

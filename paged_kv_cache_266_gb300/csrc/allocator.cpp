@@ -6,6 +6,13 @@
 // tokens outgrow the capacity; a finished sequence's pages go back to the end of the list
 // in table order.  Out-of-memory is checked before anything is taken, so a failing call
 // changes nothing (the page's sketch leaks pages popped before it runs dry).
+//
+// Block reuse (pnsm.cn TensorRT-LLM page, §3.1 KV缓存优化: enable_block_reuse; "TensorRT-LLM
+// 推理加速实战" §8: KV Cache Reuse, enable_kv_cache_reuse, like prefix caching): a new sequence
+// may share another sequence's full prefix blocks.  Every block carries a reference count; a
+// shared prefix that ends inside a block gets a private copy of that block (copy on write), so
+// later appends never write a shared block; a block rejoins the free list when its count drops
+// to zero.
 #include <cstring>
 #include <new>
 #include <unordered_map>
@@ -17,6 +24,7 @@ struct pkv_allocator {
     int num_blocks = 0;
     int block_size = 0;
     std::vector<int32_t> free_list;  // back() is handed out next
+    std::vector<int32_t> refcnt;     // holders of each block; 0 = on the free list
     std::unordered_map<int64_t, std::vector<int32_t>> tables;
 };
 
@@ -31,6 +39,7 @@ pkv_allocator* allocator_new(int num_blocks, int block_size) {
     a->block_size = block_size;
     try {
         a->free_list.resize(num_blocks);
+        a->refcnt.assign(num_blocks, 0);
     } catch (...) {
         delete a;
         return nullptr;
@@ -82,6 +91,7 @@ pkv_status pkv_seq_reserve(pkv_allocator* a, int64_t seq_id, int64_t n_tokens) {
     tbl.reserve((size_t)(held + extra));
     for (int64_t i = 0; i < extra; ++i) {
         tbl.push_back(a->free_list.back());
+        a->refcnt[a->free_list.back()] = 1;
         a->free_list.pop_back();
     }
     return PKV_OK;
@@ -104,8 +114,42 @@ pkv_status pkv_seq_release(pkv_allocator* a, int64_t seq_id) {
     if (!a) return PKV_ERR_INVALID_ARG;
     auto it = a->tables.find(seq_id);
     if (it == a->tables.end()) return PKV_ERR_NO_SEQ;
-    a->free_list.insert(a->free_list.end(), it->second.begin(), it->second.end());
+    for (int32_t blk : it->second)
+        if (--a->refcnt[blk] == 0) a->free_list.push_back(blk);
     a->tables.erase(it);
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_share_prefix(pkv_allocator* a, int64_t src_seq, int64_t dst_seq, int64_t n_tokens,
+                                int32_t* cow_src_block, int32_t* cow_dst_block) {
+    if (!a || n_tokens < 0 || !cow_src_block || !cow_dst_block || src_seq == dst_seq) return PKV_ERR_INVALID_ARG;
+    auto src = a->tables.find(src_seq);
+    if (src == a->tables.end()) return PKV_ERR_NO_SEQ;
+    if (a->tables.count(dst_seq)) return PKV_ERR_INVALID_ARG;
+    const int64_t bs = a->block_size;
+    if (n_tokens > (int64_t)src->second.size() * bs) return PKV_ERR_BOUNDS;
+    const int64_t full = n_tokens / bs;
+    const bool partial = n_tokens % bs != 0;
+    if (partial && a->free_list.empty()) return PKV_ERR_OOM;
+    std::vector<int32_t> tbl(src->second.begin(), src->second.begin() + full);
+    for (int32_t blk : tbl) ++a->refcnt[blk];
+    *cow_src_block = -1;
+    *cow_dst_block = -1;
+    if (partial) {
+        const int32_t fresh = a->free_list.back();
+        a->free_list.pop_back();
+        a->refcnt[fresh] = 1;
+        *cow_src_block = src->second[(size_t)full];
+        *cow_dst_block = fresh;
+        tbl.push_back(fresh);
+    }
+    a->tables.emplace(dst_seq, std::move(tbl));
+    return PKV_OK;
+}
+
+pkv_status pkv_block_refcount(const pkv_allocator* a, int32_t block, int* out) {
+    if (!a || !out || block < 0 || block >= a->num_blocks) return PKV_ERR_INVALID_ARG;
+    *out = a->refcnt[block];
     return PKV_OK;
 }
 

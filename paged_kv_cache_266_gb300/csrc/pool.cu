@@ -202,6 +202,25 @@ pkv_status pkv_check_device_error(pkv_pool* pool) {
     return PKV_OK;
 }
 
+pkv_status pkv_pool_copy_block(pkv_pool* pool, int32_t src_block, int32_t dst_block, pkv_stream_t stream) {
+    if (!pool || src_block < 0 || dst_block < 0 || src_block >= pool->num_blocks || dst_block >= pool->num_blocks)
+        return PKV_ERR_INVALID_ARG;
+    if (src_block == dst_block) return PKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t block_bytes = pool->kv_bytes / (size_t)pool->num_blocks;  // K and V of every head
+    uint8_t* kv = static_cast<uint8_t*>(pool->kv);
+    if (cudaMemcpyAsync(kv + (size_t)dst_block * block_bytes, kv + (size_t)src_block * block_bytes, block_bytes,
+                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (pool->scales) {
+        const size_t rec = (size_t)pool->n_kv_heads * 4;  // floats per block
+        if (cudaMemcpyAsync(pool->scales + (size_t)dst_block * rec, pool->scales + (size_t)src_block * rec,
+                            rec * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
 pkv_status pkv_decode_workspace_init(void* workspace, size_t bytes, pkv_stream_t stream) {
     if (!workspace && bytes) return PKV_ERR_INVALID_ARG;
     if (!bytes) return PKV_OK;

@@ -17,7 +17,8 @@ import numpy as np
 
 from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_allocator_set_free_order, pkv_append,
                pkv_decode_attention, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
-               pkv_seq_release, pkv_seq_reserve, pkv_slot_mapping)
+               pkv_num_free_blocks, pkv_pool_copy_block, pkv_seq_release, pkv_seq_reserve, pkv_seq_share_prefix,
+               pkv_slot_mapping)
 
 def replay(allocator: int, ops) -> None:
     for op in ops:
@@ -160,6 +161,83 @@ class DecodeStep:
         kv = _wrap_device(kv_ptr, kv_bytes).cpu().numpy()
         sc = _wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32) if sc_bytes else np.zeros(0, np.float32)
         return kv, sc
+
+    def close(self):
+        self.pool.close()
+
+
+class PrefixDecode:
+    """A decode step over children that share one prompt prefix (block reuse).
+
+    share=True: the parent sequence takes the prefix (reserve + pkv_append), every child is forked
+    from it with pkv_seq_share_prefix (the whole prefix blocks are aliased; a partial last block is
+    copied with pkv_pool_copy_block), appends its own suffix, and the parent is released.
+    share=False: every child holds and writes its own copy of the prefix (the same logical
+    contexts without reuse, for comparison).  step()/attention() are the same calls as for any
+    other batch: the attention kernel does not know which blocks are shared."""
+
+    def __init__(self, sc, share: bool = True, device: str = "cuda"):
+        import torch
+        self.torch, self.sc, self.share, self.device = torch, sc, share, device
+        fp8 = sc.kv_dtype == "fp8_e4m3"
+        nb = sc.num_blocks if share else sc.blocks_unshared() + 4
+        self.pool = KVPool(nb, sc.block_size, sc.Hkv, sc.D, PKV_KV_FP8_E4M3 if fp8 else PKV_KV_BF16)
+        a = self.pool.allocator
+        pk, pv = sc.prefix_kv()
+        dpk, dpv = _bf16(torch, pk, device), _bf16(torch, pv, device)
+        P = sc.P
+        self.cow_copies = 0
+        if share:
+            pkv_seq_reserve(a, sc.parent, P)
+            pkv_append(self.pool.handle, dpk, dpv,
+                       torch.from_numpy(pkv_slot_mapping(a, [sc.parent] * P, np.arange(P))).to(device))
+        for b in range(sc.B):
+            total = P + int(sc.suffix_lens[b]) + 1
+            if share:
+                cs, cd = pkv_seq_share_prefix(a, sc.parent, b, P)
+                if cs >= 0:
+                    pkv_pool_copy_block(self.pool.handle, cs, cd)
+                    self.cow_copies += 1
+                pkv_seq_reserve(a, b, total)
+            else:
+                pkv_seq_reserve(a, b, total)
+                pkv_append(self.pool.handle, dpk, dpv,
+                           torch.from_numpy(pkv_slot_mapping(a, [b] * P, np.arange(P))).to(device))
+            n = int(sc.suffix_lens[b])
+            if n:
+                sk, sv = sc.suffix_kv(b)
+                slots = pkv_slot_mapping(a, [b] * n, np.arange(P, P + n))
+                pkv_append(self.pool.handle, _bf16(torch, sk, device), _bf16(torch, sv, device),
+                           torch.from_numpy(slots).to(device))
+        if share:
+            pkv_seq_release(a, sc.parent)
+        torch.cuda.synchronize()
+        self.blocks_held = nb - pkv_num_free_blocks(a)
+        seqs = np.arange(sc.B)
+        self.max_blocks = sc.max_blocks
+        self.tables_host = pkv_get_block_tables(a, seqs, self.max_blocks)
+        self.tables = torch.from_numpy(self.tables_host).to(device)
+        self.lens_host = sc.attend_lens
+        self.lens = torch.from_numpy(self.lens_host).to(device)
+        self.slots_new = torch.from_numpy(pkv_slot_mapping(a, seqs, P + sc.suffix_lens)).to(device)
+        k, v, q = sc.step_inputs()
+        self.k_new, self.v_new, self.q = _bf16(torch, k, device), _bf16(torch, v, device), _bf16(torch, q, device)
+        self.scale = 1.0 / math.sqrt(sc.D)
+        self.out = torch.empty(sc.B, sc.Hq, sc.D, dtype=torch.bfloat16, device=device)
+        ws = pkv_decode_workspace_bytes(self.pool.handle, sc.B, sc.Hq, self.max_blocks)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+
+    def step(self, stream=None):
+        pkv_decode_step(self.pool.handle, self.k_new, self.v_new, self.slots_new, self.q, self.tables, self.lens,
+                        self.scale, self.out, self.workspace, stream)
+        return self.out
+
+    def attention(self, stream=None):
+        pkv_decode_attention(self.pool.handle, self.q, self.tables, self.lens, self.scale, self.out, self.workspace,
+                             stream)
+
+    def out_host(self) -> np.ndarray:
+        return self.out.view(self.torch.int16).cpu().numpy().view(np.uint16)
 
     def close(self):
         self.pool.close()

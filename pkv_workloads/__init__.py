@@ -406,3 +406,100 @@ def make_loop_script(index: int = 40, n_steps: int = 32, max_batch: int = 24, Hq
     max_len = prompt_hi + n_steps + 1
     nb = num_blocks or peak + 8
     return LoopScript(f"loop{index}", seed, Hq, Hkv, D, block_size, kv_dtype, nb, max_batch, steps, max_len)
+
+
+# ----------------------------------------------------------------------------- shared prefixes
+TAG_PFX_LENS, TAG_PFX_K, TAG_PFX_V, TAG_SFX_K, TAG_SFX_V, TAG_PFX_Q, TAG_PFX_NEW_K, TAG_PFX_NEW_V = range(30, 38)
+
+
+@dataclass
+class PrefixScript:
+    """B requests that share one P-token prompt prefix (a system prompt) and then diverge with
+    suffixes of their own (block reuse: "TensorRT-LLM 推理加速实战", §8; enable_block_reuse in
+    the pnsm.cn TensorRT-LLM page, §3.1).
+
+    The parent sequence (id B) holds the prefix; child b (id b) is forked from it at P tokens,
+    then holds suffix_lens[b] tokens of its own at positions P .. P + suffix_lens[b] - 1.  The
+    step appends one new token per child at position P + suffix_lens[b] and attends over
+    P + suffix_lens[b] + 1 tokens."""
+    name: str
+    seed: int
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    block_size: int
+    kv_dtype: str
+    P: int
+    suffix_lens: np.ndarray
+    num_blocks: int
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def parent(self) -> int:
+        return self.B
+
+    @property
+    def max_suffix(self) -> int:
+        return int(self.suffix_lens.max()) if self.B else 0
+
+    @property
+    def attend_lens(self) -> np.ndarray:
+        return (self.P + self.suffix_lens + 1).astype(np.int32)
+
+    @property
+    def max_blocks(self) -> int:
+        return _ceil_div(int(self.attend_lens.max()), self.block_size)
+
+    def prefix_kv(self):
+        row = self.Hkv * self.D
+        k = normal_bf16(stream_seed(self.seed, TAG_PFX_K), 0, self.P * row).reshape(self.P, self.Hkv, self.D)
+        v = normal_bf16(stream_seed(self.seed, TAG_PFX_V), 0, self.P * row).reshape(self.P, self.Hkv, self.D)
+        return k, v
+
+    def suffix_kv(self, b: int):
+        row, n = self.Hkv * self.D, int(self.suffix_lens[b])
+        off = b * self.max_suffix * row
+        k = normal_bf16(stream_seed(self.seed, TAG_SFX_K), off, n * row).reshape(n, self.Hkv, self.D)
+        v = normal_bf16(stream_seed(self.seed, TAG_SFX_V), off, n * row).reshape(n, self.Hkv, self.D)
+        return k, v
+
+    def step_inputs(self):
+        """(k_new, v_new, q) of the decode step, one row per child."""
+        rkv, rq = self.B * self.Hkv * self.D, self.B * self.Hq * self.D
+        k = normal_bf16(stream_seed(self.seed, TAG_PFX_NEW_K), 0, rkv).reshape(self.B, self.Hkv, self.D)
+        v = normal_bf16(stream_seed(self.seed, TAG_PFX_NEW_V), 0, rkv).reshape(self.B, self.Hkv, self.D)
+        q = normal_bf16(stream_seed(self.seed, TAG_PFX_Q), 0, rq).reshape(self.B, self.Hq, self.D)
+        return k, v, q
+
+    def logical_kv(self, b: int):
+        """Child b's whole history as one [P + suffix][Hkv][D] array (what it attends, minus the
+        step's own token)."""
+        pk, pv = self.prefix_kv()
+        sk, sv = self.suffix_kv(b)
+        return np.concatenate([pk, sk]), np.concatenate([pv, sv])
+
+    def blocks_unshared(self) -> int:
+        """Blocks the children would hold with no sharing (each its own copy of the prefix)."""
+        return int(sum(_ceil_div(int(L), self.block_size) for L in self.attend_lens))
+
+    def blocks_shared(self) -> int:
+        """Blocks held with sharing: the prefix's whole blocks once, each child its own partial
+        prefix block (copied) and suffix blocks."""
+        full = self.P // self.block_size
+        return full + int(sum(_ceil_div(int(L), self.block_size) - full for L in self.attend_lens))
+
+
+def make_prefix_script(index: int = 60, B: int = 128, Hq: int = 32, Hkv: int = 8, D: int = 128, block_size: int = 64,
+                       kv_dtype: str = "bf16", P: int = 2048, suffix_lo: int = 128,
+                       suffix_hi: int = 2048) -> PrefixScript:
+    seed = 266 * 1000 + index
+    s = stream_seed(seed, TAG_PFX_LENS)
+    suffix = np.array([uniform_int(s, b, suffix_lo, suffix_hi) for b in range(B)], dtype=np.int64)
+    sc = PrefixScript(f"prefix{index}", seed, B, Hq, Hkv, D, block_size, kv_dtype, P, suffix, 0)
+    # parent's partial block stays held until the parent is released; + spares
+    sc.num_blocks = sc.blocks_shared() + (1 if P % block_size else 0) + 4
+    return sc
