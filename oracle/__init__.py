@@ -4,7 +4,8 @@ Only tests/, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
 reference leg may import this package.  The product library never loads it, and
 it shares no code with the CUDA path: ``pkv_oracle.cpp`` is a plain fp64
 restatement of what the TensorRT-LLM pages describe (allocator, append, FP8
-E4M3 codec, decode attention, split merge, KV-memory formula); see the header of
+E4M3 codec, decode attention, split merge, block reuse, chunked-context prefill
+attention, KV-memory formula); see the header of
 that file for the page and section each function follows.
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
@@ -70,6 +71,8 @@ def _L():
         "oracle_decode_attention": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, i32, i32, f64, vp, i32]),
         "oracle_decode_attention_split": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, i32, i32, f64, i32,
                                                 vp]),
+        "oracle_prefill_attention": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, i32, f64, vp,
+                                           i32]),
         "oracle_pool_bytes": (i64, [i32, i32, i32, i32, i32]),
         "oracle_scale_floats": (i64, [i32, i32]),
         "oracle_elem_byte": (i64, [i64, i32, i32, i32, i32, i32, i32, i32, i32]),
@@ -217,6 +220,20 @@ class Pool:
                                           n_q_heads, scale, _p(out), threads)
         if rc:
             raise RuntimeError(f"oracle attention rc={rc}")
+        return out
+
+    def prefill_attention(self, q, cu_q, tables, ctx_lens, n_q_heads: int, scale: float,
+                          threads: int = 1) -> np.ndarray:
+        """Chunked-context attention: rows cu_q[b]..cu_q[b+1]-1 of q are the last queries of
+        sequence b's ctx_lens[b] cached tokens, each attending causally (see the C source)."""
+        q, c, t, l = _c(q, np.uint16), _c(cu_q, np.int32), _c(tables, np.int32), _c(ctx_lens, np.int32)
+        B = len(l)
+        out = np.zeros((int(c[-1]) if B else 0, n_q_heads, self.D), dtype=np.float64)
+        rc = _L().oracle_prefill_attention(_p(self.data), _p(self.scales), self.num_blocks, self.bs, self.Hkv, self.D,
+                                           self.fp8, _p(q), _p(c), _p(t), t.shape[1] if t.ndim == 2 else 0, _p(l), B,
+                                           n_q_heads, scale, _p(out), threads)
+        if rc:
+            raise RuntimeError(f"oracle prefill attention rc={rc}")
         return out
 
     def attention_split(self, q, tables, lens, n_q_heads: int, scale: float, chunk: int) -> np.ndarray:

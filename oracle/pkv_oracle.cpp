@@ -28,6 +28,13 @@
 //    推理实战", csdn page).
 //  * Split merge: per-chunk running max m, sum l and weighted sum o merged with
 //    M = max m_s, l = sum l_s e^(m_s - M), out = sum e^(m_s - M) o_s / l.
+//  * Block reuse: pnsm.cn TensorRT-LLM page §3.1 (enable_block_reuse) and "TensorRT-LLM
+//    推理加速实战" §8 (KV cache reuse) — a forked sequence holds its source's whole prefix
+//    pages (holder counts), a copy of the partial last one, and pages return to the free
+//    list when their last holder releases them.
+//  * Prefill (chunked-context) attention: "TensorRT-LLM 深度实战" §7.3 and "TensorRT-LLM
+//    推理加速实战" §7.2 (context_fmha) — every query of a chunk is the decode definition over
+//    the tokens up to and including its own position.
 //
 // Pool byte layout (the storage contract both sides implement independently):
 //   tile(blk, kv, h) starts at byte ((blk*2 + kv)*Hkv + h) * bs * D * esz,
@@ -442,6 +449,60 @@ int oracle_decode_attention(const uint8_t* pool, const float* scales, int num_bl
         std::vector<std::thread> pool_threads;
         for (int t = 0; t < nt; ++t) pool_threads.emplace_back(work, t, nt);
         for (auto& th : pool_threads) th.join();
+    }
+    for (int s : status)
+        if (s) return s;
+    return 0;
+}
+
+// Chunked-context (prefill) attention over the pool: "TensorRT-LLM 深度实战" §7.3 (a long input
+// is processed chunk by chunk; each chunk attends to everything cached before it and causally
+// within itself) and "TensorRT-LLM 推理加速实战" §7.2 (context_fmha, the prefill attention, with
+// use_paged_context_fmha reading the paged cache).  Sequence b's chunk is query rows
+// cu_q[b] .. cu_q[b+1]-1 of q ([cu_q[B]][Hq][D] bf16); its K/V are already the last
+// q_len = cu_q[b+1]-cu_q[b] of the ctx_lens[b] cached tokens, so query i sits at position
+// p = ctx_lens[b] - q_len + i and attends to the tokens at positions 0..p.  Each query is the
+// decode-attention definition over a context of p + 1 tokens.  out: [cu_q[B]][Hq][D] fp64.
+int oracle_prefill_attention(const uint8_t* pool, const float* scales, int num_blocks, int bs, int Hkv, int D, int fp8,
+                             const uint16_t* q, const int32_t* cu_q, const int32_t* tables, int max_blocks,
+                             const int32_t* ctx_lens, int B, int Hq, double scale, double* out, int threads) {
+    if (Hq % Hkv != 0) return 1;
+    const int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        const int64_t n = (int64_t)cu_q[b + 1] - cu_q[b];
+        if (n < 0 || n > ctx_lens[b]) return 1;
+    }
+    const int64_t units = (int64_t)B * Hkv;
+    std::vector<int> status(std::max(threads, 1), 0);
+    auto work = [&](int tid, int nt) {
+        std::vector<double> K, V, qd((size_t)G * D), o((size_t)G * D);
+        for (int64_t u = tid; u < units; u += nt) {
+            const int b = (int)(u / Hkv), h = (int)(u % Hkv);
+            const int64_t L = ctx_lens[b], n = (int64_t)cu_q[b + 1] - cu_q[b];
+            if (n == 0) continue;
+            int rc = gather(pool, scales, num_blocks, bs, Hkv, D, fp8, tables, max_blocks, b, h, L, K, V);
+            if (rc) {
+                status[tid] = rc;
+                continue;
+            }
+            for (int64_t i = 0; i < n; ++i) {
+                const int64_t row = cu_q[b] + i, p = L - n + i;
+                for (int j = 0; j < G; ++j)
+                    for (int d = 0; d < D; ++d)
+                        qd[(size_t)j * D + d] = bf16_to_double(q[(row * Hq + h * G + j) * D + d]);
+                oracle_dense_attention(qd.data(), K.data(), V.data(), p + 1, D, G, scale, o.data());
+                for (int j = 0; j < G; ++j)
+                    for (int d = 0; d < D; ++d) out[(row * Hq + h * G + j) * D + d] = o[(size_t)j * D + d];
+            }
+        }
+    };
+    const int nt = std::max(1, threads);
+    if (nt == 1) {
+        work(0, 1);
+    } else {
+        std::vector<std::thread> ths;
+        for (int t = 0; t < nt; ++t) ths.emplace_back(work, t, nt);
+        for (auto& th : ths) th.join();
     }
     for (int s : status)
         if (s) return s;
