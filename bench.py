@@ -465,6 +465,118 @@ def run_prefix(args, world, rank, local):
     }), flush=True)
 
 
+def run_prefill(args, world, rank, local):
+    """Chunked-context prefill step: 8 sequences at seeded points of 32K prompts process one
+    512-token chunk each (4096 tokens), Llama-3-8B layer shapes, block 64: append of the chunks'
+    K/V then causal attention over past + chunk on the tensor cores."""
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    from paged_kv_cache_266_gb300.runner import PrefillStep
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    sc = W.make_prefill_script()
+    st = PrefillStep(sc, device=dev)
+    flops = sc.flops()
+    tokens = int(sc.cu_q[-1])
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    K = max(3, min(args.steps, 300))
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+
+    def timed(fn):
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush.zero_()
+            e0[k].record(stream)
+            fn()
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+        return [e0[k].elapsed_time(e1[k]) for k in range(K)]
+
+    step_ms = timed(st.step)
+    attn_ms = timed(st.attention)
+    clocks = sampler.stop()
+    if pkv.pkv_check_device_error(st.pool.handle) != 0:
+        raise RuntimeError("device error flag set in the timed region")
+    ms = dist_max(statistics.mean(step_ms), world)
+    attn = statistics.mean(attn_ms)
+    peaks = {}
+    pth = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pth):
+        with open(pth) as f:
+            peaks = json.load(f)
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops / (attn * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = prefill_oracle_rate(sc, args.cpu_budget, os.cpu_count() or 1)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "chunked prefill attention over the paged pool: causal attention TFLOP/s, prompt tokens/s",
+            "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 MMA, f32 accumulate", "data": "synthetic",
+            "config": {"workload": sc.name, "description": "8 sequences at seeded points of 32K prompts, one 512-token "
+                       "chunk each (4096 tokens per step), Llama-3-8B layer shapes (32 q / 8 kv heads, head_dim 128), "
+                       "block 64", "batch": sc.B, "chunk_tokens": tokens, "past_tokens": [int(x) for x in sc.past],
+                       "causal_flops_per_step": flops, "l2": "flushed before every timed launch"},
+            "tokens_per_s": round(world * tokens / (ms * 1e-3), 1),
+            "kernel_us": {"step": round(ms * 1e3, 2), "attention": round(attn * 1e3, 2),
+                          "attention_median": round(statistics.median(attn_ms) * 1e3, 2)},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_kind": "measured" if peaks else "fallback", "kernel": "prefill_kernel",
+                         "algorithmic_flops_per_launch": flops},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }), flush=True)
+    st.close()
+
+
+def prefill_oracle_rate(sc, budget_s: float, threads: int):
+    """The oracle's causal-attention FLOP rate on a sample of the prefill workload: the first
+    rows of sequence chunks, each a one-row chunk at its own position."""
+    import oracle
+    threads = min(threads, sc.Hkv)  # the oracle runs one (sequence, KV head) unit per thread
+    t_start = time.perf_counter()
+    flops = 0
+    rows = 0
+    for b in range(sc.B):
+        P, L = int(sc.past[b]), int(sc.ctx[b])
+        a = oracle.Allocator(-(-L // sc.block_size) + 1, sc.block_size)
+        pool = oracle.Pool(-(-L // sc.block_size) + 1, sc.block_size, sc.Hkv, sc.D, False)
+        a.reserve(0, L)
+        k, v = sc.kv(b, 0, L)
+        pool.append(k, v, a.slot_mapping([0] * L, np.arange(L)))
+        tables = a.block_tables([0], -(-L // sc.block_size))
+        t0 = time.perf_counter()
+        for i in range(0, int(sc.chunk[b]), 64):
+            row = int(sc.cu_q[b]) + i
+            pool.prefill_attention(sc.query(row, row + 1), np.array([0, 1], np.int32), tables,
+                                   np.array([P + i + 1], np.int32), sc.Hq, 1 / math.sqrt(sc.D), threads=threads)
+            flops += 4 * sc.D * sc.Hq * (P + i + 1)
+            rows += 1
+            if time.perf_counter() - t_start > budget_s:
+                break
+        if time.perf_counter() - t_start > budget_s:
+            break
+    spent = time.perf_counter() - t_start
+    return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} query rows (every 64th of each chunk), each over its full causal context, "
+                      f"including the pool replica's set-up; {spent:.1f} s"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -479,6 +591,7 @@ def main():
     ap.add_argument("--loop", action="store_true", help="measure the in-flight decode loop instead of one step")
     ap.add_argument("--loop-batch", type=int, default=128)
     ap.add_argument("--prefix", action="store_true", help="measure decode over children of a shared prompt prefix")
+    ap.add_argument("--prefill", action="store_true", help="measure the chunked-context prefill step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -489,6 +602,8 @@ def main():
         run_loop(args, world, rank, local)
     elif args.prefix:
         run_prefix(args, world, rank, local)
+    elif args.prefill:
+        run_prefill(args, world, rank, local)
     else:
         run_pkv(args, world, rank, local)
     if world > 1:

@@ -220,6 +220,41 @@ pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads
 /* cudaMemsetAsync(workspace, 0, bytes, stream): prepares a fresh workspace. */
 pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------ prefill (chunked context)
+ * Chunked-context attention over the pool: "TensorRT-LLM 深度实战", §7.3 (a long input is
+ * processed chunk by chunk, each chunk interleaved with decode steps) and "TensorRT-LLM 推理
+ * 加速实战", §7.2 (context_fmha, the prefill attention; use_paged_context_fmha reads the paged
+ * cache).  Sequence b's chunk is the query rows cu_q_lens[b] .. cu_q_lens[b+1]-1; its K/V have
+ * already been appended, so its cache holds context_lens[b] tokens of which the chunk's
+ * n_b = cu_q_lens[b+1]-cu_q_lens[b] are the last.  Query i of the chunk sits at position
+ * context_lens[b] - n_b + i and attends causally to the cached tokens 0 .. that position:
+ *     out[row][j] = sum_{t <= pos} softmax_t(scale * q[row][j] . K_b[t]) V_b[t],
+ * query head j reading KV head j / (n_q_heads / n_kv_heads).
+ *   q_dev, out_dev: bf16 [cu_q_lens[B]][n_q_heads][128], 16-byte aligned (rows of all chunks
+ *     packed back to back); fp32 accumulation, output rounded to bf16 (RNE).
+ *   cu_q_lens_dev: int32 [B+1], non-decreasing, cu_q_lens[0] = 0.
+ *   max_q_len: host int >= every n_b (sizes the grid; 0 launches nothing).
+ *   block_tables_dev: int32 [B][max_blocks]; context_lens_dev: int32 [B].
+ * Supported: bf16 pools with head_dim 128; n_q_heads / n_kv_heads a power of two <= 128;
+ * B <= 65535.  Otherwise PKV_ERR_INVALID_ARG (nothing launched).  A chunk longer than its
+ * context or a context longer than max_blocks*block_size is skipped and a block id outside the
+ * pool is read as zeros; both are flagged (PKV_ERR_BOUNDS via pkv_check_device_error).  Every
+ * wait in the kernel is bounded (2 s); on expiry the results are invalid and
+ * pkv_check_device_error returns PKV_ERR_TIMEOUT.  No workspace; the caller owns every buffer. */
+pkv_status pkv_prefill_attention(pkv_pool* pool, const void* q_dev, const int32_t* cu_q_lens_dev, int32_t max_q_len,
+                                 const int32_t* block_tables_dev, int32_t max_blocks, const int32_t* context_lens_dev,
+                                 int32_t B, int32_t n_q_heads, float scale, void* out_dev, pkv_stream_t stream);
+
+/* pkv_append of the chunks' K/V (k_new/v_new [n_new][n_kv_heads][head_dim], slot_mapping
+ * [n_new]) followed by pkv_prefill_attention, the attention launched as a programmatic
+ * dependent of the append (as in pkv_decode_step).  Every argument is checked before anything
+ * is launched. */
+pkv_status pkv_prefill_step(pkv_pool* pool, const void* k_new_dev, const void* v_new_dev,
+                            const int64_t* slot_mapping_dev, int64_t n_new, const void* q_dev,
+                            const int32_t* cu_q_lens_dev, int32_t max_q_len, const int32_t* block_tables_dev,
+                            int32_t max_blocks, const int32_t* context_lens_dev, int32_t B, int32_t n_q_heads,
+                            float scale, void* out_dev, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------ decode attention without allocation
  * The pages have no counterpart to this call; it exists for callers that cannot allocate
  * device memory for a workspace: a plugin inside an engine that has already reserved nearly

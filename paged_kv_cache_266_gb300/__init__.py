@@ -19,7 +19,7 @@ __all__ = [
     "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "library_path",
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
     "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_share_prefix", "pkv_block_refcount",
-    "pkv_pool_copy_block", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
+    "pkv_pool_copy_block", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
@@ -63,6 +63,8 @@ def _L():
         "pkv_seq_share_prefix": (i32, [vp, i64, i64, i64, P(ctypes.c_int32), P(ctypes.c_int32)]),
         "pkv_block_refcount": (i32, [vp, i32, P(i32)]),
         "pkv_pool_copy_block": (i32, [vp, i32, i32, vp]),
+        "pkv_prefill_attention": (i32, [vp, vp, vp, i32, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
+        "pkv_prefill_step": (i32, [vp, vp, vp, vp, i64, vp, vp, i32, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
         "pkv_seq_num_blocks": (i32, [vp, i64, P(i32)]),
         "pkv_num_free_blocks": (i32, [vp, P(i32)]),
         "pkv_free_list": (i32, [vp, vp, i32, P(i32)]),
@@ -271,6 +273,29 @@ def pkv_decode_step(pool: int, k_new, v_new, slot_mapping, q, block_tables, cont
                                 _dev(context_lens, "i32", "context_lens"), B, Hq, float(scale), _dev(out, "bf16", "out"),
                                 _dev(workspace, "u8", "workspace"), workspace.numel(), _stream(stream)),
            "pkv_decode_step")
+
+
+def pkv_prefill_attention(pool: int, q, cu_q_lens, max_q_len: int, block_tables, context_lens, scale: float, out,
+                          stream=None) -> None:
+    """q/out: bf16 CUDA [total_q, Hq, 128]; cu_q_lens int32 [B+1]; block_tables int32 [B, max_blocks];
+    context_lens int32 [B] (the chunks' K/V already appended)."""
+    B, Hq = context_lens.shape[0], q.shape[1]
+    _check(_L().pkv_prefill_attention(pool, _dev(q, "bf16", "q"), _dev(cu_q_lens, "i32", "cu_q_lens"), int(max_q_len),
+                                      _dev(block_tables, "i32", "block_tables"), block_tables.shape[1],
+                                      _dev(context_lens, "i32", "context_lens"), B, Hq, float(scale),
+                                      _dev(out, "bf16", "out"), _stream(stream)), "pkv_prefill_attention")
+
+
+def pkv_prefill_step(pool: int, k_new, v_new, slot_mapping, q, cu_q_lens, max_q_len: int, block_tables, context_lens,
+                     scale: float, out, stream=None) -> None:
+    """pkv_append(k_new, v_new, slot_mapping) then pkv_prefill_attention(...), launched back to back."""
+    B, Hq = context_lens.shape[0], q.shape[1]
+    _check(_L().pkv_prefill_step(pool, _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"),
+                                 _dev(slot_mapping, "i64", "slot_mapping"), slot_mapping.shape[0], _dev(q, "bf16", "q"),
+                                 _dev(cu_q_lens, "i32", "cu_q_lens"), int(max_q_len),
+                                 _dev(block_tables, "i32", "block_tables"), block_tables.shape[1],
+                                 _dev(context_lens, "i32", "context_lens"), B, Hq, float(scale), _dev(out, "bf16", "out"),
+                                 _stream(stream)), "pkv_prefill_step")
 
 
 def pkv_decode_workspace_bytes(pool: int, B: int, n_q_heads: int, max_blocks: int) -> int:

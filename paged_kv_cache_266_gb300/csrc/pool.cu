@@ -16,6 +16,7 @@
 namespace pkv {
 
 void attention_configure(pkv_pool* pool);  // decode_attention.cu
+void prefill_configure(pkv_pool* pool);    // prefill_attention.cu
 
 namespace {
 
@@ -156,6 +157,7 @@ pkv_status pkv_pool_create(int num_blocks, int block_size, int n_kv_heads, int h
             break;
         }
         pkv::attention_configure(p);
+        pkv::prefill_configure(p);
         if (cudaGetLastError() != cudaSuccess) {
             st = PKV_ERR_CUDA;
             break;

@@ -17,8 +17,8 @@ import numpy as np
 
 from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_allocator_set_free_order, pkv_append,
                pkv_decode_attention, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
-               pkv_num_free_blocks, pkv_pool_copy_block, pkv_seq_release, pkv_seq_reserve, pkv_seq_share_prefix,
-               pkv_slot_mapping)
+               pkv_num_free_blocks, pkv_pool_copy_block, pkv_prefill_attention, pkv_prefill_step, pkv_seq_release,
+               pkv_seq_reserve, pkv_seq_share_prefix, pkv_slot_mapping)
 
 def replay(allocator: int, ops) -> None:
     for op in ops:
@@ -235,6 +235,61 @@ class PrefixDecode:
     def attention(self, stream=None):
         pkv_decode_attention(self.pool.handle, self.q, self.tables, self.lens, self.scale, self.out, self.workspace,
                              stream)
+
+    def out_host(self) -> np.ndarray:
+        return self.out.view(self.torch.int16).cpu().numpy().view(np.uint16)
+
+    def close(self):
+        self.pool.close()
+
+
+class PrefillStep:
+    """One chunked-context step through the C ABI: the pool holds every sequence's past tokens
+    (appended at set-up); step() appends the chunks' K/V and runs the prefill attention
+    (pkv_prefill_step), attention() runs the attention alone."""
+
+    def __init__(self, sc, device: str = "cuda"):
+        import torch
+        self.torch, self.sc, self.device = torch, sc, device
+        self.pool = KVPool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D,
+                           PKV_KV_FP8_E4M3 if sc.kv_dtype == "fp8_e4m3" else PKV_KV_BF16)
+        a = self.pool.allocator
+        pkv_allocator_set_free_order(a, sc.free_order)
+        for b in range(sc.B):
+            pkv_seq_reserve(a, b, int(sc.ctx[b]))
+        chunk_tokens = 1 << 16
+        for b in range(sc.B):
+            for t0 in range(0, int(sc.past[b]), chunk_tokens):
+                t1 = min(int(sc.past[b]), t0 + chunk_tokens)
+                k, v = sc.kv(b, t0, t1)
+                slots = pkv_slot_mapping(a, [b] * (t1 - t0), np.arange(t0, t1))
+                pkv_append(self.pool.handle, _bf16(torch, k, device), _bf16(torch, v, device),
+                           torch.from_numpy(slots).to(device))
+        torch.cuda.synchronize()
+        seqs, pos = sc.chunk_slots_positions()
+        self.slots = torch.from_numpy(pkv_slot_mapping(a, seqs, pos)).to(device)
+        k, v = sc.chunk_kv()
+        self.k_new, self.v_new = _bf16(torch, k, device), _bf16(torch, v, device)
+        self.q = _bf16(torch, sc.query(), device)
+        self.cu_q = torch.from_numpy(sc.cu_q).to(device)
+        self.max_q = int(sc.chunk.max()) if sc.B else 0
+        self.tables_host = pkv_get_block_tables(a, np.arange(sc.B), sc.max_blocks)
+        self.tables = torch.from_numpy(self.tables_host).to(device)
+        self.ctx = torch.from_numpy(sc.ctx).to(device)
+        self.scale = 1.0 / math.sqrt(sc.D)
+        self.out = torch.zeros(int(sc.cu_q[-1]), sc.Hq, sc.D, dtype=torch.bfloat16, device=device)
+
+    def step(self, stream=None):
+        pkv_prefill_step(self.pool.handle, self.k_new, self.v_new, self.slots, self.q, self.cu_q, self.max_q,
+                         self.tables, self.ctx, self.scale, self.out, stream)
+        return self.out
+
+    def append(self, stream=None):
+        pkv_append(self.pool.handle, self.k_new, self.v_new, self.slots, stream)
+
+    def attention(self, stream=None):
+        pkv_prefill_attention(self.pool.handle, self.q, self.cu_q, self.max_q, self.tables, self.ctx, self.scale,
+                              self.out, stream)
 
     def out_host(self) -> np.ndarray:
         return self.out.view(self.torch.int16).cpu().numpy().view(np.uint16)

@@ -503,3 +503,102 @@ def make_prefix_script(index: int = 60, B: int = 128, Hq: int = 32, Hkv: int = 8
     # parent's partial block stays held until the parent is released; + spares
     sc.num_blocks = sc.blocks_shared() + (1 if P % block_size else 0) + 4
     return sc
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+TAG_PF_LENS, TAG_PF_PERM, TAG_PF_K, TAG_PF_V, TAG_PF_Q = range(40, 45)
+
+
+@dataclass
+class PrefillScript:
+    """One chunked-context step ("TensorRT-LLM 深度实战", §7.3): sequence b already caches
+    past[b] tokens and now processes a chunk of chunk[b] prompt tokens — their K/V are appended
+    and each of their queries attends to the past and, causally, to the chunk.
+
+    K/V of sequence b at position t and the chunk's queries are drawn from counter streams at
+    fixed offsets, so any subset can be regenerated."""
+    name: str
+    seed: int
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    block_size: int
+    kv_dtype: str
+    past: np.ndarray
+    chunk: np.ndarray
+    num_blocks: int
+    free_order: np.ndarray
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def ctx(self) -> np.ndarray:
+        return (self.past + self.chunk).astype(np.int32)
+
+    @property
+    def max_len(self) -> int:
+        return int(self.ctx.max()) if self.B else 0
+
+    @property
+    def cu_q(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk)]).astype(np.int32)
+
+    @property
+    def max_blocks(self) -> int:
+        return max(1, _ceil_div(self.max_len, self.block_size))
+
+    def kv(self, b: int, t0: int, t1: int):
+        """K and V of sequence b, positions t0 .. t1-1, as [t1-t0][Hkv][D] bf16 bits."""
+        row = self.Hkv * self.D
+        off = (b * self.max_len + t0) * row
+        n = (t1 - t0) * row
+        k = normal_bf16(stream_seed(self.seed, TAG_PF_K), off, n).reshape(t1 - t0, self.Hkv, self.D)
+        v = normal_bf16(stream_seed(self.seed, TAG_PF_V), off, n).reshape(t1 - t0, self.Hkv, self.D)
+        return k, v
+
+    def chunk_kv(self):
+        """The chunks' K/V rows in cu_q order."""
+        ks, vs = zip(*(self.kv(b, int(self.past[b]), int(self.ctx[b])) for b in range(self.B))) if self.B else ((), ())
+        row = (0, self.Hkv, self.D)
+        return (np.concatenate(ks) if ks else np.zeros(row, np.uint16),
+                np.concatenate(vs) if vs else np.zeros(row, np.uint16))
+
+    def query(self, r0: int = 0, r1: int | None = None) -> np.ndarray:
+        """Query rows r0 .. r1-1 of the packed chunks ([rows][Hq][D] bf16 bits)."""
+        r1 = int(self.cu_q[-1]) if r1 is None else r1
+        row = self.Hq * self.D
+        return normal_bf16(stream_seed(self.seed, TAG_PF_Q), r0 * row, (r1 - r0) * row).reshape(r1 - r0, self.Hq,
+                                                                                                 self.D)
+
+    def chunk_slots_positions(self):
+        """(sequence, position) of every chunk row, in cu_q order."""
+        seqs = np.concatenate([np.full(int(self.chunk[b]), b) for b in range(self.B)]) if self.B else np.zeros(0)
+        pos = np.concatenate([np.arange(int(self.past[b]), int(self.ctx[b])) for b in range(self.B)]) if self.B \
+            else np.zeros(0)
+        return seqs.astype(np.int64), pos.astype(np.int64)
+
+    def flops(self) -> int:
+        """Causal attention FLOPs of the step: 4 * D per (query head, query, attended key)."""
+        keys = sum(int(self.chunk[b]) * int(self.past[b]) + int(self.chunk[b]) * (int(self.chunk[b]) + 1) // 2
+                   for b in range(self.B))
+        return 4 * self.D * self.Hq * keys
+
+
+def make_prefill_script(index: int = 70, B: int = 8, Hq: int = 32, Hkv: int = 8, D: int = 128, block_size: int = 64,
+                        past=None, chunk=None, past_lo: int = 0, past_hi: int = 32256, chunk_lo: int = 512,
+                        chunk_hi: int = 512, kv_dtype: str = "bf16", spare_blocks: int = 3) -> PrefillScript:
+    """Default: 8 sequences of the long-context serving setting ("TensorRT-LLM 深度实战" §7.2-7.3:
+    32K contexts, chunks of 512 tokens, 4096 tokens per step), each at a seeded point of its
+    prompt (past U[0, 32256]), Llama-3-8B layer shapes, block 64."""
+    seed = 266 * 1000 + index
+    s = stream_seed(seed, TAG_PF_LENS)
+    past = np.asarray(past if past is not None else [uniform_int(s, 2 * b, past_lo, past_hi) for b in range(B)],
+                      dtype=np.int64)
+    chunk = np.asarray(chunk if chunk is not None else [uniform_int(s, 2 * b + 1, chunk_lo, chunk_hi)
+                                                        for b in range(B)], dtype=np.int64)
+    nb = int(sum(_ceil_div(int(p + c), block_size) for p, c in zip(past, chunk))) + spare_blocks
+    order = permutation(stream_seed(seed, TAG_PF_PERM), nb)
+    return PrefillScript(f"prefill{index}", seed, len(past), Hq, Hkv, D, block_size, kv_dtype, past, chunk, nb, order)

@@ -124,3 +124,147 @@ def test_prefill_rejects_chunk_longer_than_context():
     q = _bf16_bits(rng.standard_normal((11, 1, 64)))
     with pytest.raises(RuntimeError):
         pool.prefill_attention(q, np.array([0, 11], np.int32), tables, np.array([10], np.int32), 1, 0.1)
+
+
+# ----------------------------------------------------------------------------- GPU parity
+def _gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    return torch, pkv
+
+
+def _oracle_replay(sc, threads=8):
+    """The oracle's pool after the same appends, the tables, and the prefill outputs."""
+    a = oracle.Allocator(sc.num_blocks, sc.block_size)
+    a.set_free_order(sc.free_order)
+    pool = oracle.Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, sc.kv_dtype == "fp8_e4m3")
+    for b in range(sc.B):
+        assert a.reserve(b, int(sc.ctx[b])) == 0
+    for b in range(sc.B):
+        if sc.past[b]:
+            k, v = sc.kv(b, 0, int(sc.past[b]))
+            pool.append(k, v, a.slot_mapping([b] * int(sc.past[b]), np.arange(int(sc.past[b]))))
+    seqs, pos = sc.chunk_slots_positions()
+    k, v = sc.chunk_kv()
+    pool.append(k, v, a.slot_mapping(seqs, pos))
+    tables = a.block_tables(list(range(sc.B)), sc.max_blocks)
+    out = pool.prefill_attention(sc.query(), sc.cu_q, tables, sc.ctx, sc.Hq, 1 / math.sqrt(sc.D), threads=threads)
+    return pool, tables, out
+
+
+def _check_close(got_bits, ref):
+    got = oracle.bf16_bits_to_f64(got_bits)
+    err = np.abs(got - ref)
+    assert err.max() <= 1e-2, err.max()
+    assert err.mean() <= 1e-3, err.mean()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("bs,G", [(16, 4), (64, 4), (64, 1), (16, 8), (128, 2), (32, 16)])
+def test_prefill_matches_oracle(bs, G):
+    """Chunks at the start of a prompt, of one token, ending on a block boundary, spanning
+    several KV tiles and query tiles with ragged ends; pool bytes bit-exact after the append."""
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import PrefillStep, _wrap_device
+    sc = W.make_prefill_script(71 + bs + G, Hq=2 * G, Hkv=2, D=128, block_size=bs,
+                               past=[0, 5, 64, 100, 250, 31, 0], chunk=[37, 1, 64, 150, 3, 200, 129])
+    st = PrefillStep(sc)
+    st.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+    opool, tables, ref = _oracle_replay(sc)
+    assert np.array_equal(st.tables_host, tables)
+    kv_ptr, kv_bytes, _, _ = pkv.pkv_pool_raw(st.pool.handle)
+    assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), opool.data)
+    _check_close(st.out_host(), ref)
+    st.close()
+
+
+@pytest.mark.gpu
+def test_prefill_fused_step_equals_separate_calls():
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import PrefillStep
+    sc = W.make_prefill_script(80, B=4, Hq=16, Hkv=4, block_size=64, past_hi=700, chunk_lo=1, chunk_hi=300)
+    st = PrefillStep(sc)
+    st.step()
+    torch.cuda.synchronize()
+    fused = st.out_host()
+    st.out.zero_()
+    st.append()
+    st.attention()
+    torch.cuda.synchronize()
+    assert np.array_equal(st.out_host(), fused)
+    # deterministic: the same call again gives the same bits
+    st.attention()
+    torch.cuda.synchronize()
+    assert np.array_equal(st.out_host(), fused)
+    st.close()
+
+
+@pytest.mark.gpu
+def test_prefill_full_size_sampled():
+    """8 sequences at seeded points of 32K prompts, 512-token chunks, Llama-3-8B layer shapes,
+    block 64 (the measured configuration): sampled query rows against dense attention over the
+    regenerated K/V of their sequence."""
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import PrefillStep
+    sc = W.make_prefill_script()
+    st = PrefillStep(sc)
+    st.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+    got = st.out_host()
+    scale = 1 / math.sqrt(sc.D)
+    for b in range(sc.B):
+        P = int(sc.past[b])
+        k, v = sc.kv(b, 0, int(sc.ctx[b]))
+        K, V = oracle.bf16_bits_to_f64(k), oracle.bf16_bits_to_f64(v)
+        for i in (0, 1, 130, int(sc.chunk[b]) - 1):
+            row = int(sc.cu_q[b]) + i
+            q = oracle.bf16_bits_to_f64(sc.query(row, row + 1)[0])
+            for h in (0, sc.Hkv - 1):
+                ref = oracle.dense_attention(q[h * sc.G:(h + 1) * sc.G], K[:P + i + 1, h], V[:P + i + 1, h], scale)
+                err = np.abs(oracle.bf16_bits_to_f64(got[row, h * sc.G:(h + 1) * sc.G]) - ref)
+                assert err.max() <= 1e-2 and err.mean() <= 1e-3, (b, i, h, err.max())
+    st.close()
+
+
+@pytest.mark.gpu
+def test_prefill_rejects_unsupported_and_flags_bounds():
+    torch, pkv = _gpu()
+    dev = "cuda"
+    q = torch.zeros(4, 6, 128, dtype=torch.bfloat16, device=dev)
+    out = torch.zeros_like(q)
+    cu = torch.tensor([0, 4], dtype=torch.int32, device=dev)
+    tables = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    ctx = torch.tensor([4], dtype=torch.int32, device=dev)
+    fp8 = pkv.KVPool(4, 16, 2, 128, pkv.PKV_KV_FP8_E4M3)
+    with pytest.raises(pkv.PKVError):  # fp8 pools have no prefill kernel
+        pkv.pkv_prefill_attention(fp8.handle, q, cu, 4, tables, ctx, 0.1, out)
+    fp8.close()
+    pool = pkv.KVPool(4, 16, 2, 128, pkv.PKV_KV_BF16)
+    with pytest.raises(pkv.PKVError):  # 6 query heads over 2 KV heads: 3 per group
+        pkv.pkv_prefill_attention(pool.handle, q, cu, 4, tables, ctx, 0.1, out)
+    q8 = torch.zeros(4, 8, 128, dtype=torch.bfloat16, device=dev)
+    out8 = torch.zeros_like(q8)
+    long_ctx = torch.tensor([40], dtype=torch.int32, device=dev)  # beyond 1 block of 16
+    pkv.pkv_prefill_attention(pool.handle, q8, cu, 4, tables, long_ctx, 0.1, out8)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_ERR_BOUNDS
+    short_ctx = torch.tensor([3], dtype=torch.int32, device=dev)  # chunk of 4 in a context of 3
+    pkv.pkv_prefill_attention(pool.handle, q8, cu, 4, tables, short_ctx, 0.1, out8)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_ERR_BOUNDS
+    bad_tab = torch.tensor([[7]], dtype=torch.int32, device=dev)  # block id outside a 4-block pool
+    pkv.pkv_prefill_attention(pool.handle, q8, cu, 4, bad_tab, ctx, 0.1, out8)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_ERR_BOUNDS
+    pkv.pkv_prefill_attention(pool.handle, q8, cu, 0, tables, ctx, 0.1, out8)  # max_q_len 0: nothing launched
+    pool.close()
