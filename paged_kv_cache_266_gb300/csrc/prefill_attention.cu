@@ -8,25 +8,32 @@
 // h = j / G,
 //     out[cu_q[b] + i][j] = sum_{t <= L-n+i} softmax_t(scale * q . K_b[t]) V_b[t].
 //
-// Work decomposition: one CTA per (sequence, KV head, tile of 128 query rows).  A row is a
-// (token, head-in-group) pair, so a tile covers 128/G consecutive chunk tokens and all G query
-// heads of one KV head: every K/V tile brought on chip serves the whole group.  The CTA
-// walks the KV tiles of 128 keys that its last token can see:
+// Work decomposition: one CTA per (sequence, KV head, pair of 128-row query tiles).  A row is
+// a (token, head-in-group) pair, so a tile covers 128/G consecutive chunk tokens and all G
+// query heads of one KV head, and every K/V tile brought on chip serves both query tiles and
+// the whole group.  The CTA walks the KV tiles of 128 keys its last token can see:
 //   warp 0     TMA producer: one 4-D tensor copy per page part (K and V, both 64-element
 //              panels, 128-byte swizzled) into a two-stage ring; parts past the context get a
 //              coordinate past the pool, which the copy fills with zeros.
-//   warp 1     tensor-memory owner and MMA issuer (one thread):
-//                S_j = Q K_j^T   M=128 rows, N=part, K=128 (tcgen05.mma kind::f16, bf16 in,
-//                                fp32 accumulator in TMEM, two S buffers)
-//                O  += P_j V_j   M=128, N=128, K=16 per instruction, A = P from shared
-//                                memory, B = V MN-major straight from the page copy
-//              issued one KV tile ahead (S_{j+1} runs while the softmax works on S_j).
-//   warps 2-5  one query row per thread (TMEM lane = row): the Q row into shared memory,
-//              then per KV tile the S row out of TMEM (tcgen05.ld), causal mask, online
-//              softmax in base 2, the O row rescaled in TMEM when the running maximum grows,
-//              P as bf16 into shared memory; finally O / l as bf16 to global memory.
+//   warp 1     tensor-memory owner and MMA issuer (one thread), per KV tile j and query tile t:
+//                O_t += P_t(j) V_j      M=128, N=128, K=16 per instruction, A = P straight
+//                                       from tensor memory, B = V MN-major from the page copy
+//                S_t(j+1) = Q_t K_{j+1}^T  M=128, N=part, K=128, written over P_t(j): the
+//                                       tensor pipe runs one thread's MMAs in issue order
+//              so one tile's MMAs run while the other tile's softmax works.
+//   warps 2-3  idle (they complete the control warpgroup, which gives registers away)
+//   warps 4-7, 8-11  one softmax warpgroup per query tile, one row per thread (TMEM lane =
+//              row): the Q row into shared memory, then per KV tile the S row out of TMEM,
+//              causal mask on the tiles that cross the row's position, online softmax in base
+//              2 with the scale folded into one FMA, the O row rescaled in TMEM only when the
+//              running maximum grows by more than 2^8 (the stale maximum keeps P <= 256), and
+//              P back into TMEM as bf16.  On the first KV tile P is carried as a bf16 pair
+//              (hi + lo, two MMAs): short contexts have all their weight there, and a single
+//              bf16 P would add its rounding to the output's.  Finally O / l as bf16.
+// TMEM: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t (bf16 pairs) lives in S_t's columns.
 // Every mbarrier wait is bounded; on expiry the kernel sets the pool's error word, every role
 // stops, and tensor memory is released.
+#include <cmath>
 #include <cstdlib>
 
 #include "pkv_internal.h"
@@ -36,32 +43,37 @@ namespace pkv {
 namespace prefill {
 
 constexpr int kD = 128;
-constexpr int kRows = 128;  // query rows per CTA
-constexpr int kKeys = 128;  // keys per KV tile
+constexpr int kRows = 128;   // query rows per tile
+constexpr int kTiles = 2;    // query tiles per CTA
+constexpr int kKeys = 128;   // keys per KV tile
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
-constexpr uint32_t kPanelBytes = 128u * 128u;              // 128 rows x 128 bytes
-constexpr uint32_t kQBytes = 2 * kPanelBytes;              // Q tile: two 64-element panels
-constexpr uint32_t kStageBytes = 4u * kKeys * 128u;        // K and V, two panels each
-constexpr uint32_t kPBytes = 2 * kPanelBytes;              // P tile (bf16), two 64-key panels
+constexpr int kThreads = 128 + kTiles * 128;  // control warpgroup + one softmax warpgroup per tile
+// register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded down to 8),
+// i.e. 64512 for the block; control 128 x 48 + softmax 256 x 224 = 63488 fits.
+constexpr uint32_t kRegsControl = 48, kRegsSoftmax = 224;
+static_assert(128 * kRegsControl + kTiles * 128 * kRegsSoftmax <= kThreads * 168, "register split");
+constexpr uint32_t kPanelBytes = 128u * 128u;          // 128 rows x 128 bytes
+constexpr uint32_t kQBytes = 2 * kPanelBytes;          // one Q tile: two 64-element panels
+constexpr uint32_t kStageBytes = 4u * kKeys * 128u;    // K and V, two panels each
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kQBytes;
-constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kOffKV = kOffQ + kTiles * kQBytes;
+constexpr uint32_t kOffBar = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // two S buffers of 128 columns
-constexpr uint32_t kColO = 256;  // O: 128 columns
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (P stays <= 2^8)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kEndBar = 1;  // named barrier: every role done before TMEM is released
 
 // mbarrier slots
-constexpr int kBarQ = 0;                     // Q rows written (4 softmax warps arrive)
-constexpr int kBarFull = 1;                  // [kStages] K/V copies landed (tx bytes)
-constexpr int kBarEmpty = kBarFull + kStages;  // [kStages] PV of the stage's tile done (commit)
-constexpr int kBarS = kBarEmpty + kStages;   // [2] S_j ready (commit)
-constexpr int kBarP = kBarS + 2;             // P_j written (4 softmax warps arrive)
-constexpr int kBarO = kBarP + 1;             // PV_j done (commit)
-constexpr int kNumBars = kBarO + 1;
+constexpr int kBarQ = 0;                       // Q rows of both tiles written (8 warps arrive)
+constexpr int kBarFull = 1;                    // [kStages] K/V copies landed (tx bytes)
+constexpr int kBarEmpty = kBarFull + kStages;  // [kStages] last PV of the stage's tile done
+constexpr int kBarS = kBarEmpty + kStages;     // [kTiles] S_t(j) ready (commit)
+constexpr int kBarP = kBarS + kTiles;          // [kTiles] P_t(j) in TMEM (4 warps arrive)
+constexpr int kBarO = kBarP + kTiles;          // [kTiles] last PV_t done (commit)
+constexpr int kBarDrain = kBarO + kTiles;      // MMAs in flight done (error path)
+constexpr int kNumBars = kBarDrain + 1;
 
 struct Params {
     const uint16_t* q;
@@ -88,30 +100,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const sm = smem_raw + (base - raw);
-    const uint32_t sQ = base + kOffQ, sKV = base + kOffKV, sP = base + kOffP;
+    const uint32_t sKV = base + kOffKV;
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     const int b = blockIdx.z, h = blockIdx.y;
-    const int tile = p.tiles - 1 - (int)blockIdx.x;  // deepest tiles (most keys) launch first
+    const int pair = p.tiles - 1 - (int)blockIdx.x;  // deepest pairs (most keys) launch first
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     ptx::grid_dependency_wait();  // inputs may come from the preceding append
     const int q0 = p.cu_q[b];
     const int n = p.cu_q[b + 1] - q0;
     const int L = p.ctx[b];
-    const int T = kRows / p.G;  // chunk tokens per tile
-    const int t0 = tile * T;
+    const int T = kRows / p.G;  // chunk tokens per query tile
+    const int t0 = pair * kTiles * T;
     if (t0 >= n) return;
     if (n < 0 || n > L || L > p.max_blocks * p.bs) {
         if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
         return;
     }
-    const int t_last = min(n, t0 + T) - 1;
-    const int kv_end = L - n + t_last + 1;  // keys seen by the tile's last token
-    const int n_kv = (kv_end + kKeys - 1) / kKeys;
+    // KV tiles each query tile needs (0: the tile lies past the chunk)
+    int nkv[kTiles];
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        const int first = t0 + t * T;
+        const int last = min(n, first + T) - 1;
+        nkv[t] = first < n ? (L - n + last + 1 + kKeys - 1) / kKeys : 0;
+    }
+    const int last_tile = nkv[1] > 0 ? 1 : 0;
+    const int n_kv = nkv[last_tile];  // the last active tile sees the most keys
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bar(i), (i == kBarQ || i == kBarP) ? 4u : 1u);
+        for (int i = 0; i < kNumBars; ++i) {
+            const bool wg_arrive = i == kBarQ || (i >= kBarP && i < kBarP + kTiles);
+            ptx::mbar_init(bar(i), i == kBarQ ? 8u : (wg_arrive ? 4u : 1u));
+        }
         abort_s = 0;
         ptx::fence_barrier_init();
     }
@@ -123,7 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int parts = kKeys / p.part;
     const uint32_t part_bytes = 4u * (uint32_t)p.part * 128u;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      ptx::regs_dec<kRegsControl>();  // the whole control warpgroup, one instruction
+      if (warp == 0) {
         // ---------------------------------------------------------------- producer
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
         for (int j = 0; j < n_kv; ++j) {
@@ -157,190 +181,225 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  bar(kBarFull + s));
             }
         }
-    } else if (warp == 1) {
+        ptx::named_barrier_sync(kEndBar, kThreads);
+      } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t tS = tmem + kColS, tO = tmem + kColO;
             const uint32_t idS = ptx::umma_idesc_bf16(128, p.part, 0, 0);
             const uint32_t idO = ptx::umma_idesc_bf16(128, kD, 0, 1);
+            int kv_ready = 0;  // KV tiles whose copies this thread has waited for
             bool ok = ptx::mbar_wait(bar(kBarQ), 0, p.wait_ns);
             ptx::tc_fence_after();
-            int committed_o = 0;
-            for (int j = 0; ok && j <= n_kv; ++j) {
-                if (j < n_kv) {
-                    const int s = j % kStages;
-                    ok = ptx::mbar_wait(bar(kBarFull + s), (j / kStages) & 1, p.wait_ns);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    const uint32_t kst = sKV + (uint32_t)s * kStageBytes;
-                    const uint32_t dS = tS + (uint32_t)(j & 1) * kKeys;
-                    for (int pi = 0; pi < parts; ++pi) {
-                        if (j * kKeys + pi * p.part >= L) break;  // past the context: scores unused
-                        const uint32_t kpart = kst + (uint32_t)pi * part_bytes;
+            auto wait_kv = [&](int j) -> bool {
+                if (j < kv_ready) return true;
+                if (!ptx::mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, p.wait_ns)) return false;
+                ptx::tc_fence_after();
+                kv_ready = j + 1;
+                return true;
+            };
+            auto issue_s = [&](int t, int j) {
+                const uint32_t kst = sKV + (uint32_t)(j % kStages) * kStageBytes;
+                const uint32_t qt = base + kOffQ + (uint32_t)t * kQBytes;
+                for (int pi = 0; pi < parts; ++pi) {
+                    if (j * kKeys + pi * p.part >= L) break;  // past the context: scores unused
+                    const uint32_t kpart = kst + (uint32_t)pi * part_bytes;
 #pragma unroll
-                        for (int k = 0; k < kD / 16; ++k) {
-                            const uint64_t a =
-                                ptx::umma_sdesc_sw128(sQ + (uint32_t)(k >> 2) * kPanelBytes + (uint32_t)(k & 3) * 32u,
-                                                      16, 1024);
-                            const uint64_t bd = ptx::umma_sdesc_sw128(
-                                kpart + (uint32_t)(k >> 2) * (uint32_t)p.part * 128u + (uint32_t)(k & 3) * 32u, 16,
-                                1024);
-                            ptx::umma_bf16(dS + (uint32_t)(pi * p.part), a, bd, idS, k > 0 ? 1u : 0u);
-                        }
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint64_t a = ptx::umma_sdesc_sw128(
+                            qt + (uint32_t)(k >> 2) * kPanelBytes + (uint32_t)(k & 3) * 32u, 16, 1024);
+                        const uint64_t bd = ptx::umma_sdesc_sw128(
+                            kpart + (uint32_t)(k >> 2) * (uint32_t)p.part * 128u + (uint32_t)(k & 3) * 32u, 16, 1024);
+                        ptx::umma_bf16(tmem + (uint32_t)(t * kKeys + pi * p.part), a, bd, idS, k > 0 ? 1u : 0u);
                     }
-                    ptx::umma_commit(bar(kBarS + (j & 1)));
                 }
-                if (j >= 1) {
-                    const int i = j - 1, s = i % kStages;
-                    ok = ptx::mbar_wait(bar(kBarP), i & 1, p.wait_ns);
+                ptx::umma_commit(bar(kBarS + t));
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t vst = sKV + (uint32_t)(j % kStages) * kStageBytes;
+                const uint32_t tP = tmem + (uint32_t)(t * kKeys), tO = tmem + kColO + (uint32_t)(t * kD);
+                const int halves = j == 0 ? 2 : 1;  // hi and lo parts of P on the first KV tile
+                for (int half = 0; half < halves; ++half) {
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        const int tok = 16 * kk;  // key within the tile
+                        if (j * kKeys + tok >= L) break;  // all-zero P columns from here on
+                        const int pi = tok / p.part, c = (tok % p.part) >> 4;
+                        const uint32_t vpart = vst + (uint32_t)pi * part_bytes + 2u * (uint32_t)p.part * 128u;
+                        const uint64_t bd =
+                            ptx::umma_sdesc_sw128(vpart + (uint32_t)c * 2048u, (uint32_t)p.part * 128u, 1024);
+                        ptx::umma_bf16_tmem_a(tO, tP + (uint32_t)(half * 64 + 8 * kk), bd, idO,
+                                              (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+            };
+            if (ok) ok = wait_kv(0);
+            if (ok)
+                for (int t = 0; t < kTiles; ++t)
+                    if (nkv[t] > 0) issue_s(t, 0);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                for (int t = 0; t < kTiles && ok; ++t) {
+                    if (j >= nkv[t]) continue;
+                    ok = ptx::mbar_wait(bar(kBarP + t), j & 1, p.wait_ns);
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    const uint32_t vst = sKV + (uint32_t)s * kStageBytes;
-                    for (int pi = 0; pi < parts; ++pi) {
-                        const uint32_t vpart = vst + (uint32_t)pi * part_bytes + 2u * (uint32_t)p.part * 128u;
-                        for (int c = 0; c < p.part / 16; ++c) {
-                            const int tok = pi * p.part + 16 * c;  // key within the tile
-                            if (i * kKeys + tok >= L) break;        // all-zero P columns from here on
-                            const uint64_t a = ptx::umma_sdesc_sw128(
-                                sP + (uint32_t)(tok >> 6) * kPanelBytes + (uint32_t)((tok & 63) >> 4) * 32u, 16, 1024);
-                            const uint64_t bd =
-                                ptx::umma_sdesc_sw128(vpart + (uint32_t)c * 2048u, (uint32_t)p.part * 128u, 1024);
-                            ptx::umma_bf16(tO, a, bd, idO, (i > 0 || tok > 0) ? 1u : 0u);
-                        }
+                    issue_pv(t, j);
+                    if (j == nkv[t] - 1) ptx::umma_commit(bar(kBarO + t));
+                    if (t == last_tile && j + kStages < n_kv) ptx::umma_commit(bar(kBarEmpty + j % kStages));
+                    if (j + 1 < nkv[t]) {
+                        ok = wait_kv(j + 1);
+                        if (!ok) break;
+                        issue_s(t, j + 1);
                     }
-                    ptx::umma_commit(bar(kBarO));
-                    // the producer waits for this stage only if a later tile reuses it; no
-                    // arrival is left pending when the CTA exits
-                    if (i + kStages < n_kv) ptx::umma_commit(bar(kBarEmpty + s));
-                    ++committed_o;
                 }
             }
             if (!ok) {
                 atomicOr(p.err, kErrTimeout);
                 abort_s = 1;
                 // let MMAs already issued finish before tensor memory is released
-                if (committed_o > 0) ptx::mbar_wait(bar(kBarO), (committed_o - 1) & 1, p.wait_ns);
+                ptx::umma_commit(bar(kBarDrain));
+                ptx::mbar_wait(bar(kBarDrain), 0, p.wait_ns);
             }
         }
         __syncwarp();
+        // every role has finished with tensor memory: release it
+        ptx::named_barrier_sync(kEndBar, kThreads);
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+      } else {
+        ptx::named_barrier_sync(kEndBar, kThreads);  // idle warps of the control warpgroup
+      }
     } else {
+        ptx::regs_inc<kRegsSoftmax>();
         // ---------------------------------------------------------------- softmax / epilogue
-        const int qw = warp & 3;  // TMEM lane quarter this warp may access
+        const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+        const int qw = warp & 3;        // TMEM lane quarter this warp may access
         const int r = qw * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-        const int tok = t0 + r / p.G, g = r % p.G;
+        const uint32_t tS = tmem + (uint32_t)(t * kKeys) + lane_off;
+        const uint32_t tO = tmem + kColO + (uint32_t)(t * kD) + lane_off;
+        const int tok = t0 + t * T + r / p.G, g = r % p.G;
         const bool valid = tok < n;
         const int qlim = min(L - n + tok, L - 1);  // last key this row may see
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * kD);
+            uint8_t* qt = sm + kOffQ + (uint32_t)t * kQBytes;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + kOffQ + (uint32_t)(c >> 3) * kPanelBytes + swz128(r, c & 7)) = v;
+                *reinterpret_cast<uint4*>(qt + (uint32_t)(c >> 3) * kPanelBytes + swz128(r, c & 7)) = v;
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarQ));
         }
-        float m = -INFINITY, l = 0.f;
+        const int my_nkv = nkv[t];
+        const float c2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;  // running maximum (scaled, base 2) and sum
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS + (j & 1)), (j >> 1) & 1, p.wait_ns));
+        for (int j = 0; j < my_nkv; ++j) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS + t), j & 1, p.wait_ns));
             if (!ok) break;
             ptx::tc_fence_after();
-            float x[kKeys];
-            {
-                uint32_t v[32];
+            uint32_t sraw[kKeys];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32 * c));
+            ptx::tmem_wait_ld();
+            const int kbase = j * kKeys;
+            float smax = -INFINITY;
+            if (kbase + kKeys - 1 > qlim) {  // the tile crosses this row's position: mask
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) {
+                    const float x = kbase + c <= qlim ? __uint_as_float(sraw[c]) : -INFINITY;
+                    sraw[c] = __float_as_uint(x);
+                    smax = fmaxf(smax, x);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) smax = fmaxf(smax, __uint_as_float(sraw[c]));
+            }
+            const float mt = smax * c2;  // this tile's maximum, scaled (finite: key kbase <= qlim)
+            // lazy rescale: keep the running maximum unless this tile exceeds it by 2^8
+            const bool grow = mt > m + kRescaleLog2;
+            if (__any_sync(0xffffffffu, grow && j > 0)) {
+                const float alpha = (grow && j > 0) ? ptx::exp2_approx(m - mt) : 1.f;
+                l *= alpha;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    ptx::tmem_ld32(tmem + kColS + (uint32_t)(j & 1) * kKeys + 32u * c + lane_off, v);
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tO + 32u * c, v);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    ptx::tmem_st32(tO + 32u * c, v);
                 }
             }
-            const int kbase = j * kKeys;
-            float mx = -INFINITY;
+            if (grow) m = mt;
+            const float nm = -m;
+            if (j == 0) {  // P as hi + lo bf16 pair: columns 0-63 and 64-127
 #pragma unroll
-            for (int c = 0; c < kKeys; ++c) {
-                x[c] = (kbase + c <= qlim) ? x[c] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[c]);
-            }
-            const float m_new = fmaxf(m, mx);
-            if (j >= 1) {
-                ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarO), (j - 1) & 1, p.wait_ns));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                const bool grow = m_new > m && m != -INFINITY;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float alpha = grow ? ptx::exp2_approx(m - m_new) : 1.f;
-                    l *= alpha;
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t hi[32], lo[32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
-                        ptx::tmem_ld32(tmem + kColO + 32u * c + lane_off, v);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        ptx::tmem_st32(tmem + kColO + 32u * c + lane_off, v);
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e]), c2, nm));
+                        const float p1 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e + 1]), c2, nm));
+                        hi[e] = ptx::pack_bf16x2(p0, p1);
+                        const float h0 = ptx::bf16lo_to_f32(hi[e]), h1 = ptx::bf16hi_to_f32(hi[e]);
+                        lo[e] = ptx::pack_bf16x2(p0 - h0, p1 - h1);
+                        l += (h0 + h1) + (ptx::bf16lo_to_f32(lo[e]) + ptx::bf16hi_to_f32(lo[e]));
                     }
-                    ptx::tmem_wait_st();
+                    ptx::tmem_st32(tS + 32u * c, hi);
+                    ptx::tmem_st32(tS + 64u + 32u * c, lo);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t hi[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e]), c2, nm));
+                        const float p1 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e + 1]), c2, nm));
+                        hi[e] = ptx::pack_bf16x2(p0, p1);
+                        l += ptx::bf16lo_to_f32(hi[e]) + ptx::bf16hi_to_f32(hi[e]);
+                    }
+                    ptx::tmem_st32(tS + 32u * c, hi);
                 }
             }
-            m = m_new;
-            const float mu = m == -INFINITY ? 0.f : m;
-            uint8_t* prow = sm + kOffP;
-#pragma unroll
-            for (int c16 = 0; c16 < kKeys / 8; ++c16) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ptx::exp2_approx(x[8 * c16 + 2 * e] - mu);
-                    const float p1 = ptx::exp2_approx(x[8 * c16 + 2 * e + 1] - mu);
-                    w[e] = ptx::pack_bf16x2(p0, p1);
-                    l += ptx::bf16lo_to_f32(w[e]) + ptx::bf16hi_to_f32(w[e]);
-                }
-                *reinterpret_cast<uint4*>(prow + (uint32_t)(c16 >> 3) * kPanelBytes + swz128(r, c16 & 7)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            ptx::fence_proxy_async_smem();
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(kBarP));
+            if (lane == 0) ptx::mbar_arrive(bar(kBarP + t));
         }
-        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarO), (n_kv - 1) & 1, p.wait_ns));
-        if (ok) {
-            ptx::tc_fence_after();
-            const float inv = 1.f / l;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * kD);
+        if (ok && my_nkv > 0) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarO + t), 0, p.wait_ns));
+            if (ok) {
+                ptx::tc_fence_after();
+                const float inv = 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * kD);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld32(tmem + kColO + 32u * c + lane_off, v);
-                ptx::tmem_wait_ld();
-                if (valid) {
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tO + 32u * c, v);
+                    ptx::tmem_wait_ld();
+                    if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 o;
-                        o.x = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv);
-                        o.y = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv);
-                        o.z = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv);
-                        o.w = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv);
-                        dst[4 * c + e] = o;
+                        for (int e = 0; e < 4; ++e) {
+                            uint4 o;
+                            o.x = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv);
+                            o.y = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv);
+                            o.z = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv);
+                            o.w = ptx::pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv);
+                            dst[4 * c + e] = o;
+                        }
                     }
                 }
             }
-        } else if (lane == 0) {
+        }
+        if (!ok && lane == 0) {
             atomicOr(p.err, kErrTimeout);
             abort_s = 1;
         }
-    }
-
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        ptx::tc_fence_before();
+        ptx::named_barrier_sync(kEndBar, kThreads);
     }
 }
 
@@ -363,6 +422,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
                            float scale, void* out, prefill::Params& p, dim3& grid) {
     using namespace prefill;
     if (!pool || B < 0 || max_q_len < 0 || Hq < 1) return PKV_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;  // masking relies on scale > 0
     if (pool->dtype != PKV_KV_BF16 || pool->head_dim != kD) return PKV_ERR_INVALID_ARG;
     if (Hq % pool->n_kv_heads) return PKV_ERR_INVALID_ARG;
     const int G = Hq / pool->n_kv_heads;
@@ -389,7 +449,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     p.bs = pool->block_size;
     p.part = pool->block_size < 64 ? pool->block_size : 64;
     p.num_blocks = pool->num_blocks;
-    p.tiles = (max_q_len + T - 1) / T;
+    p.tiles = (max_q_len + kTiles * T - 1) / (kTiles * T);  // pairs of query tiles
     p.oob_row = (int32_t)((int64_t)pool->num_blocks * 2 * pool->n_kv_heads * pool->block_size);
     p.scale_log2 = scale * 1.4426950408889634f;
     const int limit_ms = env_int("PKV_TEST_WAIT_LIMIT_MS", 0);
