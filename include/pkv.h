@@ -236,7 +236,8 @@ pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes
  *   max_q_len: host int >= every n_b (sizes the grid; 0 launches nothing).
  *   block_tables_dev: int32 [B][max_blocks]; context_lens_dev: int32 [B].
  * Supported: bf16 pools with head_dim 128; n_q_heads / n_kv_heads a power of two <= 128;
- * B <= 65535; scale positive and finite.  Otherwise PKV_ERR_INVALID_ARG (nothing launched).  A chunk longer than its
+ * B * n_kv_heads * ceil(max_q_len * n_q_heads / n_kv_heads / 256) < 2^31; scale positive and
+ * finite.  Otherwise PKV_ERR_INVALID_ARG (nothing launched).  A chunk longer than its
  * context or a context longer than max_blocks*block_size is skipped and a block id outside the
  * pool is read as zeros; both are flagged (PKV_ERR_BOUNDS via pkv_check_device_error).  Every
  * wait in the kernel is bounded (2 s); on expiry the results are invalid and

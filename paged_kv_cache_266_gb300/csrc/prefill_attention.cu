@@ -8,7 +8,8 @@
 // h = j / G,
 //     out[cu_q[b] + i][j] = sum_{t <= L-n+i} softmax_t(scale * q . K_b[t]) V_b[t].
 //
-// Work decomposition: one CTA per (sequence, KV head, pair of 128-row query tiles).  A row is
+// Work decomposition: one CTA per (sequence, KV head, pair of 128-row query tiles); CTAs of
+// the sequences with the most causal work are dispatched first.  A row is
 // a (token, head-in-group) pair, so a tile covers 128/G consecutive chunk tokens and all G
 // query heads of one KV head, and every K/V tile brought on chip serves both query tiles and
 // the whole group.  The CTA walks the KV tiles of 128 keys its last token can see:
@@ -63,7 +64,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (P stays <= 2^8)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kEndBar = 1;  // named barrier: every role done before TMEM is released
+constexpr uint32_t kEndBar = 1;
+constexpr int kMaxRankedSeqs = 512;  // above this the sequences are dispatched in index order  // named barrier: every role done before TMEM is released
 
 // mbarrier slots
 constexpr int kBarQ = 0;                       // Q rows of both tiles written (8 warps arrive)
@@ -82,7 +84,7 @@ struct Params {
     const int32_t* tables;
     const int32_t* ctx;
     int* err;
-    int Hq, Hkv, G, max_blocks, bs, part, num_blocks, tiles;
+    int B, Hq, Hkv, G, max_blocks, bs, part, num_blocks, tiles;
     int32_t oob_row;  // a row coordinate past the pool: the copy fills the box with zeros
     float scale_log2;
     uint64_t wait_ns;
@@ -103,11 +105,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sKV = base + kOffKV;
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int pair = p.tiles - 1 - (int)blockIdx.x;  // deepest pairs (most keys) launch first
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     ptx::grid_dependency_wait();  // inputs may come from the preceding append
+    // Dispatch order (1-D grid, CTAs start roughly in index order): sequences by decreasing
+    // causal work n (2L - n), then the pairs of a sequence deepest first, heads fastest -- the
+    // longest jobs start first, so the last wave holds the short ones.
+    const int per_seq = p.Hkv * p.tiles;
+    const int rank = (int)(blockIdx.x / (unsigned)per_seq);
+    const int rem = (int)(blockIdx.x % (unsigned)per_seq);
+    const int h = rem % p.Hkv;
+    const int pair = p.tiles - 1 - rem / p.Hkv;
+    int b = rank;
+    if (p.B <= kMaxRankedSeqs) {
+        __shared__ int seq_of_rank;
+        if (threadIdx.x == 0) seq_of_rank = -1;
+        __syncthreads();
+        auto work = [&](int i) -> int64_t {
+            const int64_t nn = p.cu_q[i + 1] - p.cu_q[i], ll = p.ctx[i];
+            return nn * (2 * ll - nn);
+        };
+        for (int i = threadIdx.x; i < p.B; i += kThreads) {
+            const int64_t wi = work(i);
+            int r = 0;
+            for (int k = 0; k < p.B; ++k) {
+                const int64_t wk = work(k);
+                r += (wk > wi || (wk == wi && k < i)) ? 1 : 0;
+            }
+            if (r == rank) seq_of_rank = i;
+        }
+        __syncthreads();
+        b = seq_of_rank;
+    }
     const int q0 = p.cu_q[b];
     const int n = p.cu_q[b + 1] - q0;
     const int L = p.ctx[b];
@@ -304,18 +333,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32 * c));
             ptx::tmem_wait_ld();
             const int kbase = j * kKeys;
-            float smax = -INFINITY;
+            // row maximum with 8 independent accumulators (no serial chain of 128 dependent ops)
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             if (kbase + kKeys - 1 > qlim) {  // the tile crosses this row's position: mask
 #pragma unroll
                 for (int c = 0; c < kKeys; ++c) {
                     const float x = kbase + c <= qlim ? __uint_as_float(sraw[c]) : -INFINITY;
                     sraw[c] = __float_as_uint(x);
-                    smax = fmaxf(smax, x);
+                    mx8[c & 7] = fmaxf(mx8[c & 7], x);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) smax = fmaxf(smax, __uint_as_float(sraw[c]));
+                for (int c = 0; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sraw[c]));
             }
+            const float smax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float mt = smax * c2;  // this tile's maximum, scaled (finite: key kbase <= qlim)
             // lazy rescale: keep the running maximum unless this tile exceeds it by 2^8
             const bool grow = mt > m + kRescaleLog2;
@@ -334,7 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (grow) m = mt;
             const float nm = -m;
-            if (j == 0) {  // P as hi + lo bf16 pair: columns 0-63 and 64-127
+            float l8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l8[e] = 0.f;
+            if (j == 0) {  // P as hi + lo bf16 pair: columns 0-63 and 64-127; l from p itself
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t hi[32], lo[32];
@@ -343,14 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e]), c2, nm));
                         const float p1 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e + 1]), c2, nm));
                         hi[e] = ptx::pack_bf16x2(p0, p1);
-                        const float h0 = ptx::bf16lo_to_f32(hi[e]), h1 = ptx::bf16hi_to_f32(hi[e]);
-                        lo[e] = ptx::pack_bf16x2(p0 - h0, p1 - h1);
-                        l += (h0 + h1) + (ptx::bf16lo_to_f32(lo[e]) + ptx::bf16hi_to_f32(lo[e]));
+                        lo[e] = ptx::pack_bf16x2(p0 - ptx::bf16lo_to_f32(hi[e]), p1 - ptx::bf16hi_to_f32(hi[e]));
+                        l8[(2 * e) & 7] += p0;
+                        l8[(2 * e + 1) & 7] += p1;
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
                     ptx::tmem_st32(tS + 64u + 32u * c, lo);
                 }
-            } else {
+            } else {  // l from the unrounded p: the rounding of P averages out over the context
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t hi[32];
@@ -359,11 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e]), c2, nm));
                         const float p1 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e + 1]), c2, nm));
                         hi[e] = ptx::pack_bf16x2(p0, p1);
-                        l += ptx::bf16lo_to_f32(hi[e]) + ptx::bf16hi_to_f32(hi[e]);
+                        l8[(2 * e) & 7] += p0;
+                        l8[(2 * e + 1) & 7] += p1;
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
                 }
             }
+            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
@@ -427,7 +466,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     if (Hq % pool->n_kv_heads) return PKV_ERR_INVALID_ARG;
     const int G = Hq / pool->n_kv_heads;
     if (G > kRows || (G & (G - 1))) return PKV_ERR_INVALID_ARG;
-    if (B > 65535 || pool->n_kv_heads > 65535) return PKV_ERR_INVALID_ARG;
+    if (pool->n_kv_heads > 65535) return PKV_ERR_INVALID_ARG;
     if (B == 0 || max_q_len == 0) {
         grid = dim3(0);
         return PKV_OK;
@@ -454,7 +493,10 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     p.scale_log2 = scale * 1.4426950408889634f;
     const int limit_ms = env_int("PKV_TEST_WAIT_LIMIT_MS", 0);
     p.wait_ns = limit_ms > 0 ? (uint64_t)limit_ms * 1000000ull : kWaitLimitNs;
-    grid = dim3((unsigned)p.tiles, (unsigned)pool->n_kv_heads, (unsigned)B);
+    p.B = B;
+    const int64_t ctas = (int64_t)B * pool->n_kv_heads * p.tiles;
+    if (ctas > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    grid = dim3((unsigned)ctas);
     return PKV_OK;
 }
 
