@@ -46,6 +46,8 @@ struct pkv_pool {
     CUtensorMap tmap_rows;
     // 16 rows of one 128-byte panel (the tail of a sequence's last page part).
     CUtensorMap tmap_tail;
+    // min(bs, 64) rows of one 128-byte panel (prefill: page parts stacked into 128-row panels).
+    CUtensorMap tmap_panel;
 
     pkv_allocator* alloc = nullptr;
 };

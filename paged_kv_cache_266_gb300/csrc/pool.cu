@@ -75,6 +75,12 @@ bool encode_rows_map(pkv_pool* p) {
     cuuint32_t box2[2] = {inner, 16};
     r = encode(&p->tmap_tail, dt, 2, p->kv, dims2, strides2, box2, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    // Panel descriptor (prefill): min(bs, 64) rows of one 128-byte panel of K or V, so that the
+    // rows of consecutive page parts land contiguously in one 128-row panel in shared memory.
+    cuuint32_t box3[2] = {inner, box_rows};
+    r = encode(&p->tmap_panel, dt, 2, p->kv, dims2, strides2, box3, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -13,14 +13,18 @@
 // a (token, head-in-group) pair, so a tile covers 128/G consecutive chunk tokens and all G
 // query heads of one KV head, and every K/V tile brought on chip serves both query tiles and
 // the whole group.  The CTA walks the KV tiles of 128 keys its last token can see:
-//   warp 0     TMA producer: one 4-D tensor copy per page part (K and V, both 64-element
-//              panels, 128-byte swizzled) into a two-stage ring; parts past the context get a
+//   warp 0     TMA producer: a stage holds four 128-row panels, K and V each split into two
+//              64-element halves, 128-byte swizzled; one 2-D tensor copy per (page part, K/V,
+//              half) stacks the parts' rows into the panels; parts past the context get a
 //              coordinate past the pool, which the copy fills with zeros.
 //   warp 1     tensor-memory owner and MMA issuer (one thread), per KV tile j and query tile t:
 //                O_t += P_t(j) V_j      M=128, N=128, K=16 per instruction, A = P straight
 //                                       from tensor memory, B = V MN-major from the page copy
-//                S_t(j+1) = Q_t K_{j+1}^T  M=128, N=part, K=128, written over P_t(j): the
-//                                       tensor pipe runs one thread's MMAs in issue order
+//                S_t(j+1) = Q_t K_{j+1}^T  M=128, N=128, K=16 per instruction, written over
+//                                       P_t(j): the tensor pipe runs one thread's MMAs in
+//                                       issue order
+//              with descriptors built once and advanced by constant offsets (issuing must
+//              stay faster than the ~65 cycles an M=128 N=128 K=16 MMA takes).
 //              so one tile's MMAs run while the other tile's softmax works.
 //   warps 2-3  idle (they complete the control warpgroup, which gives registers away)
 //   warps 4-7, 8-11  one softmax warpgroup per query tile, one row per thread (TMEM lane =
@@ -94,8 +98,11 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
 }
 
+template <int PART>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
+    static_assert(PART == 16 || PART == 32 || PART == 64, "page part of 16, 32 or 64 rows");
+    constexpr int kParts = kKeys / PART;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
@@ -171,8 +178,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_s;
-    const int parts = kKeys / p.part;
-    const uint32_t part_bytes = 4u * (uint32_t)p.part * 128u;
 
     if (warp < 4) {
       ptx::regs_dec<kRegsControl>();  // the whole control warpgroup, one instruction
@@ -196,26 +201,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__shfl_sync(0xffffffffu, abort_s, 0)) break;  // warp-uniform
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull + s), kStageBytes);
             __syncwarp();
-            if (lane < parts) {
-                const int tok = j * kKeys + lane * p.part;  // first key of this page part
+            // stage layout: four 128-row panels [K lo | K hi | V lo | V hi] (64 elements each);
+            // lane -> (page part, K/V, panel): one copy of PART rows
+            if (lane < 4 * kParts) {
+                const int pi = lane >> 2, kv = (lane >> 1) & 1, q = lane & 1;
+                const int tok = j * kKeys + pi * PART;  // first key of this page part
                 int32_t row = p.oob_row;
                 if (tok < L) {
                     const int blk = tb[tok / p.bs];
                     if (blk >= 0 && blk < p.num_blocks)
-                        row = (int32_t)(((int64_t)2 * blk * p.Hkv + h) * p.bs + (tok % p.bs));
-                    else
+                        row = (int32_t)((((int64_t)2 * blk + kv) * p.Hkv + h) * p.bs + (tok % p.bs));
+                    else if (kv == 0 && q == 0)
                         atomicOr(p.err, kErrBounds);
                 }
-                ptx::tma_load_4d(sKV + (uint32_t)s * kStageBytes + (uint32_t)lane * part_bytes, &tmap, 0, row, 0, 0,
-                                 bar(kBarFull + s));
+                ptx::tma_load_2d(sKV + (uint32_t)s * kStageBytes + (uint32_t)(2 * kv + q) * kPanelBytes +
+                                     (uint32_t)(pi * PART) * 128u,
+                                 &tmap, q * 64, row, bar(kBarFull + s));
             }
         }
         ptx::named_barrier_sync(kEndBar, kThreads);
       } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idS = ptx::umma_idesc_bf16(128, p.part, 0, 0);
-            const uint32_t idO = ptx::umma_idesc_bf16(128, kD, 0, 1);
+            // descriptors are built once; the start-address field counts 16-byte units, so moving
+            // an operand by X bytes adds X >> 4 (addresses stay below 256 KB: no carry out)
+            constexpr uint32_t idS = ptx::umma_idesc_bf16(128, kKeys, 0, 0);
+            constexpr uint32_t idO = ptx::umma_idesc_bf16(128, kD, 0, 1);
+            const uint64_t dQ0 = ptx::umma_sdesc_sw128(base + kOffQ, 16, 1024);
+            const uint64_t dK0 = ptx::umma_sdesc_sw128(sKV, 16, 1024);
+            const uint64_t dV0 = ptx::umma_sdesc_sw128(sKV + 2 * kPanelBytes, kPanelBytes, 1024);
             int kv_ready = 0;  // KV tiles whose copies this thread has waited for
             bool ok = ptx::mbar_wait(bar(kBarQ), 0, p.wait_ns);
             ptx::tc_fence_after();
@@ -226,38 +240,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kv_ready = j + 1;
                 return true;
             };
+            // S_t(j) = Q_t K_j^T: 8 MMAs of N = 128 (keys past the context give unused scores)
             auto issue_s = [&](int t, int j) {
-                const uint32_t kst = sKV + (uint32_t)(j % kStages) * kStageBytes;
-                const uint32_t qt = base + kOffQ + (uint32_t)t * kQBytes;
-                for (int pi = 0; pi < parts; ++pi) {
-                    if (j * kKeys + pi * p.part >= L) break;  // past the context: scores unused
-                    const uint32_t kpart = kst + (uint32_t)pi * part_bytes;
-#pragma unroll
-                    for (int k = 0; k < kD / 16; ++k) {
-                        const uint64_t a = ptx::umma_sdesc_sw128(
-                            qt + (uint32_t)(k >> 2) * kPanelBytes + (uint32_t)(k & 3) * 32u, 16, 1024);
-                        const uint64_t bd = ptx::umma_sdesc_sw128(
-                            kpart + (uint32_t)(k >> 2) * (uint32_t)p.part * 128u + (uint32_t)(k & 3) * 32u, 16, 1024);
-                        ptx::umma_bf16(tmem + (uint32_t)(t * kKeys + pi * p.part), a, bd, idS, k > 0 ? 1u : 0u);
-                    }
+                const uint64_t dq = dQ0 + (uint64_t)(t * (kQBytes >> 4));
+                const uint64_t dk = dK0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
+#pragma unroll 1
+                for (int k = 0; k < kD / 16; ++k) {
+                    constexpr uint32_t kPanel16 = kPanelBytes >> 4;
+                    const uint32_t off = (uint32_t)(k >> 2) * kPanel16 + (uint32_t)(k & 3) * 2u;
+                    ptx::umma_bf16(tmem + (uint32_t)(t * kKeys), dq + off, dk + off, idS, k > 0 ? 1u : 0u);
                 }
                 ptx::umma_commit(bar(kBarS + t));
             };
+            // O_t += P_t(j) V_j: 16 keys per MMA, A from TMEM; on the first KV tile also the lo part
             auto issue_pv = [&](int t, int j) {
-                const uint32_t vst = sKV + (uint32_t)(j % kStages) * kStageBytes;
+                const uint64_t dv = dV0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
                 const uint32_t tP = tmem + (uint32_t)(t * kKeys), tO = tmem + kColO + (uint32_t)(t * kD);
-                const int halves = j == 0 ? 2 : 1;  // hi and lo parts of P on the first KV tile
-                for (int half = 0; half < halves; ++half) {
-                    for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        const int tok = 16 * kk;  // key within the tile
-                        if (j * kKeys + tok >= L) break;  // all-zero P columns from here on
-                        const int pi = tok / p.part, c = (tok % p.part) >> 4;
-                        const uint32_t vpart = vst + (uint32_t)pi * part_bytes + 2u * (uint32_t)p.part * 128u;
-                        const uint64_t bd =
-                            ptx::umma_sdesc_sw128(vpart + (uint32_t)c * 2048u, (uint32_t)p.part * 128u, 1024);
-                        ptx::umma_bf16_tmem_a(tO, tP + (uint32_t)(half * 64 + 8 * kk), bd, idO,
-                                              (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
-                    }
+                const int left = L - j * kKeys;  // keys of this tile inside the context (> 0)
+                const int nk = left >= kKeys ? kKeys / 16 : (left + 15) / 16;
+#pragma unroll 1
+                for (int kk = 0; kk < nk; ++kk)
+                    ptx::umma_bf16_tmem_a(tO, tP + (uint32_t)(8 * kk), dv + (uint64_t)(kk * 128), idO,
+                                          (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == 0) {
+#pragma unroll 1
+                    for (int kk = 0; kk < nk; ++kk)
+                        ptx::umma_bf16_tmem_a(tO, tP + (uint32_t)(64 + 8 * kk), dv + (uint64_t)(kk * 128), idO, 1u);
                 }
             };
             if (ok) ok = wait_kv(0);
@@ -451,7 +459,11 @@ int env_int(const char* name, int dflt) {
 
 void prefill_configure(pkv_pool* pool) {
     (void)pool;
-    cudaFuncSetAttribute(prefill::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(prefill::prefill_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)prefill::kSmemBytes);
+    cudaFuncSetAttribute(prefill::prefill_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)prefill::kSmemBytes);
+    cudaFuncSetAttribute(prefill::prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)prefill::kSmemBytes);
 }
 
@@ -511,8 +523,13 @@ pkv_status prefill_launch(const pkv_pool* pool, const prefill::Params& p, dim3 g
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill::prefill_kernel, pool->tmap_rows, p) == cudaSuccess ? PKV_OK
-                                                                                                  : PKV_ERR_CUDA;
+    cudaError_t e;
+    switch (p.part) {
+        case 16: e = cudaLaunchKernelEx(&cfg, prefill::prefill_kernel<16>, pool->tmap_panel, p); break;
+        case 32: e = cudaLaunchKernelEx(&cfg, prefill::prefill_kernel<32>, pool->tmap_panel, p); break;
+        default: e = cudaLaunchKernelEx(&cfg, prefill::prefill_kernel<64>, pool->tmap_panel, p); break;
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv
