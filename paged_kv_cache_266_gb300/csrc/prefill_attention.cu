@@ -13,10 +13,11 @@
 // a (token, head-in-group) pair, so a tile covers 128/G consecutive chunk tokens and all G
 // query heads of one KV head, and every K/V tile brought on chip serves both query tiles and
 // the whole group.  The CTA walks the KV tiles of 128 keys its last token can see:
-//   warp 0     TMA producer: a stage holds four 128-row panels, K and V each split into two
-//              64-element halves, 128-byte swizzled; one 2-D tensor copy per (page part, K/V,
-//              half) stacks the parts' rows into the panels; parts past the context get a
-//              coordinate past the pool, which the copy fills with zeros.
+//   warps 0, 2 TMA producers of a K ring (3 tiles) and a V ring (2 tiles): a tile is two
+//              128-row panels (the 64-element halves, 128-byte swizzled), one 2-D tensor copy
+//              per (page part, half) stacking the parts' rows; parts past the context get a
+//              coordinate past the pool, which the copy fills with zeros.  K and V are released
+//              separately (after the last S, after the last PV), so K runs further ahead.
 //   warp 1     tensor-memory owner and MMA issuer (one thread), per KV tile j and query tile t:
 //                O_t += P_t(j) V_j      M=128, N=128, K=16 per instruction, A = P straight
 //                                       from tensor memory, B = V MN-major from the page copy
@@ -26,7 +27,7 @@
 //              with descriptors built once and advanced by constant offsets (issuing must
 //              stay faster than the ~65 cycles an M=128 N=128 K=16 MMA takes).
 //              so one tile's MMAs run while the other tile's softmax works.
-//   warps 2-3  idle (they complete the control warpgroup, which gives registers away)
+//   warp 3     idle (it completes the control warpgroup, which gives registers away)
 //   warps 4-7, 8-11  one softmax warpgroup per query tile, one row per thread (TMEM lane =
 //              row): the Q row into shared memory, then per KV tile the S row out of TMEM,
 //              causal mask on the tiles that cross the row's position, online softmax in base
@@ -51,35 +52,41 @@ constexpr int kD = 128;
 constexpr int kRows = 128;   // query rows per tile
 constexpr int kTiles = 2;    // query tiles per CTA
 constexpr int kKeys = 128;   // keys per KV tile
-constexpr int kStages = 2;
+constexpr int kKStages = 3;  // K ring: a K tile is free once both tiles' S MMAs have read it
+constexpr int kVStages = 2;  // V ring: a V tile is free once both tiles' PV MMAs have read it
 constexpr int kThreads = 128 + kTiles * 128;  // control warpgroup + one softmax warpgroup per tile
 // register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded down to 8),
 // i.e. 64512 for the block; control 128 x 48 + softmax 256 x 224 = 63488 fits.
 constexpr uint32_t kRegsControl = 48, kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + kTiles * 128 * kRegsSoftmax <= kThreads * 168, "register split");
-constexpr uint32_t kPanelBytes = 128u * 128u;          // 128 rows x 128 bytes
-constexpr uint32_t kQBytes = 2 * kPanelBytes;          // one Q tile: two 64-element panels
-constexpr uint32_t kStageBytes = 4u * kKeys * 128u;    // K and V, two panels each
+constexpr uint32_t kPanelBytes = 128u * 128u;      // 128 rows x 128 bytes
+constexpr uint32_t kQBytes = 2 * kPanelBytes;      // one Q tile: two 64-element panels
+constexpr uint32_t kHalfBytes = 2 * kPanelBytes;   // K (or V) of one KV tile: two panels
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kTiles * kQBytes;
-constexpr uint32_t kOffBar = kOffKV + kStages * kStageBytes;
+constexpr uint32_t kOffK = kOffQ + kTiles * kQBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kHalfBytes;
+constexpr uint32_t kOffBar = kOffV + kVStages * kHalfBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (P stays <= 2^8)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kEndBar = 1;
-constexpr int kMaxRankedSeqs = 512;  // above this the sequences are dispatched in index order  // named barrier: every role done before TMEM is released
+constexpr uint32_t kEndBar = 1;      // named barrier: every role done before TMEM is released
+constexpr int kMaxRankedSeqs = 512;  // above this the sequences are dispatched in index order
 
 // mbarrier slots
-constexpr int kBarQ = 0;                       // Q rows of both tiles written (8 warps arrive)
-constexpr int kBarFull = 1;                    // [kStages] K/V copies landed (tx bytes)
-constexpr int kBarEmpty = kBarFull + kStages;  // [kStages] last PV of the stage's tile done
-constexpr int kBarS = kBarEmpty + kStages;     // [kTiles] S_t(j) ready (commit)
-constexpr int kBarP = kBarS + kTiles;          // [kTiles] P_t(j) in TMEM (4 warps arrive)
-constexpr int kBarO = kBarP + kTiles;          // [kTiles] last PV_t done (commit)
-constexpr int kBarDrain = kBarO + kTiles;      // MMAs in flight done (error path)
+constexpr int kBarQ = 0;                          // Q rows of both tiles written (8 warps arrive)
+constexpr int kBarKFull = 1;                      // [kKStages] K copies landed (tx bytes)
+constexpr int kBarKEmpty = kBarKFull + kKStages;  // [kKStages] last S MMA reading the K tile done
+constexpr int kBarVFull = kBarKEmpty + kKStages;  // [kVStages] V copies landed (tx bytes)
+constexpr int kBarVEmpty = kBarVFull + kVStages;  // [kVStages] last PV MMA reading the V tile done
+constexpr int kBarS = kBarVEmpty + kVStages;      // [kTiles] S_t(j) ready (commit)
+constexpr int kBarP = kBarS + kTiles;             // [kTiles] P_t(j) in TMEM (4 warps arrive)
+constexpr int kBarO = kBarP + kTiles;             // [kTiles] last PV_t done (commit)
+constexpr int kBarDrain = kBarO + kTiles;         // MMAs in flight done (error path)
 constexpr int kNumBars = kBarDrain + 1;
+static_assert(kNumBars * 8 <= 256, "barrier area");
 
 struct Params {
     const uint16_t* q;
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const sm = smem_raw + (base - raw);
-    const uint32_t sKV = base + kOffKV;
+    const uint32_t sK = base + kOffK, sV = base + kOffV;
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,14 +188,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
       ptx::regs_dec<kRegsControl>();  // the whole control warpgroup, one instruction
-      if (warp == 0) {
-        // ---------------------------------------------------------------- producer
+      if (warp == 0 || warp == 2) {
+        // ---------------------------------------------------------------- producers
+        // warp 0 fills the K ring, warp 2 the V ring; each KV tile is two 128-row panels (the
+        // 64-element halves), one 2-D copy of PART rows per (page part, half)
+        const int kv = warp == 0 ? 0 : 1;
+        const int stages = kv ? kVStages : kKStages;
+        const uint32_t ring = kv ? sV : sK;
+        const int full = kv ? kBarVFull : kBarKFull, empty = kv ? kBarVEmpty : kBarKEmpty;
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
         for (int j = 0; j < n_kv; ++j) {
-            const int s = j % kStages;
-            if (j >= kStages) {
+            const int s = j % stages;
+            if (j >= stages) {
                 bool ok = true;
-                if (lane == 0) ok = ptx::mbar_wait(bar(kBarEmpty + s), ((j / kStages) - 1) & 1, p.wait_ns);
+                if (lane == 0) ok = ptx::mbar_wait(bar(empty + s), ((j / stages) - 1) & 1, p.wait_ns);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) {
                     if (lane == 0) {
@@ -199,12 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (__shfl_sync(0xffffffffu, abort_s, 0)) break;  // warp-uniform
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull + s), kStageBytes);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(full + s), kHalfBytes);
             __syncwarp();
-            // stage layout: four 128-row panels [K lo | K hi | V lo | V hi] (64 elements each);
-            // lane -> (page part, K/V, panel): one copy of PART rows
-            if (lane < 4 * kParts) {
-                const int pi = lane >> 2, kv = (lane >> 1) & 1, q = lane & 1;
+            if (lane < 2 * kParts) {
+                const int pi = lane >> 1, q = lane & 1;
                 const int tok = j * kKeys + pi * PART;  // first key of this page part
                 int32_t row = p.oob_row;
                 if (tok < L) {
@@ -214,9 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else if (kv == 0 && q == 0)
                         atomicOr(p.err, kErrBounds);
                 }
-                ptx::tma_load_2d(sKV + (uint32_t)s * kStageBytes + (uint32_t)(2 * kv + q) * kPanelBytes +
-                                     (uint32_t)(pi * PART) * 128u,
-                                 &tmap, q * 64, row, bar(kBarFull + s));
+                ptx::tma_load_2d(ring + (uint32_t)s * kHalfBytes + (uint32_t)q * kPanelBytes + (uint32_t)(pi * PART) * 128u,
+                                 &tmap, q * 64, row, bar(full + s));
             }
         }
         ptx::named_barrier_sync(kEndBar, kThreads);
@@ -227,62 +237,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             // an operand by X bytes adds X >> 4 (addresses stay below 256 KB: no carry out)
             constexpr uint32_t idS = ptx::umma_idesc_bf16(128, kKeys, 0, 0);
             constexpr uint32_t idO = ptx::umma_idesc_bf16(128, kD, 0, 1);
+            // a descriptor's high half (stride, version, swizzle) is the same for Q and K; V's
+            // differs only in the low half (its panel stride)
             const uint64_t dQ0 = ptx::umma_sdesc_sw128(base + kOffQ, 16, 1024);
-            const uint64_t dK0 = ptx::umma_sdesc_sw128(sKV, 16, 1024);
-            const uint64_t dV0 = ptx::umma_sdesc_sw128(sKV + 2 * kPanelBytes, kPanelBytes, 1024);
-            int kv_ready = 0;  // KV tiles whose copies this thread has waited for
+            const uint64_t dK0 = ptx::umma_sdesc_sw128(sK, 16, 1024);
+            const uint64_t dV0 = ptx::umma_sdesc_sw128(sV, kPanelBytes, 1024);
+            const uint32_t hi = (uint32_t)(dQ0 >> 32);
+            const uint32_t q_lo = (uint32_t)dQ0, k_lo = (uint32_t)dK0, v_lo = (uint32_t)dV0;
+            int k_ready = 0, v_ready = 0;  // K / V tiles whose copies this thread has waited for
             bool ok = ptx::mbar_wait(bar(kBarQ), 0, p.wait_ns);
             ptx::tc_fence_after();
-            auto wait_kv = [&](int j) -> bool {
-                if (j < kv_ready) return true;
-                if (!ptx::mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, p.wait_ns)) return false;
+            auto wait_k = [&](int j) -> bool {
+                if (j < k_ready) return true;
+                if (!ptx::mbar_wait(bar(kBarKFull + j % kKStages), (j / kKStages) & 1, p.wait_ns)) return false;
                 ptx::tc_fence_after();
-                kv_ready = j + 1;
+                k_ready = j + 1;
                 return true;
             };
-            // S_t(j) = Q_t K_j^T: 8 MMAs of N = 128 (keys past the context give unused scores)
+            auto wait_v = [&](int j) -> bool {
+                if (j < v_ready) return true;
+                if (!ptx::mbar_wait(bar(kBarVFull + j % kVStages), (j / kVStages) & 1, p.wait_ns)) return false;
+                ptx::tc_fence_after();
+                v_ready = j + 1;
+                return true;
+            };
+            // S_t(j) = Q_t K_j^T: 8 MMAs of N = 128 (keys past the context give unused scores),
+            // issued as one asm block: the issuing thread cannot run ahead of the tensor pipe, so
+            // any arithmetic between two MMAs would be exposed.
             auto issue_s = [&](int t, int j) {
-                const uint64_t dq = dQ0 + (uint64_t)(t * (kQBytes >> 4));
-                const uint64_t dk = dK0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
-#pragma unroll 1
-                for (int k = 0; k < kD / 16; ++k) {
-                    constexpr uint32_t kPanel16 = kPanelBytes >> 4;
-                    const uint32_t off = (uint32_t)(k >> 2) * kPanel16 + (uint32_t)(k & 3) * 2u;
-                    ptx::umma_bf16(tmem + (uint32_t)(t * kKeys), dq + off, dk + off, idS, k > 0 ? 1u : 0u);
-                }
+                ptx::umma_ss_k128_x8(tmem + (uint32_t)(t * kKeys), q_lo + (uint32_t)t * (kQBytes >> 4),
+                                     k_lo + (uint32_t)(j % kKStages) * (kHalfBytes >> 4), hi, idS);
                 ptx::umma_commit(bar(kBarS + t));
+                // the last tile's S releases the K tile, if a later tile reuses its slot
+                if (t == last_tile && j + kKStages < n_kv) ptx::umma_commit(bar(kBarKEmpty + j % kKStages));
             };
             // O_t += P_t(j) V_j: 16 keys per MMA, A from TMEM; on the first KV tile also the lo part
             auto issue_pv = [&](int t, int j) {
-                const uint64_t dv = dV0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
+                const uint32_t dv = v_lo + (uint32_t)(j % kVStages) * (kHalfBytes >> 4);
                 const uint32_t tP = tmem + (uint32_t)(t * kKeys), tO = tmem + kColO + (uint32_t)(t * kD);
                 const int left = L - j * kKeys;  // keys of this tile inside the context (> 0)
                 const int nk = left >= kKeys ? kKeys / 16 : (left + 15) / 16;
-#pragma unroll 1
-                for (int kk = 0; kk < nk; ++kk)
-                    ptx::umma_bf16_tmem_a(tO, tP + (uint32_t)(8 * kk), dv + (uint64_t)(kk * 128), idO,
-                                          (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == 0) {
-#pragma unroll 1
-                    for (int kk = 0; kk < nk; ++kk)
-                        ptx::umma_bf16_tmem_a(tO, tP + (uint32_t)(64 + 8 * kk), dv + (uint64_t)(kk * 128), idO, 1u);
-                }
+                ptx::umma_ts_x8(tO, tP, dv, hi, idO, j > 0 ? 1u : 0u, nk);
+                if (j == 0) ptx::umma_ts_x8(tO, tP + 64u, dv, hi, idO, 1u, nk);
             };
-            if (ok) ok = wait_kv(0);
+            if (ok) ok = wait_k(0);
             if (ok)
                 for (int t = 0; t < kTiles; ++t)
                     if (nkv[t] > 0) issue_s(t, 0);
             for (int j = 0; ok && j < n_kv; ++j) {
                 for (int t = 0; t < kTiles && ok; ++t) {
                     if (j >= nkv[t]) continue;
+                    ok = wait_v(j);
+                    if (!ok) break;
                     ok = ptx::mbar_wait(bar(kBarP + t), j & 1, p.wait_ns);
                     if (!ok) break;
                     ptx::tc_fence_after();
                     issue_pv(t, j);
                     if (j == nkv[t] - 1) ptx::umma_commit(bar(kBarO + t));
-                    if (t == last_tile && j + kStages < n_kv) ptx::umma_commit(bar(kBarEmpty + j % kStages));
+                    if (t == last_tile && j + kVStages < n_kv) ptx::umma_commit(bar(kBarVEmpty + j % kVStages));
                     if (j + 1 < nkv[t]) {
-                        ok = wait_kv(j + 1);
+                        ok = wait_k(j + 1);
                         if (!ok) break;
                         issue_s(t, j + 1);
                     }
@@ -302,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
       } else {
-        ptx::named_barrier_sync(kEndBar, kThreads);  // idle warps of the control warpgroup
+        ptx::named_barrier_sync(kEndBar, kThreads);  // warp 3: idle member of the control warpgroup
       }
     } else {
         ptx::regs_inc<kRegsSoftmax>();

@@ -247,6 +247,85 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// The same two MMAs with each shared-memory descriptor given as its 32-bit halves: the start
+// address lives in the low half, so operands can be advanced with one 32-bit add while the
+// constant high half (stride, version, swizzle) stays in one register.
+__device__ __forceinline__ void umma_bf16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_bf16_tmem_a_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                      uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
+}
+
+// Eight K-steps of D = A B^T with A and B K-major 128-byte-swizzled panels of 128 rows: K steps
+// of 16 elements advance both operands by 32 bytes inside a 128-byte row (+2 in the start field),
+// and the second half of K sits one 16 KB panel further (+1024).  One asm block, so nothing runs
+// between the MMAs.  The first step overwrites D.
+__device__ __forceinline__ void umma_ss_k128_x8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 al, bl;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 pf, %1, %1;\n\tsetp.eq.b32 pt, %1, %1;\n\t"
+        "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pf;\n\t"
+        "add.u32 al, %1, 2;\n\tadd.u32 bl, %2, 2;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 4;\n\tadd.u32 bl, %2, 4;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 6;\n\tadd.u32 bl, %2, 6;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 1024;\n\tadd.u32 bl, %2, 1024;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 1026;\n\tadd.u32 bl, %2, 1026;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 1028;\n\tadd.u32 bl, %2, 1028;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 1030;\n\tadd.u32 bl, %2, 1030;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc));
+}
+
+// Eight steps of D += A B with A (P) in tensor memory, 8 columns (16 elements) per step, and B an
+// MN-major 128-byte-swizzled operand advancing 2048 bytes (16 rows, +128 in the start field) per
+// step.  Step kk runs only if kk < nk; step 0 accumulates only if acc0 != 0.
+__device__ __forceinline__ void umma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                           uint32_t idesc, uint32_t acc0, int nk) {
+    asm volatile(
+        "{\n\t.reg .pred pa, pt, g1, g2, g3, g4, g5, g6, g7;\n\t.reg .b32 ta, bl;\n\t.reg .b64 b;\n\t"
+        "setp.ne.b32 pa, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+        "setp.gt.s32 g1, %6, 1;\n\tsetp.gt.s32 g2, %6, 2;\n\tsetp.gt.s32 g3, %6, 3;\n\t"
+        "setp.gt.s32 g4, %6, 4;\n\tsetp.gt.s32 g5, %6, 5;\n\tsetp.gt.s32 g6, %6, 6;\n\t"
+        "setp.gt.s32 g7, %6, 7;\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, pa;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g1 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.u32 bl, %2, 256;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g2 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.u32 bl, %2, 384;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g3 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 32;\n\tadd.u32 bl, %2, 512;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g4 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 40;\n\tadd.u32 bl, %2, 640;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g5 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 48;\n\tadd.u32 bl, %2, 768;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g6 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 56;\n\tadd.u32 bl, %2, 896;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g7 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc0), "r"(nk));
+}
+
 // Arrive once on the mbarrier when every tcgen05.mma this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
