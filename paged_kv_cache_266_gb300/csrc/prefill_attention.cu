@@ -287,19 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < n_kv; ++j) {
                 for (int t = 0; t < kTiles && ok; ++t) {
                     if (j >= nkv[t]) continue;
-                    ok = wait_v(j);
+                    const bool more = j + 1 < nkv[t];
+                    // everything PV_t(j) and S_t(j+1) need, before either is issued: the two
+                    // batches then go out back to back and the tensor pipe's short queue stays full
+                    ok = wait_v(j) && (!more || wait_k(j + 1));
                     if (!ok) break;
                     ok = ptx::mbar_wait(bar(kBarP + t), j & 1, p.wait_ns);
                     if (!ok) break;
                     ptx::tc_fence_after();
                     issue_pv(t, j);
-                    if (j == nkv[t] - 1) ptx::umma_commit(bar(kBarO + t));
+                    if (more) issue_s(t, j + 1);  // commits S_t and, for the last tile, K_{j+1}'s slot
+                    else ptx::umma_commit(bar(kBarO + t));
                     if (t == last_tile && j + kVStages < n_kv) ptx::umma_commit(bar(kBarVEmpty + j % kVStages));
-                    if (j + 1 < nkv[t]) {
-                        ok = wait_k(j + 1);
-                        if (!ok) break;
-                        issue_s(t, j + 1);
-                    }
                 }
             }
             if (!ok) {
