@@ -5,7 +5,7 @@ reference leg may import this package.  The product library never loads it, and
 it shares no code with the CUDA path: ``pkv_oracle.cpp`` is a plain fp64
 restatement of what the TensorRT-LLM pages describe (allocator, append, FP8
 E4M3 codec, decode attention, split merge, block reuse, chunked-context prefill
-attention, KV-memory formula); see the header of
+attention, RoPE, KV-memory formula); see the header of
 that file for the page and section each function follows.
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
@@ -73,6 +73,9 @@ def _L():
                                                 vp]),
         "oracle_prefill_attention": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, i32, f64, vp,
                                            i32]),
+        "oracle_rope": (None, [vp, vp, i64, i32, i32, f64, vp]),
+        "oracle_rope_f64": (None, [vp, vp, i64, i32, i32, f64, vp]),
+        "oracle_f64_to_bf16_bits": (ctypes.c_uint16, [f64]),
         "oracle_pool_bytes": (i64, [i32, i32, i32, i32, i32]),
         "oracle_scale_floats": (i64, [i32, i32]),
         "oracle_elem_byte": (i64, [i64, i32, i32, i32, i32, i32, i32, i32, i32]),
@@ -246,6 +249,30 @@ class Pool:
         if rc:
             raise RuntimeError(f"oracle split attention rc={rc}")
         return out
+
+
+def rope(x_bits, positions, base: float) -> np.ndarray:
+    """RoPE ("rotate half") of bf16 rows [N][H][D] at the given positions, rounded to bf16 bits."""
+    x = _c(x_bits, np.uint16)
+    pos = _c(positions, np.int64)
+    N, H, D = x.shape
+    out = np.empty_like(x)
+    _L().oracle_rope(_p(x), _p(pos), N, H, D, float(base), _p(out))
+    return out
+
+
+def rope_f64(x, positions, base: float) -> np.ndarray:
+    """The same rotation in fp64 without rounding (x: float64 [N][H][D])."""
+    x = _c(x, np.float64)
+    pos = _c(positions, np.int64)
+    N, H, D = x.shape
+    out = np.empty_like(x)
+    _L().oracle_rope_f64(_p(x), _p(pos), N, H, D, float(base), _p(out))
+    return out
+
+
+def f64_to_bf16_bits(x: float) -> int:
+    return int(_L().oracle_f64_to_bf16_bits(float(x)))
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:

@@ -32,6 +32,8 @@
 //    推理加速实战" §8 (KV cache reuse) — a forked sequence holds its source's whole prefix
 //    pages (holder counts), a copy of the partial last one, and pages return to the free
 //    list when their last holder releases them.
+//  * RoPE fused into the append: "TensorRT-LLM 深度实战" §3.3-3.4 (use_fused_rope), the
+//    Llama "rotate half" form (see the function).
 //  * Prefill (chunked-context) attention: "TensorRT-LLM 深度实战" §7.3 and "TensorRT-LLM
 //    推理加速实战" §7.2 (context_fmha) — every query of a chunk is the decode definition over
 //    the tokens up to and including its own position.
@@ -508,6 +510,77 @@ int oracle_prefill_attention(const uint8_t* pool, const float* scales, int num_b
         if (s) return s;
     return 0;
 }
+
+// ---------------------------------------------------------------------------- RoPE
+// Rotary position embedding fused into the append ("TensorRT-LLM 深度实战" §3.3: the attention
+// kernels also fuse RoPE; the build option use_fused_rope, §3.4).  The pages do not spell RoPE
+// out; this is the form the Llama models the workloads follow use ("rotate half"): element d of
+// the first half pairs with d + D/2, and at position p the pair turns by the angle
+// p * base^(-2d/D):
+//     y[d]       = x[d] cos - x[d + D/2] sin
+//     y[d + D/2] = x[d + D/2] cos + x[d] sin
+// computed in fp64 (products and sums rounded separately), then rounded to bf16 (nearest, ties
+// to even).
+
+// fp64 -> bf16 bits, round to nearest even: written from the format's definition (8 significant
+// bits, exponent range of fp32, subnormals down to 2^-133).
+static uint16_t oracle_f64_to_bf16(double x) {
+    if (std::isnan(x)) return 0x7fc0;
+    const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+    double a = std::fabs(x);
+    if (std::isinf(a)) return sign | 0x7f80;
+    if (a == 0.0) return sign;
+    int e;
+    std::frexp(a, &e);  // a = f * 2^e, f in [0.5, 1): the leading bit has weight 2^(e-1)
+    int lead = e - 1;
+    if (lead < -126) lead = -126;              // subnormal: fixed unit 2^-133
+    const double unit = std::ldexp(1.0, lead - 7);  // one bf16 ulp at this exponent
+    double k = std::nearbyint(a / unit);        // exact division by a power of two; ties to even
+    double r = k * unit;                        // the rounded magnitude (may carry to 2^(lead+1))
+    if (r >= std::ldexp(1.0, 128)) return sign | 0x7f80;
+    // r is a bf16 value, so as fp32 its low 16 bits are zero
+    const float rf = (float)r;
+    uint32_t bits;
+    std::memcpy(&bits, &rf, 4);
+    return sign | (uint16_t)(bits >> 16);
+}
+
+// x, out: [N][H][D] bf16 bits; pos: [N].  out may alias x.
+void oracle_rope(const uint16_t* x, const int64_t* pos, int64_t N, int H, int D, double base, uint16_t* out) {
+    std::vector<double> row(D);
+    for (int64_t i = 0; i < N; ++i)
+        for (int h = 0; h < H; ++h) {
+            const int64_t off = (i * H + h) * D;
+            for (int d = 0; d < D; ++d) row[d] = bf16_to_double(x[off + d]);
+            for (int d = 0; d < D / 2; ++d) {
+                const double inv_freq = std::pow(base, -2.0 * d / D);
+                const double ang = (double)pos[i] * inv_freq;
+                const double c = std::cos(ang), s = std::sin(ang);
+                const double a = row[d], b = row[d + D / 2];
+                const double y0 = a * c - b * s;
+                const double y1 = b * c + a * s;
+                out[off + d] = oracle_f64_to_bf16(y0);
+                out[off + d + D / 2] = oracle_f64_to_bf16(y1);
+            }
+        }
+}
+
+// The same rotation without the final rounding (fp64 out), for the invariants.
+void oracle_rope_f64(const double* x, const int64_t* pos, int64_t N, int H, int D, double base, double* out) {
+    for (int64_t i = 0; i < N; ++i)
+        for (int h = 0; h < H; ++h) {
+            const int64_t off = (i * H + h) * D;
+            for (int d = 0; d < D / 2; ++d) {
+                const double ang = (double)pos[i] * std::pow(base, -2.0 * d / D);
+                const double c = std::cos(ang), s = std::sin(ang);
+                const double a = x[off + d], b = x[off + d + D / 2];
+                out[off + d] = a * c - b * s;
+                out[off + d + D / 2] = b * c + a * s;
+            }
+        }
+}
+
+uint16_t oracle_f64_to_bf16_bits(double x) { return oracle_f64_to_bf16(x); }
 
 // Same result computed split-wise: the context is cut into chunks of `chunk` tokens, each chunk
 // yields (m, l, o) and the chunks are merged with the log-sum-exp rule.  Single-threaded.
