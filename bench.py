@@ -544,6 +544,65 @@ def run_prefill(args, world, rank, local):
     st.close()
 
 
+def run_rope(args, world, rank, local):
+    """Decode step with RoPE fused into the append (Llama-3-8B GQA batch of workload c2): the
+    step's new K rows and query rows are rotated in the append kernel, then the attention runs
+    as its programmatic dependent. Timed beside the same step without RoPE."""
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    torch.cuda.set_device(local)
+    w = W.make_workload("c2")
+    st = DecodeStep(w, device=f"cuda:{local}")
+    pos = torch.from_numpy(w.lens.astype(np.int64)).to(st.device)
+    base = 500000.0
+    nbytes = algorithmic_bytes(w)
+    stream = torch.cuda.current_stream()
+    K = max(3, min(args.steps, 2000))
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        torch.cuda.synchronize()
+        for k in range(K):
+            e0[k].record(stream)
+            fn()
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e0[k].elapsed_time(e1[k]) for k in range(K))
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    step_ms = timed(lambda: st.step())
+    rope_ms = timed(lambda: pkv.pkv_decode_step_rope(st.pool.handle, st.k_new, st.v_new, st.slots_new, pos, base, st.q,
+                                                     st.tables, st.lens, st.scale, st.out, st.workspace))
+    append_ms = timed(lambda: st.append())
+    append_rope_ms = timed(lambda: pkv.pkv_append_rope(st.pool.handle, st.k_new, st.v_new, st.slots_new, pos, base,
+                                                       q=st.q))
+    clocks = sampler.stop()
+    if pkv.pkv_check_device_error(st.pool.handle) != 0:
+        raise RuntimeError("device error flag set")
+    if rank == 0:
+        print(json.dumps({
+            "metric": "decode step with RoPE fused into the append: KV GB/s (c2 batch)",
+            "value": round(world * nbytes["step"] / (rope_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(rope_ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32-accumulate on bf16 KV; RoPE in fp64",
+            "data": "synthetic", "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                                            "head_dim": w.D, "rope_base": base,
+                                            "l2": "inputs larger than L2 (KV read per step > L2)"},
+            "kernel_us": {"step_without_rope": round(step_ms * 1e3, 2), "step_with_rope": round(rope_ms * 1e3, 2),
+                          "append": round(append_ms * 1e3, 2), "append_with_rope_and_q": round(append_rope_ms * 1e3, 2)},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+        }), flush=True)
+    st.close()
+
+
 def prefill_oracle_rate(sc, budget_s: float, threads: int):
     """The oracle's causal-attention FLOP rate on a sample of the prefill workload: the first
     rows of sequence chunks, each a one-row chunk at its own position."""
@@ -592,6 +651,7 @@ def main():
     ap.add_argument("--loop-batch", type=int, default=128)
     ap.add_argument("--prefix", action="store_true", help="measure decode over children of a shared prompt prefix")
     ap.add_argument("--prefill", action="store_true", help="measure the chunked-context prefill step")
+    ap.add_argument("--rope", action="store_true", help="measure the decode step with RoPE fused into the append")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -604,6 +664,8 @@ def main():
         run_prefix(args, world, rank, local)
     elif args.prefill:
         run_prefill(args, world, rank, local)
+    elif args.rope:
+        run_rope(args, world, rank, local)
     else:
         run_pkv(args, world, rank, local)
     if world > 1:

@@ -176,6 +176,26 @@ pkv_status pkv_check_device_error(pkv_pool* pool);
 pkv_status pkv_append(pkv_pool* pool, const void* k_new_dev, const void* v_new_dev, const int64_t* slot_mapping_dev,
                       int64_t N, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------ RoPE fused into the append
+ * "TensorRT-LLM 深度实战", §3.3-3.4: RoPE is fused with the attention's neighbouring kernels
+ * (use_fused_rope).  Rotary position embedding in the Llama "rotate half" form: element d of the
+ * first half of a row pairs with d + D/2 and, at position p, the pair turns by the angle
+ * p * rope_base^(-2d/D):  y[d] = x[d] cos - x[d+D/2] sin,  y[d+D/2] = x[d+D/2] cos + x[d] sin.
+ * Angle, cosine, sine and rotation are computed in fp64 and rounded to bf16 (nearest, ties to
+ * even) once.
+ *   k_new_dev: bf16 [N][n_kv_heads][head_dim], rotated IN PLACE at positions_dev, then appended
+ *     like pkv_append (bf16 pools: the rotation and the scatter are one kernel; fp8 pools: the
+ *     rotated rows then go through the quantising append).
+ *   v_new_dev, slot_mapping_dev: as pkv_append.
+ *   positions_dev: int64 [N], the tokens' positions in their sequences (>= 0).
+ *   q_dev: optional bf16 [N][n_q_heads][head_dim] (the same tokens' queries), rotated in place
+ *     with the same positions; NULL to skip.
+ *   rope_base: > 1 and finite (10000 for Llama-2, 500000 for Llama-3).
+ * Errors as pkv_append; PKV_ERR_INVALID_ARG for a bad base, positions or q. */
+pkv_status pkv_append_rope(pkv_pool* pool, void* k_new_dev, const void* v_new_dev, const int64_t* slot_mapping_dev,
+                           const int64_t* positions_dev, int64_t N, double rope_base, void* q_dev, int n_q_heads,
+                           pkv_stream_t stream);
+
 /* ------------------------------------------------------------------ decode attention (device)
  * For each sequence b and query head j, with KV head h = j / (n_q_heads / n_kv_heads):
  *   out[b][j] = softmax_t(scale * <q[b][j], K_b[t]>) . V_b[t],  t < context_lens[b],
@@ -213,6 +233,16 @@ pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new_dev, const void* v_
                            const int32_t* block_tables_dev, int max_blocks, const int32_t* context_lens_dev, int B,
                            int n_q_heads, float scale, void* out_dev, void* workspace_dev, size_t workspace_bytes,
                            pkv_stream_t stream);
+
+/* pkv_decode_step with RoPE fused into its append (pkv_append_rope): the step's new K rows and
+ * query rows are rotated at positions_dev (in place, k_new_dev and q_dev), K/V appended, then
+ * the attention runs over the grown contexts as a programmatic dependent of the append; it
+ * reads q only after the append has finished.  N must equal B (one new token per sequence). */
+pkv_status pkv_decode_step_rope(pkv_pool* pool, void* k_new_dev, const void* v_new_dev,
+                                const int64_t* slot_mapping_dev, const int64_t* positions_dev, int64_t N,
+                                double rope_base, void* q_dev, const int32_t* block_tables_dev, int max_blocks,
+                                const int32_t* context_lens_dev, int B, int n_q_heads, float scale, void* out_dev,
+                                void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
 
 /* Workspace size for pkv_decode_attention with these B, n_q_heads and max_blocks. */
 pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out);

@@ -19,7 +19,7 @@ __all__ = [
     "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "library_path",
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
     "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_share_prefix", "pkv_block_refcount",
-    "pkv_pool_copy_block", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
+    "pkv_pool_copy_block", "pkv_append_rope", "pkv_decode_step_rope", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
@@ -63,6 +63,9 @@ def _L():
         "pkv_seq_share_prefix": (i32, [vp, i64, i64, i64, P(ctypes.c_int32), P(ctypes.c_int32)]),
         "pkv_block_refcount": (i32, [vp, i32, P(i32)]),
         "pkv_pool_copy_block": (i32, [vp, i32, i32, vp]),
+        "pkv_append_rope": (i32, [vp, vp, vp, vp, vp, i64, ctypes.c_double, vp, i32, vp]),
+        "pkv_decode_step_rope": (i32, [vp, vp, vp, vp, vp, i64, ctypes.c_double, vp, vp, i32, vp, i32, i32,
+                                       ctypes.c_float, vp, vp, ctypes.c_size_t, vp]),
         "pkv_prefill_attention": (i32, [vp, vp, vp, i32, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
         "pkv_prefill_step": (i32, [vp, vp, vp, vp, i64, vp, vp, i32, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
         "pkv_seq_num_blocks": (i32, [vp, i64, P(i32)]),
@@ -252,6 +255,16 @@ def pkv_append(pool: int, k_new, v_new, slot_mapping, stream=None) -> None:
                            _dev(slot_mapping, "i64", "slot_mapping"), N, _stream(stream)), "pkv_append")
 
 
+def pkv_append_rope(pool: int, k_new, v_new, slot_mapping, positions, rope_base: float, q=None, stream=None) -> None:
+    """k_new (and q, if given) are rotated in place at `positions` (int64 CUDA [N]), then K/V are
+    appended like pkv_append."""
+    N = slot_mapping.shape[0]
+    _check(_L().pkv_append_rope(pool, _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"),
+                                _dev(slot_mapping, "i64", "slot_mapping"), _dev(positions, "i64", "positions"), N,
+                                float(rope_base), _dev(q, "bf16", "q") if q is not None else None,
+                                q.shape[1] if q is not None else 0, _stream(stream)), "pkv_append_rope")
+
+
 def pkv_decode_attention(pool: int, q, block_tables, context_lens, scale: float, out, workspace,
                          stream=None) -> None:
     """q/out: bf16 CUDA [B, Hq, D]; block_tables int32 [B, max_blocks]; context_lens int32 [B];
@@ -296,6 +309,19 @@ def pkv_prefill_step(pool: int, k_new, v_new, slot_mapping, q, cu_q_lens, max_q_
                                  _dev(block_tables, "i32", "block_tables"), block_tables.shape[1],
                                  _dev(context_lens, "i32", "context_lens"), B, Hq, float(scale), _dev(out, "bf16", "out"),
                                  _stream(stream)), "pkv_prefill_step")
+
+
+def pkv_decode_step_rope(pool: int, k_new, v_new, slot_mapping, positions, rope_base: float, q, block_tables,
+                         context_lens, scale: float, out, workspace, stream=None) -> None:
+    """pkv_append_rope(k_new, v_new, slot_mapping, positions, rope_base, q) then pkv_decode_attention(...)."""
+    B, Hq = q.shape[0], q.shape[1]
+    _check(_L().pkv_decode_step_rope(pool, _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"),
+                                     _dev(slot_mapping, "i64", "slot_mapping"), _dev(positions, "i64", "positions"),
+                                     slot_mapping.shape[0], float(rope_base), _dev(q, "bf16", "q"),
+                                     _dev(block_tables, "i32", "block_tables"), block_tables.shape[1],
+                                     _dev(context_lens, "i32", "context_lens"), B, Hq, float(scale),
+                                     _dev(out, "bf16", "out"), _dev(workspace, "u8", "workspace"), workspace.numel(),
+                                     _stream(stream)), "pkv_decode_step_rope")
 
 
 def pkv_decode_workspace_bytes(pool: int, B: int, n_q_heads: int, max_blocks: int) -> int:

@@ -964,6 +964,26 @@ pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new, const void* v_new,
     return pkv::attn::launch(pool, pl, p, reinterpret_cast<cudaStream_t>(stream), N > 0);
 }
 
+pkv_status pkv_decode_step_rope(pkv_pool* pool, void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                const int64_t* positions, int64_t N, double rope_base, void* q,
+                                const int32_t* block_tables, int max_blocks, const int32_t* context_lens, int B,
+                                int n_q_heads, float scale, void* out, void* workspace, size_t workspace_bytes,
+                                pkv_stream_t stream) {
+    pkv::attn::Plan pl;
+    pkv::attn::Params p;
+    pkv_status st = pkv::append_check(pool, k_new, v_new, slot_mapping, N);
+    if (st != PKV_OK) return st;
+    if (N != B) return PKV_ERR_INVALID_ARG;  // one new token (and one query row) per sequence
+    st = pkv::attn::prepare(pool, q, block_tables, max_blocks, context_lens, B, n_q_heads, scale, out, workspace,
+                            workspace_bytes, pl, p);
+    if (st != PKV_OK) return st;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // rotates k_new and q in place and appends; the attention reads q only after waiting on it
+    st = pkv::append_rope_launch(pool, k_new, v_new, slot_mapping, positions, N, rope_base, q, n_q_heads, cs);
+    if (st != PKV_OK || B == 0) return st;
+    return pkv::attn::launch(pool, pl, p, cs, true);
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------ allocation-free variant

@@ -18,6 +18,9 @@ constexpr int kErrTimeout = 2;
 bool valid_block_size(int bs);
 pkv_status append_check(const pkv_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping,
                         int64_t N);
+pkv_status append_rope_launch(pkv_pool* pool, void* k_new, const void* v_new, const int64_t* slot_mapping,
+                              const int64_t* positions, int64_t N, double rope_base, void* q, int n_q_heads,
+                              cudaStream_t cs);
 pkv_allocator* allocator_new(int num_blocks, int block_size);
 void allocator_delete(pkv_allocator* a);
 

@@ -116,3 +116,139 @@ def test_rope_matches_torch_rotate_half_in_fp64():
     # and the rounded values agree with rounding torch's values, except on a rounding edge
     same = np.array([oracle.f64_to_bf16_bits(v) for v in ref.reshape(-1)]).reshape(ref.shape) == oracle.rope(x, pos, base)
     assert same.mean() > 0.9999
+
+
+# ----------------------------------------------------------------------------- GPU
+@pytest.mark.gpu
+@pytest.mark.parametrize("kv_dtype,D,bs", [("bf16", 128, 16), ("bf16", 64, 64), ("fp8_e4m3", 128, 16)])
+def test_append_rope_matches_oracle(kv_dtype, D, bs):
+    """K and q rotated in place bit-exact against the oracle's fp64 rotation; the pool holds the
+    rotated K (bf16 bit-exact; fp8: the oracle's quantisation of the oracle's rotated K); the
+    decode attention over the rotated data within tolerance."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    fp8 = kv_dtype == "fp8_e4m3"
+    rng = np.random.default_rng(7)
+    Hkv, G, nb, base = 2, 4, 40, 500000.0
+    Hq = Hkv * G
+    lens = [37, 1, 130, 64]
+    pool = pkv.KVPool(nb, bs, Hkv, D, pkv.PKV_KV_FP8_E4M3 if fp8 else pkv.PKV_KV_BF16)
+    a = pool.allocator
+    oa, op = oracle.Allocator(nb, bs), oracle.Pool(nb, bs, Hkv, D, fp8)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    host = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b, L in enumerate(lens):
+        pkv.pkv_seq_reserve(a, b, L)
+        oa.reserve(b, L)
+    # the whole history appended through the RoPE path, in two calls (prompt, then the rest)
+    seqs = np.concatenate([np.full(L, b) for b, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int64)
+    k = (rng.standard_normal((len(pos), Hkv, D)) * 2).astype(np.float32)
+    v = rng.standard_normal((len(pos), Hkv, D)).astype(np.float32)
+    kb, vb = _bits(k), _bits(v)
+    cut = len(pos) // 2
+    for lo, hi in ((0, cut), (cut, len(pos))):
+        slots = pkv.pkv_slot_mapping(a, seqs[lo:hi], pos[lo:hi])
+        assert np.array_equal(slots, oa.slot_mapping(seqs[lo:hi], pos[lo:hi]))
+        kd = dev(kb[lo:hi])
+        pkv.pkv_append_rope(pool.handle, kd, dev(vb[lo:hi]), torch.from_numpy(slots).cuda(),
+                            torch.from_numpy(pos[lo:hi]).cuda(), base)
+        torch.cuda.synchronize()
+        kr = oracle.rope(kb[lo:hi], pos[lo:hi], base)
+        assert np.array_equal(host(kd), kr)
+        op.append(kr, vb[lo:hi], slots)
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_OK
+    kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(pool.handle)
+    assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), op.data)
+    if fp8:
+        assert np.array_equal(_wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32), op.scales)
+    # a decode-style call: q rotated with the same kernel (no K/V rows: N = 0 appends nothing, so
+    # rotate q alongside a one-token append at each sequence's last position)
+    qb = _bits(rng.standard_normal((len(lens), Hq, D)))
+    qd = dev(qb)
+    last = np.array([L - 1 for L in lens], np.int64)
+    slots_last = pkv.pkv_slot_mapping(a, np.arange(len(lens)), last)
+    k_last = kb[np.cumsum(lens) - 1]
+    v_last = vb[np.cumsum(lens) - 1]
+    pkv.pkv_append_rope(pool.handle, dev(k_last), dev(v_last), torch.from_numpy(slots_last).cuda(),
+                        torch.from_numpy(last).cuda(), base, q=qd)
+    torch.cuda.synchronize()
+    qr = oracle.rope(qb, last, base)
+    assert np.array_equal(host(qd), qr)
+    op.append(oracle.rope(k_last, last, base), v_last, slots_last)  # the same re-append on the oracle's pool
+    assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), op.data)
+    mb = max(-(-L // bs) for L in lens)
+    tables = pkv.pkv_get_block_tables(a, list(range(len(lens))), mb)
+    ctx = np.array(lens, np.int32)
+    out = torch.empty(len(lens), Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(pkv.pkv_decode_workspace_bytes(pool.handle, len(lens), Hq, mb), dtype=torch.uint8, device="cuda")
+    pkv.pkv_decode_attention(pool.handle, qd, torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(),
+                             1 / math.sqrt(D), out, ws)
+    torch.cuda.synchronize()
+    ref = op.attention(qr, tables, ctx, Hq, 1 / math.sqrt(D))
+    err = np.abs(oracle.bf16_bits_to_f64(host(out)) - ref)
+    assert err.max() <= (3e-2 if fp8 else 1e-2) and err.mean() <= 1e-3
+    pool.close()
+
+
+@pytest.mark.gpu
+def test_append_rope_rejects_bad_arguments():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    pool = pkv.KVPool(4, 16, 1, 128)
+    k = torch.zeros(1, 1, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for base in (0.0, 1.0, float("inf"), float("nan")):
+        with pytest.raises(pkv.PKVError):
+            pkv.pkv_append_rope(pool.handle, k, k.clone(), s, s, base)
+    pool.close()
+
+
+@pytest.mark.gpu
+def test_decode_step_rope_equals_separate_calls_and_oracle():
+    """pkv_decode_step_rope on a GQA batch: the same bits as pkv_append_rope followed by
+    pkv_decode_attention, and within tolerance of the oracle's rotate-then-attend."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    w = W.custom_workload(330, 6, 16, 4, 128, 16, [3, 40, 100, 17, 64, 250])
+    base = 10000.0
+    outs = []
+    for fused in (True, False):
+        st = DecodeStep(w)
+        pos = torch.from_numpy(w.lens.astype(np.int64)).cuda()
+        k, q = st.k_new.clone(), st.q.clone()
+        if fused:
+            pkv.pkv_decode_step_rope(st.pool.handle, k, st.v_new, st.slots_new, pos, base, q, st.tables, st.lens,
+                                     st.scale, st.out, st.workspace)
+        else:
+            pkv.pkv_append_rope(st.pool.handle, k, st.v_new, st.slots_new, pos, base, q=q)
+            pkv.pkv_decode_attention(st.pool.handle, q, st.tables, st.lens, st.scale, st.out, st.workspace)
+        torch.cuda.synchronize()
+        assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+        outs.append(st.out_host())
+        if fused:
+            from oracle import drive as odrive
+            opool, oalloc, tables = odrive.build(w, with_new_token=False)
+            kr = oracle.rope(w.new_k(), w.lens.astype(np.int64), base)
+            opool.append(kr, w.new_v(), oalloc.slot_mapping(w.seq_ids, w.lens))
+            qr = oracle.rope(w.query(), w.lens.astype(np.int64), base)
+            ref = opool.attention(qr, tables, w.attend_lens, w.Hq, st.scale)
+            err = np.abs(oracle.bf16_bits_to_f64(outs[0]) - ref)
+            assert err.max() <= 1e-2 and err.mean() <= 1e-3
+        st.close()
+    assert np.array_equal(outs[0], outs[1])
