@@ -52,8 +52,9 @@ typedef enum {
 } pkv_status;
 
 typedef enum {
-    PKV_KV_BF16 = 0,     /* K/V stored as bf16 */
-    PKV_KV_FP8_E4M3 = 1  /* K/V stored as OCP E4M3 codes with one fp32 scale per (block, K|V, head) */
+    PKV_KV_BF16 = 0,      /* K/V stored as bf16 */
+    PKV_KV_FP8_E4M3 = 1,  /* K/V stored as OCP E4M3 codes with one fp32 scale per (block, K|V, head) */
+    PKV_KV_INT8 = 2       /* K/V stored as int8 codes in [-127, 127], same scale layout (amax / 127) */
 } pkv_dtype;
 
 /* ------------------------------------------------------------------ block allocator (host)

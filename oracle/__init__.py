@@ -76,6 +76,7 @@ def _L():
         "oracle_rope": (None, [vp, vp, i64, i32, i32, f64, vp]),
         "oracle_rope_f64": (None, [vp, vp, i64, i32, i32, f64, vp]),
         "oracle_f64_to_bf16_bits": (ctypes.c_uint16, [f64]),
+        "oracle_int8_encode_array": (None, [vp, i64, vp]),
         "oracle_pool_bytes": (i64, [i32, i32, i32, i32, i32]),
         "oracle_scale_floats": (i64, [i32, i32]),
         "oracle_elem_byte": (i64, [i64, i32, i32, i32, i32, i32, i32, i32, i32]),
@@ -197,7 +198,8 @@ def dense_attention(q, K, V, scale: float) -> np.ndarray:
 class Pool:
     """Host replica of the paged KV pool (same byte layout as the device pool)."""
 
-    def __init__(self, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int, fp8: bool):
+    def __init__(self, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int, fp8):
+        """fp8: the element code — False/0 bf16, True/1 fp8 e4m3, 2 int8."""
         self.num_blocks, self.bs, self.Hkv, self.D, self.fp8 = num_blocks, block_size, n_kv_heads, head_dim, int(fp8)
         self.data = np.zeros(_L().oracle_pool_bytes(num_blocks, block_size, n_kv_heads, head_dim, self.fp8),
                              dtype=np.uint8)
@@ -273,6 +275,14 @@ def rope_f64(x, positions, base: float) -> np.ndarray:
 
 def f64_to_bf16_bits(x: float) -> int:
     return int(_L().oracle_f64_to_bf16_bits(float(x)))
+
+
+def int8_encode_array(q) -> np.ndarray:
+    """INT8 codes of fp32 quotients x / scale (nearest even, clamped to [-127, 127])."""
+    qs = np.ascontiguousarray(np.asarray(q, dtype=np.float32)).reshape(-1)
+    out = np.empty(qs.size, dtype=np.int8)
+    _L().oracle_int8_encode_array(_p(qs), qs.size, _p(out))
+    return out.reshape(np.shape(q))
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:

@@ -13,6 +13,8 @@ import numpy as np
 
 from . import Allocator, Pool
 
+KV_CODE = {"bf16": 0, "fp8_e4m3": 1, "int8": 2}  # element codes of the oracle's pool
+
 
 def build(w, with_new_token: bool = True):
     """(pool, allocator, block_tables) after the history and (optionally) the step's append."""
@@ -21,7 +23,7 @@ def build(w, with_new_token: bool = True):
         raise RuntimeError("oracle: bad free order")
     alloc.replay(w.alloc_ops)
     tables = alloc.block_tables(w.seq_ids, max(1, w.max_blocks()))
-    pool = Pool(w.num_blocks, w.block_size, w.Hkv, w.D, w.kv_dtype == "fp8_e4m3")
+    pool = Pool(w.num_blocks, w.block_size, w.Hkv, w.D, KV_CODE[w.kv_dtype])
     for t0, t1 in w.hist_chunks():
         seqs, pos = w.hist_positions(t0, t1)
         rc = pool.append(w.history_k(t0, t1), w.history_v(t0, t1), alloc.slot_mapping(seqs, pos))
@@ -51,7 +53,7 @@ def run_loop(script, n_steps: int | None = None, threads: int | None = None):
     from . import Allocator, Pool
     sc = script
     alloc = Allocator(sc.num_blocks, sc.block_size)
-    pool = Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, sc.kv_dtype == "fp8_e4m3")
+    pool = Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, KV_CODE[sc.kv_dtype])
     max_blocks = -(-sc.max_len // sc.block_size)
     lens, running = {}, []
     steps = sc.steps if n_steps is None else sc.steps[:n_steps]

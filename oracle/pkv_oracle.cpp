@@ -40,9 +40,10 @@
 //
 // Pool byte layout (the storage contract both sides implement independently):
 //   tile(blk, kv, h) starts at byte ((blk*2 + kv)*Hkv + h) * bs * D * esz,
-//   kv = 0 for K, 1 for V, esz = 2 (bf16) or 1 (fp8).
-//   bf16 K and V, fp8 K: row-major [bs][D].
-//   fp8 V: bs/16 column panels, each [D][16]: (t, d) at (t/16)*D*16 + d*16 + pos(t%16), where
+//   kv = 0 for K, 1 for V, esz = 2 (bf16) or 1 (fp8, int8).  The `fp8` argument of the pool
+//   functions is the element code: 0 bf16, 1 fp8 e4m3, 2 int8 (both 1-byte codes share the layout).
+//   bf16 K and V, fp8/int8 K: row-major [bs][D].
+//   fp8/int8 V: bs/16 column panels, each [D][16]: (t, d) at (t/16)*D*16 + d*16 + pos(t%16), where
 //   a panel row stores its 16 tokens in the order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15.
 //   fp8 scales: float[num_blocks][Hkv][4]: [.., 0] K scale, [.., 1] V scale.
 #include <algorithm>
@@ -296,15 +297,35 @@ static double pool_value(const uint8_t* pool, const float* scales, int64_t blk, 
         return bf16_to_double(b);
     }
     double s = (double)scales[(blk * Hkv + h) * 4 + kv];
+    if (fp8 == 2) return (double)(int8_t)pool[base + off] * s;  // INT8 code times its scale
     return oracle_e4m3_decode(pool[base + off]) * s;
+}
+
+// ----------------------------------------------------------------- INT8 KV
+// INT8 KV cache (a NEXT variant; the pages list INT8 among TensorRT-LLM's quantisation formats,
+// pnsm.cn page §1.2, "TensorRT-LLM 深度实战" §4): symmetric codes with the same per-(block,
+// K|V, head) scale semantics as the fp8 cache, the scale being amax/127.  A quotient q = x / s
+// (fp32) becomes round-to-nearest-even(q) clamped to [-127, 127]; the value read back is
+// code * s.
+int8_t oracle_int8_encode(float q) {
+    if (std::isnan(q)) return 0;
+    double r = std::nearbyint((double)q);  // the default rounding mode: ties to even
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int8_t)r;
+}
+
+void oracle_int8_encode_array(const float* q, int64_t n, int8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_int8_encode(q[i]);
 }
 
 // ----------------------------------------------------------------- append
 // Write each token's K and V rows (bf16 bit patterns, [N][Hkv][D]) into its slot.
-// bf16 pools store the bits.  fp8 pools: for every (block, K|V, head) whose offset 0 is
-// written by this call, the scale becomes amax/448 over this call's tokens in that block
-// (1.0 if amax is 0); other blocks keep their stored scale; codes are e4m3(x / scale) with
-// an fp32 division.  Slots < 0 are skipped.  Returns 0, or 4 for a slot beyond the pool.
+// bf16 pools store the bits.  fp8 (dtype code 1) and int8 (code 2) pools: for every (block,
+// K|V, head) whose offset 0 is written by this call, the scale becomes amax/448 (int8: /127)
+// over this call's tokens in that block (1.0 if amax is 0); other blocks keep their stored
+// scale; codes are e4m3(x / scale) or int8(x / scale) with an fp32 division.  Slots < 0 are
+// skipped.  Returns 0, or 4 for a slot beyond the pool.
 int oracle_append(uint8_t* pool, float* scales, int num_blocks, int bs, int Hkv, int D, int fp8,
                   const uint16_t* k_new, const uint16_t* v_new, const int64_t* slots, int64_t N) {
     for (int64_t i = 0; i < N; ++i)
@@ -345,7 +366,7 @@ int oracle_append(uint8_t* pool, float* scales, int num_blocks, int bs, int Hkv,
         for (int h = 0; h < Hkv; ++h)
             for (int kv = 0; kv < 2; ++kv) {
                 float a = amax[(blk * Hkv + h) * 2 + kv];
-                scales[(blk * Hkv + h) * 4 + kv] = a > 0.0f ? a / 448.0f : 1.0f;
+                scales[(blk * Hkv + h) * 4 + kv] = a > 0.0f ? a / (fp8 == 2 ? 127.0f : 448.0f) : 1.0f;
             }
     }
     for (int64_t i = 0; i < N; ++i) {
@@ -358,7 +379,7 @@ int oracle_append(uint8_t* pool, float* scales, int num_blocks, int bs, int Hkv,
                 for (int d = 0; d < D; ++d) {
                     float x = (float)bf16_to_double(src[kv][(i * Hkv + h) * D + d]);
                     pool[tile_base(blk, kv, h, Hkv, bs, D, 1) + elem_offset(kv, t, d, bs, D, 1)] =
-                        oracle_e4m3_encode(x / s);
+                        fp8 == 2 ? (uint8_t)oracle_int8_encode(x / s) : oracle_e4m3_encode(x / s);
                 }
             }
     }

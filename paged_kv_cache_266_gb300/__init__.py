@@ -16,7 +16,7 @@ import numpy as np
 from . import build as _build
 
 __all__ = [
-    "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "library_path",
+    "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "PKV_KV_INT8", "KV_DTYPES", "library_path",
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
     "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_share_prefix", "pkv_block_refcount",
     "pkv_pool_copy_block", "pkv_append_rope", "pkv_decode_step_rope", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
@@ -27,7 +27,8 @@ __all__ = [
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OOM, PKV_ERR_NO_SEQ, PKV_ERR_BOUNDS, PKV_ERR_CUDA, PKV_ERR_TIMEOUT = range(7)
-PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
+PKV_KV_BF16, PKV_KV_FP8_E4M3, PKV_KV_INT8 = 0, 1, 2
+KV_DTYPES = {"bf16": PKV_KV_BF16, "fp8_e4m3": PKV_KV_FP8_E4M3, "int8": PKV_KV_INT8}
 PKV_STATIC_WORKSPACE_BYTES = 8 << 20  # include/pkv.h
 
 _lib = None

@@ -24,7 +24,7 @@ import math
 
 import numpy as np
 
-from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
+from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
                pkv_get_block_tables, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many, pkv_slot_mapping)
 
 DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
@@ -77,9 +77,7 @@ class DecodeLoop:
         import torch
         self.prompts = prompts or {}
         self.torch, self.script, self.graphs, self.device = torch, script, graphs, device
-        fp8 = script.kv_dtype == "fp8_e4m3"
-        self.pool = KVPool(script.num_blocks, script.block_size, script.Hkv, script.D,
-                           PKV_KV_FP8_E4M3 if fp8 else PKV_KV_BF16)
+        self.pool = KVPool(script.num_blocks, script.block_size, script.Hkv, script.D, KV_DTYPES[script.kv_dtype])
         self.alloc = self.pool.allocator
         self.max_blocks = -(-script.max_len // script.block_size)
         self.scale = 1.0 / math.sqrt(script.D)

@@ -15,7 +15,7 @@ import math
 
 import numpy as np
 
-from . import (PKV_KV_BF16, PKV_KV_FP8_E4M3, KVPool, pkv_allocator_set_free_order, pkv_append,
+from . import (KV_DTYPES, KVPool, pkv_allocator_set_free_order, pkv_append,
                pkv_decode_attention, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
                pkv_num_free_blocks, pkv_pool_copy_block, pkv_prefill_attention, pkv_prefill_step, pkv_seq_release,
                pkv_seq_reserve, pkv_seq_share_prefix, pkv_slot_mapping)
@@ -36,8 +36,7 @@ class DecodeStep:
     def __init__(self, w, device: str = "cuda"):
         import torch
         self.torch, self.w, self.device = torch, w, device
-        fp8 = w.kv_dtype == "fp8_e4m3"
-        self.pool = KVPool(w.num_blocks, w.block_size, w.Hkv, w.D, PKV_KV_FP8_E4M3 if fp8 else PKV_KV_BF16)
+        self.pool = KVPool(w.num_blocks, w.block_size, w.Hkv, w.D, KV_DTYPES[w.kv_dtype])
         a = self.pool.allocator
         pkv_allocator_set_free_order(a, w.free_order)
         replay(a, w.alloc_ops)
@@ -179,9 +178,8 @@ class PrefixDecode:
     def __init__(self, sc, share: bool = True, device: str = "cuda"):
         import torch
         self.torch, self.sc, self.share, self.device = torch, sc, share, device
-        fp8 = sc.kv_dtype == "fp8_e4m3"
         nb = sc.num_blocks if share else sc.blocks_unshared() + 4
-        self.pool = KVPool(nb, sc.block_size, sc.Hkv, sc.D, PKV_KV_FP8_E4M3 if fp8 else PKV_KV_BF16)
+        self.pool = KVPool(nb, sc.block_size, sc.Hkv, sc.D, KV_DTYPES[sc.kv_dtype])
         a = self.pool.allocator
         pk, pv = sc.prefix_kv()
         dpk, dpv = _bf16(torch, pk, device), _bf16(torch, pv, device)
@@ -251,8 +249,7 @@ class PrefillStep:
     def __init__(self, sc, device: str = "cuda"):
         import torch
         self.torch, self.sc, self.device = torch, sc, device
-        self.pool = KVPool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D,
-                           PKV_KV_FP8_E4M3 if sc.kv_dtype == "fp8_e4m3" else PKV_KV_BF16)
+        self.pool = KVPool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, KV_DTYPES[sc.kv_dtype])
         a = self.pool.allocator
         pkv_allocator_set_free_order(a, sc.free_order)
         for b in range(sc.B):

@@ -135,7 +135,7 @@ class Workload:
     Hkv: int
     D: int
     block_size: int
-    kv_dtype: str  # "bf16" | "fp8_e4m3"
+    kv_dtype: str  # "bf16" | "fp8_e4m3" | "int8"
     num_blocks: int
     lens: np.ndarray
     append: bool
@@ -166,7 +166,7 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 1 if self.kv_dtype == "fp8_e4m3" else 2
+        return 2 if self.kv_dtype == "bf16" else 1
 
     def kv_read_bytes(self) -> int:
         """K+V bytes one attention pass must read: 2*D*bytes per (token, kv head)."""
