@@ -45,7 +45,7 @@ def algorithmic_bytes(w) -> dict:
     L = w.attend_lens.astype(np.int64)
     pages = ((L + w.block_size - 1) // w.block_size).sum()
     kv = int(L.sum()) * w.Hkv * 2 * w.D * w.elem_bytes
-    scales = int(pages) * w.Hkv * 8 if w.kv_dtype == "fp8_e4m3" else 0
+    scales = int(pages) * w.Hkv * 8 if w.kv_dtype != "bf16" else 0
     q_out = 2 * w.B * w.Hq * w.D * 2
     meta = int(pages) * 4 + w.B * 4
     attn = kv + scales + q_out + meta
@@ -241,6 +241,9 @@ def run_pkv(args, world, rank, local):
 
     torch.cuda.set_device(local)
     w = W.make_workload(args.workload)
+    if args.kv and args.kv != w.kv_dtype:  # the same workload over another KV element type
+        import dataclasses
+        w = dataclasses.replace(w, kv_dtype=args.kv, name=f"{w.name}-{args.kv}")
     step = DecodeStep(w, device=f"cuda:{local}")
     if args.seqs:
         step.limit_batch(args.seqs)
@@ -318,7 +321,7 @@ def run_pkv(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32-accumulate on bf16 KV" if w.kv_dtype == "bf16" else "f32-accumulate on fp8 KV",
+        "vs_baseline": None, "dtype": f"f32-accumulate on {w.kv_dtype} KV",
         "data": "synthetic",
         "config": {"workload": w.name, "description": w.description, "batch": w.B, "q_heads": w.Hq,
                    "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
@@ -652,6 +655,8 @@ def main():
     ap.add_argument("--prefix", action="store_true", help="measure decode over children of a shared prompt prefix")
     ap.add_argument("--prefill", action="store_true", help="measure the chunked-context prefill step")
     ap.add_argument("--rope", action="store_true", help="measure the decode step with RoPE fused into the append")
+    ap.add_argument("--kv", default="", choices=["", "bf16", "fp8_e4m3", "int8"],
+                    help="override the workload's KV element type")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -8,7 +8,8 @@
 // both the read of k_new/v_new and the write of the row are coalesced.
 //
 // fp8 pools ("TensorRT-LLM 深度实战" §4.5 E4M3; "TensorRT-LLM 推理加速实战" §8 fp8_e4m3 KV
-// cache): one fp32 scale per (block, K|V, head).  A block's scales are derived by the call
+// cache) and int8 pools (the same with amax/127 and symmetric int8 codes): one fp32 scale per
+// (block, K|V, head).  A block's scales are derived by the call
 // that writes its offset 0, as amax/448 over that call's tokens in the block (1 when the
 // amax is 0); later calls reuse them and saturate.  Three short passes do this without any
 // grid-wide synchronisation inside a kernel:
@@ -112,7 +113,14 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_amax_kernel(const uint16_t
     if (slot - blk * bs == 0 && r.kv == 0 && r.h == 0) fresh[blk] = 1;
 }
 
-template <int D>
+// INT8 code of a quotient x / scale: nearest integer, ties to even (cvt.rni), clamped to
+// [-127, 127] (symmetric: -128 is never produced); the byte in the low 8 bits.
+__device__ __forceinline__ uint32_t int8_code(float q) {
+    const int c = __float2int_rn(q);
+    return (uint32_t)(c < -127 ? -127 : (c > 127 ? 127 : c)) & 0xffu;
+}
+
+template <int D, bool I8>
 __global__ void __launch_bounds__(kAppendThreads) fp8_quant_kernel(uint8_t* __restrict__ pool,
                                                                     float* __restrict__ scales,
                                                                     const uint16_t* __restrict__ k_new,
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_quant_kernel(uint8_t* __re
     float s;
     if (fresh[blk]) {
         const float a = __uint_as_float(amax[(blk * Hkv + r.h) * 2 + r.kv]);
-        s = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+        s = a > 0.0f ? __fdiv_rn(a, I8 ? 127.0f : 448.0f) : 1.0f;
         if (t == 0 && part == 0) *sp = s;
     } else {
         s = *sp;
@@ -149,7 +157,10 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_quant_kernel(uint8_t* __re
         const float x0 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e]), s), x1 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e]), s);
         const float x2 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e + 1]), s),
                     x3 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e + 1]), s);
-        codes[e] = ptx::f32x2_to_e4m3x2(x0, x1) | (ptx::f32x2_to_e4m3x2(x2, x3) << 16);
+        if constexpr (I8)
+            codes[e] = int8_code(x0) | (int8_code(x1) << 8) | (int8_code(x2) << 16) | (int8_code(x3) << 24);
+        else
+            codes[e] = ptx::f32x2_to_e4m3x2(x0, x1) | (ptx::f32x2_to_e4m3x2(x2, x3) << 16);
     }
     uint8_t* tile = pool + tile_elem(blk, r.kv, r.h, Hkv, bs, D);
     if (r.kv == 0) {
@@ -339,9 +350,14 @@ pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, cons
     } else {
         fp8_amax_kernel<D><<<grid, kAppendThreads, 0, st>>>(k, v, slots, N, p->n_kv_heads, p->block_size,
                                                             p->num_blocks, p->amax_scratch, p->fresh_scratch, p->err);
-        fp8_quant_kernel<D><<<grid, kAppendThreads, 0, st>>>(static_cast<uint8_t*>(p->kv), p->scales, k, v, slots, N,
-                                                             p->n_kv_heads, p->block_size, p->num_blocks,
-                                                             p->amax_scratch, p->fresh_scratch);
+        if (p->dtype == PKV_KV_INT8)
+            fp8_quant_kernel<D, true><<<grid, kAppendThreads, 0, st>>>(static_cast<uint8_t*>(p->kv), p->scales, k, v,
+                                                                       slots, N, p->n_kv_heads, p->block_size,
+                                                                       p->num_blocks, p->amax_scratch, p->fresh_scratch);
+        else
+            fp8_quant_kernel<D, false><<<grid, kAppendThreads, 0, st>>>(static_cast<uint8_t*>(p->kv), p->scales, k, v,
+                                                                        slots, N, p->n_kv_heads, p->block_size,
+                                                                        p->num_blocks, p->amax_scratch, p->fresh_scratch);
         fp8_reset_kernel<D><<<grid, kAppendThreads, 0, st>>>(slots, N, p->n_kv_heads, p->block_size, p->num_blocks,
                                                              p->amax_scratch, p->fresh_scratch);
     }

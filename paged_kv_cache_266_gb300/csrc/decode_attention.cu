@@ -362,7 +362,23 @@ __device__ __forceinline__ uint32_t fp8_v_addr(uint32_t vst, int row0, int d) {
     return vst + line * 64 + (((d & 3) ^ ((line >> 1) & 3)) << 4);
 }
 
-template <int D>
+// Four 1-byte codes (byte 0 first) -> two f16x2 (codes 0,1 and 2,3), exactly: E4M3 codes by the
+// hardware conversion; int8 codes in [-127, 127] by placing code + 128 (the sign bit flipped)
+// into the mantissa of 1024.0 (f16 bits 0x6400 | byte) and subtracting 1152 (both steps exact
+// in this range): one flip for four codes, one byte permute and one f16x2 subtraction per pair.
+template <bool I8>
+__device__ __forceinline__ void widen4(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    if constexpr (I8) {
+        const uint32_t x = four ^ 0x80808080u;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(__byte_perm(x, 0x64u, 0x4140)), "r"(0x64806480u));
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(__byte_perm(x, 0x64u, 0x4342)), "r"(0x64806480u));
+    } else {
+        lo = ptx::e4m3x2_to_f16x2(four);
+        hi = ptx::e4m3x2_to_f16x2(four >> 16);
+    }
+}
+
+template <int D, bool I8>
 __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, int nvalid,
                                          const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], SoftmaxState& st,
                                          float sl, float sk, float sv, float& sv_prev, int lane) {
@@ -374,10 +390,13 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
     for (int kk = 0; kk < KS / 2; ++kk) {
         uint32_t r0, r1, r2, r3;
         ptx::ldsm_x4(fp8_k_addr<D>(kst, krow, 2 * kk + (mat >> 1)), r0, r1, r2, r3);
-        ptx::mma_f16(acc, ptx::e4m3x2_to_f16x2(r0), ptx::e4m3x2_to_f16x2(r1), ptx::e4m3x2_to_f16x2(r0 >> 16),
-                     ptx::e4m3x2_to_f16x2(r1 >> 16), qf[2 * kk][0], qf[2 * kk][1]);
-        ptx::mma_f16(acc2, ptx::e4m3x2_to_f16x2(r2), ptx::e4m3x2_to_f16x2(r3), ptx::e4m3x2_to_f16x2(r2 >> 16),
-                     ptx::e4m3x2_to_f16x2(r3 >> 16), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+        uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+        widen4<I8>(r0, l0, h0);
+        widen4<I8>(r1, l1, h1);
+        widen4<I8>(r2, l2, h2);
+        widen4<I8>(r3, l3, h3);
+        ptx::mma_f16(acc, l0, l1, h0, h1, qf[2 * kk][0], qf[2 * kk][1]);
+        ptx::mma_f16(acc2, l2, l3, h2, h3, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
@@ -413,10 +432,13 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
         r1 &= bm;
         r2 &= bm;
         r3 &= bm;
-        ptx::mma_f16(o[2 * mm], ptx::e4m3x2_to_f16x2(r0), ptx::e4m3x2_to_f16x2(r1), ptx::e4m3x2_to_f16x2(r0 >> 16),
-                     ptx::e4m3x2_to_f16x2(r1 >> 16), pb0, pb1);
-        ptx::mma_f16(o[2 * mm + 1], ptx::e4m3x2_to_f16x2(r2), ptx::e4m3x2_to_f16x2(r3),
-                     ptx::e4m3x2_to_f16x2(r2 >> 16), ptx::e4m3x2_to_f16x2(r3 >> 16), pb0, pb1);
+        uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+        widen4<I8>(r0, l0, h0);
+        widen4<I8>(r1, l1, h1);
+        widen4<I8>(r2, l2, h2);
+        widen4<I8>(r3, l3, h3);
+        ptx::mma_f16(o[2 * mm], l0, l1, h0, h1, pb0, pb1);
+        ptx::mma_f16(o[2 * mm + 1], l2, l3, h2, h3, pb0, pb1);
     }
 }
 
@@ -614,7 +636,7 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
     ptx::named_barrier_sync(kCombineBar, kCT);
 }
 
-template <bool FP8, int D>
+template <bool FP8, int D, bool I8>
 __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* lens_s, int64_t R0, int64_t R1,
                          int64_t Ng, int64_t C, uint8_t* smem, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
                          volatile int* misc) {
@@ -659,7 +681,7 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
             const uint32_t vst = kst + part_bytes / 2;
             if (FP8) {
                 const float2 sc = *reinterpret_cast<const float2*>(smem + (st_addr - sbase) + p.off_s + 8 * pidx);
-                tile_fp8<D>(kst, vst, prow, nvalid, qf, o, st, p.scale_log2, sc.x, sc.y, sv_prev, lane);
+                tile_fp8<D, I8>(kst, vst, prow, nvalid, qf, o, st, p.scale_log2, sc.x, sc.y, sv_prev, lane);
             } else {
                 tile_bf16<D>(kst, vst, prow, (uint32_t)p.box_rows * 128, nvalid, qf, o, st, p.scale_log2, lane);
             }
@@ -687,7 +709,7 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
     }
 }
 
-template <bool FP8, int D>
+template <bool FP8, int D, bool I8 = false>
 __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                           const __grid_constant__ CUtensorMap tmap_tail,
                                                                           const Params p) {
@@ -767,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
         uint4* row = reinterpret_cast<uint4*>(p.out + (int64_t)bb * p.Hq * D);
         for (int i = tid; i < p.Hq * D / 8; i += kConsumerWarps * 32) row[i] = make_uint4(0, 0, 0, 0);
     }
-    if (R0 < R1) consumer<FP8, D>(p, cumg, lens_s, R0, R1, Ng, C, smem, sbase, bar_full, bar_empty, misc);
+    if (R0 < R1) consumer<FP8, D, I8>(p, cumg, lens_s, R0, R1, Ng, C, smem, sbase, bar_full, bar_empty, misc);
 }
 
 // ------------------------------------------------------------------ host side
@@ -781,10 +803,13 @@ struct Plan {
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 const void* kernel_for(const pkv_pool* pool) {
-    const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
+    const bool i8 = pool->dtype == PKV_KV_INT8;
+    const bool fp8 = pool->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     if (pool->head_dim == 128)
-        return fp8 ? (const void*)decode_kernel<true, 128> : (const void*)decode_kernel<false, 128>;
-    return fp8 ? (const void*)decode_kernel<true, 64> : (const void*)decode_kernel<false, 64>;
+        return i8 ? (const void*)decode_kernel<true, 128, true>
+                  : fp8 ? (const void*)decode_kernel<true, 128> : (const void*)decode_kernel<false, 128>;
+    return i8 ? (const void*)decode_kernel<true, 64, true>
+              : fp8 ? (const void*)decode_kernel<true, 64> : (const void*)decode_kernel<false, 64>;
 }
 
 int env_int(const char* name, int dflt) {
@@ -793,7 +818,7 @@ int env_int(const char* name, int dflt) {
 }
 
 bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
-    const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
+    const bool fp8 = pool->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     const uint32_t D = (uint32_t)pool->head_dim, esz = fp8 ? 1 : 2;
     const uint32_t region = kGroup * D * esz;
     pl.off_q = 2 * region;  // kGroup rows of K and of V, as ppg page parts
@@ -903,14 +928,17 @@ pkv_status launch(const pkv_pool* pool, const Plan& pl, const Params& p, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const bool fp8 = pool->dtype == PKV_KV_FP8_E4M3;
+    const bool i8 = pool->dtype == PKV_KV_INT8;
+    const bool fp8 = pool->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     cudaError_t e;
     if (pool->head_dim == 128)
-        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 128>, pool->tmap_rows, pool->tmap_tail, p)
-                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 128>, pool->tmap_rows, pool->tmap_tail, p);
+        e = i8    ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 128, true>, pool->tmap_rows, pool->tmap_tail, p)
+            : fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 128>, pool->tmap_rows, pool->tmap_tail, p)
+                  : cudaLaunchKernelEx(&cfg, decode_kernel<false, 128>, pool->tmap_rows, pool->tmap_tail, p);
     else
-        e = fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 64>, pool->tmap_rows, pool->tmap_tail, p)
-                : cudaLaunchKernelEx(&cfg, decode_kernel<false, 64>, pool->tmap_rows, pool->tmap_tail, p);
+        e = i8    ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 64, true>, pool->tmap_rows, pool->tmap_tail, p)
+            : fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<true, 64>, pool->tmap_rows, pool->tmap_tail, p)
+                  : cudaLaunchKernelEx(&cfg, decode_kernel<false, 64>, pool->tmap_rows, pool->tmap_tail, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -43,7 +43,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 bool encode_rows_map(pkv_pool* p) {
     auto encode = get_encode_fn();
     if (!encode) return false;
-    const bool fp8 = p->dtype == PKV_KV_FP8_E4M3;
+    const bool fp8 = p->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     const uint64_t esz = fp8 ? 1 : 2;
     const uint64_t row_bytes = (uint64_t)p->head_dim * esz;
     const uint64_t rows = (uint64_t)p->num_blocks * 2 * p->n_kv_heads * p->block_size;
@@ -103,7 +103,8 @@ extern "C" {
 pkv_status pkv_pool_create(int num_blocks, int block_size, int n_kv_heads, int head_dim, pkv_dtype kv_dtype,
                            pkv_pool** out) {
     if (!out || num_blocks < 1 || n_kv_heads < 1 || !pkv::valid_block_size(block_size) ||
-        (head_dim != 64 && head_dim != 128) || (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3))
+        (head_dim != 64 && head_dim != 128) ||
+        (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3 && kv_dtype != PKV_KV_INT8))
         return PKV_ERR_INVALID_ARG;
     const uint64_t rows = (uint64_t)num_blocks * 2 * n_kv_heads * block_size;
     if (rows >= (1ull << 31)) return PKV_ERR_INVALID_ARG;  // TMA row coordinates are int32
@@ -114,7 +115,7 @@ pkv_status pkv_pool_create(int num_blocks, int block_size, int n_kv_heads, int h
     p->n_kv_heads = n_kv_heads;
     p->head_dim = head_dim;
     p->dtype = kv_dtype;
-    const bool fp8 = kv_dtype == PKV_KV_FP8_E4M3;
+    const bool fp8 = kv_dtype != PKV_KV_BF16;  // one-byte codes with scales (fp8 or int8)
     p->alloc = pkv::allocator_new(num_blocks, block_size);
     if (!p->alloc) {
         pkv::free_pool(p);

@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the same seeded
 inputs.  Block tables, slot mappings and appended pool bytes (and fp8 scales) must be
 bit-exact; bf16 attention outputs within max |err| 1e-2 and mean |err| 1e-3 of the oracle,
-fp8-KV outputs within 3e-2 (computed by the oracle from the same fp8 bytes and scales)."""
+fp8- and int8-KV outputs within 3e-2 (computed by the oracle from the same code bytes and
+scales)."""
 import math
 import os
 
@@ -53,11 +54,11 @@ def _check_against_oracle(pkv, w, step, check_pool=True):
     if check_pool:
         kv, sc = step.pool_bytes_host()
         assert np.array_equal(kv, pool.data), "appended pool bytes differ from the oracle"
-        if w.kv_dtype == "fp8_e4m3":
-            assert np.array_equal(sc, pool.scales), "fp8 block scales differ from the oracle"
+        if w.kv_dtype != "bf16":
+            assert np.array_equal(sc, pool.scales), "block scales differ from the oracle"
     ref = odrive.attention(w, pool, tables)
     got, err = _errors(step, ref)
-    tol = TOL_FP8_MAX if w.kv_dtype == "fp8_e4m3" else TOL_BF16_MAX
+    tol = TOL_FP8_MAX if w.kv_dtype != "bf16" else TOL_BF16_MAX
     assert np.isfinite(got).all()
     assert err.max() <= tol, f"max |err| {err.max():.3e}"
     assert err.mean() <= TOL_MEAN, f"mean |err| {err.mean():.3e}"
@@ -73,7 +74,17 @@ def test_workload_parity(pkv, name):
     step.close()
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_int8_churned_pool_parity(pkv):
+    """The churned 200-request workload with an INT8 pool instead of fp8 (same shapes, blocks
+    and inputs): pool codes and scales bit-exact, every output within the low-precision bound."""
+    import dataclasses
+    w = dataclasses.replace(W.make_workload("c4"), kv_dtype="int8")
+    step = _run(pkv, w)
+    _check_against_oracle(pkv, w, step)
+    step.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3", "int8"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("bs", [16, 32, 64, 128])
 def test_shapes(pkv, dtype, D, bs):
