@@ -817,7 +817,44 @@ int env_int(const char* name, int dflt) {
     return v && *v ? std::atoi(v) : dflt;
 }
 
+bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, Plan& pl);
+
+// The launch plan depends only on these values (not on the pool's address or contents), so the
+// plans of recent shapes are kept per host thread: a decode loop pays the shared-memory layout
+// and the occupancy query once per batch shape instead of once per step.
+struct PlanKey {
+    int B, G, Hkv, dtype, D, bs, sm_count, smem_block, smem_sm, device, pref, max_stages;
+    bool operator==(const PlanKey& o) const {
+        return B == o.B && G == o.G && Hkv == o.Hkv && dtype == o.dtype && D == o.D && bs == o.bs &&
+               sm_count == o.sm_count && smem_block == o.smem_block && smem_sm == o.smem_sm && device == o.device &&
+               pref == o.pref && max_stages == o.max_stages;
+    }
+};
+
 bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
+    const bool q8 = pool->dtype != PKV_KV_BF16;
+    const int pref = env_int("PKV_ATTN_CTAS_PER_SM", q8 ? 3 : 2);
+    const int max_stages = env_int("PKV_ATTN_MAX_STAGES", kMaxStages);
+    const PlanKey key{B, G, pool->n_kv_heads, (int)pool->dtype, pool->head_dim, pool->block_size, pool->sm_count,
+                      pool->max_smem_per_block, pool->max_smem_per_sm, pool->device, pref, max_stages};
+    constexpr int kSlots = 8;
+    thread_local PlanKey keys[kSlots];
+    thread_local Plan plans[kSlots];
+    thread_local int used = 0, next = 0;
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == key) {
+            pl = plans[i];
+            return true;
+        }
+    if (!compute_plan(pool, B, G, pref, max_stages, pl)) return false;
+    keys[next] = key;
+    plans[next] = pl;
+    next = (next + 1) % kSlots;
+    if (used < kSlots) ++used;
+    return true;
+}
+
+bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, Plan& pl) {
     const bool fp8 = pool->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     const uint32_t D = (uint32_t)pool->head_dim, esz = fp8 ? 1 : 2;
     const uint32_t region = kGroup * D * esz;
@@ -829,8 +866,8 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     const uint32_t fixed = 1024 + 32 + cmb + lens;
     // fp8 tiles carry half the bytes of bf16 ones, so fp8 runs three CTAs per SM (its kernel is
     // compiled for that register budget) to keep enough tiles in flight
-    const int pref = env_int("PKV_ATTN_CTAS_PER_SM", fp8 ? 3 : 2);
-    const int max_stages = std::max(2, std::min(kMaxStages, env_int("PKV_ATTN_MAX_STAGES", kMaxStages)));
+    const int pref = pref_ctas;
+    const int max_stages = std::max(2, std::min(kMaxStages, max_stages_env));
     pl.stages = 0;
     for (int ctas = std::max(1, pref); ctas >= 1; --ctas) {
         const int budget = std::min(pool->max_smem_per_block, pool->max_smem_per_sm / ctas - 1024);

@@ -126,10 +126,24 @@ class DecodeStep:
                       "v": Dv["v"].view(torch.bfloat16), "tables": Dv["tables"], "lens": Dv["lens"],
                       "slots": Dv["slots"], "out": torch.empty(n, w.Hq, w.D, dtype=torch.int16).pin_memory()}
 
-    def step_host(self, stream=None):
+    def _issue_host_step(self, stream):
+        """Copy-in, the step, copy-out, on `stream` (no synchronisation)."""
+        torch, w, X = self.torch, self.w, self._host
+        X["dbuf"].copy_(X["hbuf"], non_blocking=True)
+        if w.append:
+            pkv_decode_step(self.pool.handle, X["k"], X["v"], X["slots"], X["q"], X["tables"], X["lens"], self.scale,
+                            self.out, self.workspace, stream)
+        else:
+            pkv_decode_attention(self.pool.handle, X["q"], X["tables"], X["lens"], self.scale, self.out,
+                                 self.workspace, stream)
+        X["out"].copy_(self.out.view(torch.int16), non_blocking=True)
+
+    def step_host(self, stream=None, graph: bool = True):
         """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The allocator writes the block
         tables and the slot mapping into the pinned staging buffer, one copy takes every input
-        to the device, the fused step runs, and the output comes back."""
+        to the device, the fused step runs, and the output comes back.  With `graph` the copy-in,
+        step and copy-out are captured once as a CUDA graph and replayed (the launch-bound part
+        of a decode step, "TensorRT-LLM 推理加速实战" §7.1); the staging buffer is read at replay."""
         torch, w, a = self.torch, self.w, self.pool.allocator
         if self._host is None:
             self._prepare_host()
@@ -139,14 +153,21 @@ class DecodeStep:
         pkv_get_block_tables(a, w.seq_ids[:n], self.max_blocks, out=H["tables"])
         if w.append:
             pkv_slot_mapping(a, w.seq_ids[:n], w.lens[:n], out=H["slots"])
-        X["dbuf"].copy_(X["hbuf"], non_blocking=True)
-        if w.append:
-            pkv_decode_step(self.pool.handle, X["k"], X["v"], X["slots"], X["q"], X["tables"], X["lens"], self.scale,
-                            self.out, self.workspace, stream)
+        if not graph:
+            self._issue_host_step(stream)
         else:
-            pkv_decode_attention(self.pool.handle, X["q"], X["tables"], X["lens"], self.scale, self.out,
-                                 self.workspace, stream)
-        X["out"].copy_(self.out.view(torch.int16), non_blocking=True)
+            if X.get("graph") is None:
+                self._issue_host_step(None)  # warm-up outside capture (plans, modules)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        self._issue_host_step(side)
+                torch.cuda.current_stream().wait_stream(side)
+                X["graph"] = g
+            X["graph"].replay()
         torch.cuda.current_stream().synchronize()
         return X["hbuf"].numel(), X["out"].numel() * 2
 
