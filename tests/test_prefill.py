@@ -268,3 +268,51 @@ def test_prefill_rejects_unsupported_and_flags_bounds():
     assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_ERR_BOUNDS
     pkv.pkv_prefill_attention(pool.handle, q8, cu, 0, tables, ctx, 0.1, out8)  # max_q_len 0: nothing launched
     pool.close()
+
+
+@pytest.mark.gpu
+def test_chunked_prefill_with_rope_matches_oracle():
+    """A chunk's K and queries rotated by pkv_append_rope at their positions (which also appends
+    the chunk's K/V), then the prefill attention: against the oracle's rotate-then-attend."""
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    sc = W.make_prefill_script(90, Hq=8, Hkv=2, D=128, block_size=16, past=[33, 0, 100], chunk=[20, 65, 1])
+    base = 10000.0
+    pool = pkv.KVPool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D)
+    a = pool.allocator
+    pkv.pkv_allocator_set_free_order(a, sc.free_order)
+    oa = oracle.Allocator(sc.num_blocks, sc.block_size)
+    oa.set_free_order(sc.free_order)
+    op = oracle.Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, False)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    for b in range(sc.B):
+        pkv.pkv_seq_reserve(a, b, int(sc.ctx[b]))
+        oa.reserve(b, int(sc.ctx[b]))
+    # the past, already rotated (as a previous chunk's append would have left it)
+    for b in range(sc.B):
+        P = int(sc.past[b])
+        if P:
+            k, v = sc.kv(b, 0, P)
+            kr = oracle.rope(k, np.arange(P), base)
+            slots = pkv.pkv_slot_mapping(a, [b] * P, np.arange(P))
+            pkv.pkv_append(pool.handle, dev(kr), dev(v), torch.from_numpy(slots).cuda())
+            op.append(kr, v, slots)
+    seqs, pos = sc.chunk_slots_positions()
+    k, v = sc.chunk_kv()
+    q = sc.query()
+    slots = pkv.pkv_slot_mapping(a, seqs, pos)
+    kd, qd = dev(k), dev(q)
+    pkv.pkv_append_rope(pool.handle, kd, dev(v), torch.from_numpy(slots).cuda(), torch.from_numpy(pos).cuda(), base,
+                        q=qd)
+    tables = pkv.pkv_get_block_tables(a, list(range(sc.B)), sc.max_blocks)
+    out = torch.empty(int(sc.cu_q[-1]), sc.Hq, sc.D, dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_prefill_attention(pool.handle, qd, torch.from_numpy(sc.cu_q).cuda(), int(sc.chunk.max()),
+                              torch.from_numpy(tables).cuda(), torch.from_numpy(sc.ctx).cuda(), 1 / math.sqrt(sc.D), out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_OK
+    kr, qr = oracle.rope(k, pos, base), oracle.rope(q, pos, base)
+    assert np.array_equal(kd.view(torch.int16).cpu().numpy().view(np.uint16), kr)
+    op.append(kr, v, slots)
+    ref = op.prefill_attention(qr, sc.cu_q, tables, sc.ctx, sc.Hq, 1 / math.sqrt(sc.D))
+    _check_close(out.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+    pool.close()
