@@ -99,6 +99,7 @@ struct Params {
     int32_t oob_row;  // a row coordinate past the pool: the copy fills the box with zeros
     float scale_log2;
     uint64_t wait_ns;
+    uint32_t stall_tx;  // test hook: extra bytes every K/V stage expects and no copy delivers
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (__shfl_sync(0xffffffffu, abort_s, 0)) break;  // warp-uniform
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(full + s), kHalfBytes);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(full + s), kHalfBytes + p.stall_tx);
             __syncwarp();
             if (lane < 2 * kParts) {
                 const int pi = lane >> 1, q = lane & 1;
@@ -516,8 +517,12 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     p.tiles = (max_q_len + kTiles * T - 1) / (kTiles * T);  // pairs of query tiles
     p.oob_row = (int32_t)((int64_t)pool->num_blocks * 2 * pool->n_kv_heads * pool->block_size);
     p.scale_log2 = scale * 1.4426950408889634f;
+    // Test hooks for the bounded waits (failure detection is tested without a GPU fault):
+    // PKV_TEST_WAIT_LIMIT_MS shortens every wait, PKV_TEST_STALL_COPIES makes every K/V stage
+    // expect 16 bytes no copy delivers, so the waits run out and the call reports PKV_ERR_TIMEOUT.
     const int limit_ms = env_int("PKV_TEST_WAIT_LIMIT_MS", 0);
     p.wait_ns = limit_ms > 0 ? (uint64_t)limit_ms * 1000000ull : kWaitLimitNs;
+    p.stall_tx = env_int("PKV_TEST_STALL_COPIES", 0) ? 16u : 0u;
     p.B = B;
     const int64_t ctas = (int64_t)B * pool->n_kv_heads * p.tiles;
     if (ctas > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;

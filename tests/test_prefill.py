@@ -316,3 +316,33 @@ def test_chunked_prefill_with_rope_matches_oracle():
     ref = op.prefill_attention(qr, sc.cu_q, tables, sc.ctx, sc.Hq, 1 / math.sqrt(sc.D))
     _check_close(out.view(torch.int16).cpu().numpy().view(np.uint16), ref)
     pool.close()
+
+
+@pytest.mark.gpu
+def test_prefill_bounded_waits_report_timeout_and_leave_the_context_usable(monkeypatch):
+    """Every mbarrier wait in the prefill kernel is bounded. With the test hooks each K/V stage
+    expects bytes no copy delivers and the waits give up after 20 ms: the call reports
+    PKV_ERR_TIMEOUT without a fault, tensor memory is released, and the next normal call gives the
+    same bits as before."""
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import PrefillStep
+    sc = W.make_prefill_script(91, B=3, Hq=8, Hkv=2, block_size=64, past=[300, 0, 40], chunk=[200, 90, 17])
+    st = PrefillStep(sc)
+    st.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+    good = st.out_host().copy()
+    monkeypatch.setenv("PKV_TEST_WAIT_LIMIT_MS", "20")
+    monkeypatch.setenv("PKV_TEST_STALL_COPIES", "1")
+    st.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_ERR_TIMEOUT
+    monkeypatch.delenv("PKV_TEST_WAIT_LIMIT_MS")
+    monkeypatch.delenv("PKV_TEST_STALL_COPIES")
+    st.out.zero_()
+    st.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+    assert np.array_equal(st.out_host(), good)
+    st.close()
