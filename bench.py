@@ -656,6 +656,70 @@ def prefill_oracle_rate(sc, budget_s: float, threads: int):
                       f"including the pool replica's set-up; {spent:.1f} s"}
 
 
+def run_chunk_loop(args, world, rank, local):
+    """In-flight batching with chunked context (one layer, Llama-3-8B shapes, block 64): joining
+    prompts are prefilled 512 tokens per step on the tensor cores while the others decode (the
+    scheduling of "TensorRT-LLM 深度实战" §7.3); every step is one prefill call plus one
+    graph-replayed decode step."""
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+    from paged_kv_cache_266_gb300 import pkv_check_device_error
+    from paged_kv_cache_266_gb300.engine import DecodeLoop
+    torch.cuda.set_device(local)
+    n = args.warmup + args.steps
+    sc = W.make_chunked_loop_script(index=55, n_steps=n, max_batch=args.loop_batch, Hq=32, Hkv=8, D=128,
+                                    block_size=64, kv_dtype="bf16", prompt_lo=256, prompt_hi=4096, p_finish=0.02,
+                                    chunk=args.chunk)
+    dev = f"cuda:{local}"
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    prompts = {}
+    for _, joined in sc.steps:
+        for s, m in joined:
+            k, v = sc.prompt_kv(s, m)
+            prompts[s] = (to_dev(k), to_dev(v), to_dev(sc.prompt_q(s, 0, m)))
+    inputs = [None] * n
+    loop = DecodeLoop(sc, graphs=True, device=dev, prompts=prompts)
+    state: dict = {}
+    plans = []
+    for t in range(n):  # the decode inputs of each step, drawn before the timed region
+        pre, dec = sc.plan_step(t, state)
+        for s_, p0, p1 in pre:
+            state[s_][1] = p1
+        for s_ in dec:
+            state[s_][2] += 1
+        plans.append((sum(p1 - p0 for _, p0, p1 in pre), len(dec)))
+        inputs[t] = sc.step_inputs(t, dec) if dec else None
+    for t in range(args.warmup):
+        loop.step(inputs[t])
+    torch.cuda.synchronize()
+    loop.timing = {k: 0.0 for k in loop.timing}
+    dist_barrier(world)
+    t0 = time.perf_counter()
+    for t in range(args.warmup, n):
+        loop.step(inputs[t])
+    torch.cuda.synchronize()
+    dt = dist_max(time.perf_counter() - t0, world)
+    if pkv_check_device_error(loop.pool.handle) != 0:
+        raise RuntimeError("device error flag set in the chunked loop")
+    pre_tok = sum(p[0] for p in plans[args.warmup:])
+    dec_tok = sum(p[1] for p in plans[args.warmup:])
+    if rank == 0:
+        K = args.steps
+        print(json.dumps({
+            "metric": "in-flight loop with chunked context (one layer): prompt + decode tokens/s",
+            "value": round(world * (pre_tok + dec_tok) / dt, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 KV; bf16 MMA / f32 accumulate", "data": "synthetic",
+            "config": {"workload": sc.name, "batch": sc.max_batch, "q_heads": sc.Hq, "kv_heads": sc.Hkv,
+                       "head_dim": sc.D, "block_size": sc.block_size, "chunk": sc.chunk, "prompts": "U[256,4096]",
+                       "finish_prob_per_step": 0.02, "graphs": "decode: one per batch bucket"},
+            "prompt_tokens_per_s": round(world * pre_tok / dt, 1), "decode_tokens_per_s": round(world * dec_tok / dt, 1),
+            "host_ms_per_step": {k: round(v / K * 1e3, 4) for k, v in loop.timing.items()},
+        }), flush=True)
+    loop.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -669,6 +733,7 @@ def main():
     ap.add_argument("--seqs", type=int, default=0, help="profiling: step over the first N sequences only")
     ap.add_argument("--loop", action="store_true", help="measure the in-flight decode loop instead of one step")
     ap.add_argument("--loop-batch", type=int, default=128)
+    ap.add_argument("--chunk", type=int, default=0, help="with --loop: chunked context, prompt tokens per step")
     ap.add_argument("--prefix", action="store_true", help="measure decode over children of a shared prompt prefix")
     ap.add_argument("--prefill", action="store_true", help="measure the chunked-context prefill step")
     ap.add_argument("--rope", action="store_true", help="measure the decode step with RoPE fused into the append")
@@ -680,6 +745,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.loop and args.chunk:
+        run_chunk_loop(args, world, rank, local)
     elif args.loop:
         run_loop(args, world, rank, local)
     elif args.prefix:

@@ -46,6 +46,63 @@ def attention(w, pool, tables, threads: int | None = None, seqs=None) -> np.ndar
     return pool.attention(q, tables, lens, w.Hq, 1.0 / math.sqrt(w.D), threads=threads or os.cpu_count() or 1)
 
 
+def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = None):
+    """Replay a chunked-context decode loop ("TensorRT-LLM 深度实战" §7.3): each step, finished
+    sequences release their pages; every prefilling sequence appends its next prompt chunk and
+    its chunk's queries attend causally over its cache (one append call for all chunks of the
+    step); every decoding sequence appends one token and attends.  Yields per step (decode ids,
+    fp64 decode output [B][Hq][D], prefill chunks [(seq, p0, p1)], fp64 prefill output
+    [sum(p1 - p0)][Hq][D]); the pool replica is returned last."""
+    from . import Allocator, Pool
+    sc = script
+    alloc = Allocator(sc.num_blocks, sc.block_size)
+    pool = Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, KV_CODE[sc.kv_dtype])
+    max_blocks = -(-sc.max_len // sc.block_size)
+    scale = 1.0 / math.sqrt(sc.D)
+    nthreads = threads or os.cpu_count() or 1
+    state: dict = {}
+    outs = []
+    for t in range(len(sc.steps) if n_steps is None else n_steps):
+        for s in sc.steps[t][0]:
+            if alloc.release(s):
+                raise RuntimeError("oracle loop: release failed")
+        prefill, decode = sc.plan_step(t, state)
+        out_pre = np.zeros((0, sc.Hq, sc.D))
+        if prefill:
+            ks, vs, qs, seqs, pos = [], [], [], [], []
+            for s, p0, p1 in prefill:
+                if alloc.reserve(s, p1):
+                    raise RuntimeError("oracle loop: out of pages")
+                k, v = sc.prompt_kv(s, state[s][0])
+                ks.append(k[p0:p1])
+                vs.append(v[p0:p1])
+                qs.append(sc.prompt_q(s, p0, p1))
+                seqs += [s] * (p1 - p0)
+                pos += list(range(p0, p1))
+            pool.append(np.concatenate(ks), np.concatenate(vs), alloc.slot_mapping(seqs, pos))
+            cu = np.concatenate([[0], np.cumsum([p1 - p0 for _, p0, p1 in prefill])]).astype(np.int32)
+            ids = [s for s, _, _ in prefill]
+            tables = alloc.block_tables(ids, max_blocks)
+            ctx = np.array([p1 for _, _, p1 in prefill], dtype=np.int32)
+            out_pre = pool.prefill_attention(np.concatenate(qs), cu, tables, ctx, sc.Hq, scale, threads=nthreads)
+            for s, p0, p1 in prefill:
+                state[s][1] = p1
+        out_dec = np.zeros((0, sc.Hq, sc.D))
+        if decode:
+            lens = np.array([state[s][0] + state[s][2] for s in decode], dtype=np.int64)
+            for s, L in zip(decode, lens):
+                if alloc.reserve(s, int(L) + 1):
+                    raise RuntimeError("oracle loop: out of pages")
+            k, v, q = sc.step_inputs(t, decode)
+            pool.append(k, v, alloc.slot_mapping(decode, lens))
+            tables = alloc.block_tables(decode, max_blocks)
+            out_dec = pool.attention(q, tables, (lens + 1).astype(np.int32), sc.Hq, scale, threads=nthreads)
+            for s in decode:
+                state[s][2] += 1
+        outs.append((list(decode), out_dec, list(prefill), out_pre))
+    return outs, pool
+
+
 def run_loop(script, n_steps: int | None = None, threads: int | None = None):
     """Replay a decode-loop schedule (finished sequences release their pages, joiners get their
     prompt appended, every running sequence appends one token and attends).  Yields, per step,

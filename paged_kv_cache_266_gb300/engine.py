@@ -24,7 +24,7 @@ import math
 
 import numpy as np
 
-from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
+from . import (KV_DTYPES, KVPool, pkv_prefill_step, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
                pkv_get_block_tables, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many, pkv_slot_mapping)
 
 DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
@@ -73,7 +73,13 @@ class DecodeLoop:
     def __init__(self, script, graphs: bool = True, buckets=DEFAULT_BUCKETS, device: str = "cuda",
                  prompts=None):
         """prompts: optional {seq_id: (k, v)} of device bf16 tensors [n][Hkv][D] (a joining
-        sequence's prompt K/V as its prefill produced them); else drawn from the script."""
+        sequence's prompt K/V as its prefill produced them; with chunked context (a script with
+        chunk > 0) also (k, v, q), q [n][Hq][D] the prompt's queries); else drawn from the script.
+
+        Chunked context (script.chunk > 0, "TensorRT-LLM 深度实战" §7.3): a joining sequence's
+        prompt is prefilled `chunk` tokens per step (its chunk's K/V appended and its queries
+        attending causally, one pkv_prefill_step for all prefilling sequences of the step) and
+        the sequence decodes from the step after its last chunk."""
         import torch
         self.prompts = prompts or {}
         self.torch, self.script, self.graphs, self.device = torch, script, graphs, device
@@ -87,6 +93,8 @@ class DecodeLoop:
         self.running: list[int] = []
         self.t = 0
         self.timing = {"admit_s": 0.0, "prepare_s": 0.0, "device_s": 0.0}  # host wall time per phase
+        self.state: dict = {}  # chunked context: seq -> [prompt_len, prefilled, decoded]
+        self.last_prefill = ([], None)  # chunked context: (chunks [(seq, p0, p1)], output bits)
 
     def _bucket(self, B: int) -> _Bucket:
         Bp = next((b for b in self.buckets if b >= B), None)
@@ -111,21 +119,72 @@ class DecodeLoop:
         self.lens[seq] = n
         self.running.append(seq)
 
+    def _prefill_chunks(self, prefill):
+        """One chunked-context prefill call for all of this step's prompt chunks."""
+        torch, sc = self.torch, self.script
+        ks, vs, qs, seqs, pos = [], [], [], [], []
+        for s, p0, p1 in prefill:
+            pkv_seq_reserve(self.alloc, s, p1)
+            if s in self.prompts:
+                dk, dv, dq = self.prompts[s]
+                ks.append(dk[p0:p1])
+                vs.append(dv[p0:p1])
+                qs.append(dq[p0:p1])
+            else:
+                k, v = sc.prompt_kv(s, self.state[s][0])
+                to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(
+                    self.device)
+                ks.append(to_dev(k[p0:p1]))
+                vs.append(to_dev(v[p0:p1]))
+                qs.append(to_dev(sc.prompt_q(s, p0, p1)))
+            seqs += [s] * (p1 - p0)
+            pos += list(range(p0, p1))
+        ids = [s for s, _, _ in prefill]
+        slots = pkv_slot_mapping(self.alloc, seqs, np.asarray(pos, dtype=np.int64))
+        cu = np.concatenate([[0], np.cumsum([p1 - p0 for _, p0, p1 in prefill])]).astype(np.int32)
+        ctx = np.array([p1 for _, _, p1 in prefill], dtype=np.int32)
+        tables = pkv_get_block_tables(self.alloc, ids, self.max_blocks)
+        dev = self.device
+        out = torch.empty(int(cu[-1]), sc.Hq, sc.D, dtype=torch.bfloat16, device=dev)
+        pkv_prefill_step(self.pool.handle, torch.cat(ks), torch.cat(vs), torch.from_numpy(slots).to(dev),
+                         torch.cat(qs), torch.from_numpy(cu).to(dev), int(np.diff(cu).max()),
+                         torch.from_numpy(tables).to(dev), torch.from_numpy(ctx).to(dev), self.scale, out)
+        for s, p0, p1 in prefill:
+            self.state[s][1] = p1
+        return out
+
     def step(self, inputs=None):
-        """Run the next scheduled step; returns (running sequence ids, output [B][Hq][D] bf16 bits).
-        inputs: optional (k_new, v_new, q) for the running sequences (else drawn from the script)."""
+        """Run the next scheduled step; returns (decoding sequence ids, output [B][Hq][D] bf16 bits).
+        inputs: optional (k_new, v_new, q) for the decoding sequences (else drawn from the script).
+        With chunked context the step's prefill chunks and their output are in self.last_prefill."""
         import time
         torch, sc = self.torch, self.script
         t0 = time.perf_counter()
         finished, joined = sc.steps[self.t]
         for s in finished:
             pkv_seq_release(self.alloc, s)
+            if sc.chunk:
+                continue
             self.running.remove(s)
             del self.lens[s]
-        for s, n in joined:
-            self._admit(s, n)
+        if sc.chunk:
+            prefill, decode = sc.plan_step(self.t, self.state)
+            pre_out = self._prefill_chunks(prefill) if prefill else None
+            self.running = decode
+            self.lens = {s: self.state[s][0] + self.state[s][2] for s in decode}
+            for s in decode:
+                self.state[s][2] += 1
+            self.last_prefill = (prefill, pre_out)
+        else:
+            for s, n in joined:
+                self._admit(s, n)
         t1 = time.perf_counter()
         run = list(self.running)
+        if not run:
+            self.t += 1
+            if sc.chunk and self.last_prefill[1] is not None:
+                torch.cuda.current_stream().synchronize()
+            return run, np.zeros((0, sc.Hq, sc.D), dtype=np.uint16)
         B = len(run)
         pos = np.array([self.lens[s] for s in run], dtype=np.int64)
         pkv_seq_reserve_many(self.alloc, run, pos + 1)  # room for this step's token
@@ -165,8 +224,9 @@ class DecodeLoop:
         self.timing["admit_s"] += t1 - t0
         self.timing["prepare_s"] += t2 - t1
         self.timing["device_s"] += t3 - t2
-        for s in run:
-            self.lens[s] += 1
+        if not sc.chunk:
+            for s in run:
+                self.lens[s] += 1
         self.t += 1
         return run, bk.out_host.numpy()[:B].view(np.uint16).copy()
 

@@ -328,6 +328,7 @@ def truncated(w: Workload, n: int) -> Workload:
 
 # ----------------------------------------------------------------------------- decode loop
 TAG_LOOP_SCHED, TAG_LOOP_PROMPT_K, TAG_LOOP_PROMPT_V, TAG_LOOP_K, TAG_LOOP_V, TAG_LOOP_Q = range(20, 26)
+TAG_LOOP_PROMPT_Q = 26
 
 
 @dataclass
@@ -349,10 +350,39 @@ class LoopScript:
     max_batch: int
     steps: list
     max_len: int
+    chunk: int = 0  # chunked context: prompt tokens prefilled per step (0: prompts appended at once)
 
     @property
     def G(self) -> int:
         return self.Hq // self.Hkv
+
+    def prompt_q(self, seq_id: int, p0: int, p1: int):
+        """Queries of a joining sequence's prompt tokens p0 .. p1-1 ([p1-p0][Hq][D] bf16 bits), for
+        the chunked prefill of its prompt."""
+        row = self.Hq * self.D
+        off = (seq_id * self.max_len + p0) * row
+        return normal_bf16(stream_seed(self.seed, TAG_LOOP_PROMPT_Q), off, (p1 - p0) * row).reshape(p1 - p0, self.Hq,
+                                                                                                      self.D)
+
+    def plan_step(self, t: int, state: dict):
+        """Chunked context ("TensorRT-LLM 深度实战", §7.3): what step t does, given `state` (the
+        sequences admitted and not finished, in admission order: seq -> [prompt_len, prefilled,
+        cached]).  Applies step t's finishes and joins to `state` and returns (prefill, decode):
+        prefill = [(seq, p0, p1)] chunks of prompt tokens processed this step, decode = the
+        sequences (prompt done before this step) that append one token and attend.  After the
+        step the caller adds p1 - p0 to `prefilled` and one token to `cached` of the decoders."""
+        finished, joined = self.steps[t]
+        for s in finished:
+            del state[s]
+        for s, n in joined:
+            state[s] = [n, 0, 0]
+        prefill, decode = [], []
+        for s, (n, done, cached) in state.items():
+            if done < n:
+                prefill.append((s, done, min(n, done + self.chunk)))
+            else:
+                decode.append(s)
+        return prefill, decode
 
     def prompt_kv(self, seq_id: int, n: int):
         """History K and V ([n][Hkv][D] bf16 bits) of a joining sequence's prompt."""
@@ -371,6 +401,48 @@ class LoopScript:
         v = normal_bf16(stream_seed(self.seed, TAG_LOOP_V), t * self.max_batch * row_kv, n * row_kv)
         q = normal_bf16(stream_seed(self.seed, TAG_LOOP_Q), t * self.max_batch * row_q, n * row_q)
         return k.reshape(n, self.Hkv, self.D), v.reshape(n, self.Hkv, self.D), q.reshape(n, self.Hq, self.D)
+
+
+def make_chunked_loop_script(index: int = 45, n_steps: int = 32, max_batch: int = 16, Hq: int = 8, Hkv: int = 2,
+                             D: int = 128, block_size: int = 16, kv_dtype: str = "bf16", prompt_lo: int = 1,
+                             prompt_hi: int = 300, p_finish: float = 0.12, chunk: int = 64,
+                             num_blocks: int | None = None) -> LoopScript:
+    """Seeded churn with chunked context: a joining sequence first prefills its prompt, `chunk`
+    tokens per step, and decodes from the step after its last chunk; each step every decoding
+    sequence finishes with probability p_finish, then new sequences (prompt lengths U[prompt_lo,
+    prompt_hi]) fill the batch back to max_batch."""
+    seed = 266 * 1000 + index
+    s = stream_seed(seed, TAG_LOOP_SCHED)
+    draw = 0
+    state: dict = {}
+    steps, next_id, peak = [], 0, 0
+    for t in range(n_steps):
+        finished = []
+        for sid in list(state):
+            n, done, _ = state[sid]
+            if done >= n:  # only decoding sequences finish
+                if unit(s, draw) < p_finish:
+                    finished.append(sid)
+                    del state[sid]
+                draw += 1
+        joined = []
+        while len(state) < max_batch:
+            n = uniform_int(s, draw, prompt_lo, prompt_hi)
+            draw += 1
+            joined.append((next_id, n))
+            state[next_id] = [n, 0, 0]
+            next_id += 1
+        steps.append((finished, joined))
+        for sid, st in state.items():  # the step: a chunk for prefilling sequences, a token for decoders
+            if st[1] < st[0]:
+                st[1] = min(st[0], st[1] + chunk)
+            else:
+                st[2] += 1
+        peak = max(peak, sum(_ceil_div(st[1] + st[2], block_size) for st in state.values()))
+    max_len = prompt_hi + n_steps + 1
+    nb = num_blocks or peak + 8
+    return LoopScript(f"chunkloop{index}", seed, Hq, Hkv, D, block_size, kv_dtype, nb, max_batch, steps, max_len,
+                      chunk)
 
 
 def make_loop_script(index: int = 40, n_steps: int = 32, max_batch: int = 24, Hq: int = 8, Hkv: int = 2, D: int = 128,

@@ -61,3 +61,58 @@ def test_decode_loop_matches_oracle_every_step(kv_dtype, bs, graphs):
     if sc_bytes:
         assert np.array_equal(_wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32), pool.scales)
     loop.close()
+
+
+def test_chunked_loop_schedule_matches_its_generator():
+    """The per-step plan (prefill chunks, decoders) replays the generator's state: every prompt
+    is prefilled in chunks of at most `chunk` tokens covering it exactly once, a sequence decodes
+    only after its prompt, and only decoding sequences finish."""
+    sc = W.make_chunked_loop_script(index=46, n_steps=40, chunk=48)
+    state, covered = {}, {}
+    for t in range(len(sc.steps)):
+        finished, joined = sc.steps[t]
+        for s in finished:
+            assert state[s][1] == state[s][0], "a sequence finished while prefilling"
+        prefill, decode = sc.plan_step(t, state)
+        for s, p0, p1 in prefill:
+            assert p0 == covered.get(s, 0) and 0 < p1 - p0 <= sc.chunk and p1 <= state[s][0]
+            covered[s] = p1
+            state[s][1] = p1
+        for s in decode:
+            assert state[s][1] == state[s][0] and s not in [c[0] for c in prefill]
+            state[s][2] += 1
+        assert len(state) <= sc.max_batch
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("bs,graphs", [(16, True), (64, False)])
+def test_chunked_context_loop_matches_oracle_every_step(bs, graphs):
+    """Chunked context in the in-flight loop: every step's prefill-chunk outputs and decode
+    outputs against the oracle's replay, and the final pool bytes bit-exact."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    from paged_kv_cache_266_gb300.engine import DecodeLoop
+    sc = W.make_chunked_loop_script(index=47, n_steps=20, block_size=bs, chunk=48)
+    ref, pool = odrive.run_chunked_loop(sc)
+    loop = DecodeLoop(sc, graphs=graphs)
+    for t in range(len(sc.steps)):
+        run, out = loop.step()
+        assert run == ref[t][0]
+        if run:
+            err = np.abs(oracle.bf16_bits_to_f64(out) - ref[t][1])
+            assert err.max() <= 1e-2 and err.mean() <= TOL_MEAN, ("decode", t, err.max(), err.mean())
+        chunks, pre = loop.last_prefill
+        assert chunks == ref[t][2]
+        if chunks:
+            got = oracle.bf16_bits_to_f64(pre.view(torch.int16).cpu().numpy().view(np.uint16))
+            err = np.abs(got - ref[t][3])
+            assert err.max() <= 1e-2 and err.mean() <= TOL_MEAN, ("prefill", t, err.max(), err.mean())
+    assert pkv.pkv_check_device_error(loop.pool.handle) == pkv.PKV_OK
+    kv, kv_bytes, _, _ = pkv.pkv_pool_raw(loop.pool.handle)
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    assert np.array_equal(_wrap_device(kv, kv_bytes).cpu().numpy(), pool.data)
+    loop.close()
