@@ -670,20 +670,26 @@ def run_chunk_loop(args, world, rank, local):
     n = args.warmup + args.steps
     sc = W.make_chunked_loop_script(index=55, n_steps=n, max_batch=args.loop_batch, Hq=32, Hkv=8, D=128,
                                     block_size=64, kv_dtype="bf16", prompt_lo=256, prompt_hi=4096, p_finish=0.02,
-                                    chunk=args.chunk)
+                                    chunk=args.chunk, system=args.system, reuse=not args.no_reuse)
     dev = f"cuda:{local}"
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     prompts = {}
+    base = sc.system if sc.reuse else 0
     for _, joined in sc.steps:
         for s, m in joined:
-            k, v = sc.prompt_kv(s, m)
-            prompts[s] = (to_dev(k), to_dev(v), to_dev(sc.prompt_q(s, 0, m)))
+            k, v, q = sc.prompt_rows(s, base, sc.system + m)
+            prompts[s] = (to_dev(k), to_dev(v), to_dev(q))
     inputs = [None] * n
     loop = DecodeLoop(sc, graphs=True, device=dev, prompts=prompts)
     state: dict = {}
     plans = []
+    joined_at, first_decode = {}, {}
     for t in range(n):  # the decode inputs of each step, drawn before the timed region
+        for s_, _ in sc.steps[t][1]:
+            joined_at[s_] = t
         pre, dec = sc.plan_step(t, state)
+        for s_ in dec:
+            first_decode.setdefault(s_, t)
         for s_, p0, p1 in pre:
             state[s_][1] = p1
         for s_ in dec:
@@ -704,6 +710,7 @@ def run_chunk_loop(args, world, rank, local):
         raise RuntimeError("device error flag set in the chunked loop")
     pre_tok = sum(p[0] for p in plans[args.warmup:])
     dec_tok = sum(p[1] for p in plans[args.warmup:])
+    ttft = [first_decode[s_] - joined_at[s_] for s_ in first_decode if joined_at[s_] >= args.warmup]
     if rank == 0:
         K = args.steps
         print(json.dumps({
@@ -715,6 +722,9 @@ def run_chunk_loop(args, world, rank, local):
                        "head_dim": sc.D, "block_size": sc.block_size, "chunk": sc.chunk, "prompts": "U[256,4096]",
                        "finish_prob_per_step": 0.02, "graphs": "decode: one per batch bucket"},
             "prompt_tokens_per_s": round(world * pre_tok / dt, 1), "decode_tokens_per_s": round(world * dec_tok / dt, 1),
+            "system_prompt": {"tokens": sc.system, "cached": bool(sc.system and sc.reuse)},
+            "first_token_steps_mean": round(float(np.mean(ttft)), 3) if ttft else None,
+            "first_token_ms_mean": round(float(np.mean(ttft)) * dt / K * 1e3, 3) if ttft else None,
             "host_ms_per_step": {k: round(v / K * 1e3, 4) for k, v in loop.timing.items()},
         }), flush=True)
     loop.close()
@@ -734,6 +744,8 @@ def main():
     ap.add_argument("--loop", action="store_true", help="measure the in-flight decode loop instead of one step")
     ap.add_argument("--loop-batch", type=int, default=128)
     ap.add_argument("--chunk", type=int, default=0, help="with --loop: chunked context, prompt tokens per step")
+    ap.add_argument("--system", type=int, default=0, help="with --chunk: a shared system prompt of this many tokens")
+    ap.add_argument("--no-reuse", action="store_true", help="with --system: every request prefills it")
     ap.add_argument("--prefix", action="store_true", help="measure decode over children of a shared prompt prefix")
     ap.add_argument("--prefill", action="store_true", help="measure the chunked-context prefill step")
     ap.add_argument("--rope", action="store_true", help="measure the decode step with RoPE fused into the append")

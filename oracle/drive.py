@@ -62,10 +62,23 @@ def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = N
     nthreads = threads or os.cpu_count() or 1
     state: dict = {}
     outs = []
+    if sc.system:  # the shared system prompt, cached once (prefix caching)
+        from pkv_workloads import SYSTEM_SEQ
+        if alloc.reserve(SYSTEM_SEQ, sc.system):
+            raise RuntimeError("oracle loop: out of pages")
+        k, v = sc.system_kv()
+        pool.append(k, v, alloc.slot_mapping([SYSTEM_SEQ] * sc.system, np.arange(sc.system)))
     for t in range(len(sc.steps) if n_steps is None else n_steps):
         for s in sc.steps[t][0]:
             if alloc.release(s):
                 raise RuntimeError("oracle loop: release failed")
+        if sc.system and sc.reuse:  # joiners fork the cached system prompt
+            for s, _ in sc.steps[t][1]:
+                rc, cs, cd = alloc.share_prefix(SYSTEM_SEQ, s, sc.system)
+                if rc:
+                    raise RuntimeError(f"oracle loop: fork failed ({rc})")
+                if cs >= 0:
+                    pool.copy_block(cs, cd)
         prefill, decode = sc.plan_step(t, state)
         out_pre = np.zeros((0, sc.Hq, sc.D))
         if prefill:
@@ -73,10 +86,10 @@ def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = N
             for s, p0, p1 in prefill:
                 if alloc.reserve(s, p1):
                     raise RuntimeError("oracle loop: out of pages")
-                k, v = sc.prompt_kv(s, state[s][0])
-                ks.append(k[p0:p1])
-                vs.append(v[p0:p1])
-                qs.append(sc.prompt_q(s, p0, p1))
+                k, v, q = sc.prompt_rows(s, p0, p1)
+                ks.append(k)
+                vs.append(v)
+                qs.append(q)
                 seqs += [s] * (p1 - p0)
                 pos += list(range(p0, p1))
             pool.append(np.concatenate(ks), np.concatenate(vs), alloc.slot_mapping(seqs, pos))

@@ -8,15 +8,20 @@ batch-size bucket because a graph is fixed to its shapes.
 
 Each step here:
   1. releases the finished sequences' blocks (pkv_seq_release);
-  2. admits joining sequences: blocks for their prompt (pkv_seq_reserve) and the prompt's K/V
-     written with pkv_append (prefill attention itself is not part of this library);
-  3. gives every running sequence room for one more token (pkv_seq_reserve grows by whole
+  2. admits joining sequences.  Without chunked context their prompt's K/V are written at once
+     (pkv_seq_reserve + pkv_append, as a prefill would leave them).  With chunked context
+     ("TensorRT-LLM 深度实战" §7.3) a joiner's prompt is prefilled `chunk` tokens per step: one
+     pkv_prefill_step appends every prefilling sequence's next chunk and attends its queries
+     causally, and the sequence decodes from the step after its last chunk.  With a system
+     prompt (prefix caching, "TensorRT-LLM 推理加速实战" §8 KV cache reuse) the shared prefix
+     is cached once and every joiner forks it (pkv_seq_share_prefix) instead of prefilling it;
+  3. gives every decoding sequence room for one more token (pkv_seq_reserve_many grows by whole
      blocks), writes block tables, new-token slots and context lengths straight into a pinned
      staging buffer together with the step's q / new K / new V;
-  4. runs, on the batch padded to its bucket, one host-to-device copy, pkv_decode_step (append +
-     attention) and the copy of the output back — captured once per bucket as a CUDA graph and
-     replayed.  Padding rows have context length 0 and slot -1, so they write nothing and read
-     nothing; their outputs are zeros.
+  4. runs, on the decode batch padded to its bucket, one host-to-device copy, pkv_decode_step
+     (append + attention) and the copy of the output back — captured once per bucket as a CUDA
+     graph and replayed.  Padding rows have context length 0 and slot -1, so they write nothing
+     and read nothing; their outputs are zeros.
 """
 from __future__ import annotations
 
@@ -24,8 +29,9 @@ import math
 
 import numpy as np
 
-from . import (KV_DTYPES, KVPool, pkv_prefill_step, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
-               pkv_get_block_tables, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many, pkv_slot_mapping)
+from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
+               pkv_pool_copy_block, pkv_prefill_step, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many,
+               pkv_seq_share_prefix, pkv_slot_mapping)
 
 DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
 
@@ -74,7 +80,8 @@ class DecodeLoop:
                  prompts=None):
         """prompts: optional {seq_id: (k, v)} of device bf16 tensors [n][Hkv][D] (a joining
         sequence's prompt K/V as its prefill produced them; with chunked context (a script with
-        chunk > 0) also (k, v, q), q [n][Hq][D] the prompt's queries); else drawn from the script.
+        chunk > 0) (k, v, q), q [n][Hq][D] the prompt's queries, rows from the first position the
+        request prefills: after the system prompt when it is cached); else drawn from the script.
 
         Chunked context (script.chunk > 0, "TensorRT-LLM 深度实战" §7.3): a joining sequence's
         prompt is prefilled `chunk` tokens per step (its chunk's K/V appended and its queries
@@ -94,6 +101,16 @@ class DecodeLoop:
         self.t = 0
         self.timing = {"admit_s": 0.0, "prepare_s": 0.0, "device_s": 0.0}  # host wall time per phase
         self.state: dict = {}  # chunked context: seq -> [prompt_len, prefilled, decoded]
+        if script.chunk and script.system:
+            # prefix caching ("TensorRT-LLM 推理加速实战" §8, KV cache reuse): the shared system
+            # prompt is cached once under its own sequence; joiners fork it
+            from pkv_workloads import SYSTEM_SEQ
+            self.system_seq = SYSTEM_SEQ
+            k, v = script.system_kv()
+            pkv_seq_reserve(self.alloc, SYSTEM_SEQ, script.system)
+            slots = pkv_slot_mapping(self.alloc, [SYSTEM_SEQ] * script.system, np.arange(script.system))
+            to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+            pkv_append(self.pool.handle, to_dev(k), to_dev(v), torch.from_numpy(slots).to(device))
         self.last_prefill = ([], None)  # chunked context: (chunks [(seq, p0, p1)], output bits)
 
     def _bucket(self, B: int) -> _Bucket:
@@ -125,18 +142,19 @@ class DecodeLoop:
         ks, vs, qs, seqs, pos = [], [], [], [], []
         for s, p0, p1 in prefill:
             pkv_seq_reserve(self.alloc, s, p1)
-            if s in self.prompts:
+            if s in self.prompts:  # staged rows from position `base` (after a cached system prompt)
+                base = sc.system if sc.reuse else 0
                 dk, dv, dq = self.prompts[s]
-                ks.append(dk[p0:p1])
-                vs.append(dv[p0:p1])
-                qs.append(dq[p0:p1])
+                ks.append(dk[p0 - base:p1 - base])
+                vs.append(dv[p0 - base:p1 - base])
+                qs.append(dq[p0 - base:p1 - base])
             else:
-                k, v = sc.prompt_kv(s, self.state[s][0])
+                k, v, q = sc.prompt_rows(s, p0, p1)
                 to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(
                     self.device)
-                ks.append(to_dev(k[p0:p1]))
-                vs.append(to_dev(v[p0:p1]))
-                qs.append(to_dev(sc.prompt_q(s, p0, p1)))
+                ks.append(to_dev(k))
+                vs.append(to_dev(v))
+                qs.append(to_dev(q))
             seqs += [s] * (p1 - p0)
             pos += list(range(p0, p1))
         ids = [s for s, _, _ in prefill]
@@ -168,6 +186,11 @@ class DecodeLoop:
             self.running.remove(s)
             del self.lens[s]
         if sc.chunk:
+            if sc.system and sc.reuse:  # joiners fork the cached system prompt (partial block copied)
+                for s, _ in joined:
+                    cs, cd = pkv_seq_share_prefix(self.alloc, self.system_seq, s, sc.system)
+                    if cs >= 0:
+                        pkv_pool_copy_block(self.pool.handle, cs, cd)
             prefill, decode = sc.plan_step(self.t, self.state)
             pre_out = self._prefill_chunks(prefill) if prefill else None
             self.running = decode

@@ -328,7 +328,8 @@ def truncated(w: Workload, n: int) -> Workload:
 
 # ----------------------------------------------------------------------------- decode loop
 TAG_LOOP_SCHED, TAG_LOOP_PROMPT_K, TAG_LOOP_PROMPT_V, TAG_LOOP_K, TAG_LOOP_V, TAG_LOOP_Q = range(20, 26)
-TAG_LOOP_PROMPT_Q = 26
+TAG_LOOP_PROMPT_Q, TAG_LOOP_SYSTEM_K, TAG_LOOP_SYSTEM_V = 26, 27, 28
+SYSTEM_SEQ = 1 << 40  # sequence id of the cached system prompt (prefix caching in the loop)
 
 
 @dataclass
@@ -351,10 +352,37 @@ class LoopScript:
     steps: list
     max_len: int
     chunk: int = 0  # chunked context: prompt tokens prefilled per step (0: prompts appended at once)
+    system: int = 0  # every prompt starts with this many shared system-prompt tokens
+    reuse: bool = True  # prefix caching: joiners fork the cached system prompt (else they prefill it)
 
     @property
     def G(self) -> int:
         return self.Hq // self.Hkv
+
+    def system_kv(self):
+        """K and V of the shared system prompt ([system][Hkv][D] bf16 bits), from their own streams."""
+        n, row = self.system, self.Hkv * self.D
+        k = normal_bf16(stream_seed(self.seed, TAG_LOOP_SYSTEM_K), 0, n * row).reshape(n, self.Hkv, self.D)
+        v = normal_bf16(stream_seed(self.seed, TAG_LOOP_SYSTEM_V), 0, n * row).reshape(n, self.Hkv, self.D)
+        return k, v
+
+    def prompt_rows(self, seq_id: int, p0: int, p1: int):
+        """K, V and queries of prompt tokens p0 .. p1-1 of a request: with a system prompt, the
+        request's own tokens start at position `system` and are drawn from its own streams."""
+        S = self.system
+        ks, vs, qs = [], [], []
+        if p0 < S:  # system-prompt rows (only without reuse): shared K/V, the request's own queries
+            sk, sv = self.system_kv()
+            ks.append(sk[p0:min(p1, S)])
+            vs.append(sv[p0:min(p1, S)])
+            qs.append(self.prompt_q(seq_id, self.max_len - S + p0, self.max_len - S + min(p1, S)))
+        if p1 > S:
+            lo = max(p0, S)
+            k, v = self.prompt_kv(seq_id, p1 - S)
+            ks.append(k[lo - S:])
+            vs.append(v[lo - S:])
+            qs.append(self.prompt_q(seq_id, lo - S, p1 - S))
+        return np.concatenate(ks), np.concatenate(vs), np.concatenate(qs)
 
     def prompt_q(self, seq_id: int, p0: int, p1: int):
         """Queries of a joining sequence's prompt tokens p0 .. p1-1 ([p1-p0][Hq][D] bf16 bits), for
@@ -374,8 +402,8 @@ class LoopScript:
         finished, joined = self.steps[t]
         for s in finished:
             del state[s]
-        for s, n in joined:
-            state[s] = [n, 0, 0]
+        for s, n in joined:  # with prefix caching the request starts with the system prompt cached
+            state[s] = [self.system + n, self.system if self.reuse else 0, 0]
         prefill, decode = [], []
         for s, (n, done, cached) in state.items():
             if done < n:
@@ -405,12 +433,14 @@ class LoopScript:
 
 def make_chunked_loop_script(index: int = 45, n_steps: int = 32, max_batch: int = 16, Hq: int = 8, Hkv: int = 2,
                              D: int = 128, block_size: int = 16, kv_dtype: str = "bf16", prompt_lo: int = 1,
-                             prompt_hi: int = 300, p_finish: float = 0.12, chunk: int = 64,
-                             num_blocks: int | None = None) -> LoopScript:
+                             prompt_hi: int = 300, p_finish: float = 0.12, chunk: int = 64, system: int = 0,
+                             reuse: bool = True, num_blocks: int | None = None) -> LoopScript:
     """Seeded churn with chunked context: a joining sequence first prefills its prompt, `chunk`
     tokens per step, and decodes from the step after its last chunk; each step every decoding
     sequence finishes with probability p_finish, then new sequences (prompt lengths U[prompt_lo,
-    prompt_hi]) fill the batch back to max_batch."""
+    prompt_hi]) fill the batch back to max_batch.  With `system` > 0 every prompt starts with the
+    same `system` tokens, cached once (prefix caching, "TensorRT-LLM 推理加速实战" §8 KV cache
+    reuse): a request forks them and prefills only its own prompt_lo..prompt_hi tokens."""
     seed = 266 * 1000 + index
     s = stream_seed(seed, TAG_LOOP_SCHED)
     draw = 0
@@ -430,7 +460,7 @@ def make_chunked_loop_script(index: int = 45, n_steps: int = 32, max_batch: int 
             n = uniform_int(s, draw, prompt_lo, prompt_hi)
             draw += 1
             joined.append((next_id, n))
-            state[next_id] = [n, 0, 0]
+            state[next_id] = [system + n, system if reuse else 0, 0]
             next_id += 1
         steps.append((finished, joined))
         for sid, st in state.items():  # the step: a chunk for prefilling sequences, a token for decoders
@@ -438,11 +468,15 @@ def make_chunked_loop_script(index: int = 45, n_steps: int = 32, max_batch: int 
                 st[1] = min(st[0], st[1] + chunk)
             else:
                 st[2] += 1
-        peak = max(peak, sum(_ceil_div(st[1] + st[2], block_size) for st in state.values()))
-    max_len = prompt_hi + n_steps + 1
-    nb = num_blocks or peak + 8
-    return LoopScript(f"chunkloop{index}", seed, Hq, Hkv, D, block_size, kv_dtype, nb, max_batch, steps, max_len,
-                      chunk)
+        # blocks held: shared system blocks once, each request its own (and a copied partial one)
+        shared = system // block_size if reuse else 0
+        peak = max(peak, shared + (1 if system % block_size else 0) +
+                   sum(_ceil_div(st[1] + st[2], block_size) - shared for st in state.values()))
+    max_len = 2 * system + prompt_hi + n_steps + 1  # room for the system-prompt queries' stream rows
+    nb = num_blocks or peak + 8 + (system // block_size + 1 if system else 0)
+    name = f"chunkloop{index}" + (f"-sys{system}" + ("" if reuse else "-noreuse") if system else "")
+    return LoopScript(name, seed, Hq, Hkv, D, block_size, kv_dtype, nb, max_batch, steps, max_len, chunk, system,
+                      reuse)
 
 
 def make_loop_script(index: int = 40, n_steps: int = 32, max_batch: int = 24, Hq: int = 8, Hkv: int = 2, D: int = 128,

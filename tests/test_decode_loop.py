@@ -116,3 +116,41 @@ def test_chunked_context_loop_matches_oracle_every_step(bs, graphs):
     from paged_kv_cache_266_gb300.runner import _wrap_device
     assert np.array_equal(_wrap_device(kv, kv_bytes).cpu().numpy(), pool.data)
     loop.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("reuse", [True, False])
+def test_chunked_loop_with_cached_system_prompt_matches_oracle(reuse):
+    """Prefix caching in the loop: every prompt starts with a shared 70-token system prompt
+    (a partial last block) cached once; joiners fork it and prefill only their own tokens. Every
+    step's outputs against the oracle's replay (which forks the same way), final pool bit-exact,
+    and the system prompt's whole blocks are held by every running request."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_266_gb300 import build
+    build.build()
+    import paged_kv_cache_266_gb300 as pkv
+    from paged_kv_cache_266_gb300.engine import DecodeLoop
+    sc = W.make_chunked_loop_script(index=48, n_steps=16, block_size=16, chunk=48, system=70, reuse=reuse)
+    ref, pool = odrive.run_chunked_loop(sc)
+    loop = DecodeLoop(sc, graphs=True)
+    for t in range(len(sc.steps)):
+        run, out = loop.step()
+        assert run == ref[t][0]
+        if run:
+            err = np.abs(oracle.bf16_bits_to_f64(out) - ref[t][1])
+            assert err.max() <= 1e-2 and err.mean() <= TOL_MEAN, ("decode", t, err.max(), err.mean())
+        chunks, pre = loop.last_prefill
+        assert chunks == ref[t][2]
+        if chunks:
+            got = oracle.bf16_bits_to_f64(pre.view(torch.int16).cpu().numpy().view(np.uint16))
+            err = np.abs(got - ref[t][3])
+            assert err.max() <= 1e-2 and err.mean() <= TOL_MEAN, ("prefill", t, err.max(), err.mean())
+    assert pkv.pkv_check_device_error(loop.pool.handle) == pkv.PKV_OK
+    kv, kv_bytes, _, _ = pkv.pkv_pool_raw(loop.pool.handle)
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    assert np.array_equal(_wrap_device(kv, kv_bytes).cpu().numpy(), pool.data)
+    first = int(pkv.pkv_get_block_tables(loop.alloc, [W.SYSTEM_SEQ], 5)[0, 0])
+    assert pkv.pkv_block_refcount(loop.alloc, first) == (1 + len(loop.state) if reuse else 1)
+    loop.close()
