@@ -193,12 +193,13 @@ def oracle_rate(w, budget_s: float, threads: int):
     description of the sample)."""
     import oracle.drive as odrive
     pool, _, tables = odrive.build(w)
+    q = w.query()  # drawn once: input generation stays outside the timed region
     lens = w.attend_lens.astype(np.int64)
     done_tokens, passes, spent = 0, 0, 0.0
     t0 = time.perf_counter()
     while spent < budget_s:
         for b in range(w.B):
-            odrive.attention(w, pool, tables, threads=threads, seqs=[b])
+            odrive.attention(w, pool, tables, threads=threads, seqs=[b], q=q)
             done_tokens += int(lens[b])
             spent = time.perf_counter() - t0
             if spent >= budget_s:
@@ -216,10 +217,11 @@ def run_reference(args, world, rank):
     w = W.make_workload(args.workload)
     threads = os.cpu_count() or 1
     pool, _, tables = odrive.build(w)
+    q = w.query()  # drawn once: input generation stays outside the timed region
     lens = w.attend_lens.astype(np.int64)
     b_mid = int(np.argsort(lens)[len(lens) // 2])
     t0 = time.perf_counter()
-    odrive.attention(w, pool, tables, threads=threads, seqs=[b_mid])
+    odrive.attention(w, pool, tables, threads=threads, seqs=[b_mid], q=q)
     per_seq = time.perf_counter() - t0
     budget_total = 120.0
     per_step = budget_total / max(1, args.steps + args.warmup)
@@ -227,10 +229,10 @@ def run_reference(args, world, rank):
     n_seq = max(1, min(w.B, int(per_step / max(per_seq, 1e-9))))
     seqs = [int(b) for b in np.argsort(lens)[len(lens) // 2:][:n_seq]]
     for _ in range(args.warmup):
-        odrive.attention(w, pool, tables, threads=threads, seqs=seqs)
+        odrive.attention(w, pool, tables, threads=threads, seqs=seqs, q=q)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        odrive.attention(w, pool, tables, threads=threads, seqs=seqs)
+        odrive.attention(w, pool, tables, threads=threads, seqs=seqs, q=q)
     dt = (time.perf_counter() - t0) / args.steps
     kv = int(lens[seqs].sum()) * w.Hkv * 2 * w.D * w.elem_bytes
     value = kv / dt / 1e9
@@ -631,6 +633,7 @@ def prefill_oracle_rate(sc, budget_s: float, threads: int):
     t_start = time.perf_counter()
     flops = 0
     rows = 0
+    spent = 0.0  # attention calls only; the pool replica's set-up is not timed
     for b in range(sc.B):
         P, L = int(sc.past[b]), int(sc.ctx[b])
         a = oracle.Allocator(-(-L // sc.block_size) + 1, sc.block_size)
@@ -639,21 +642,22 @@ def prefill_oracle_rate(sc, budget_s: float, threads: int):
         k, v = sc.kv(b, 0, L)
         pool.append(k, v, a.slot_mapping([0] * L, np.arange(L)))
         tables = a.block_tables([0], -(-L // sc.block_size))
-        t0 = time.perf_counter()
         for i in range(0, int(sc.chunk[b]), 64):
             row = int(sc.cu_q[b]) + i
-            pool.prefill_attention(sc.query(row, row + 1), np.array([0, 1], np.int32), tables,
+            q = sc.query(row, row + 1)
+            t0 = time.perf_counter()
+            pool.prefill_attention(q, np.array([0, 1], np.int32), tables,
                                    np.array([P + i + 1], np.int32), sc.Hq, 1 / math.sqrt(sc.D), threads=threads)
+            spent += time.perf_counter() - t0
             flops += 4 * sc.D * sc.Hq * (P + i + 1)
             rows += 1
             if time.perf_counter() - t_start > budget_s:
                 break
         if time.perf_counter() - t_start > budget_s:
             break
-    spent = time.perf_counter() - t_start
     return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows} query rows (every 64th of each chunk), each over its full causal context, "
-                      f"including the pool replica's set-up; {spent:.1f} s"}
+            "sample": f"{rows} query rows (every 64th of each chunk), each over its full causal context; "
+                      f"{spent:.1f} s of attention calls"}
 
 
 def run_chunk_loop(args, world, rank, local):

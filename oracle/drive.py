@@ -36,9 +36,10 @@ def build(w, with_new_token: bool = True):
     return pool, alloc, tables
 
 
-def attention(w, pool, tables, threads: int | None = None, seqs=None) -> np.ndarray:
-    """fp64 decode attention of the step, [B, Hq, D]; `seqs` limits it to some sequences."""
-    q = w.query()
+def attention(w, pool, tables, threads: int | None = None, seqs=None, q=None) -> np.ndarray:
+    """fp64 decode attention of the step, [B, Hq, D]; `seqs` limits it to some sequences; `q` is
+    the step's query (`w.query()`) when the caller has already drawn it."""
+    q = w.query() if q is None else q
     lens = w.attend_lens
     if seqs is not None:
         seqs = np.asarray(seqs)
