@@ -151,16 +151,18 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
     // load while batch 0 is issued.
     GroupDesc cur, nxt, nxt2;
     describe(R0 + lane, cur);
-    fetch_scales(cur);
     describe(R0 + 32 + lane, nxt);
     int s = 0;
     uint32_t round = 0;
     int64_t issued = 0;
     bool ok = true;
     const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * kEsz;  // K rows + V rows of one page part
-    // When launched behind this step's append (programmatic dependent launch), the pool is read
-    // only after that kernel has finished; otherwise this returns at once.
+    // When launched behind this step's append (programmatic dependent launch), the pool and its
+    // block scales (which the append sets on a block's first write) are read only after that
+    // kernel has finished; otherwise this returns at once.  Block tables and lengths are inputs
+    // the append does not write, so their look-ups above overlap it.
     ptx::grid_dependency_wait();
+    fetch_scales(cur);
     for (int64_t e0 = R0; e0 < R1 && ok; e0 += 32) {
         describe(e0 + 64 + lane, nxt2);
         fetch_scales(nxt);

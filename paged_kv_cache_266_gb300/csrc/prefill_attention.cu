@@ -355,23 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32 * c));
             ptx::tmem_wait_ld();
             const int kbase = j * kKeys;
-            // row maximum with 8 independent accumulators (no serial chain of 128 dependent ops)
-            float mx8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             if (kbase + kKeys - 1 > qlim) {  // the tile crosses this row's position: mask
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    const float x = kbase + c <= qlim ? __uint_as_float(sraw[c]) : -INFINITY;
-                    sraw[c] = __float_as_uint(x);
-                    mx8[c & 7] = fmaxf(mx8[c & 7], x);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sraw[c]));
+                for (int c = 0; c < kKeys; ++c)
+                    if (kbase + c > qlim) sraw[c] = __float_as_uint(-INFINITY);
             }
-            const float smax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // row maximum: three-input max into 4 independent accumulators (64 instructions,
+            // no serial chain of 128 dependent ones)
+            float mx4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kKeys; c += 2)
+                mx4[(c >> 1) & 3] = ptx::max3(mx4[(c >> 1) & 3], __uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1]));
+            const float smax = ptx::max3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
             const float mt = smax * c2;  // this tile's maximum, scaled (finite: key kbase <= qlim)
             // lazy rescale: keep the running maximum unless this tile exceeds it by 2^8
             const bool grow = mt > m + kRescaleLog2;
@@ -389,22 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (grow) m = mt;
-            const float nm = -m;
-            float l8[8];
+            // p = 2^(s * c2 - m) for a pair of columns per instruction; l accumulates in 4
+            // packed pairs (8 independent sums, columns 2e, 2e + 1 into pair e mod 4)
+            const uint64_t c2x2 = ptx::f32x2(c2, c2), nmx2 = ptx::f32x2(-m, -m);
+            uint64_t l4[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) l8[e] = 0.f;
+            for (int e = 0; e < 4; ++e) l4[e] = 0ull;  // +0.0f in both halves
             if (j == 0) {  // P as hi + lo bf16 pair: columns 0-63 and 64-127; l from p itself
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t hi[32], lo[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e]), c2, nm));
-                        const float p1 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e + 1]), c2, nm));
+                        const float2 x = ptx::f32x2_split(ptx::fma_f32x2(
+                            ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
+                            c2x2, nmx2));
+                        const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
                         hi[e] = ptx::pack_bf16x2(p0, p1);
                         lo[e] = ptx::pack_bf16x2(p0 - ptx::bf16lo_to_f32(hi[e]), p1 - ptx::bf16hi_to_f32(hi[e]));
-                        l8[(2 * e) & 7] += p0;
-                        l8[(2 * e + 1) & 7] += p1;
+                        l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
                     ptx::tmem_st32(tS + 64u + 32u * c, lo);
@@ -415,16 +415,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t hi[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e]), c2, nm));
-                        const float p1 = ptx::exp2_approx(fmaf(__uint_as_float(sraw[64 * c + 2 * e + 1]), c2, nm));
+                        const float2 x = ptx::f32x2_split(ptx::fma_f32x2(
+                            ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
+                            c2x2, nmx2));
+                        const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
                         hi[e] = ptx::pack_bf16x2(p0, p1);
-                        l8[(2 * e) & 7] += p0;
-                        l8[(2 * e + 1) & 7] += p1;
+                        l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
                 }
             }
-            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            {
+                const float2 a = ptx::f32x2_split(l4[0]), b = ptx::f32x2_split(l4[1]);
+                const float2 cc = ptx::f32x2_split(l4[2]), d = ptx::f32x2_split(l4[3]);
+                l += ((a.x + a.y) + (b.x + b.y)) + ((cc.x + cc.y) + (d.x + d.y));
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();

@@ -191,6 +191,36 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// Blackwell issues two fp32 lanes per instruction for fma/add (each lane rounds exactly like
+// the scalar fmaf / __fadd_rn), and a three-input max; both halve the instruction count of
+// element-wise softmax work.  A pair lives in one 64-bit register, `lo` in the low half.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f32x2_split(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return make_float2(lo, hi);
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Warpgroup register reallocation (all four warps of a warpgroup execute it).  The block's
 // total never exceeds what it was launched with: the caller's shares must add up to at most
 // threads x registers-per-thread at launch.

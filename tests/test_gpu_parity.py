@@ -158,6 +158,59 @@ def test_empty_and_single_token_contexts(pkv):
     step.close()
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_empty_batches_are_no_ops(pkv, kv):
+    """Calls over zero tokens or zero sequences (an in-flight step where nothing joins, nothing
+    decodes or nothing prefills) return OK and change neither the pool nor the outputs."""
+    import torch
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    dev = torch.device("cuda")
+    pool = pkv.KVPool(8, 16, 2, 128, pkv.KV_DTYPES[kv])
+    g = torch.Generator().manual_seed(7)
+    k = torch.randn(20, 2, 128, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(20, 2, 128, generator=g).to(torch.bfloat16).to(dev)
+    pkv.pkv_append(pool.handle, k, v, torch.arange(20, dtype=torch.int64, device=dev))
+
+    def snapshot():
+        torch.cuda.synchronize()
+        kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(pool.handle)
+        return (_wrap_device(kv_ptr, kv_bytes).cpu().numpy().copy(),
+                _wrap_device(sc_ptr, sc_bytes).cpu().numpy().copy() if sc_bytes else None)
+
+    before = snapshot()
+    e_kv = torch.empty(0, 2, 128, dtype=torch.bfloat16, device=dev)
+    e_slot = torch.empty(0, dtype=torch.int64, device=dev)
+    e_q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device=dev)
+    e_tab = torch.empty(0, 4, dtype=torch.int32, device=dev)
+    e_len = torch.empty(0, dtype=torch.int32, device=dev)
+    ws = torch.zeros(pkv.pkv_decode_workspace_bytes(pool.handle, 1, 8, 4), dtype=torch.uint8, device=dev)
+    pkv.pkv_append(pool.handle, e_kv, e_kv, e_slot)
+    pkv.pkv_append_rope(pool.handle, e_kv, e_kv, e_slot, e_slot, 10000.0, q=e_q)
+    pkv.pkv_decode_attention(pool.handle, e_q, e_tab, e_len, 0.125, e_q, ws)
+    pkv.pkv_decode_step(pool.handle, e_kv, e_kv, e_slot, e_q, e_tab, e_len, 0.125, e_q, ws)
+    pkv.pkv_decode_step_rope(pool.handle, e_kv, e_kv, e_slot, e_slot, 10000.0, e_q, e_tab, e_len, 0.125, e_q, ws)
+    pkv.pkv_decode_attention_static(pool.handle, e_q, e_tab, e_len, 0.125, e_q)
+    if kv == "bf16":  # prefill: zero sequences, and sequences whose chunks are all empty
+        cu = torch.zeros(1, dtype=torch.int32, device=dev)
+        pkv.pkv_prefill_step(pool.handle, e_kv, e_kv, e_slot, e_q, cu, 0, e_tab, e_len, 0.125, e_q)
+        tab = torch.tensor([[0, 1]], dtype=torch.int32, device=dev)
+        ctx = torch.tensor([20], dtype=torch.int32, device=dev)
+        pkv.pkv_prefill_attention(pool.handle, e_q, torch.zeros(2, dtype=torch.int32, device=dev), 0, tab, ctx,
+                                  0.125, e_q)
+    # a decode step over one sequence with no new token: attention only, the pool unchanged
+    q = torch.randn(1, 8, 128, generator=g).to(torch.bfloat16).to(dev)
+    out = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device=dev)
+    tab = torch.tensor([[0, 1, 0, 0]], dtype=torch.int32, device=dev)
+    ctx = torch.tensor([20], dtype=torch.int32, device=dev)
+    pkv.pkv_decode_step(pool.handle, e_kv, e_kv, e_slot, q, tab, ctx, 0.125, out, ws)
+    after = snapshot()
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_OK
+    assert np.array_equal(before[0], after[0])
+    assert (before[1] is None) or np.array_equal(before[1], after[1])
+    assert out.abs().sum().item() > 0
+    pool.close()
+
+
 def test_long_context_split_over_every_cta(pkv):
     """One sequence of 40000 tokens: its 625 groups are spread over all CTAs, so the final
     output comes from the last-arriving CTA's merge of hundreds of partial states."""
