@@ -35,6 +35,7 @@ import pkv_workloads as W  # noqa: E402
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak), decode tokens/s"
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, for context beside the measured peak
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -303,8 +304,20 @@ def run_pkv(args, world, rank, local):
         step.attention()
         ev_c[k].record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
     attn_ms = [ev_b[k].elapsed_time(ev_c[k]) for k in range(K_attn)]
+    # The append on its own (reported separately): the same step's K/V rewritten into their slots.
+    append_us = None
+    if w.append:
+        K_app = max(3, min(K, 500))
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ea.record(stream)
+        for _ in range(K_app):
+            step.append()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        append_us = round(ea.elapsed_time(eb) / K_app * 1e3, 2)
+    clocks = sampler.stop()
     ms_per_step = dist_max(total_ms / K, world)
     if pkv_check_device_error(step.pool.handle) != 0:
         raise RuntimeError("device error flag set in the timed region")
@@ -331,8 +344,11 @@ def run_pkv(args, world, rank, local):
     if rank == 0 and not args.no_cpu:
         threads = os.cpu_count() or 1
         rate, spent, sample = oracle_rate(w, args.cpu_budget, threads)
+        rate1, spent1, sample1 = oracle_rate(w, max(1.0, args.cpu_budget / 3), 1)
         cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{sample}; {spent:.1f} s"}
+               "sample": f"{sample}; {spent:.1f} s",
+               "single_thread": {"value": round(rate1, 4), "unit": "GB/s", "cores": 1,
+                                 "sample": f"{sample1}; {spent1:.1f} s"}}
 
     if rank != 0:
         return
@@ -347,12 +363,15 @@ def run_pkv(args, world, rank, local):
                    "step_bytes": nbytes["step"], "l2": "inputs larger than L2 (KV read per step "
                    f"{nbytes['kv'] / 2**20:.0f} MiB > {L2_BYTES // 2**20} MiB)", "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
+        "tokens_per_s_unit": "decode tokens per attention layer-step per second",
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "kernel_us": {"attention": round(attn_mean * 1e3, 2), "attention_median": round(statistics.median(attn_ms) * 1e3, 2),
-                      "step": round(ms_per_step * 1e3, 2), "attention_launches_timed": K_attn},
+                      "step": round(ms_per_step * 1e3, 2), "attention_launches_timed": K_attn,
+                      "append": append_us},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
-                     "peak_kind": peak_kind,
+                     "peak_kind": peak_kind, "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": "decode_kernel", "algorithmic_bytes_per_launch": nbytes["attention"]},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4)},
