@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_quant_kernel(uint8_t* __re
                                                                     const uint32_t* __restrict__ amax,
                                                                     const uint8_t* __restrict__ fresh) {
     ptx::grid_launch_dependents();  // a following decode step may begin its set-up
+    ptx::grid_dependency_wait();    // launched behind the amax kernel: its maxima are complete
     constexpr int TPR = D / 8;
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gt / TPR;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_reset_kernel(const int64_t
                                                                     int Hkv, int bs, int num_blocks,
                                                                     uint32_t* amax, uint8_t* fresh) {
     ptx::grid_launch_dependents();  // a following decode step may begin its set-up
+    ptx::grid_dependency_wait();    // launched behind the quantising kernel: it has read the scratch
     constexpr int TPR = D / 8;
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gt / TPR;
@@ -337,6 +339,24 @@ __global__ void __launch_bounds__(128) rope_append_kernel(uint16_t* __restrict__
     }
 }
 
+// Launch `kernel` on `st` as a programmatic dependent of the preceding kernel on the stream: it
+// may be scheduled while that one runs and must execute griddepcontrol.wait before reading what
+// that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAppendThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <int D>
 pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, const int64_t* slots, int64_t N,
                          cudaStream_t st) {
@@ -348,18 +368,25 @@ pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, cons
         append_bf16_kernel<D><<<grid, kAppendThreads, 0, st>>>(static_cast<uint16_t*>(p->kv), k, v, slots, N,
                                                                p->n_kv_heads, p->block_size, p->num_blocks, p->err);
     } else {
+        // three kernels in a chain of programmatic dependents: the amax kernel waits for the
+        // stream as usual; the quantising kernel and the reset are scheduled while their
+        // predecessor runs and wait for it before touching the scratch (a decode attention
+        // launched behind the reset waits for it in turn, which covers the quantised bytes)
         fp8_amax_kernel<D><<<grid, kAppendThreads, 0, st>>>(k, v, slots, N, p->n_kv_heads, p->block_size,
                                                             p->num_blocks, p->amax_scratch, p->fresh_scratch, p->err);
-        if (p->dtype == PKV_KV_INT8)
-            fp8_quant_kernel<D, true><<<grid, kAppendThreads, 0, st>>>(static_cast<uint8_t*>(p->kv), p->scales, k, v,
-                                                                       slots, N, p->n_kv_heads, p->block_size,
-                                                                       p->num_blocks, p->amax_scratch, p->fresh_scratch);
-        else
-            fp8_quant_kernel<D, false><<<grid, kAppendThreads, 0, st>>>(static_cast<uint8_t*>(p->kv), p->scales, k, v,
-                                                                        slots, N, p->n_kv_heads, p->block_size,
-                                                                        p->num_blocks, p->amax_scratch, p->fresh_scratch);
-        fp8_reset_kernel<D><<<grid, kAppendThreads, 0, st>>>(slots, N, p->n_kv_heads, p->block_size, p->num_blocks,
-                                                             p->amax_scratch, p->fresh_scratch);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        uint8_t* const kv8 = static_cast<uint8_t*>(p->kv);
+        const uint32_t* const amax = p->amax_scratch;
+        const uint8_t* const fresh = p->fresh_scratch;
+        cudaError_t e = p->dtype == PKV_KV_INT8
+                            ? launch_dependent(fp8_quant_kernel<D, true>, grid, st, kv8, p->scales, k, v, slots, N,
+                                               p->n_kv_heads, p->block_size, p->num_blocks, amax, fresh)
+                            : launch_dependent(fp8_quant_kernel<D, false>, grid, st, kv8, p->scales, k, v, slots, N,
+                                               p->n_kv_heads, p->block_size, p->num_blocks, amax, fresh);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        e = launch_dependent(fp8_reset_kernel<D>, grid, st, slots, N, p->n_kv_heads, p->block_size, p->num_blocks,
+                             p->amax_scratch, p->fresh_scratch);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
