@@ -310,6 +310,22 @@ pkv_status pkv_decode_attention_static(const pkv_pool* pool, const void* q_dev, 
                                        int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads,
                                        float scale, void* out_dev, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------ host-driven steps
+ * Kernel-driven copy for the per-step transfers of a decode step driven from the host (the
+ * step's q/K/V, block tables, slots and lengths staged in pinned host memory, the output read
+ * back): the SMs move 16-byte vectors instead of a copy engine, whose start-up dominates
+ * transfers of this size.  The launch overhead of a decode step is what "TensorRT-LLM 推理加速
+ * 实战" §7.1 removes with CUDA graphs; this copy can be captured into the same graph.
+ *   dst, src: device memory of the current device, or host memory pinned with CUDA
+ *             (cudaHostAlloc / cudaHostRegister), reached through its mapped address; both
+ *             16-byte aligned, the ranges [p, p + bytes) must not overlap.
+ *   bytes:    a multiple of 16; 0 is a no-op.
+ * The caller owns both buffers and guarantees `bytes` lies inside each (as for a memcpy).
+ * Asynchronous on `stream`; the host sees copied-to-host bytes after synchronising it.
+ * PKV_ERR_INVALID_ARG (nothing launched): null or misaligned pointers, bytes % 16, overlap,
+ * pageable host memory or another device's memory; PKV_ERR_CUDA: the launch failed. */
+pkv_status pkv_stage_copy(void* dst, const void* src, size_t bytes, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------ utilities
  * KV memory ("TensorRT-LLM 推理加速实战" §8.1; aiqz.cc page, KV缓存管理):
  *   M_kv = 2 * n_layers * n_kv_heads * head_dim * n_tokens * batch * bytes_per_elem. */

@@ -22,7 +22,7 @@ __all__ = [
     "pkv_pool_copy_block", "pkv_append_rope", "pkv_decode_step_rope", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
-    "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_kv_bytes",
+    "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_stage_copy", "pkv_kv_bytes",
     "pkv_status_str", "KVPool",
 ]
 
@@ -85,6 +85,7 @@ def _L():
         "pkv_decode_step": (i32, [vp, vp, vp, vp, i64, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp, sz, vp]),
         "pkv_decode_workspace_init": (i32, [vp, sz, vp]),
         "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
+        "pkv_stage_copy": (i32, [vp, vp, sz, vp]),
         "pkv_kv_bytes": (ctypes.c_uint64, [i64, i64, i64, i64, i64, ctypes.c_double]),
         "pkv_status_str": (ctypes.c_char_p, [i32]),
     }
@@ -350,6 +351,24 @@ def pkv_decode_attention_static(pool: int, q, block_tables, context_lens, scale:
             raise PKVError(rc, f"pkv_decode_attention_static: needs {need} bytes of scratch, the fixed limit is "
                                f"{PKV_STATIC_WORKSPACE_BYTES}")
     _check(rc, "pkv_decode_attention_static")
+
+
+def pkv_stage_copy(dst, src, nbytes: int | None = None, stream=None) -> None:
+    """Kernel-driven copy between torch tensors: each one a CUDA tensor or a pinned CPU tensor,
+    contiguous; nbytes defaults to the smaller of the two sizes (a multiple of 16)."""
+    def ptr(t, what):
+        import torch
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise TypeError(f"{what}: expected a contiguous torch tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{what}: a CPU tensor must be pinned")
+        return t.data_ptr(), t.numel() * t.element_size()
+    d, dn = ptr(dst, "dst")
+    s, sn = ptr(src, "src")
+    n = min(dn, sn) if nbytes is None else int(nbytes)
+    if n < 0 or n > dn or n > sn:
+        raise ValueError(f"pkv_stage_copy: {n} bytes do not fit the buffers ({dn}, {sn})")
+    _check(_L().pkv_stage_copy(d, s, n, _stream(stream)), "pkv_stage_copy")
 
 
 def pkv_kv_bytes(n_layers: int, n_kv_heads: int, head_dim: int, n_tokens: int, batch: int,

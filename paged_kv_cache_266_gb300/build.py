@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
-SOURCES = ["allocator.cpp", "pool.cu", "append.cu", "decode_attention.cu", "prefill_attention.cu"]
+SOURCES = ["allocator.cpp", "pool.cu", "append.cu", "decode_attention.cu", "prefill_attention.cu", "stage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

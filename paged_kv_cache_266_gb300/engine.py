@@ -31,7 +31,7 @@ import numpy as np
 
 from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
                pkv_pool_copy_block, pkv_prefill_step, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many,
-               pkv_seq_share_prefix, pkv_slot_mapping)
+               pkv_seq_share_prefix, pkv_slot_mapping, pkv_stage_copy)
 
 DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
 
@@ -68,11 +68,12 @@ class _Bucket:
         self.graph = None
 
     def run(self, torch, loop):
-        """Copy the staged inputs in, run the fused step, copy the output out (no sync)."""
-        self.dbuf.copy_(self.hbuf, non_blocking=True)
+        """Copy the staged inputs in, run the fused step, copy the output out (no sync); both
+        copies are pkv_stage_copy (SM-driven: faster than a copy engine at these sizes)."""
+        pkv_stage_copy(self.dbuf, self.hbuf)
         pkv_decode_step(loop.pool.handle, self.k, self.v, self.Dv["slots"], self.q, self.Dv["tables"],
                         self.Dv["lens"], loop.scale, self.out, self.workspace)
-        self.out_host.copy_(self.out.view(torch.int16), non_blocking=True)
+        pkv_stage_copy(self.out_host, self.out)
 
 
 class DecodeLoop:

@@ -15,10 +15,11 @@ import math
 
 import numpy as np
 
+from . import _L, _check
 from . import (KV_DTYPES, KVPool, pkv_allocator_set_free_order, pkv_append,
                pkv_decode_attention, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
                pkv_num_free_blocks, pkv_pool_copy_block, pkv_prefill_attention, pkv_prefill_step, pkv_seq_release,
-               pkv_seq_reserve, pkv_seq_share_prefix, pkv_slot_mapping)
+               pkv_seq_reserve, pkv_seq_share_prefix, pkv_slot_mapping, pkv_stage_copy)
 
 def replay(allocator: int, ops) -> None:
     for op in ops:
@@ -98,7 +99,8 @@ class DecodeStep:
     def _prepare_host(self):
         """One pinned staging buffer holding every input of a step (q, new K/V, block tables,
         context lengths, slots) and a device buffer of the same layout whose slices are the
-        kernel arguments, so a step needs one host-to-device copy and one copy back."""
+        kernel arguments, so a step needs one host-to-device copy and one copy back (both
+        pkv_stage_copy: the SMs move these few hundred KB faster than a copy engine starts)."""
         torch, w = self.torch, self.w
         n = self.batch
         parts = [("q", (n, w.Hq, w.D), np.int16), ("k", (n, w.Hkv, w.D), np.int16),
@@ -121,7 +123,12 @@ class DecodeStep:
         H["k"][...] = w.new_k()[:n].view(np.int16)
         H["v"][...] = w.new_v()[:n].view(np.int16)
         H["lens"][...] = self.lens_host
-        self._host = {"hbuf": hbuf, "dbuf": dbuf, "H": H,
+        # the allocator writes tables and slots straight into the staging buffer; the sequence
+        # ids and positions are fixed for the batch, so every host address is taken once here
+        ids = np.ascontiguousarray(w.seq_ids[:n], dtype=np.int64)
+        pos = np.ascontiguousarray(w.lens[:n], dtype=np.int64)
+        ptrs = (ids.ctypes.data, pos.ctypes.data, H["tables"].ctypes.data, H["slots"].ctypes.data)
+        self._host = {"hbuf": hbuf, "dbuf": dbuf, "H": H, "ids": ids, "pos": pos, "ptrs": ptrs,
                       "q": Dv["q"].view(torch.bfloat16), "k": Dv["k"].view(torch.bfloat16),
                       "v": Dv["v"].view(torch.bfloat16), "tables": Dv["tables"], "lens": Dv["lens"],
                       "slots": Dv["slots"], "out": torch.empty(n, w.Hq, w.D, dtype=torch.int16).pin_memory()}
@@ -129,14 +136,14 @@ class DecodeStep:
     def _issue_host_step(self, stream):
         """Copy-in, the step, copy-out, on `stream` (no synchronisation)."""
         torch, w, X = self.torch, self.w, self._host
-        X["dbuf"].copy_(X["hbuf"], non_blocking=True)
+        pkv_stage_copy(X["dbuf"], X["hbuf"], stream=stream)
         if w.append:
             pkv_decode_step(self.pool.handle, X["k"], X["v"], X["slots"], X["q"], X["tables"], X["lens"], self.scale,
                             self.out, self.workspace, stream)
         else:
             pkv_decode_attention(self.pool.handle, X["q"], X["tables"], X["lens"], self.scale, self.out,
                                  self.workspace, stream)
-        X["out"].copy_(self.out.view(torch.int16), non_blocking=True)
+        pkv_stage_copy(X["out"], self.out, stream=stream)
 
     def step_host(self, stream=None, graph: bool = True):
         """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The allocator writes the block
@@ -148,11 +155,12 @@ class DecodeStep:
         if self._host is None:
             self._prepare_host()
         X = self._host
-        H = X["H"]
         n = self.batch
-        pkv_get_block_tables(a, w.seq_ids[:n], self.max_blocks, out=H["tables"])
+        lib = _L()
+        ids, pos, tables, slots = X["ptrs"]
+        _check(lib.pkv_get_block_tables(a, ids, n, self.max_blocks, tables), "pkv_get_block_tables")
         if w.append:
-            pkv_slot_mapping(a, w.seq_ids[:n], w.lens[:n], out=H["slots"])
+            _check(lib.pkv_slot_mapping(a, ids, pos, n, slots), "pkv_slot_mapping")
         if not graph:
             self._issue_host_step(stream)
         else:

@@ -71,6 +71,12 @@ def test_invalid_arguments_are_rejected_without_device_work(pkv):
         pkv.PKV_ERR_INVALID_ARG
     assert L.pkv_allocator_create(0, 16, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG
     assert L.pkv_allocator_create(4, 48, ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG
+    # staging copy: checked before any CUDA call (these addresses are never dereferenced)
+    assert L.pkv_stage_copy(None, None, 0, None) == pkv.PKV_OK  # nothing to copy
+    assert L.pkv_stage_copy(None, 4096, 64, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_stage_copy(4096, 8192 + 8, 64, None) == pkv.PKV_ERR_INVALID_ARG  # misaligned
+    assert L.pkv_stage_copy(4096, 8192, 40, None) == pkv.PKV_ERR_INVALID_ARG  # not a multiple of 16
+    assert L.pkv_stage_copy(4096, 4096 + 32, 64, None) == pkv.PKV_ERR_INVALID_ARG  # overlapping ranges
 
 
 def _both(pkv, nb, bs, order=None):

@@ -158,6 +158,35 @@ def test_empty_and_single_token_contexts(pkv):
     step.close()
 
 
+def test_stage_copy_moves_exact_bytes_and_refuses_pageable_memory(pkv):
+    """Host-to-device, device-to-host and device-to-device copies of ragged sizes (multiples of
+    16 bytes, from one vector to several grid-strides) return the bytes unchanged and touch
+    nothing past the copied range; pageable host memory is refused without a launch."""
+    import ctypes
+    import torch
+    rng = np.random.default_rng(11)
+    for n in (16, 48, 4096, 4096 * 16 + 32, 3 * 2 ** 20 + 16 * 7):
+        src = torch.from_numpy(rng.integers(0, 256, n + 64, dtype=np.uint8)).pin_memory()
+        dev = torch.full((n + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+        back = torch.zeros(n + 64, dtype=torch.uint8).pin_memory()
+        dev2 = torch.full((n + 64,), 0x5A, dtype=torch.uint8, device="cuda")
+        pkv.pkv_stage_copy(dev, src, n)
+        pkv.pkv_stage_copy(dev2, dev, n)
+        pkv.pkv_stage_copy(back, dev2, n)
+        torch.cuda.synchronize()
+        assert torch.equal(back[:n], src[:n])
+        assert not back[n:].any()
+        assert (dev[n:].cpu() == 0xA5).all() and (dev2[n:].cpu() == 0x5A).all()
+    pageable = np.zeros(1024, np.uint8)
+    dev = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    L = pkv._L()
+    stream = torch.cuda.current_stream().cuda_stream
+    assert L.pkv_stage_copy(dev.data_ptr(), pageable.ctypes.data, 1024, stream) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_stage_copy(pageable.ctypes.data, dev.data_ptr(), 1024, stream) == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        pkv.pkv_stage_copy(dev, torch.zeros(1024, dtype=torch.uint8))  # not pinned
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
 def test_empty_batches_are_no_ops(pkv, kv):
     """Calls over zero tokens or zero sequences (an in-flight step where nothing joins, nothing
