@@ -74,6 +74,8 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (P stays <= 2^8)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kEndBar = 1;      // named barrier: every role done before TMEM is released
 constexpr int kMaxRankedSeqs = 512;  // above this the sequences are dispatched in index order
+constexpr int kSmallRankedSeqs = 64;  // up to this the ranking reads the inputs directly
+static_assert(kMaxRankedSeqs * sizeof(int64_t) <= kTiles * kQBytes, "dispatch ranking fits the Q tiles' space");
 
 // mbarrier slots
 constexpr int kBarQ = 0;                          // Q rows of both tiles written (8 warps arrive)
@@ -132,9 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = rem % p.Hkv;
     const int pair = p.tiles - 1 - rem / p.Hkv;
     int b = rank;
-    if (p.B <= kMaxRankedSeqs) {
-        __shared__ int seq_of_rank;
-        if (threadIdx.x == 0) seq_of_rank = -1;
+    if (p.B <= kSmallRankedSeqs) {
+        // few sequences: rank straight from the (cached) global inputs
+        __shared__ int seq_of_rank_small;
+        if (threadIdx.x == 0) seq_of_rank_small = -1;
         __syncthreads();
         auto work = [&](int i) -> int64_t {
             const int64_t nn = p.cu_q[i + 1] - p.cu_q[i], ll = p.ctx[i];
@@ -145,6 +148,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             int r = 0;
             for (int k = 0; k < p.B; ++k) {
                 const int64_t wk = work(k);
+                r += (wk > wi || (wk == wi && k < i)) ? 1 : 0;
+            }
+            if (r == rank) seq_of_rank_small = i;
+        }
+        __syncthreads();
+        b = seq_of_rank_small;
+    } else if (p.B <= kMaxRankedSeqs) {
+        // each sequence's work, loaded once into the Q tiles' space (free until the softmax
+        // warps stage Q, after the block barrier below); then every thread ranks its sequences
+        // against all of them from shared memory (B^2 comparisons per CTA)
+        __shared__ int seq_of_rank;
+        int64_t* work_s = reinterpret_cast<int64_t*>(sm + kOffQ);
+        for (int i = threadIdx.x; i < p.B; i += kThreads) {
+            const int64_t nn = p.cu_q[i + 1] - p.cu_q[i], ll = p.ctx[i];
+            work_s[i] = nn * (2 * ll - nn);
+        }
+        if (threadIdx.x == 0) seq_of_rank = -1;
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.B; i += kThreads) {
+            const int64_t wi = work_s[i];
+            int r = 0;
+            for (int k = 0; k < p.B; ++k) {
+                const int64_t wk = work_s[k];
                 r += (wk > wi || (wk == wi && k < i)) ? 1 : 0;
             }
             if (r == rank) seq_of_rank = i;

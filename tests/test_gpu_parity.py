@@ -240,6 +240,27 @@ def test_empty_batches_are_no_ops(pkv, kv):
     pool.close()
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_maximum_batch_and_group(pkv, kv):
+    """The largest batch one call takes (4096 sequences) with the largest query-head group (8
+    per KV head): ragged short contexts, every output against the oracle.  One sequence more, or
+    a larger group, is refused before any launch."""
+    import torch
+    rng = np.random.default_rng(4096)
+    lens = rng.integers(0, 40, 4096)
+    lens[::97] = 0
+    w = W.custom_workload(310, 4096, 16, 2, 128, 16, lens, append=True, kv_dtype=kv)
+    step = _run(pkv, w)
+    _check_against_oracle(pkv, w, step)
+    L = pkv._L()
+    s = torch.cuda.current_stream().cuda_stream
+    args = (step.q.data_ptr(), step.tables.data_ptr(), step.max_blocks, step.lens.data_ptr())
+    tail = (1.0 / math.sqrt(w.D), step.out.data_ptr(), step.workspace.data_ptr(), step.ws_bytes, s)
+    assert L.pkv_decode_attention(step.pool.handle, *args, 4097, 16, *tail) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(step.pool.handle, *args, 4096, 32, *tail) == pkv.PKV_ERR_INVALID_ARG
+    step.close()
+
+
 def test_long_context_split_over_every_cta(pkv):
     """One sequence of 40000 tokens: its 625 groups are spread over all CTAs, so the final
     output comes from the last-arriving CTA's merge of hundreds of partial states."""

@@ -186,6 +186,28 @@ def test_prefill_matches_oracle(bs, G):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("B", [512, 600])
+def test_prefill_many_sequences_matches_oracle(B):
+    """Many small chunks in one call: 512 sequences (the largest batch the kernel dispatches in
+    order of causal work) and 600 (beyond it: index order); chunks of 1-3 tokens over pasts of
+    0-79 tokens, every output against the oracle."""
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import PrefillStep
+    rng = np.random.default_rng(B)
+    sc = W.make_prefill_script(90 + B, Hq=8, Hkv=2, D=128, block_size=16,
+                               past=rng.integers(0, 80, B).tolist(), chunk=rng.integers(1, 4, B).tolist())
+    st = PrefillStep(sc)
+    st.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+    _, tables, ref = _oracle_replay(sc)
+    assert np.array_equal(st.tables_host, tables)
+    _check_close(st.out_host(), ref)
+    st.close()
+
+
+@pytest.mark.gpu
 def test_prefill_fused_step_equals_separate_calls():
     torch, pkv = _gpu()
     import pkv_workloads as W
