@@ -126,6 +126,30 @@ pkv_status pkv_get_block_tables(const pkv_allocator* a, const int64_t* seq_ids_h
 pkv_status pkv_slot_mapping(const pkv_allocator* a, const int64_t* seq_ids_host, const int64_t* positions_host,
                             int64_t N, int64_t* out_host);
 
+/* Host inputs of one step in one call (the bookkeeping of an in-flight batching step, page
+ * "TensorRT-LLM 深度实战" §3.2, §7.3), equal to the composition of the calls above.
+ *
+ * pkv_stage_prefill: a chunked prefill call of n sequences, sequence i prefilling positions
+ * p0[i] .. p1[i]-1.  In order, every sequence is grown to hold p1[i] tokens (pkv_seq_reserve;
+ * stops at the first failure, earlier reservations stay), then written: tables_out
+ * [n][max_blocks] (pkv_get_block_tables), slots_out [sum(p1 - p0)] the chunk rows' slots packed
+ * sequence after sequence, cu_out [n + 1] the packed offsets (cu_out[0] = 0) and ctx_out [n] =
+ * p1.  Caller-owned host buffers of at least those sizes.  PKV_ERR_INVALID_ARG (nothing changed)
+ * when p0 < 0, p1 < p0, a count or position exceeds int32 or max_blocks < 1; otherwise the
+ * status of the failing reservation or table write. */
+pkv_status pkv_stage_prefill(pkv_allocator* a, const int64_t* seq_ids_host, const int64_t* p0_host,
+                             const int64_t* p1_host, int n, int max_blocks, int64_t* slots_out_host,
+                             int32_t* cu_out_host, int32_t* ctx_out_host, int32_t* tables_out_host);
+
+/* pkv_stage_decode: one decode step of n sequences, sequence i appending its token at position
+ * pos[i].  In order, every sequence is grown to hold pos[i] + 1 tokens (as above), then written:
+ * tables_out [n_pad][max_blocks], slots_out [n_pad] (the slot of position pos[i]) and lens_out
+ * [n_pad] = pos[i] + 1; rows n .. n_pad-1 are padding (table row -1, slot -1, length 0), as a
+ * batch-size bucket of a captured step needs.  PKV_ERR_INVALID_ARG (nothing changed) when
+ * n_pad < n, pos < 0 or pos + 1 exceeds int32. */
+pkv_status pkv_stage_decode(pkv_allocator* a, const int64_t* seq_ids_host, const int64_t* pos_host, int n, int n_pad,
+                            int max_blocks, int32_t* tables_out_host, int64_t* slots_out_host, int32_t* lens_out_host);
+
 /* ------------------------------------------------------------------ pool (device)
  * Device layout ("block pool"): block b, K (kv=0) or V (kv=1), KV head h form one
  * contiguous tile of block_size*head_dim elements starting at element

@@ -20,7 +20,7 @@ __all__ = [
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
     "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_share_prefix", "pkv_block_refcount",
     "pkv_pool_copy_block", "pkv_append_rope", "pkv_decode_step_rope", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
-    "pkv_slot_mapping", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
+    "pkv_slot_mapping", "pkv_stage_prefill", "pkv_stage_decode", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_stage_copy", "pkv_kv_bytes",
     "pkv_status_str", "KVPool",
@@ -74,6 +74,8 @@ def _L():
         "pkv_free_list": (i32, [vp, vp, i32, P(i32)]),
         "pkv_get_block_tables": (i32, [vp, vp, i32, i32, vp]),
         "pkv_slot_mapping": (i32, [vp, vp, vp, i64, vp]),
+        "pkv_stage_prefill": (i32, [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]),
+        "pkv_stage_decode": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
         "pkv_pool_create": (i32, [i32, i32, i32, i32, i32, P(vp)]),
         "pkv_pool_destroy": (i32, [vp]),
         "pkv_pool_allocator": (i32, [vp, P(vp)]),
@@ -214,6 +216,50 @@ def pkv_slot_mapping(a: int, seq_ids, positions, out: np.ndarray | None = None) 
     out = _out_array(out, (len(s),), np.int64)
     _check(_L().pkv_slot_mapping(a, s.ctypes.data, p.ctypes.data, len(s), out.ctypes.data), "pkv_slot_mapping")
     return out
+
+
+def _out_flat(out, n: int, dtype, what: str) -> np.ndarray:
+    """A contiguous array of `dtype` with room for n elements (new if out is None)."""
+    if out is None:
+        return np.empty(n, dtype=dtype)
+    if out.dtype != dtype or not out.flags["C_CONTIGUOUS"] or out.size < n:
+        raise ValueError(f"{what} must be a contiguous {np.dtype(dtype).name} array of at least {n} elements")
+    return out
+
+
+def pkv_stage_prefill(a: int, seq_ids, p0, p1, max_blocks: int, slots_out=None, cu_out=None, ctx_out=None,
+                      tables_out=None):
+    """Reserve and write one chunked prefill call's host inputs (see pkv.h); returns (slots
+    [sum(p1 - p0)], cu [n + 1], ctx [n], tables [n][max_blocks]) as views of the outputs."""
+    s, b, e = _np(seq_ids, np.int64), _np(p0, np.int64), _np(p1, np.int64)
+    if not (s.shape == b.shape == e.shape) or s.ndim != 1:
+        raise ValueError("seq_ids, p0 and p1 must be 1-D of the same length")
+    n = len(s)
+    total = int((e - b).sum()) if n else 0
+    slots = _out_flat(slots_out, max(total, 0), np.int64, "slots_out")
+    cu = _out_flat(cu_out, n + 1, np.int32, "cu_out")
+    ctx = _out_flat(ctx_out, n, np.int32, "ctx_out")
+    tables = _out_flat(tables_out, n * max_blocks, np.int32, "tables_out")
+    _check(_L().pkv_stage_prefill(a, s.ctypes.data, b.ctypes.data, e.ctypes.data, n, max_blocks, slots.ctypes.data,
+                                  cu.ctypes.data, ctx.ctypes.data, tables.ctypes.data), "pkv_stage_prefill")
+    return (slots.reshape(-1)[:total], cu.reshape(-1)[:n + 1], ctx.reshape(-1)[:n],
+            tables.reshape(-1)[:n * max_blocks].reshape(n, max_blocks))
+
+
+def pkv_stage_decode(a: int, seq_ids, pos, n_pad: int, max_blocks: int, tables_out=None, slots_out=None,
+                     lens_out=None):
+    """Reserve and write one decode step's host inputs, padded to n_pad rows (see pkv.h);
+    returns (tables [n_pad][max_blocks], slots [n_pad], lens [n_pad])."""
+    s, p = _np(seq_ids, np.int64), _np(pos, np.int64)
+    if s.shape != p.shape or s.ndim != 1:
+        raise ValueError("seq_ids and pos must be 1-D of the same length")
+    tables = _out_flat(tables_out, n_pad * max_blocks, np.int32, "tables_out")
+    slots = _out_flat(slots_out, n_pad, np.int64, "slots_out")
+    lens = _out_flat(lens_out, n_pad, np.int32, "lens_out")
+    _check(_L().pkv_stage_decode(a, s.ctypes.data, p.ctypes.data, len(s), n_pad, max_blocks, tables.ctypes.data,
+                                 slots.ctypes.data, lens.ctypes.data), "pkv_stage_decode")
+    return (tables.reshape(-1)[:n_pad * max_blocks].reshape(n_pad, max_blocks), slots.reshape(-1)[:n_pad],
+            lens.reshape(-1)[:n_pad])
 
 
 # ----------------------------------------------------------------------------- pool

@@ -219,6 +219,63 @@ pkv_status pkv_slot_mapping(const pkv_allocator* a, const int64_t* seq_ids, cons
     return PKV_OK;
 }
 
+pkv_status pkv_stage_prefill(pkv_allocator* a, const int64_t* seq_ids, const int64_t* p0, const int64_t* p1, int n,
+                             int max_blocks, int64_t* slots_out, int32_t* cu_out, int32_t* ctx_out,
+                             int32_t* tables_out) {
+    if (!a || n < 0 || max_blocks < 1 || !cu_out) return PKV_ERR_INVALID_ARG;
+    if (n > 0 && (!seq_ids || !p0 || !p1 || !slots_out || !ctx_out || !tables_out)) return PKV_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {  // validate before changing anything
+        if (p0[i] < 0 || p1[i] < p0[i] || p1[i] > INT32_MAX) return PKV_ERR_INVALID_ARG;
+        total += p1[i] - p0[i];
+        if (total > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < n; ++i) {
+        const pkv_status st = pkv_seq_reserve(a, seq_ids[i], p1[i]);
+        if (st != PKV_OK) return st;
+    }
+    const pkv_status st = pkv_get_block_tables(a, seq_ids, n, max_blocks, tables_out);
+    if (st != PKV_OK) return st;
+    const int64_t bs = a->block_size;
+    int64_t r = 0;
+    cu_out[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        const std::vector<int32_t>& tbl = a->tables.find(seq_ids[i])->second;  // reserved above
+        for (int64_t pos = p0[i]; pos < p1[i]; ++pos) slots_out[r++] = (int64_t)tbl[(size_t)(pos / bs)] * bs + pos % bs;
+        cu_out[i + 1] = (int32_t)r;
+        ctx_out[i] = (int32_t)p1[i];
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_stage_decode(pkv_allocator* a, const int64_t* seq_ids, const int64_t* pos, int n, int n_pad,
+                            int max_blocks, int32_t* tables_out, int64_t* slots_out, int32_t* lens_out) {
+    if (!a || n < 0 || n_pad < n || max_blocks < 1) return PKV_ERR_INVALID_ARG;
+    if (n_pad > 0 && (!tables_out || !slots_out || !lens_out)) return PKV_ERR_INVALID_ARG;
+    if (n > 0 && (!seq_ids || !pos)) return PKV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)  // validate before changing anything
+        if (pos[i] < 0 || pos[i] >= INT32_MAX) return PKV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const pkv_status st = pkv_seq_reserve(a, seq_ids[i], pos[i] + 1);
+        if (st != PKV_OK) return st;
+    }
+    const pkv_status st = pkv_get_block_tables(a, seq_ids, n, max_blocks, tables_out);
+    if (st != PKV_OK) return st;
+    const int64_t bs = a->block_size;
+    for (int i = 0; i < n; ++i) {
+        const std::vector<int32_t>& tbl = a->tables.find(seq_ids[i])->second;  // reserved above
+        slots_out[i] = (int64_t)tbl[(size_t)(pos[i] / bs)] * bs + pos[i] % bs;
+        lens_out[i] = (int32_t)(pos[i] + 1);
+    }
+    for (int i = n; i < n_pad; ++i) {
+        slots_out[i] = -1;
+        lens_out[i] = 0;
+        int32_t* row = tables_out + (int64_t)i * max_blocks;
+        for (int k = 0; k < max_blocks; ++k) row[k] = -1;
+    }
+    return PKV_OK;
+}
+
 uint64_t pkv_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, int64_t n_tokens, int64_t batch,
                       double bytes_per_elem) {
     // Integer product first (exact), then the element size; 2 * ... keeps half-byte sizes whole.

@@ -137,13 +137,15 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
     };
     // fp8: the pages' scale pairs, once their block ids have arrived (out-of-range ids read 0)
     auto fetch_scales = [&](GroupDesc& d) {
-        if (!FP8 || d.b < 0) return;
+        if constexpr (FP8) {
+            if (d.b < 0) return;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int blk = (d.id[i] >= 0 && d.id[i] < p.num_blocks) ? d.id[i] : 0;
-            const float2 v = __ldg(reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + d.h) * 4));
-            d.sk[i] = v.x;
-            d.sv[i] = v.y;
+            for (int i = 0; i < 4; ++i) {
+                const int blk = (d.id[i] >= 0 && d.id[i] < p.num_blocks) ? d.id[i] : 0;
+                const float2 v = __ldg(reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + d.h) * 4));
+                d.sk[i] = v.x;
+                d.sv[i] = v.y;
+            }
         }
     };
 

@@ -12,12 +12,13 @@ Each step here:
      (pkv_seq_reserve + pkv_append, as a prefill would leave them).  With chunked context
      ("TensorRT-LLM 深度实战" §7.3) a joiner's prompt is prefilled `chunk` tokens per step: one
      pkv_prefill_step appends every prefilling sequence's next chunk and attends its queries
-     causally, and the sequence decodes from the step after its last chunk.  With a system
+     causally (its slots, chunk offsets and tables written by one pkv_stage_prefill), and the
+     sequence decodes from the step after its last chunk.  With a system
      prompt (prefix caching, "TensorRT-LLM 推理加速实战" §8 KV cache reuse) the shared prefix
      is cached once and every joiner forks it (pkv_seq_share_prefix) instead of prefilling it;
-  3. gives every decoding sequence room for one more token (pkv_seq_reserve_many grows by whole
-     blocks), writes block tables, new-token slots and context lengths straight into a pinned
-     staging buffer together with the step's q / new K / new V;
+  3. gives every decoding sequence room for one more token and writes block tables, new-token
+     slots and context lengths (padding rows included) straight into a pinned staging buffer,
+     in one pkv_stage_decode call, next to the step's q / new K / new V;
   4. runs, on the decode batch padded to its bucket, one host-to-device copy, pkv_decode_step
      (append + attention) and the copy of the output back — captured once per bucket as a CUDA
      graph and replayed.  Padding rows have context length 0 and slot -1, so they write nothing
@@ -29,8 +30,9 @@ import math
 
 import numpy as np
 
-from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes, pkv_get_block_tables,
-               pkv_pool_copy_block, pkv_prefill_step, pkv_seq_release, pkv_seq_reserve, pkv_seq_reserve_many,
+from . import _L, _check
+from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_workspace_bytes,
+               pkv_pool_copy_block, pkv_prefill_step, pkv_seq_release, pkv_seq_reserve,
                pkv_seq_share_prefix, pkv_slot_mapping, pkv_stage_copy)
 
 DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
@@ -66,6 +68,7 @@ class _Bucket:
         ws = pkv_decode_workspace_bytes(loop.pool.handle, Bp, sc.Hq, loop.max_blocks)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
         self.graph = None
+        self.out_ptrs = tuple(self.H[k].ctypes.data for k in ("tables", "slots", "lens"))
 
     def run(self, torch, loop):
         """Copy the staged inputs in, run the fused step, copy the output out (no sync); both
@@ -74,6 +77,33 @@ class _Bucket:
         pkv_decode_step(loop.pool.handle, self.k, self.v, self.Dv["slots"], self.q, self.Dv["tables"],
                         self.Dv["lens"], loop.scale, self.out, self.workspace)
         pkv_stage_copy(self.out_host, self.out)
+
+
+class _PrefillStaging:
+    """Pinned and device buffers for the small inputs of one chunked prefill call (slots, chunk
+    offsets, context lengths, block tables), sized for `tokens` chunk tokens and `seqs`
+    sequences: the allocator writes into the pinned copy and one pkv_stage_copy moves it."""
+
+    def __init__(self, torch, tokens: int, seqs: int, max_blocks: int, device):
+        self.tokens, self.seqs = tokens, seqs
+        parts = [("slots", (tokens,), np.int64), ("cu", (seqs + 1,), np.int32), ("ctx", (seqs,), np.int32),
+                 ("tables", (seqs, max_blocks), np.int32)]
+        offs, total = {}, 0
+        for name, shape, dt in parts:
+            offs[name] = total
+            total += (int(np.prod(shape)) * np.dtype(dt).itemsize + 255) // 256 * 256
+        self.hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dbuf = torch.empty(total, dtype=torch.uint8, device=device)
+        tdt = {np.int32: torch.int32, np.int64: torch.int64}
+        hnp = self.hbuf.numpy()
+        self.H, self.D = {}, {}
+        for name, shape, dt in parts:
+            nbytes = int(np.prod(shape)) * np.dtype(dt).itemsize
+            self.H[name] = hnp[offs[name]:offs[name] + nbytes].view(dt).reshape(shape)
+            self.D[name] = self.dbuf[offs[name]:offs[name] + nbytes].view(tdt[dt]).view(shape)
+        # host addresses the allocator writes to, and the copy's (fixed for the buffer's life)
+        self.out_ptrs = tuple(self.H[k].ctypes.data for k in ("slots", "cu", "ctx", "tables"))
+        self.copy = (self.dbuf.data_ptr(), self.hbuf.data_ptr(), total)
 
 
 class DecodeLoop:
@@ -113,6 +143,7 @@ class DecodeLoop:
             to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
             pkv_append(self.pool.handle, to_dev(k), to_dev(v), torch.from_numpy(slots).to(device))
         self.last_prefill = ([], None)  # chunked context: (chunks [(seq, p0, p1)], output bits)
+        self._pf = None  # chunked context: staging of the prefill call's small inputs
 
     def _bucket(self, B: int) -> _Bucket:
         Bp = next((b for b in self.buckets if b >= B), None)
@@ -138,13 +169,18 @@ class DecodeLoop:
         self.running.append(seq)
 
     def _prefill_chunks(self, prefill):
-        """One chunked-context prefill call for all of this step's prompt chunks."""
+        """One chunked-context prefill call for all of this step's prompt chunks: the chunks'
+        rows gathered on the device, the allocator's slots and tables written into pinned
+        staging and moved by one pkv_stage_copy."""
         torch, sc = self.torch, self.script
-        ks, vs, qs, seqs, pos = [], [], [], [], []
+        n = len(prefill)
+        rows = np.array(prefill, dtype=np.int64).reshape(n, 3).T.copy()  # seq ids, p0, p1
+        counts = rows[2] - rows[1]
+        total = int(counts.sum())
+        ks, vs, qs = [], [], []
+        base = sc.system if sc.reuse else 0  # staged rows start after a cached system prompt
         for s, p0, p1 in prefill:
-            pkv_seq_reserve(self.alloc, s, p1)
-            if s in self.prompts:  # staged rows from position `base` (after a cached system prompt)
-                base = sc.system if sc.reuse else 0
+            if s in self.prompts:
                 dk, dv, dq = self.prompts[s]
                 ks.append(dk[p0 - base:p1 - base])
                 vs.append(dv[p0 - base:p1 - base])
@@ -156,19 +192,21 @@ class DecodeLoop:
                 ks.append(to_dev(k))
                 vs.append(to_dev(v))
                 qs.append(to_dev(q))
-            seqs += [s] * (p1 - p0)
-            pos += list(range(p0, p1))
-        ids = [s for s, _, _ in prefill]
-        slots = pkv_slot_mapping(self.alloc, seqs, np.asarray(pos, dtype=np.int64))
-        cu = np.concatenate([[0], np.cumsum([p1 - p0 for _, p0, p1 in prefill])]).astype(np.int32)
-        ctx = np.array([p1 for _, _, p1 in prefill], dtype=np.int32)
-        tables = pkv_get_block_tables(self.alloc, ids, self.max_blocks)
-        dev = self.device
-        out = torch.empty(int(cu[-1]), sc.Hq, sc.D, dtype=torch.bfloat16, device=dev)
-        pkv_prefill_step(self.pool.handle, torch.cat(ks), torch.cat(vs), torch.from_numpy(slots).to(dev),
-                         torch.cat(qs), torch.from_numpy(cu).to(dev), int(np.diff(cu).max()),
-                         torch.from_numpy(tables).to(dev), torch.from_numpy(ctx).to(dev), self.scale, out)
-        for s, p0, p1 in prefill:
+        if self._pf is None or self._pf.tokens < total or self._pf.seqs < n:
+            old = self._pf
+            self._pf = _PrefillStaging(torch, max(total, 2 * old.tokens if old else total),
+                                       max(n, 2 * old.seqs if old else n), self.max_blocks, self.device)
+        S = self._pf
+        lib = _L()
+        r = rows.ctypes.data  # reserve, then slots / offsets / lengths / tables into the staging
+        _check(lib.pkv_stage_prefill(self.alloc, r, r + 8 * n, r + 16 * n, n, self.max_blocks, *S.out_ptrs),
+               "pkv_stage_prefill")
+        _check(lib.pkv_stage_copy(*S.copy, torch.cuda.current_stream().cuda_stream), "pkv_stage_copy")
+        out = torch.empty(total, sc.Hq, sc.D, dtype=torch.bfloat16, device=self.device)
+        cat = (lambda xs: xs[0]) if n == 1 else torch.cat  # one sequence: its rows are contiguous already
+        pkv_prefill_step(self.pool.handle, cat(ks), cat(vs), S.D["slots"][:total], cat(qs),
+                         S.D["cu"][:n + 1], int(counts.max()), S.D["tables"][:n], S.D["ctx"][:n], self.scale, out)
+        for s, _, p1 in prefill:
             self.state[s][1] = p1
         return out
 
@@ -210,9 +248,12 @@ class DecodeLoop:
                 torch.cuda.current_stream().synchronize()
             return run, np.zeros((0, sc.Hq, sc.D), dtype=np.uint16)
         B = len(run)
+        ids = np.array(run, dtype=np.int64)
         pos = np.array([self.lens[s] for s in run], dtype=np.int64)
-        pkv_seq_reserve_many(self.alloc, run, pos + 1)  # room for this step's token
         bk = self._bucket(B)
+        # room for this step's token, then tables, slots and lengths (padding rows included)
+        _check(_L().pkv_stage_decode(self.alloc, ids.ctypes.data, pos.ctypes.data, B, bk.Bp, self.max_blocks,
+                                     *bk.out_ptrs), "pkv_stage_decode")
         H = bk.H
         k, v, q = inputs if inputs is not None else sc.step_inputs(self.t, run)
         H["q"][:B] = q.view(np.int16)
@@ -221,12 +262,6 @@ class DecodeLoop:
         H["q"][B:] = 0
         H["k"][B:] = 0
         H["v"][B:] = 0
-        pkv_get_block_tables(self.alloc, run, self.max_blocks, out=H["tables"][:B])
-        H["tables"][B:] = -1
-        pkv_slot_mapping(self.alloc, run, pos, out=H["slots"][:B])
-        H["slots"][B:] = -1
-        H["lens"][:B] = pos + 1
-        H["lens"][B:] = 0
         t2 = time.perf_counter()
         if self.graphs:
             if bk.graph is None:

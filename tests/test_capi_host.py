@@ -193,3 +193,60 @@ def test_reserve_many_equals_sequential_reserves(pkv):
         assert o.reserve(int(seqs[s]), int(grow[s])) == 0
     _same_state(pkv, a, o, set(seqs.tolist()))
     pkv.pkv_allocator_destroy(a)
+
+
+def test_stage_calls_equal_their_composition(pkv):
+    """pkv_stage_prefill / pkv_stage_decode against reserve + block tables + slot mapping run
+    on a second allocator with the same state: identical outputs and identical free lists."""
+    rng = np.random.default_rng(7)
+    for bs in (16, 64):
+        a, b = pkv.pkv_allocator_create(400, bs), pkv.pkv_allocator_create(400, bs)
+        order = rng.permutation(400).astype(np.int32)
+        pkv.pkv_allocator_set_free_order(a, order)
+        pkv.pkv_allocator_set_free_order(b, order)
+        held = {}
+        for step in range(30):
+            ids = rng.choice(60, size=int(rng.integers(1, 8)), replace=False).astype(np.int64)
+            p0 = np.array([held.get(int(s), 0) for s in ids], dtype=np.int64)
+            p1 = p0 + rng.integers(0, 40, len(ids))
+            mb = 50
+            slots, cu, ctx, tables = pkv.pkv_stage_prefill(a, ids, p0, p1, mb)
+            for s, e in zip(ids, p1):
+                pkv.pkv_seq_reserve(b, int(s), int(e))
+            seqs = np.repeat(ids, p1 - p0)
+            pos = np.concatenate([np.arange(x, y) for x, y in zip(p0, p1)]) if len(ids) else np.zeros(0)
+            assert np.array_equal(slots, pkv.pkv_slot_mapping(b, seqs, pos))
+            assert np.array_equal(tables, pkv.pkv_get_block_tables(b, ids, mb))
+            assert cu.tolist() == [0] + np.cumsum(p1 - p0).tolist() and ctx.tolist() == p1.tolist()
+            for s, e in zip(ids, p1):
+                held[int(s)] = int(e)
+            # one decode step over some held sequences, padded to a bucket
+            dec = np.array(sorted(held)[: int(rng.integers(0, 6))], dtype=np.int64)
+            dpos = np.array([held[int(s)] for s in dec], dtype=np.int64)
+            n_pad = len(dec) + int(rng.integers(0, 3))
+            t2, s2, l2 = pkv.pkv_stage_decode(a, dec, dpos, n_pad, mb)
+            for s, q in zip(dec, dpos):
+                pkv.pkv_seq_reserve(b, int(s), int(q) + 1)
+            assert np.array_equal(t2[: len(dec)], pkv.pkv_get_block_tables(b, dec, mb))
+            assert np.array_equal(s2[: len(dec)], pkv.pkv_slot_mapping(b, dec, dpos))
+            assert l2[: len(dec)].tolist() == (dpos + 1).tolist()
+            assert (t2[len(dec):] == -1).all() and (s2[len(dec):] == -1).all() and (l2[len(dec):] == 0).all()
+            for s, q in zip(dec, dpos):
+                held[int(s)] = int(q) + 1
+            if rng.random() < 0.3 and held:  # a sequence finishes
+                s = int(rng.choice(sorted(held)))
+                pkv.pkv_seq_release(a, s)
+                pkv.pkv_seq_release(b, s)
+                del held[s]
+            assert pkv.pkv_free_list(a).tolist() == pkv.pkv_free_list(b).tolist()
+        L = pkv._L()
+        one = np.zeros(4, np.int64)
+        assert L.pkv_stage_prefill(a, one.ctypes.data, one.ctypes.data, one.ctypes.data, 1, 0, one.ctypes.data,
+                                   one.ctypes.data, one.ctypes.data, one.ctypes.data) == pkv.PKV_ERR_INVALID_ARG
+        bad = np.array([5], np.int64)
+        assert L.pkv_stage_prefill(a, one.ctypes.data, bad.ctypes.data, one.ctypes.data, 1, 4, one.ctypes.data,
+                                   one.ctypes.data, one.ctypes.data, one.ctypes.data) == pkv.PKV_ERR_INVALID_ARG  # p1 < p0
+        assert L.pkv_stage_decode(a, one.ctypes.data, one.ctypes.data, 2, 1, 4, one.ctypes.data, one.ctypes.data,
+                                  one.ctypes.data) == pkv.PKV_ERR_INVALID_ARG  # n_pad < n
+        pkv.pkv_allocator_destroy(a)
+        pkv.pkv_allocator_destroy(b)
