@@ -305,18 +305,31 @@ def run_pkv(args, world, rank, local):
         ev_c[k].record(stream)
     torch.cuda.synchronize()
     attn_ms = [ev_b[k].elapsed_time(ev_c[k]) for k in range(K_attn)]
-    # The append on its own (reported separately): the same step's K/V rewritten into their slots.
+    # The append on its own (reported separately): the same step's K/V rewritten into their
+    # slots, 50 appends captured in a CUDA graph so the device time is not bounded by how fast
+    # the host issues such short launches; median over 10 replays.
     append_us = None
     if w.append:
-        K_app = max(3, min(K, 500))
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_app = 50
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(n_app):
+                    step.append(side)
+        stream.wait_stream(side)
+        g.replay()
         torch.cuda.synchronize()
-        ea.record(stream)
-        for _ in range(K_app):
-            step.append()
-        eb.record(stream)
-        torch.cuda.synchronize()
-        append_us = round(ea.elapsed_time(eb) / K_app * 1e3, 2)
+        reps = []
+        for _ in range(10):
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            g.replay()
+            eb.record(stream)
+            torch.cuda.synchronize()
+            reps.append(ea.elapsed_time(eb) / n_app * 1e3)
+        append_us = round(statistics.median(reps), 2)
     clocks = sampler.stop()
     ms_per_step = dist_max(total_ms / K, world)
     if pkv_check_device_error(step.pool.handle) != 0:

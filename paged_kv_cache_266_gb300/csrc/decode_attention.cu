@@ -75,6 +75,8 @@ struct Params {
 // misc words in shared memory
 constexpr int kMiscAbort = 0;
 constexpr int kMiscMergeParts = 1;
+constexpr int kQuickMergeParts = 4;  // merges of up to this many parts load everything at once
+                                     // (bf16 only: the one-byte kernels are capped at 128 registers)
 constexpr int kMiscMergeFirst = 2;
 
 __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* misc, uint64_t limit_ns) {
@@ -472,7 +474,7 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const uint8_t*
 // Shared-memory combine area: O [4 warps][G][D+4], m and l [4][G], merge weights [4][G], and the
 // pair's max and sum [G] each.  Partial states in the workspace: O [slot][G][D] and (m, l)
 // [slot][G][2]; slot = pair + CTA index.
-template <int D>
+template <int D, int QUICK>
 __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const SoftmaxState& st, float osc, int b,
                             int h, bool complete, int64_t Ng, int64_t C, const int32_t* cumg, uint8_t* smem,
                             volatile int* misc) {
@@ -557,8 +559,9 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
     }
     if (!complete) {
         if (tid < G) *reinterpret_cast<float2*>(p.part_ml + (slot * G + tid) * 2) = make_float2(cMp[tid], cLp[tid]);
-        // One thread publishes the CTA's partial state (fence after the barrier covers every
-        // thread's stores) and takes the pair's ticket; the last of its parts merges them.
+        // One thread takes the pair's ticket with an acquire-release atomic: the release publishes
+        // the CTA's partial state (every thread's stores precede it through the barrier), the
+        // acquire lets the last of the parts read all the others' after the next barrier.
         ptx::named_barrier_sync(kCombineBar, kCT);
         if (tid == 0) {
             const int ng = cumg[b + 1] - cumg[b];
@@ -566,16 +569,55 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
             const int64_t e_last = e_first + ng - 1;
             const int c1 = (int)(((e_first + 1) * C - 1) / Ng);
             const int c2 = (int)(((e_last + 1) * C - 1) / Ng);
-            __threadfence();
-            const int ticket = atomicAdd(p.counters + pair, 1);
+            const int ticket = ptx::atomic_add_acq_rel_gpu(p.counters + pair, 1);
             const bool last_part = ticket == c2 - c1;
-            if (last_part) __threadfence();
             misc[kMiscMergeParts] = last_part ? c2 - c1 + 1 : 0;
             misc[kMiscMergeFirst] = c1;
         }
         ptx::named_barrier_sync(kCombineBar, kCT);
         const int nparts = misc[kMiscMergeParts];
-        if (nparts) {
+        if (nparts && nparts <= QUICK) {
+            if constexpr (QUICK > 0) {
+                // A pair cut into a few parts (the usual case: a CTA boundary falls inside it, and the
+                // CTA reaching the pair last merges as its final work): every thread loads the parts'
+                // (m, l) and its slice of their O at once -- one round trip -- and forms the maximum,
+                // the sum and the weighted O itself, in part order.
+                const int64_t s0 = (int64_t)pair + misc[kMiscMergeFirst];
+                for (int e = tid; e < G * (D / 4); e += kCT) {
+                    const int j = e / (D / 4), d = (e % (D / 4)) * 4;
+                    float2 ml[QUICK];
+                    float4 v[QUICK];
+#pragma unroll
+                    for (int u = 0; u < QUICK; ++u) {
+                        if (u < nparts) {
+                            ml[u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((s0 + u) * G + j) * 2));
+                            v[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + ((s0 + u) * G + j) * D + d));
+                        }
+                    }
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int u = 0; u < QUICK; ++u)
+                        if (u < nparts) M = fmaxf(M, ml[u].x);
+                    float L = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < QUICK; ++u) {
+                        if (u < nparts) {
+                            const float w = ptx::exp2_approx(ml[u].x - M);
+                            L += w * ml[u].y;
+                            acc.x += w * v[u].x;
+                            acc.y += w * v[u].y;
+                            acc.z += w * v[u].z;
+                            acc.w += w * v[u].w;
+                        }
+                    }
+                    const float inv = 1.f / L;
+                    *reinterpret_cast<uint2*>(out + j * D + d) =
+                        make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv), ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
+                }
+                if (tid == 0) p.counters[pair] = 0;
+            }
+        } else if (nparts) {
             const int64_t s0 = (int64_t)pair + misc[kMiscMergeFirst];
             // per head: max and sum over the parts, 16 threads per head
             {
@@ -694,7 +736,7 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
         // A warp that gave up waiting no longer releases stages: the stage's phase is unknown, so
         // the producer must not reuse it (its own bounded wait then runs out).
         if (lane == 0 && alive) ptx::mbar_arrive(bar_empty + 8 * s);
-        if (last) finish_pair<D>(p, o, st, FP8 ? sv_prev : 1.f, b, h, g_first == 0 && g == ng - 1, Ng, C, cumg, smem,
+        if (last) finish_pair<D, FP8 ? 0 : kQuickMergeParts>(p, o, st, FP8 ? sv_prev : 1.f, b, h, g_first == 0 && g == ng - 1, Ng, C, cumg, smem,
                                  misc);
         if (++s == p.stages) {
             s = 0;

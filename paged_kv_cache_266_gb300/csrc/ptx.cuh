@@ -184,6 +184,15 @@ __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
     return make_float2(lo, hi);
 }
 
+// Atomic add at GPU scope with acquire-release ordering: writes ordered before it (the caller's,
+// and after a CTA barrier its CTA's) are visible to a thread that reads the value it produces,
+// and the caller sees every write ordered before the additions it observed.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // 2^x with the hardware approximation (flushes denormal results; 2^-inf = +0).
 __device__ __forceinline__ float exp2_approx(float x) {
     float y;
