@@ -75,6 +75,7 @@ class DecodeStep:
         self.lens, self.lens_host = self.lens[:n], self.lens_host[:n]
         self.out = self.out[:n]
         self.batch = n
+        self._host = None  # host staging (and its captured graph) follows the batch
 
     def append(self, stream=None):
         if self.w.append:
