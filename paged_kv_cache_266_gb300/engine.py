@@ -144,6 +144,7 @@ class DecodeLoop:
             pkv_append(self.pool.handle, to_dev(k), to_dev(v), torch.from_numpy(slots).to(device))
         self.last_prefill = ([], None)  # chunked context: (chunks [(seq, p0, p1)], output bits)
         self._pf = None  # chunked context: staging of the prefill call's small inputs
+        self._adm = None  # staging of the joiners' prompt slots
 
     def _bucket(self, B: int) -> _Bucket:
         Bp = next((b for b in self.buckets if b >= B), None)
@@ -153,20 +154,40 @@ class DecodeLoop:
             self._bk[Bp] = _Bucket(self.torch, self, Bp, self.device)
         return self._bk[Bp]
 
-    def _admit(self, seq: int, n: int):
+    def _admit(self, joined):
+        """Admit the step's joining sequences: every prompt reserved and its slots written by one
+        pkv_stage_prefill (positions 0 .. n-1) into pinned staging, moved by one pkv_stage_copy,
+        then each prompt's K/V appended from its slice of the staged slots."""
         torch = self.torch
-        pkv_seq_reserve(self.alloc, seq, n)
-        if n:
-            slots = pkv_slot_mapping(self.alloc, [seq] * n, np.arange(n, dtype=np.int64))
-            if seq in self.prompts:
-                dk, dv = self.prompts[seq]
-            else:
-                k, v = self.script.prompt_kv(seq, n)
-                dk = torch.from_numpy(np.ascontiguousarray(k).view(np.int16)).view(torch.bfloat16).to(self.device)
-                dv = torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).to(self.device)
-            pkv_append(self.pool.handle, dk, dv, torch.from_numpy(slots).to(self.device, non_blocking=True))
-        self.lens[seq] = n
-        self.running.append(seq)
+        n = len(joined)
+        rows = np.zeros((3, n), dtype=np.int64)  # seq ids, first position (0), prompt length
+        rows[0] = [s for s, _ in joined]
+        rows[2] = [m for _, m in joined]
+        total = int(rows[2].sum())
+        if self._adm is None or self._adm.tokens < total or self._adm.seqs < n:
+            old = self._adm
+            self._adm = _PrefillStaging(torch, max(total, 2 * old.tokens if old else total, 1),
+                                        max(n, 2 * old.seqs if old else n), self.max_blocks, self.device)
+        S = self._adm
+        lib = _L()
+        r = rows.ctypes.data
+        _check(lib.pkv_stage_prefill(self.alloc, r, r + 8 * n, r + 16 * n, n, self.max_blocks, *S.out_ptrs),
+               "pkv_stage_prefill")
+        if total:
+            _check(lib.pkv_stage_copy(*S.copy, torch.cuda.current_stream().cuda_stream), "pkv_stage_copy")
+        off = 0
+        for seq, m in joined:
+            if m:
+                if seq in self.prompts:
+                    dk, dv = self.prompts[seq]
+                else:
+                    k, v = self.script.prompt_kv(seq, m)
+                    dk = torch.from_numpy(np.ascontiguousarray(k).view(np.int16)).view(torch.bfloat16).to(self.device)
+                    dv = torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).to(self.device)
+                pkv_append(self.pool.handle, dk, dv, S.D["slots"][off:off + m])
+                off += m
+            self.lens[seq] = m
+            self.running.append(seq)
 
     def _prefill_chunks(self, prefill):
         """One chunked-context prefill call for all of this step's prompt chunks: the chunks'
@@ -237,9 +258,8 @@ class DecodeLoop:
             for s in decode:
                 self.state[s][2] += 1
             self.last_prefill = (prefill, pre_out)
-        else:
-            for s, n in joined:
-                self._admit(s, n)
+        elif joined:
+            self._admit(joined)
         t1 = time.perf_counter()
         run = list(self.running)
         if not run:
