@@ -250,3 +250,42 @@ def test_stage_calls_equal_their_composition(pkv):
                                   one.ctypes.data) == pkv.PKV_ERR_INVALID_ARG  # n_pad < n
         pkv.pkv_allocator_destroy(a)
         pkv.pkv_allocator_destroy(b)
+
+
+def test_stage_calls_match_the_oracle_allocator(pkv):
+    """The same random admission / decode script through pkv_stage_prefill / pkv_stage_decode
+    and through the oracle's allocator replica: slots and block tables bit-identical."""
+    rng = np.random.default_rng(31)
+    a = pkv.pkv_allocator_create(300, 16)
+    o = oracle.Allocator(300, 16)
+    order = rng.permutation(300).astype(np.int32)
+    pkv.pkv_allocator_set_free_order(a, order)
+    assert o.set_free_order(order) == 0
+    held, mb = {}, 40
+    for step in range(25):
+        new = [s for s in rng.choice(200, size=int(rng.integers(0, 4)), replace=False).tolist() if s not in held]
+        if new:
+            ids = np.array(new, dtype=np.int64)
+            p1 = rng.integers(0, 120, len(ids)).astype(np.int64)
+            slots, _, _, tables = pkv.pkv_stage_prefill(a, ids, np.zeros_like(p1), p1, mb)
+            for s_, n_ in zip(new, p1.tolist()):
+                assert o.reserve(s_, n_) == 0
+            seqs = np.repeat(ids, p1)
+            pos = np.concatenate([np.arange(n_) for n_ in p1.tolist()])
+            assert np.array_equal(slots, o.slot_mapping(seqs, pos))
+            assert np.array_equal(tables, o.block_tables(new, mb))
+            held.update(zip(new, p1.tolist()))
+        dec = np.array(sorted(held), dtype=np.int64)
+        dpos = np.array([held[s_] for s_ in dec.tolist()], dtype=np.int64)
+        t2, s2, _ = pkv.pkv_stage_decode(a, dec, dpos, len(dec) + 1, mb)
+        for s_, q_ in zip(dec.tolist(), dpos.tolist()):
+            assert o.reserve(s_, q_ + 1) == 0
+            held[s_] = q_ + 1
+        if len(dec):
+            assert np.array_equal(s2[:-1], o.slot_mapping(dec, dpos))
+            assert np.array_equal(t2[:-1], o.block_tables(dec.tolist(), mb))
+        for s_ in [s_ for s_ in sorted(held) if rng.random() < 0.15]:
+            assert pkv.pkv_seq_release(a, s_) is None and o.release(s_) == 0
+            del held[s_]
+        assert pkv.pkv_free_list(a).tolist() == o.free_list().tolist()
+    pkv.pkv_allocator_destroy(a)
