@@ -1,11 +1,12 @@
 """Benchmark: one decode step (append of one token per sequence + paged decode attention)
 on a synthetic in-flight batch, timed on the GPU.  Prints one JSON line.
 
-Default workload: Llama-2-7B-shape MHA layer decode (32 query / 32 KV heads, head_dim 128,
-bf16, block 64, batch 32, contexts U[128, 2048]).  `--workload c2|c3|c4` selects the other
-shapes (for measurement runs; the default line is the headline).
+Headline workload: the 70B-shape long-context batch (64 query / 8 KV heads, head_dim 128, bf16,
+block 64, 8 sequences of 32K..128K tokens), the largest; the Llama-2-7B MHA batch, the
+Llama-3-8B GQA batch and the churned 200-request FP8 pool follow as sub-records ("configs") of
+the same JSON line.  `--workload` picks the headline, `--also` the sub-records.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--workload c1]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--workload c3] [--also c1,c2,c4]
 
 For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the workload
 (independent sequences, no data exchange); the value is the sum over ranks divided by the
@@ -251,24 +252,20 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- main arm
-def run_pkv(args, world, rank, local):
+def measure_decode(w, args, world, local, stream):
+    """One workload's decode step on this rank: K timed fused steps (append + attention), then
+    the attention kernel alone (at least 50 launches, one event pair each), the append alone (a
+    replayed graph of 50 appends) and the host-driven step through the public API.  Returns the
+    workload's record (everything but the CPU baseline) and its DecodeStep."""
     import torch
-    from paged_kv_cache_266_gb300 import build as pkv_build
-    pkv_build.build()
     from paged_kv_cache_266_gb300 import pkv_check_device_error
     from paged_kv_cache_266_gb300.runner import DecodeStep
 
-    torch.cuda.set_device(local)
-    w = W.make_workload(args.workload)
-    if args.kv and args.kv != w.kv_dtype:  # the same workload over another KV element type
-        import dataclasses
-        w = dataclasses.replace(w, kv_dtype=args.kv, name=f"{w.name}-{args.kv}")
     step = DecodeStep(w, device=f"cuda:{local}")
     if args.seqs:
         step.limit_batch(args.seqs)
         w = W.truncated(w, args.seqs)
     nbytes = algorithmic_bytes(w)
-    stream = torch.cuda.current_stream()
     launches_per_step = (0 if not w.append else (1 if w.kv_dtype == "bf16" else 3)) + 1
 
     for _ in range(args.warmup):
@@ -294,8 +291,9 @@ def run_pkv(args, world, rank, local):
     t_wall = time.perf_counter() - t_wall
     dist_barrier(world)
     total_ms = ev0.elapsed_time(ev1)
-    # The attention kernel on its own (for the roofline): K launches, one event pair each.
-    K_attn = max(3, min(K, 2000))
+    # The attention kernel on its own (for the roofline): at least 50 launches whatever K is, one
+    # event pair each.
+    K_attn = max(50, min(K, 2000))
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K_attn)]
     ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(K_attn)]
     torch.cuda.synchronize()
@@ -341,7 +339,8 @@ def run_pkv(args, world, rank, local):
     achieved = nbytes["attention"] / (attn_mean * 1e-3) / 1e9
     traffic, traffic_note = ncu_traffic(w)
 
-    # end to end from host buffers through the public API
+    # end to end through the public API: the caller's host arrays copied into pinned staging, the
+    # allocator's tables and slots written there, one copy in, the fused step, the output back
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     for _ in range(2):
         step.step_host()
@@ -353,23 +352,9 @@ def run_pkv(args, world, rank, local):
     e2e_s = dist_max(e2e_s, world)
     e2e_value = world * nbytes["step"] / e2e_s / 1e9
 
-    cpu = None
-    if rank == 0 and not args.no_cpu:
-        threads = os.cpu_count() or 1
-        rate, spent, sample = oracle_rate(w, args.cpu_budget, threads)
-        rate1, spent1, sample1 = oracle_rate(w, max(1.0, args.cpu_budget / 3), 1)
-        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{sample}; {spent:.1f} s",
-               "single_thread": {"value": round(rate1, 4), "unit": "GB/s", "cores": 1,
-                                 "sample": f"{sample1}; {spent1:.1f} s"}}
-
-    if rank != 0:
-        return
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": f"f32-accumulate on {w.kv_dtype} KV",
-        "data": "synthetic",
+    rec = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms_per_step, 5),
+        "dtype": f"f32-accumulate on {w.kv_dtype} KV",
         "config": {"workload": w.name, "description": w.description, "batch": w.B, "q_heads": w.Hq,
                    "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
                    "context_tokens": int(w.attend_lens.sum()), "kv_bytes_per_step": nbytes["kv"],
@@ -387,14 +372,67 @@ def run_pkv(args, world, rank, local):
                      "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": "decode_kernel", "algorithmic_bytes_per_launch": nbytes["attention"]},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_s * 1e3, 4)},
+                "ms_per_step": round(e2e_s * 1e3, 4),
+                "path": "caller's host q/K/V/lengths copied into pinned staging, allocator tables and slots "
+                        "written there, one copy to the device, fused step, output copied back (graph-replayed)"},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
-        "cpu_baseline": cpu,
         "wall_s_timed": round(t_wall, 3),
     }
-    print(json.dumps(line), flush=True)
+    return rec, step, w
+
+
+def run_pkv(args, world, rank, local):
+    import torch
+    from paged_kv_cache_266_gb300 import build as pkv_build
+    pkv_build.build()
+
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+
+    def workload(name):
+        w = W.make_workload(name)
+        if args.kv and args.kv != w.kv_dtype:  # the same workload over another KV element type
+            import dataclasses
+            w = dataclasses.replace(w, kv_dtype=args.kv, name=f"{w.name}-{args.kv}")
+        return w
+
+    # the headline workload, then the other target workloads as sub-records of the same line
+    rec, step, w = measure_decode(workload(args.workload), args, world, local, stream)
     step.close()
+    del step
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        threads = os.cpu_count() or 1
+        rate, spent, sample = oracle_rate(w, args.cpu_budget, threads)
+        rate1, spent1, sample1 = oracle_rate(w, max(1.0, args.cpu_budget / 3), 1)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{sample}; {spent:.1f} s",
+               "single_thread": {"value": round(rate1, 4), "unit": "GB/s", "cores": 1,
+                                 "sample": f"{sample1}; {spent1:.1f} s"}}
+    others = {}
+    for name in [x for x in args.also.split(",") if x and x != args.workload]:
+        sub, sstep, _ = measure_decode(workload(name), args, world, local, stream)
+        sstep.close()
+        del sstep
+        torch.cuda.empty_cache()
+        others[name] = sub
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": rec["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": rec["dtype"], "data": "synthetic", "config": rec["config"],
+    }
+    for k in ("tokens_per_s", "tokens_per_s_unit", "pct_of_hbm_peak", "kernel_us", "roofline", "e2e", "gpu_launches",
+              "clocks"):
+        line[k] = rec[k]
+    line["cpu_baseline"] = cpu
+    line["wall_s_timed"] = rec["wall_s_timed"]
+    if others:
+        line["configs"] = others
+    print(json.dumps(line), flush=True)
 
 
 def run_loop(args, world, rank, local):
@@ -772,7 +810,9 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--workload", default="c1", choices=list(W.WORKLOADS))
+    ap.add_argument("--workload", default="c3", choices=list(W.WORKLOADS))
+    ap.add_argument("--also", default="c1,c2,c4",
+                    help="workloads measured after the headline one, reported as sub-records ('' for none)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")

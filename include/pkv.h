@@ -328,7 +328,10 @@ pkv_status pkv_prefill_step(pkv_pool* pool, const void* k_new_dev, const void* v
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *     with the pool's device current; make that first call before any stream capture.
  *   - All calls share the one array, so calls that overlap on the GPU (other streams, other
- *     threads) race and corrupt each other's results: serialise them. */
+ *     threads) race and corrupt each other's results: serialise them.
+ *   - The looked-up address is kept for the life of the process.  cudaDeviceReset (or anything
+ *     else that destroys the device's primary context) invalidates it: do not use this call on
+ *     a device after resetting it. */
 #define PKV_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
 pkv_status pkv_decode_attention_static(const pkv_pool* pool, const void* q_dev, const int32_t* block_tables_dev,
                                        int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads,
@@ -349,6 +352,17 @@ pkv_status pkv_decode_attention_static(const pkv_pool* pool, const void* q_dev, 
  * PKV_ERR_INVALID_ARG (nothing launched): null or misaligned pointers, bytes % 16, overlap,
  * pageable host memory or another device's memory; PKV_ERR_CUDA: the launch failed. */
 pkv_status pkv_stage_copy(void* dst, const void* src, size_t bytes, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------ testing and tuning
+ * The library reads these environment variables when it loads, not on every call:
+ *   PKV_TEST_WAIT_LIMIT_MS (> 0: every bounded wait in the kernels gives up after this many ms
+ *   instead of 2 s), PKV_TEST_STALL_COPIES (non-zero: every pipeline stage waits for 16 bytes
+ *   that no copy delivers, so the waits run out and calls report PKV_ERR_TIMEOUT: failure
+ *   detection tested without a fault), PKV_ATTN_CTAS_PER_SM and PKV_ATTN_MAX_STAGES (decode
+ *   attention launch shape; 0 or unset: the defaults).  Leave them unset in normal use.
+ * pkv_debug_reload_env reads them again (for tests that switch the hooks on and off); it must
+ * not run concurrently with other calls of the library. */
+pkv_status pkv_debug_reload_env(void);
 
 /* ------------------------------------------------------------------ utilities
  * KV memory ("TensorRT-LLM 推理加速实战" §8.1; aiqz.cc page, KV缓存管理):

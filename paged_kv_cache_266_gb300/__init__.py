@@ -23,7 +23,7 @@ __all__ = [
     "pkv_slot_mapping", "pkv_stage_prefill", "pkv_stage_decode", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
     "pkv_check_device_error", "pkv_append", "pkv_decode_attention", "pkv_decode_step", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_decode_attention_static", "PKV_STATIC_WORKSPACE_BYTES", "pkv_stage_copy", "pkv_kv_bytes",
-    "pkv_status_str", "KVPool",
+    "pkv_status_str", "pkv_debug_reload_env", "KVPool",
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OOM, PKV_ERR_NO_SEQ, PKV_ERR_BOUNDS, PKV_ERR_CUDA, PKV_ERR_TIMEOUT = range(7)
@@ -88,6 +88,7 @@ def _L():
         "pkv_decode_workspace_init": (i32, [vp, sz, vp]),
         "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]),
         "pkv_stage_copy": (i32, [vp, vp, sz, vp]),
+        "pkv_debug_reload_env": (i32, []),
         "pkv_kv_bytes": (ctypes.c_uint64, [i64, i64, i64, i64, i64, ctypes.c_double]),
         "pkv_status_str": (ctypes.c_char_p, [i32]),
     }
@@ -450,3 +451,9 @@ class KVPool:
             self.close()
         except Exception:
             pass
+
+
+def pkv_debug_reload_env() -> None:
+    """Re-read the library's PKV_TEST_* / PKV_ATTN_* environment settings (tests switching the
+    bounded-wait hooks on and off)."""
+    _check(_L().pkv_debug_reload_env(), "pkv_debug_reload_env")

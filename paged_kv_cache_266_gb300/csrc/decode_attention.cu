@@ -22,7 +22,9 @@
 //        P^T -> B fragment via movmatrix (register transpose, no shared-memory round trip)
 //        O^T[D][8 heads] += V^T[D][16 tok] . P^T       (ldmatrix.trans for bf16 V)
 //    fp8 codes are widened to f16 in registers (exact); the K scale multiplies the scores,
-//    the V scale is folded into the running rescale factor.
+//    the V scale is folded into the running rescale factor.  The query rows are scaled per
+//    head by a power of two into f16's range before their conversion, which keeps it exact
+//    for any bf16 query; the inverse power of two joins the head's score scale.
 //  * When a pair ends inside the CTA the four warps' (max, sum, O) states are merged through
 //    shared memory and the result is written as bf16.  A pair cut between CTAs leaves one
 //    partial state per CTA in the workspace; the last CTA to finish (atomic ticket, no
@@ -274,10 +276,11 @@ struct SoftmaxState {
 };
 
 // Online-softmax step on one 16-token S^T tile.  acc: (t=g, j=2c), (g, 2c+1), (g+8, 2c),
-// (g+8, 2c+1).  Returns the rescale factors of the two heads and the probabilities.
-__device__ __forceinline__ void softmax_step(const float (&acc)[4], float sl, int nvalid, int g8, SoftmaxState& st,
-                                             float (&pr)[4], float& a0, float& a1) {
-    float z0 = acc[0] * sl, z1 = acc[1] * sl, z2 = acc[2] * sl, z3 = acc[3] * sl;
+// (g+8, 2c+1); sl0 / sl1 scale the scores of heads 2c / 2c+1.  Returns the rescale factors of
+// the two heads and the probabilities.
+__device__ __forceinline__ void softmax_step(const float (&acc)[4], float sl0, float sl1, int nvalid, int g8,
+                                             SoftmaxState& st, float (&pr)[4], float& a0, float& a1) {
+    float z0 = acc[0] * sl0, z1 = acc[1] * sl1, z2 = acc[2] * sl0, z3 = acc[3] * sl1;
     if (nvalid < 16) {
         if (g8 >= nvalid) z0 = z1 = -INFINITY;
         if (g8 + 8 >= nvalid) z2 = z3 = -INFINITY;
@@ -321,7 +324,7 @@ __device__ __forceinline__ void tile_bf16(uint32_t kst, uint32_t vst, int row0, 
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
     float pr[4], f0, f1;
-    softmax_step(acc, sl, nvalid, g8, st, pr, f0, f1);
+    softmax_step(acc, sl, sl, nvalid, g8, st, pr, f0, f1);
     const uint32_t p01 = ptx::pack_bf16x2(pr[0], pr[1]), p23 = ptx::pack_bf16x2(pr[2], pr[3]);
     // the sums use the rounded probabilities the MMA multiplies with
     st.l[0] = st.l[0] * f0 + ptx::bf16lo_to_f32(p01) + ptx::bf16lo_to_f32(p23);
@@ -384,10 +387,13 @@ __device__ __forceinline__ void widen4(uint32_t four, uint32_t& lo, uint32_t& hi
     }
 }
 
+// qinv0 / qinv1: 2^-e of heads 2c / 2c+1, undoing the power-of-two scaling of their query rows
+// (load_q_f16).
 template <int D, bool I8>
 __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, int nvalid,
                                          const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], SoftmaxState& st,
-                                         float sl, float sk, float sv, float& sv_prev, int lane) {
+                                         float sl, float sk, float sv, float& sv_prev, float qinv0, float qinv1,
+                                         int lane) {
     constexpr int KS = D / 16;
     const int rr = lane & 7, mat = lane >> 3, g8 = lane >> 2, c4 = lane & 3;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -407,7 +413,8 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
     float pr[4], f0, f1;
-    softmax_step(acc, sl * sk, nvalid, g8, st, pr, f0, f1);
+    const float slk = sl * sk;  // then an exact power-of-two factor per head
+    softmax_step(acc, slk * qinv0, slk * qinv1, nvalid, g8, st, pr, f0, f1);
     const uint32_t p01 = ptx::pack_f16x2(pr[0], pr[1]), p23 = ptx::pack_f16x2(pr[2], pr[3]);
     const float2 q01 = ptx::f16x2_to_f32x2(p01), q23 = ptx::f16x2_to_f32x2(p23);
     st.l[0] = st.l[0] * f0 + q01.x + q23.x;
@@ -448,24 +455,72 @@ __device__ __forceinline__ void tile_fp8(uint32_t kst, uint32_t vst, int row0, i
     }
 }
 
-// Query B-fragments of the group's G heads (rows >= G are zero).
-template <bool FP8, int D>
-__device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const uint8_t* qs, int G, int lane) {
+// 2^k as fp32 for k in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2f(int k) {
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+// Query B-fragments of the group's G heads (rows >= G are zero), bf16 KV: the bf16 bits as they
+// are.
+template <int D>
+__device__ __forceinline__ void load_q_bf16(uint32_t (&qf)[D / 16][2], const uint8_t* qs, int G, int lane) {
     const int g8 = lane >> 2, c4 = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         if (g8 >= G) {
             qf[ks][0] = qf[ks][1] = 0u;
-        } else if (!FP8) {
+        } else {
             const uint32_t* row = reinterpret_cast<const uint32_t*>(qs + (size_t)g8 * D * 2);
             qf[ks][0] = row[(16 * ks + 2 * c4) >> 1];
             qf[ks][1] = row[(16 * ks + 8 + 2 * c4) >> 1];
-        } else {  // logical k 2c,2c+1 | 2c+8,2c+9 <-> physical d 4c..4c+3 (matches the fp8 K fragment)
-            const uint2 v = *reinterpret_cast<const uint2*>(qs + ((size_t)g8 * D + 16 * ks + 4 * c4) * 2);
-            qf[ks][0] = ptx::pack_f16x2(ptx::bf16lo_to_f32(v.x), ptx::bf16hi_to_f32(v.x));
-            qf[ks][1] = ptx::pack_f16x2(ptx::bf16lo_to_f32(v.y), ptx::bf16hi_to_f32(v.y));
         }
     }
+}
+
+// One-byte KV: the codes widen exactly to f16 and the MMA runs on f16, so the query rows are
+// converted to f16 too.  To keep that conversion exact for any bf16 row, each head's row is first
+// multiplied by 2^e, e chosen so that the row's largest magnitude lands in [2^15, 2^16) (bf16's
+// 8-bit significand then fits f16 exactly up to 65280 < 65504); *qinv0 / *qinv1 receive 2^-e of
+// heads 2c and 2c+1, which the caller folds into those heads' score scale (a power of two: the
+// scores equal the unscaled ones, roundings included).  Elements more than 2^29 below the row's
+// maximum fall under f16's normal range and are rounded to its subnormal grid: an error below
+// 2^-39 of the row maximum per element, under the fp32 accumulation's own rounding.  A zero row
+// keeps e = 0.
+template <int D>
+__device__ __forceinline__ void load_q_f16(uint32_t (&qf)[D / 16][2], const uint8_t* qs, int G, int lane,
+                                           float& qinv0, float& qinv1) {
+    constexpr int KS = D / 16;
+    const int g8 = lane >> 2, c4 = lane & 3;
+    uint2 raw[KS];
+    uint32_t mx = 0;  // largest |q| of the row, as bf16 magnitude bits (they order like the values)
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        // logical k 2c,2c+1 | 2c+8,2c+9 <-> physical d 4c..4c+3 (matches the one-byte K fragment)
+        raw[ks] = g8 < G ? *reinterpret_cast<const uint2*>(qs + ((size_t)g8 * D + 16 * ks + 4 * c4) * 2)
+                         : make_uint2(0u, 0u);
+        mx = max(mx, max(max(raw[ks].x & 0x7fffu, (raw[ks].x >> 16) & 0x7fffu),
+                         max(raw[ks].y & 0x7fffu, (raw[ks].y >> 16) & 0x7fffu)));
+    }
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int e = 0;
+    if (mx) {
+        const int E = (int)(mx >> 7);  // biased exponent; 0 for a subnormal maximum
+        const int lead = E ? E - 127 : (31 - __clz((int)mx)) - 133;  // exponent of its leading bit
+        e = 15 - lead;  // in [-113, 148]
+    }
+    // 2^e as two factors, each a normal fp32 power of two
+    const int ea = e >> 1;
+    const float fa = pow2f(ea), fb = pow2f(e - ea);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][0] = ptx::pack_f16x2(ptx::bf16lo_to_f32(raw[ks].x) * fa * fb, ptx::bf16hi_to_f32(raw[ks].x) * fa * fb);
+        qf[ks][1] = ptx::pack_f16x2(ptx::bf16lo_to_f32(raw[ks].y) * fa * fb, ptx::bf16hi_to_f32(raw[ks].y) * fa * fb);
+    }
+    // heads 2c and 2c+1 are held by lanes 8c.. and 8c+4..
+    const int e0 = __shfl_sync(0xffffffffu, e, 8 * c4), e1 = __shfl_sync(0xffffffffu, e, 8 * c4 + 4);
+    qinv0 = pow2f(-e0);
+    qinv1 = pow2f(-e1);
 }
 
 // Merge the four warps' states of pair (b, h) and write the output (pair complete in this CTA)
@@ -692,6 +747,7 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
     float o[KS][4];
     SoftmaxState st;
     float sv_prev = 1.f;
+    float qinv0 = 1.f, qinv1 = 1.f;  // one-byte KV: per-head undo of the query scaling
     int b = find_seq(cumg, p.B, p.Hkv, R0);
     int ng = cumg[b + 1] - cumg[b];
     const int r = (int)(R0 - (int64_t)p.Hkv * cumg[b]);
@@ -713,7 +769,10 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
             flag_abort(p, misc);
         }
         if (first) {
-            load_q<FP8, D>(qf, smem + (st_addr - sbase) + p.off_q, p.G, lane);
+            if constexpr (FP8)
+                load_q_f16<D>(qf, smem + (st_addr - sbase) + p.off_q, p.G, lane, qinv0, qinv1);
+            else
+                load_q_bf16<D>(qf, smem + (st_addr - sbase) + p.off_q, p.G, lane);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
             st.m[0] = st.m[1] = -INFINITY;
@@ -727,7 +786,8 @@ __device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* le
             const uint32_t vst = kst + part_bytes / 2;
             if (FP8) {
                 const float2 sc = *reinterpret_cast<const float2*>(smem + (st_addr - sbase) + p.off_s + 8 * pidx);
-                tile_fp8<D, I8>(kst, vst, prow, nvalid, qf, o, st, p.scale_log2, sc.x, sc.y, sv_prev, lane);
+                tile_fp8<D, I8>(kst, vst, prow, nvalid, qf, o, st, p.scale_log2, sc.x, sc.y, sv_prev, qinv0, qinv1,
+                                lane);
             } else {
                 tile_bf16<D>(kst, vst, prow, (uint32_t)p.box_rows * 128, nvalid, qf, o, st, p.scale_log2, lane);
             }
@@ -858,11 +918,6 @@ const void* kernel_for(const pkv_pool* pool) {
               : fp8 ? (const void*)decode_kernel<true, 64> : (const void*)decode_kernel<false, 64>;
 }
 
-int env_int(const char* name, int dflt) {
-    const char* v = std::getenv(name);
-    return v && *v ? std::atoi(v) : dflt;
-}
-
 bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, Plan& pl);
 
 // The launch plan depends only on these values (not on the pool's address or contents), so the
@@ -879,8 +934,9 @@ struct PlanKey {
 
 bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     const bool q8 = pool->dtype != PKV_KV_BF16;
-    const int pref = env_int("PKV_ATTN_CTAS_PER_SM", q8 ? 3 : 2);
-    const int max_stages = env_int("PKV_ATTN_MAX_STAGES", kMaxStages);
+    const Settings& cfg = settings();
+    const int pref = cfg.attn_ctas_per_sm > 0 ? cfg.attn_ctas_per_sm : (q8 ? 3 : 2);
+    const int max_stages = cfg.attn_max_stages > 0 ? cfg.attn_max_stages : kMaxStages;
     const PlanKey key{B, G, pool->n_kv_heads, (int)pool->dtype, pool->head_dim, pool->block_size, pool->sm_count,
                       pool->max_smem_per_block, pool->max_smem_per_sm, pool->device, pref, max_stages};
     constexpr int kSlots = 8;
@@ -988,12 +1044,12 @@ pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tab
     p.off_cmb = pl.off_cmb;
     p.off_lens = pl.off_lens;
     p.scale_log2 = scale * 1.4426950408889634f;
-    // Test hooks for the bounded waits (failure detection is tested without a GPU fault):
-    // PKV_TEST_WAIT_LIMIT_MS shortens every wait, PKV_TEST_STALL_COPIES makes every stage expect
-    // 16 bytes no copy delivers, so the waits run out and the call reports PKV_ERR_TIMEOUT.
-    const int limit_ms = env_int("PKV_TEST_WAIT_LIMIT_MS", 0);
-    p.wait_ns = limit_ms > 0 ? (uint64_t)limit_ms * 1000000ull : kWaitLimitNs;
-    p.stall_tx = env_int("PKV_TEST_STALL_COPIES", 0) ? 16u : 0u;
+    // Test hooks for the bounded waits (failure detection is tested without a GPU fault): a
+    // shorter wait limit, and stages that expect 16 bytes no copy delivers, so the waits run out
+    // and the call reports PKV_ERR_TIMEOUT (both off unless set, see Settings).
+    const Settings& hooks = settings();
+    p.wait_ns = hooks.wait_limit_ms > 0 ? (uint64_t)hooks.wait_limit_ms * 1000000ull : kWaitLimitNs;
+    p.stall_tx = hooks.stall_copies ? 16u : 0u;
     return PKV_OK;
 }
 

@@ -24,6 +24,21 @@ pkv_status append_rope_launch(pkv_pool* pool, void* k_new, const void* v_new, co
 pkv_allocator* allocator_new(int num_blocks, int block_size);
 void allocator_delete(pkv_allocator* a);
 
+// Launch settings and test hooks taken from the environment when the library loads (and again
+// by pkv_debug_reload_env), not on every launch:
+//   PKV_TEST_WAIT_LIMIT_MS  > 0: bound of every kernel wait in ms (default 2 s);
+//   PKV_TEST_STALL_COPIES   != 0: every pipeline stage expects 16 bytes no copy delivers, so the
+//                           bounded waits run out (failure detection tested without a fault);
+//   PKV_ATTN_CTAS_PER_SM    decode attention CTAs per SM (0: the kernel's default);
+//   PKV_ATTN_MAX_STAGES     decode attention pipeline stages at most (0: default).
+struct Settings {
+    int wait_limit_ms;
+    int stall_copies;
+    int attn_ctas_per_sm;
+    int attn_max_stages;
+};
+const Settings& settings();
+
 }  // namespace pkv
 
 struct pkv_pool {

@@ -15,6 +15,24 @@
 
 namespace pkv {
 
+namespace {
+
+int env_int(const char* name) {
+    const char* v = std::getenv(name);
+    return v && *v ? std::atoi(v) : 0;
+}
+
+Settings read_settings() {
+    return Settings{env_int("PKV_TEST_WAIT_LIMIT_MS"), env_int("PKV_TEST_STALL_COPIES"),
+                    env_int("PKV_ATTN_CTAS_PER_SM"), env_int("PKV_ATTN_MAX_STAGES")};
+}
+
+Settings g_settings = read_settings();
+
+}  // namespace
+
+const Settings& settings() { return g_settings; }
+
 void attention_configure(pkv_pool* pool);  // decode_attention.cu
 void prefill_configure(pkv_pool* pool);    // prefill_attention.cu
 
@@ -237,3 +255,8 @@ pkv_status pkv_decode_workspace_init(void* workspace, size_t bytes, pkv_stream_t
 }
 
 }  // extern "C"
+
+extern "C" pkv_status pkv_debug_reload_env(void) {
+    pkv::g_settings = pkv::read_settings();
+    return PKV_OK;
+}

@@ -495,11 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int env_int(const char* name, int dflt) {
-    const char* v = std::getenv(name);
-    return v && *v ? std::atoi(v) : dflt;
-}
-
 }  // namespace prefill
 
 void prefill_configure(pkv_pool* pool) {
@@ -548,12 +543,12 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     p.tiles = (max_q_len + kTiles * T - 1) / (kTiles * T);  // pairs of query tiles
     p.oob_row = (int32_t)((int64_t)pool->num_blocks * 2 * pool->n_kv_heads * pool->block_size);
     p.scale_log2 = scale * 1.4426950408889634f;
-    // Test hooks for the bounded waits (failure detection is tested without a GPU fault):
-    // PKV_TEST_WAIT_LIMIT_MS shortens every wait, PKV_TEST_STALL_COPIES makes every K/V stage
-    // expect 16 bytes no copy delivers, so the waits run out and the call reports PKV_ERR_TIMEOUT.
-    const int limit_ms = env_int("PKV_TEST_WAIT_LIMIT_MS", 0);
-    p.wait_ns = limit_ms > 0 ? (uint64_t)limit_ms * 1000000ull : kWaitLimitNs;
-    p.stall_tx = env_int("PKV_TEST_STALL_COPIES", 0) ? 16u : 0u;
+    // Test hooks for the bounded waits (failure detection is tested without a GPU fault): a
+    // shorter wait limit, and K/V stages that expect 16 bytes no copy delivers, so the waits run
+    // out and the call reports PKV_ERR_TIMEOUT (both off unless set, see Settings).
+    const Settings& hooks = settings();
+    p.wait_ns = hooks.wait_limit_ms > 0 ? (uint64_t)hooks.wait_limit_ms * 1000000ull : kWaitLimitNs;
+    p.stall_tx = hooks.stall_copies ? 16u : 0u;
     p.B = B;
     const int64_t ctas = (int64_t)B * pool->n_kv_heads * p.tiles;
     if (ctas > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;

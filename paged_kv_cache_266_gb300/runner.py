@@ -5,9 +5,10 @@ lengths, an allocation script and seeded inputs), builds the pool on the GPU,
 replays the allocation script on the pool's allocator, writes every sequence's
 history K/V with ``pkv_append`` and keeps the step's inputs resident.  ``step()``
 is the hot path: append the new token of every sequence, then decode attention
-over the grown contexts.  ``step_host()`` is the same step starting from host
-buffers (block tables and slot mapping rebuilt by the allocator, inputs copied in
-from pinned memory, the output copied back).
+over the grown contexts.  ``step_host()`` is the same step starting from the
+caller's host arrays (q, new K/V and lengths copied into a pinned staging buffer,
+block tables and slot mapping written there by the allocator, one copy to the
+device, the output copied back).
 """
 from __future__ import annotations
 
@@ -120,16 +121,18 @@ class DecodeStep:
             nbytes = int(np.prod(shape)) * np.dtype(dt).itemsize
             H[name] = hnp[offs[name]:offs[name] + nbytes].view(dt).reshape(shape)
             Dv[name] = dbuf[offs[name]:offs[name] + nbytes].view(tdt[dt]).view(shape)
-        H["q"][...] = w.query()[:n].view(np.int16)
-        H["k"][...] = w.new_k()[:n].view(np.int16)
-        H["v"][...] = w.new_v()[:n].view(np.int16)
-        H["lens"][...] = self.lens_host
+        # the caller's inputs of the step, in ordinary (pageable) host memory: every host-driven
+        # step copies them into the pinned staging buffer first
+        src = {"q": np.ascontiguousarray(w.query()[:n]).view(np.int16),
+               "k": np.ascontiguousarray(w.new_k()[:n]).view(np.int16),
+               "v": np.ascontiguousarray(w.new_v()[:n]).view(np.int16),
+               "lens": np.ascontiguousarray(self.lens_host[:n])}
         # the allocator writes tables and slots straight into the staging buffer; the sequence
         # ids and positions are fixed for the batch, so every host address is taken once here
         ids = np.ascontiguousarray(w.seq_ids[:n], dtype=np.int64)
         pos = np.ascontiguousarray(w.lens[:n], dtype=np.int64)
         ptrs = (ids.ctypes.data, pos.ctypes.data, H["tables"].ctypes.data, H["slots"].ctypes.data)
-        self._host = {"hbuf": hbuf, "dbuf": dbuf, "H": H, "ids": ids, "pos": pos, "ptrs": ptrs,
+        self._host = {"hbuf": hbuf, "dbuf": dbuf, "H": H, "src": src, "ids": ids, "pos": pos, "ptrs": ptrs,
                       "q": Dv["q"].view(torch.bfloat16), "k": Dv["k"].view(torch.bfloat16),
                       "v": Dv["v"].view(torch.bfloat16), "tables": Dv["tables"], "lens": Dv["lens"],
                       "slots": Dv["slots"], "out": torch.empty(n, w.Hq, w.D, dtype=torch.int16).pin_memory()}
@@ -147,16 +150,19 @@ class DecodeStep:
         pkv_stage_copy(X["out"], self.out, stream=stream)
 
     def step_host(self, stream=None, graph: bool = True):
-        """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The allocator writes the block
-        tables and the slot mapping into the pinned staging buffer, one copy takes every input
-        to the device, the fused step runs, and the output comes back.  With `graph` the copy-in,
-        step and copy-out are captured once as a CUDA graph and replayed (the launch-bound part
-        of a decode step, "TensorRT-LLM 推理加速实战" §7.1); the staging buffer is read at replay."""
+        """Host-to-host step; returns (h2d_bytes, d2h_bytes).  The step's q / new K / new V are
+        copied from the caller's host arrays into the pinned staging buffer, the allocator writes
+        the block tables and the slot mapping next to them, one copy takes every input to the
+        device, the fused step runs, and the output comes back.  With `graph` the copy-in, step
+        and copy-out are captured once as a CUDA graph and replayed (the launch-bound part of a
+        decode step, "TensorRT-LLM 推理加速实战" §7.1); the staging buffer is read at replay."""
         torch, w, a = self.torch, self.w, self.pool.allocator
         if self._host is None:
             self._prepare_host()
         X = self._host
         n = self.batch
+        for name in ("q", "k", "v", "lens"):
+            np.copyto(X["H"][name], X["src"][name])
         lib = _L()
         ids, pos, tables, slots = X["ptrs"]
         _check(lib.pkv_get_block_tables(a, ids, n, self.max_blocks, tables), "pkv_get_block_tables")

@@ -299,7 +299,7 @@ def test_out_of_range_block_id_is_flagged_not_faulted(pkv):
     step.close()
 
 
-def test_bounded_waits_report_timeout_and_leave_the_context_usable(pkv, monkeypatch):
+def test_bounded_waits_report_timeout_and_leave_the_context_usable(pkv, stall_hooks):
     """Every mbarrier wait in the attention kernel is bounded.  With the test hooks the stages
     expect bytes no copy delivers and the waits give up after 20 ms: the call reports
     PKV_ERR_TIMEOUT, no fault, and the next normal call gives the same results as before."""
@@ -307,13 +307,11 @@ def test_bounded_waits_report_timeout_and_leave_the_context_usable(pkv, monkeypa
     w = W.custom_workload(306, 3, 8, 2, 128, 64, [300, 70, 900], append=False)
     step = _run(pkv, w)
     good = step.out_host().copy()
-    monkeypatch.setenv("PKV_TEST_WAIT_LIMIT_MS", "20")
-    monkeypatch.setenv("PKV_TEST_STALL_COPIES", "1")
+    stall_hooks[0]()
     step.attention()
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_TIMEOUT
-    monkeypatch.delenv("PKV_TEST_WAIT_LIMIT_MS")
-    monkeypatch.delenv("PKV_TEST_STALL_COPIES")
+    stall_hooks[1]()
     pkv.pkv_decode_workspace_init(step.workspace)  # merge tickets may have been left mid-count
     step.attention()
     torch.cuda.synchronize()
@@ -409,3 +407,49 @@ def test_fp8_encode_matches_oracle_on_ties_and_subnormals(pkv):
     assert np.array_equal(sc, ref.scales)
     assert np.array_equal(kv, ref.data)
     pkv.pkv_pool_destroy(handle)
+
+
+def _wide_range_queries(q_bits: np.ndarray, seed: int) -> np.ndarray:
+    """bf16 query rows whose magnitudes span 2^-30 .. 2^40 (the f16 range is about 2^-24 ..
+    65504): each row is the drawn N(0,1) row times 2^u for its own u, and a few rows mix
+    magnitudes inside the row or hold values just above 65504 or bf16 subnormals.  Every result
+    is a bf16 value (power-of-two multiples of bf16 values, or exactly written bits)."""
+    B, Hq, D = q_bits.shape
+    f = (q_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    rng = np.random.default_rng(seed)
+    u = rng.choice([-30, -24, -16, -14, -8, 0, 4, 12, 16, 17, 24, 32, 40], size=(B, Hq))
+    f = f * np.exp2(u)[:, :, None]
+    f[0, 0, : D // 2] *= 2.0 ** 40  # one row spanning 2^-30 .. 2^40 inside itself
+    f[0, 0, D // 2:] *= 2.0 ** -30
+    f[0, 1, :] = np.where(np.arange(D) % 3 == 0, 98304.0, f[0, 1, :])  # beyond f16's largest finite value
+    f[1, 0, :] = 69632.0 * np.where(f[1, 0, :] < 0, -1.0, 1.0)
+    bits = (f.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64), f), "not bf16 values"
+    bits[1, 1, :] = np.arange(1, D + 1, dtype=np.uint16) & 0x807F  # bf16 subnormals (and signs)
+    return bits
+
+
+@pytest.mark.parametrize("dtype", ["fp8_e4m3", "int8", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_queries_across_the_bf16_range(pkv, dtype, D):
+    """One-byte KV multiplies f16 operands: the query rows are scaled per head by a power of two
+    into f16's range, so queries far outside it (2^-30 .. 2^40, values > 65504, bf16 subnormals)
+    still give the oracle's result (the masked_mha decode of "TensorRT-LLM 推理加速实战" §7.2 with
+    a bf16 query).  Outputs within the low-precision bound of the oracle run on the same codes."""
+    import torch
+    lens = [1, 37, 300, 64, 513, 129, 900, 2]
+    w = W.custom_workload(320 + D, len(lens), 8, 2, D, 16, lens, append=True, kv_dtype=dtype)
+    step = _run(pkv, w)
+    q = _wide_range_queries(w.query(), 5 + D)
+    step.q.copy_(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(step.q.device))
+    step.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_OK
+    pool, _, tables = odrive.build(w)
+    ref = odrive.attention(w, pool, tables, q=q)
+    got, err = _errors(step, ref)
+    tol = TOL_FP8_MAX if dtype != "bf16" else TOL_BF16_MAX
+    assert np.isfinite(got).all()
+    assert err.max() <= tol, f"max |err| {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+    assert err.mean() <= TOL_MEAN, f"mean |err| {err.mean():.3e}"
+    step.close()

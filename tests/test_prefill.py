@@ -341,7 +341,7 @@ def test_chunked_prefill_with_rope_matches_oracle():
 
 
 @pytest.mark.gpu
-def test_prefill_bounded_waits_report_timeout_and_leave_the_context_usable(monkeypatch):
+def test_prefill_bounded_waits_report_timeout_and_leave_the_context_usable(stall_hooks):
     """Every mbarrier wait in the prefill kernel is bounded. With the test hooks each K/V stage
     expects bytes no copy delivers and the waits give up after 20 ms: the call reports
     PKV_ERR_TIMEOUT without a fault, tensor memory is released, and the next normal call gives the
@@ -355,13 +355,11 @@ def test_prefill_bounded_waits_report_timeout_and_leave_the_context_usable(monke
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
     good = st.out_host().copy()
-    monkeypatch.setenv("PKV_TEST_WAIT_LIMIT_MS", "20")
-    monkeypatch.setenv("PKV_TEST_STALL_COPIES", "1")
+    stall_hooks[0]()
     st.attention()
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_ERR_TIMEOUT
-    monkeypatch.delenv("PKV_TEST_WAIT_LIMIT_MS")
-    monkeypatch.delenv("PKV_TEST_STALL_COPIES")
+    stall_hooks[1]()
     st.out.zero_()
     st.attention()
     torch.cuda.synchronize()

@@ -3,15 +3,19 @@
 Some callers cannot hand the library a workspace: an engine that has already given almost
 all free device memory to its own KV pool, or a decode loop that must not call cudaMalloc
 because it can stall the device.  pkv_decode_attention_static serves them from a fixed scratch
-array inside the library.  These tests call it through the C ABI and check it against the
-workspace-taking entry point, twice in a row (the scratch keeps the previous call's contents),
-and check that a call needing more scratch than the fixed size is refused."""
+array inside the library.  These tests call it through the C ABI, twice in a row (the scratch
+keeps the previous call's contents), and require the same output bits as the workspace-taking
+entry point (the same plan and kernel run on both) and the oracle's result within tolerance.
+A call right after one whose bounded waits ran out (merge tickets left mid-count in the shared
+scratch) must give the same bits again, and a call needing more scratch than the fixed size is
+refused."""
 import ctypes
 
 import numpy as np
 import pytest
 
 import oracle
+import oracle.drive as odrive
 import pkv_workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -40,27 +44,66 @@ def _static_call(pkv, step, out):
         torch.cuda.current_stream().cuda_stream)
 
 
+def _bits(out):
+    import torch
+    return out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _workload(name):
+    if name == "long":  # one sequence split over every CTA: hundreds of partial states merged
+        return W.custom_workload(310, 1, 8, 1, 128, 64, [40000])
+    return W.make_workload(name)
+
+
 @pytest.mark.parametrize("name", ["c2", "c4", "long"])
 def test_static_scratch_matches_the_workspace_entry_point(pkv, name):
     import torch
     from paged_kv_cache_266_gb300.runner import DecodeStep
-    w = W.custom_workload(310, 1, 8, 1, 128, 64, [40000]) if name == "long" else W.make_workload(name)
+    w = _workload(name)
     step = DecodeStep(w)
     step.step()  # append, then attention with the caller-provided workspace
     torch.cuda.synchronize()
-    ref = oracle.bf16_bits_to_f64(step.out_host())
+    want = step.out_host().copy()
     need = pkv.pkv_decode_workspace_bytes(step.pool.handle, w.B, w.Hq, step.tables.shape[1])
     assert need <= pkv.PKV_STATIC_WORKSPACE_BYTES
+    pool, _, tables = odrive.build(w)
+    ref = odrive.attention(w, pool, tables)
     tol = TOL_FP8_MAX if w.kv_dtype == "fp8_e4m3" else TOL_MAX
     for _ in range(2):
         out = torch.full_like(step.out, float("nan"))
         assert _static_call(pkv, step, out) == pkv.PKV_OK
         torch.cuda.synchronize()
         assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_OK
-        got = oracle.bf16_bits_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
-        err = np.abs(got - ref)
-        assert np.isfinite(got).all()
+        got = _bits(out)
+        assert np.array_equal(got, want), "static scratch output differs from the workspace call's"
+        err = np.abs(oracle.bf16_bits_to_f64(got) - ref)
         assert err.max() <= tol and err.mean() <= TOL_MEAN, (err.max(), err.mean())
+    step.close()
+
+
+def test_static_scratch_after_a_timed_out_call(pkv, stall_hooks):
+    """The bounded-wait hooks make one static call give up (PKV_ERR_TIMEOUT, no fault) and leave
+    the shared scratch's merge tickets wherever they were; the next static call clears them itself
+    and gives the workspace call's bits."""
+    import torch
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    w = _workload("long")
+    step = DecodeStep(w)
+    step.step()
+    torch.cuda.synchronize()
+    want = step.out_host().copy()
+    stall_hooks[0]()
+    out = torch.zeros_like(step.out)
+    assert _static_call(pkv, step, out) == pkv.PKV_OK  # launched; the device reports the timeout
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_TIMEOUT
+    stall_hooks[1]()
+    for _ in range(2):
+        out = torch.full_like(step.out, float("nan"))
+        assert _static_call(pkv, step, out) == pkv.PKV_OK
+        torch.cuda.synchronize()
+        assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_OK
+        assert np.array_equal(_bits(out), want)
     step.close()
 
 
