@@ -739,7 +739,7 @@ def run_chunk_loop(args, world, rank, local):
     from paged_kv_cache_266_gb300 import build as pkv_build
     pkv_build.build()
     from paged_kv_cache_266_gb300 import pkv_check_device_error
-    from paged_kv_cache_266_gb300.engine import DecodeLoop
+    from paged_kv_cache_266_gb300.engine import ChunkedContextScheduler, DecodeLoop
     torch.cuda.set_device(local)
     n = args.warmup + args.steps
     sc = W.make_chunked_loop_script(index=55, n_steps=n, max_batch=args.loop_batch, Hq=32, Hkv=8, D=128,
@@ -754,20 +754,20 @@ def run_chunk_loop(args, world, rank, local):
             k, v, q = sc.prompt_rows(s, base, sc.system + m)
             prompts[s] = (to_dev(k), to_dev(v), to_dev(q))
     inputs = [None] * n
-    loop = DecodeLoop(sc, graphs=True, device=dev, prompts=prompts)
-    state: dict = {}
+    loop = DecodeLoop(sc, graphs=True, device=dev, prompts=prompts, system_seq=W.SYSTEM_SEQ)
+    sched = ChunkedContextScheduler(sc.chunk, sc.system, sc.reuse)  # the loop's schedule, ahead of time
     plans = []
     joined_at, first_decode = {}, {}
     for t in range(n):  # the decode inputs of each step, drawn before the timed region
-        for s_, _ in sc.steps[t][1]:
+        for s_ in sc.steps[t][0]:
+            sched.finish(s_)
+        for s_, m in sc.steps[t][1]:
             joined_at[s_] = t
-        pre, dec = sc.plan_step(t, state)
+            sched.admit(s_, m)
+        pre, dec = sched.plan()
+        sched.mark_decoded(dec)
         for s_ in dec:
             first_decode.setdefault(s_, t)
-        for s_, p0, p1 in pre:
-            state[s_][1] = p1
-        for s_ in dec:
-            state[s_][2] += 1
         plans.append((sum(p1 - p0 for _, p0, p1 in pre), len(dec)))
         inputs[t] = sc.step_inputs(t, dec) if dec else None
     for t in range(args.warmup):

@@ -74,6 +74,16 @@ pkv_status pkv_allocator_destroy(pkv_allocator* a);
  * no sequence holds blocks; order must be a permutation of 0..num_blocks-1. */
 pkv_status pkv_allocator_set_free_order(pkv_allocator* a, const int32_t* order_host, int n);
 
+/* Shuffle the current free list in place with a seeded Fisher-Yates (Durstenfeld) pass: for
+ * i = n-1 down to 1, swap entries i and j, where the k-th swap (k = 0, 1, ...) takes
+ * j = ((x_k >> 11) * (i + 1)) >> 53 and x_k is the k-th output of splitmix64 started from `seed`
+ * (x_k = mix(seed + (k + 1) * 0x9E3779B97F4A7C15), mix: z ^= z >> 30, z *= 0xBF58476D1CE4E5B9,
+ * z ^= z >> 27, z *= 0x94D049BB133111EB, z ^= z >> 31).  On a fresh allocator the list becomes
+ * that permutation of 0..num_blocks-1 (a seeded, fragmented allocation order for tests and
+ * benchmarks, "TensorRT-LLM 深度实战" §3.1's free-page list); blocks held by sequences are not
+ * affected.  Deterministic and identical on every platform. */
+pkv_status pkv_allocator_shuffle_free_list(pkv_allocator* a, uint64_t seed);
+
 /* Make seq_id able to hold n_tokens tokens: an unknown seq_id is created with
  * ceil(n_tokens / block_size) blocks, a known one takes ceil((n_tokens - capacity) /
  * block_size) more when n_tokens exceeds its capacity.  PKV_ERR_OOM if the free list is

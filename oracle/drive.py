@@ -47,6 +47,57 @@ def attention(w, pool, tables, threads: int | None = None, seqs=None, q=None) ->
     return pool.attention(q, tables, lens, w.Hq, 1.0 / math.sqrt(w.D), threads=threads or os.cpu_count() or 1)
 
 
+class ChunkedContextPlan:
+    """The chunked-context schedule of "TensorRT-LLM 深度实战" §7.3 (ChunkedContextScheduler), as
+    the oracle's own restatement: a request's input is cut into chunks of at most chunk_size
+    tokens; every step, each admitted request in admission order either processes its next chunk
+    (input[prefill_progress : prefill_progress + chunk_size], then the progress advances and the
+    request stops prefilling once the progress reaches the input's length) or, once it has
+    stopped prefilling, decodes one token.  So a request decodes from the step after its last
+    chunk.  With a shared system prompt of `system` tokens every input starts with it; when the
+    prompt is cached and forked (reuse), a request's progress starts at `system`."""
+
+    def __init__(self, chunk_size: int, system: int = 0, reuse: bool = True):
+        self.chunk_size, self.system, self.reuse = chunk_size, system, reuse
+        self.requests = []  # admission order: dicts with id, input_len, prefill_progress, is_prefilling, decoded
+
+    def step(self, finished, joined):
+        """Apply the step's departures and arrivals, then schedule it: returns ([(id, p0, p1)]
+        chunks, [decoding ids]), both in admission order."""
+        gone = set(finished)
+        for r in self.requests:
+            if r["id"] in gone and r["is_prefilling"]:
+                raise RuntimeError(f"request {r['id']} left while prefilling")
+        self.requests = [r for r in self.requests if r["id"] not in gone]
+        for rid, n in joined:
+            start = self.system if (self.system and self.reuse) else 0
+            self.requests.append({"id": rid, "input_len": self.system + n, "prefill_progress": start,
+                                  "is_prefilling": start < self.system + n, "decoded": 0})
+        chunks, decode = [], []
+        for r in self.requests:
+            if r["is_prefilling"]:
+                p0 = r["prefill_progress"]
+                p1 = min(r["input_len"], p0 + self.chunk_size)
+                chunks.append((r["id"], p0, p1))
+                r["prefill_progress"] = p1
+                if p1 >= r["input_len"]:
+                    r["is_prefilling"] = False
+            else:
+                decode.append(r["id"])
+        return chunks, decode
+
+    def cached(self, rid: int) -> int:
+        """Tokens request `rid` holds before its decode token of this step: its input plus the
+        tokens it decoded in earlier steps."""
+        r = next(r for r in self.requests if r["id"] == rid)
+        return r["input_len"] + r["decoded"]
+
+    def decoded(self, ids) -> None:
+        for r in self.requests:
+            if r["id"] in ids:
+                r["decoded"] += 1
+
+
 def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = None):
     """Replay a chunked-context decode loop ("TensorRT-LLM 深度实战" §7.3): each step, finished
     sequences release their pages; every prefilling sequence appends its next prompt chunk and
@@ -61,7 +112,7 @@ def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = N
     max_blocks = -(-sc.max_len // sc.block_size)
     scale = 1.0 / math.sqrt(sc.D)
     nthreads = threads or os.cpu_count() or 1
-    state: dict = {}
+    plan = ChunkedContextPlan(sc.chunk, sc.system, sc.reuse)
     outs = []
     if sc.system:  # the shared system prompt, cached once (prefix caching)
         from pkv_workloads import SYSTEM_SEQ
@@ -80,7 +131,7 @@ def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = N
                     raise RuntimeError(f"oracle loop: fork failed ({rc})")
                 if cs >= 0:
                     pool.copy_block(cs, cd)
-        prefill, decode = sc.plan_step(t, state)
+        prefill, decode = plan.step(sc.steps[t][0], sc.steps[t][1])
         out_pre = np.zeros((0, sc.Hq, sc.D))
         if prefill:
             ks, vs, qs, seqs, pos = [], [], [], [], []
@@ -99,11 +150,9 @@ def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = N
             tables = alloc.block_tables(ids, max_blocks)
             ctx = np.array([p1 for _, _, p1 in prefill], dtype=np.int32)
             out_pre = pool.prefill_attention(np.concatenate(qs), cu, tables, ctx, sc.Hq, scale, threads=nthreads)
-            for s, p0, p1 in prefill:
-                state[s][1] = p1
         out_dec = np.zeros((0, sc.Hq, sc.D))
         if decode:
-            lens = np.array([state[s][0] + state[s][2] for s in decode], dtype=np.int64)
+            lens = np.array([plan.cached(s) for s in decode], dtype=np.int64)
             for s, L in zip(decode, lens):
                 if alloc.reserve(s, int(L) + 1):
                     raise RuntimeError("oracle loop: out of pages")
@@ -111,8 +160,7 @@ def run_chunked_loop(script, n_steps: int | None = None, threads: int | None = N
             pool.append(k, v, alloc.slot_mapping(decode, lens))
             tables = alloc.block_tables(decode, max_blocks)
             out_dec = pool.attention(q, tables, (lens + 1).astype(np.int32), sc.Hq, scale, threads=nthreads)
-            for s in decode:
-                state[s][2] += 1
+            plan.decoded(set(decode))
         outs.append((list(decode), out_dec, list(prefill), out_pre))
     return outs, pool
 

@@ -17,7 +17,8 @@ from . import build as _build
 
 __all__ = [
     "PKVError", "PKV_KV_BF16", "PKV_KV_FP8_E4M3", "PKV_KV_INT8", "KV_DTYPES", "library_path",
-    "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order", "pkv_seq_reserve",
+    "pkv_allocator_create", "pkv_allocator_destroy", "pkv_allocator_set_free_order",
+    "pkv_allocator_shuffle_free_list", "pkv_seq_reserve",
     "pkv_seq_release", "pkv_seq_reserve_many", "pkv_seq_share_prefix", "pkv_block_refcount",
     "pkv_pool_copy_block", "pkv_append_rope", "pkv_decode_step_rope", "pkv_prefill_attention", "pkv_prefill_step", "pkv_seq_num_blocks", "pkv_num_free_blocks", "pkv_free_list", "pkv_get_block_tables",
     "pkv_slot_mapping", "pkv_stage_prefill", "pkv_stage_decode", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocator", "pkv_pool_raw",
@@ -58,6 +59,7 @@ def _L():
         "pkv_allocator_create": (i32, [i32, i32, P(vp)]),
         "pkv_allocator_destroy": (i32, [vp]),
         "pkv_allocator_set_free_order": (i32, [vp, vp, i32]),
+        "pkv_allocator_shuffle_free_list": (i32, [vp, ctypes.c_uint64]),
         "pkv_seq_reserve": (i32, [vp, i64, i64]),
         "pkv_seq_release": (i32, [vp, i64]),
         "pkv_seq_reserve_many": (i32, [vp, vp, vp, i64, P(i64)]),
@@ -142,6 +144,10 @@ def pkv_allocator_destroy(a: int) -> None:
 def pkv_allocator_set_free_order(a: int, order) -> None:
     o = _np(order, np.int32)
     _check(_L().pkv_allocator_set_free_order(a, o.ctypes.data, len(o)), "pkv_allocator_set_free_order")
+
+
+def pkv_allocator_shuffle_free_list(a: int, seed: int) -> None:
+    _check(_L().pkv_allocator_shuffle_free_list(a, seed & ((1 << 64) - 1)), "pkv_allocator_shuffle_free_list")
 
 
 def pkv_seq_reserve(a: int, seq_id: int, n_tokens: int) -> None:

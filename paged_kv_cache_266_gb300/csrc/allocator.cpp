@@ -16,6 +16,7 @@
 #include <cstring>
 #include <new>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "pkv_internal.h"
@@ -76,6 +77,29 @@ pkv_status pkv_allocator_set_free_order(pkv_allocator* a, const int32_t* order, 
         seen[order[i]] = 1;
     }
     std::memcpy(a->free_list.data(), order, sizeof(int32_t) * (size_t)n);
+    return PKV_OK;
+}
+
+// Seeded shuffle of the free list: Fisher-Yates in Durstenfeld's form (positions n-1 down to 1,
+// each swapped with a uniformly chosen position at or below it), the k-th swap partner drawn
+// from the k-th output of splitmix64 (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", 2014: state advanced by the golden-ratio increment, then the mix with
+// shifts 30 / 27 / 31 and the two published multipliers).  A partner in [0, i] is the top 53 bits
+// of the draw times i + 1, shifted down by 53 (multiply-shift, no modulo bias beyond 2^-53).
+pkv_status pkv_allocator_shuffle_free_list(pkv_allocator* a, uint64_t seed) {
+    if (!a) return PKV_ERR_INVALID_ARG;
+    std::vector<int32_t>& f = a->free_list;
+    uint64_t k = 0;
+    for (size_t i = f.size(); i-- > 1;) {
+        uint64_t z = seed + (k + 1) * 0x9E3779B97F4A7C15ull;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        z ^= z >> 31;
+        ++k;
+        const unsigned __int128 prod = (unsigned __int128)(z >> 11) * (unsigned __int128)(i + 1);
+        const size_t j = (size_t)(prod >> 53);
+        std::swap(f[i], f[j]);
+    }
     return PKV_OK;
 }
 

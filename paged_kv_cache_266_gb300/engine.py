@@ -38,6 +38,59 @@ from . import (KV_DTYPES, KVPool, pkv_append, pkv_decode_step, pkv_decode_worksp
 DEFAULT_BUCKETS = (8, 16, 32, 64, 128, 256, 512, 1024)
 
 
+class ChunkedContextScheduler:
+    """Chunked context ("TensorRT-LLM 深度实战" §7.3): a joining request's input is processed in
+    pieces of at most `chunk` tokens, one piece per step, while the other requests decode; a
+    request decodes from the step after its last piece.  Requests are kept in admission order.
+
+    With a shared system prompt of `system` tokens every input starts with it; if the prompt is
+    cached once and forked into each request (`reuse`, "TensorRT-LLM 推理加速实战" §8 KV cache
+    reuse), a request's prefill starts after it.  Pure host bookkeeping, no device work."""
+
+    def __init__(self, chunk: int, system: int = 0, reuse: bool = True):
+        if chunk < 1:
+            raise ValueError("chunk must be positive")
+        self.chunk, self.system, self.reuse = chunk, system, reuse
+        self._req: dict[int, list[int]] = {}  # seq -> [input tokens, prefilled, decoded], admission order
+
+    def __len__(self) -> int:
+        return len(self._req)
+
+    def finish(self, seq: int) -> None:
+        """A decoding request leaves (a request still prefilling cannot finish)."""
+        n, done, _ = self._req[seq]
+        if done < n:
+            raise ValueError(f"sequence {seq} finished before its prompt was prefilled")
+        del self._req[seq]
+
+    def admit(self, seq: int, prompt_tokens: int) -> None:
+        if seq in self._req:
+            raise ValueError(f"sequence {seq} is already admitted")
+        self._req[seq] = [self.system + prompt_tokens, self.system if self.reuse else 0, 0]
+
+    def plan(self):
+        """This step's work: ([(seq, p0, p1)] pieces prefilled now, positions p0..p1-1; [seq]
+        decoding).  The pieces count as prefilled from here on."""
+        prefill, decode = [], []
+        for seq, r in self._req.items():
+            if r[1] < r[0]:
+                p1 = min(r[0], r[1] + self.chunk)
+                prefill.append((seq, r[1], p1))
+                r[1] = p1
+            else:
+                decode.append(seq)
+        return prefill, decode
+
+    def cached(self, seq: int) -> int:
+        """Tokens `seq` holds before this step's decode token: its input and its decoded tokens."""
+        r = self._req[seq]
+        return r[0] + r[2]
+
+    def mark_decoded(self, seqs) -> None:
+        for seq in seqs:
+            self._req[seq][2] += 1
+
+
 class _Bucket:
     """Device buffers, pinned staging and (optionally) the captured graph for one batch size."""
 
@@ -108,7 +161,7 @@ class _PrefillStaging:
 
 class DecodeLoop:
     def __init__(self, script, graphs: bool = True, buckets=DEFAULT_BUCKETS, device: str = "cuda",
-                 prompts=None):
+                 prompts=None, system_seq: int | None = None):
         """prompts: optional {seq_id: (k, v)} of device bf16 tensors [n][Hkv][D] (a joining
         sequence's prompt K/V as its prefill produced them; with chunked context (a script with
         chunk > 0) (k, v, q), q [n][Hq][D] the prompt's queries, rows from the first position the
@@ -117,7 +170,10 @@ class DecodeLoop:
         Chunked context (script.chunk > 0, "TensorRT-LLM 深度实战" §7.3): a joining sequence's
         prompt is prefilled `chunk` tokens per step (its chunk's K/V appended and its queries
         attending causally, one pkv_prefill_step for all prefilling sequences of the step) and
-        the sequence decodes from the step after its last chunk."""
+        the sequence decodes from the step after its last chunk.
+
+        system_seq: the sequence id under which a script's shared system prompt is cached (any id
+        no request uses; needed when the script has a system prompt and reuses it)."""
         import torch
         self.prompts = prompts or {}
         self.torch, self.script, self.graphs, self.device = torch, script, graphs, device
@@ -131,15 +187,17 @@ class DecodeLoop:
         self.running: list[int] = []
         self.t = 0
         self.timing = {"admit_s": 0.0, "prepare_s": 0.0, "device_s": 0.0}  # host wall time per phase
-        self.state: dict = {}  # chunked context: seq -> [prompt_len, prefilled, decoded]
-        if script.chunk and script.system:
+        self.scheduler = (ChunkedContextScheduler(script.chunk, script.system, script.reuse) if script.chunk
+                          else None)
+        self.system_seq = system_seq
+        if script.chunk and script.system and script.reuse:
             # prefix caching ("TensorRT-LLM 推理加速实战" §8, KV cache reuse): the shared system
             # prompt is cached once under its own sequence; joiners fork it
-            from pkv_workloads import SYSTEM_SEQ
-            self.system_seq = SYSTEM_SEQ
+            if system_seq is None:
+                raise ValueError("a script with a cached system prompt needs system_seq")
             k, v = script.system_kv()
-            pkv_seq_reserve(self.alloc, SYSTEM_SEQ, script.system)
-            slots = pkv_slot_mapping(self.alloc, [SYSTEM_SEQ] * script.system, np.arange(script.system))
+            pkv_seq_reserve(self.alloc, system_seq, script.system)
+            slots = pkv_slot_mapping(self.alloc, [system_seq] * script.system, np.arange(script.system))
             to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
             pkv_append(self.pool.handle, to_dev(k), to_dev(v), torch.from_numpy(slots).to(device))
         self.last_prefill = ([], None)  # chunked context: (chunks [(seq, p0, p1)], output bits)
@@ -227,8 +285,6 @@ class DecodeLoop:
         cat = (lambda xs: xs[0]) if n == 1 else torch.cat  # one sequence: its rows are contiguous already
         pkv_prefill_step(self.pool.handle, cat(ks), cat(vs), S.D["slots"][:total], cat(qs),
                          S.D["cu"][:n + 1], int(counts.max()), S.D["tables"][:n], S.D["ctx"][:n], self.scale, out)
-        for s, _, p1 in prefill:
-            self.state[s][1] = p1
         return out
 
     def step(self, inputs=None):
@@ -242,21 +298,22 @@ class DecodeLoop:
         for s in finished:
             pkv_seq_release(self.alloc, s)
             if sc.chunk:
+                self.scheduler.finish(s)
                 continue
             self.running.remove(s)
             del self.lens[s]
         if sc.chunk:
-            if sc.system and sc.reuse:  # joiners fork the cached system prompt (partial block copied)
-                for s, _ in joined:
+            for s, m in joined:
+                if sc.system and sc.reuse:  # the joiner forks the cached system prompt (partial block copied)
                     cs, cd = pkv_seq_share_prefix(self.alloc, self.system_seq, s, sc.system)
                     if cs >= 0:
                         pkv_pool_copy_block(self.pool.handle, cs, cd)
-            prefill, decode = sc.plan_step(self.t, self.state)
+                self.scheduler.admit(s, m)
+            prefill, decode = self.scheduler.plan()
             pre_out = self._prefill_chunks(prefill) if prefill else None
             self.running = decode
-            self.lens = {s: self.state[s][0] + self.state[s][2] for s in decode}
-            for s in decode:
-                self.state[s][2] += 1
+            self.lens = {s: self.scheduler.cached(s) for s in decode}
+            self.scheduler.mark_decoded(decode)
             self.last_prefill = (prefill, pre_out)
         elif joined:
             self._admit(joined)

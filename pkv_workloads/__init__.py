@@ -392,26 +392,6 @@ class LoopScript:
         return normal_bf16(stream_seed(self.seed, TAG_LOOP_PROMPT_Q), off, (p1 - p0) * row).reshape(p1 - p0, self.Hq,
                                                                                                       self.D)
 
-    def plan_step(self, t: int, state: dict):
-        """Chunked context ("TensorRT-LLM 深度实战", §7.3): what step t does, given `state` (the
-        sequences admitted and not finished, in admission order: seq -> [prompt_len, prefilled,
-        cached]).  Applies step t's finishes and joins to `state` and returns (prefill, decode):
-        prefill = [(seq, p0, p1)] chunks of prompt tokens processed this step, decode = the
-        sequences (prompt done before this step) that append one token and attend.  After the
-        step the caller adds p1 - p0 to `prefilled` and one token to `cached` of the decoders."""
-        finished, joined = self.steps[t]
-        for s in finished:
-            del state[s]
-        for s, n in joined:  # with prefix caching the request starts with the system prompt cached
-            state[s] = [self.system + n, self.system if self.reuse else 0, 0]
-        prefill, decode = [], []
-        for s, (n, done, cached) in state.items():
-            if done < n:
-                prefill.append((s, done, min(n, done + self.chunk)))
-            else:
-                decode.append(s)
-        return prefill, decode
-
     def prompt_kv(self, seq_id: int, n: int):
         """History K and V ([n][Hkv][D] bf16 bits) of a joining sequence's prompt."""
         row = self.Hkv * self.D

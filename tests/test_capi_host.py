@@ -289,3 +289,50 @@ def test_stage_calls_match_the_oracle_allocator(pkv):
             del held[s_]
         assert pkv.pkv_free_list(a).tolist() == o.free_list().tolist()
     pkv.pkv_allocator_destroy(a)
+
+
+def _golden_splitmix():
+    rows = []
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "splitmix64.txt")):
+        if line.strip() and not line.startswith("#"):
+            seed, i, out = line.split()
+            rows.append((int(seed), int(i), int(out, 16)))
+    return rows
+
+
+def test_input_generator_splitmix64_matches_its_published_outputs():
+    """The seeded inputs of every workload come from splitmix64; its published reference outputs
+    pin the generator (and, through the shuffle test below, the library's own restatement)."""
+    import pkv_workloads as W
+    for seed, i, out in _golden_splitmix():
+        assert W.splitmix64_at(seed, i) == out
+
+
+def test_shuffle_free_list_is_the_workloads_seeded_permutation(pkv):
+    """pkv_allocator_shuffle_free_list on a fresh allocator gives the generator's seeded
+    Fisher-Yates permutation, so a C caller reproduces the workloads' allocation state from the
+    seed alone; on a list that is no longer 0..n-1 it applies the same permutation to the
+    entries; held blocks are untouched."""
+    import pkv_workloads as W
+    for n in (1, 2, 3, 32, 1000, 8192):
+        for seed in (0, 1, 266002, 2 ** 64 - 1, W.stream_seed(266 * 1000 + 2, W.TAG_PERM)):
+            a = pkv.pkv_allocator_create(n, 16)
+            pkv.pkv_allocator_shuffle_free_list(a, seed)
+            assert np.array_equal(pkv.pkv_free_list(a), W.permutation(seed, n)), (n, seed)
+            pkv.pkv_allocator_destroy(a)
+    w = W.make_workload("c2")
+    a = pkv.pkv_allocator_create(w.num_blocks, w.block_size)
+    pkv.pkv_allocator_shuffle_free_list(a, W.stream_seed(w.seed, W.TAG_PERM))
+    assert np.array_equal(pkv.pkv_free_list(a), w.free_order)
+    pkv.pkv_allocator_destroy(a)
+    # after some allocation: the remaining entries are permuted, the held blocks stay held
+    a = pkv.pkv_allocator_create(64, 16)
+    pkv.pkv_seq_reserve(a, 7, 16 * 5)
+    pkv.pkv_seq_reserve(a, 8, 16 * 3)
+    pkv.pkv_seq_release(a, 7)
+    before = pkv.pkv_free_list(a)
+    held = pkv.pkv_get_block_tables(a, [8], 3)[0]
+    pkv.pkv_allocator_shuffle_free_list(a, 99)
+    assert np.array_equal(pkv.pkv_free_list(a), before[W.permutation(99, len(before))])
+    assert np.array_equal(pkv.pkv_get_block_tables(a, [8], 3)[0], held)
+    pkv.pkv_allocator_destroy(a)

@@ -63,25 +63,91 @@ def test_decode_loop_matches_oracle_every_step(kv_dtype, bs, graphs):
     loop.close()
 
 
-def test_chunked_loop_schedule_matches_its_generator():
-    """The per-step plan (prefill chunks, decoders) replays the generator's state: every prompt
-    is prefilled in chunks of at most `chunk` tokens covering it exactly once, a sequence decodes
-    only after its prompt, and only decoding sequences finish."""
-    sc = W.make_chunked_loop_script(index=46, n_steps=40, chunk=48)
-    state, covered = {}, {}
-    for t in range(len(sc.steps)):
-        finished, joined = sc.steps[t]
-        for s in finished:
-            assert state[s][1] == state[s][0], "a sequence finished while prefilling"
-        prefill, decode = sc.plan_step(t, state)
-        for s, p0, p1 in prefill:
-            assert p0 == covered.get(s, 0) and 0 < p1 - p0 <= sc.chunk and p1 <= state[s][0]
-            covered[s] = p1
-            state[s][1] = p1
-        for s in decode:
-            assert state[s][1] == state[s][0] and s not in [c[0] for c in prefill]
-            state[s][2] += 1
-        assert len(state) <= sc.max_batch
+def _golden_schedules():
+    """Cases of tests/golden/chunked_schedule.txt: (name, chunk, system, reuse, steps), steps a
+    list of (finished, joined, expected chunks, expected decoders)."""
+    import os
+    cases = []
+    ids = lambda f: [] if f == "-" else [int(x) for x in f.split(",")]
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "chunked_schedule.txt")):
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "case":
+            cases.append((f[1], int(f[3]), int(f[5]), bool(int(f[7])), []))
+        else:  # step t fin F join J => pre P dec D
+            join = [] if f[5] == "-" else [tuple(int(y) for y in x.split(":")) for x in f[5].split(",")]
+            pre = [] if f[8] == "-" else [(int(x.split(":")[0]),) + tuple(int(y) for y in x.split(":")[1].split("-"))
+                                          for x in f[8].split(",")]
+            cases[-1][4].append((ids(f[3]), join, pre, ids(f[10])))
+    return cases
+
+
+def test_oracle_chunk_plan_matches_the_hand_traced_schedules():
+    """The oracle's chunked-context planner against schedules traced by hand from the page's
+    scheduler (joins, finishes, a prompt shorter than one chunk, a forked system prompt)."""
+    for name, chunk, system, reuse, steps in _golden_schedules():
+        plan = odrive.ChunkedContextPlan(chunk, system, reuse)
+        for t, (fin, join, pre, dec) in enumerate(steps):
+            assert plan.step(fin, join) == (pre, dec), (name, t)
+
+
+def _oracle_plans(sc):
+    plan = odrive.ChunkedContextPlan(sc.chunk, sc.system, sc.reuse)
+    return [plan.step(f, j) for f, j in sc.steps]
+
+
+@pytest.mark.parametrize("index,chunk,system,reuse", [(46, 48, 0, True), (47, 7, 0, True), (48, 48, 70, True),
+                                                      (49, 16, 70, False), (50, 1, 5, True)])
+def test_engine_scheduler_matches_the_oracle_plan(index, chunk, system, reuse):
+    """The engine's scheduler and the oracle's planner, written separately, plan every step of
+    the hand-traced cases and of seeded churn scripts identically."""
+    from paged_kv_cache_266_gb300.engine import ChunkedContextScheduler
+    scripts = [(steps, c, sy, r) for _, c, sy, r, steps in _golden_schedules()]
+    sc = W.make_chunked_loop_script(index=index, n_steps=40, chunk=chunk, system=system, reuse=reuse)
+    scripts.append(([(f, j, None, None) for f, j in sc.steps], chunk, system, reuse))
+    for steps, c, sy, r in scripts:
+        eng = ChunkedContextScheduler(c, sy, r)
+        ora = odrive.ChunkedContextPlan(c, sy, r)
+        for fin, join, _, _ in steps:
+            for s in fin:
+                eng.finish(s)
+            for s, m in join:
+                eng.admit(s, m)
+            got = eng.plan()
+            want = ora.step(fin, join)
+            assert got == want
+            for s in got[1]:
+                assert eng.cached(s) == ora.cached(s)
+            eng.mark_decoded(got[1])
+            ora.decoded(set(want[1]))
+
+
+def test_chunk_plans_cover_every_prompt_once():
+    """Invariants of the oracle's plan on seeded scripts: every prompt is prefilled in order, in
+    pieces of at most `chunk` tokens covering it exactly once; a sequence decodes only after its
+    last piece (from the next step on); only sequences whose prompt is done finish."""
+    for index, chunk, system, reuse in [(46, 48, 0, True), (48, 48, 70, True), (49, 16, 70, False)]:
+        sc = W.make_chunked_loop_script(index=index, n_steps=40, chunk=chunk, system=system, reuse=reuse)
+        covered, need, decoding, just_done = {}, {}, set(), set()
+        for (fin, join), (pre, dec) in zip(sc.steps, _oracle_plans(sc)):
+            for s in fin:
+                assert covered[s] == need[s], "a sequence finished while prefilling"
+                decoding.discard(s)
+                just_done.discard(s)
+            assert just_done <= set(dec), "a prefilled sequence did not decode in the next step"
+            for s, m in join:
+                need[s] = system + m
+                covered[s] = system if (system and reuse) else 0
+            for s, p0, p1 in pre:
+                assert p0 == covered[s] and 0 < p1 - p0 <= chunk and p1 <= need[s]
+                covered[s] = p1
+            assert not set(dec) & {s for s, _, _ in pre}
+            for s in dec:
+                assert covered[s] == need[s]
+            just_done = {s for s, _, p1 in pre if p1 == need[s]}
+            decoding |= set(dec)
+        assert decoding, "the script never decodes"
 
 
 @pytest.mark.gpu
@@ -134,7 +200,7 @@ def test_chunked_loop_with_cached_system_prompt_matches_oracle(reuse):
     from paged_kv_cache_266_gb300.engine import DecodeLoop
     sc = W.make_chunked_loop_script(index=48, n_steps=16, block_size=16, chunk=48, system=70, reuse=reuse)
     ref, pool = odrive.run_chunked_loop(sc)
-    loop = DecodeLoop(sc, graphs=True)
+    loop = DecodeLoop(sc, graphs=True, system_seq=W.SYSTEM_SEQ)
     for t in range(len(sc.steps)):
         run, out = loop.step()
         assert run == ref[t][0]
@@ -152,5 +218,5 @@ def test_chunked_loop_with_cached_system_prompt_matches_oracle(reuse):
     from paged_kv_cache_266_gb300.runner import _wrap_device
     assert np.array_equal(_wrap_device(kv, kv_bytes).cpu().numpy(), pool.data)
     first = int(pkv.pkv_get_block_tables(loop.alloc, [W.SYSTEM_SEQ], 5)[0, 0])
-    assert pkv.pkv_block_refcount(loop.alloc, first) == (1 + len(loop.state) if reuse else 1)
+    assert pkv.pkv_block_refcount(loop.alloc, first) == (1 + len(loop.scheduler) if reuse else 1)
     loop.close()
