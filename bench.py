@@ -266,7 +266,8 @@ def measure_decode(w, args, world, local, stream):
         step.limit_batch(args.seqs)
         w = W.truncated(w, args.seqs)
     nbytes = algorithmic_bytes(w)
-    launches_per_step = (0 if not w.append else (1 if w.kv_dtype == "bf16" else 3)) + 1
+    # append kernels per step (bf16: one; one-byte KV: one up to 1024 tokens, else three) + attention
+    launches_per_step = (0 if not w.append else (1 if w.kv_dtype == "bf16" or w.B <= 1024 else 3)) + 1
 
     for _ in range(args.warmup):
         step.step()

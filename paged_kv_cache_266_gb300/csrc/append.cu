@@ -11,8 +11,10 @@
 // cache) and int8 pools (the same with amax/127 and symmetric int8 codes): one fp32 scale per
 // (block, K|V, head).  A block's scales are derived by the call
 // that writes its offset 0, as amax/448 over that call's tokens in the block (1 when the
-// amax is 0); later calls reuse them and saturate.  Three short passes do this without any
-// grid-wide synchronisation inside a kernel:
+// amax is 0); later calls reuse them and saturate.  Calls of up to 1024 tokens (decode steps)
+// do this in one kernel, a warp per token that finds the call's other tokens in its block by
+// scanning the call's slots (quant_append_small_kernel).  Larger calls take three short passes,
+// with no grid-wide synchronisation inside a kernel:
 //   1. amax: per row |x| max, atomicMax into a per-(block, K|V, head) scratch word, and a
 //      per-block "offset 0 written" flag;
 //   2. quantise: derive/lookup the scale, x / scale (IEEE division), RNE-satfinite to E4M3;
@@ -75,6 +77,18 @@ __global__ void __launch_bounds__(kAppendThreads) append_bf16_kernel(uint16_t* _
     *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
 }
 
+// max |x| over eight bf16 elements, as fp32 bits (non-negative floats order like their bits)
+__device__ __forceinline__ uint32_t amax_bits(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = (w[e] << 16) & 0x7fffffffu, hi = w[e] & 0x7fff0000u;
+        m = max(m, max(lo, hi));
+    }
+    return m;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) fp8_amax_kernel(const uint16_t* __restrict__ k_new,
                                                                    const uint16_t* __restrict__ v_new,
@@ -91,13 +105,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_amax_kernel(const uint16_t
     RowIndex r{0, 0, 0};
     if (in_range) {
         r = row_index(row, Hkv);
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>((r.kv ? v_new : k_new) + (r.i * Hkv + r.h) * D + part * 8));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t lo = (w[e] << 16) & 0x7fffffffu, hi = w[e] & 0x7fff0000u;
-            m = max(m, max(lo, hi));
-        }
+        m = amax_bits(__ldg(reinterpret_cast<const uint4*>((r.kv ? v_new : k_new) + (r.i * Hkv + r.h) * D + part * 8)));
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -118,6 +126,34 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_amax_kernel(const uint16_t
 __device__ __forceinline__ uint32_t int8_code(float q) {
     const int c = __float2int_rn(q);
     return (uint32_t)(c < -127 ? -127 : (c > 127 ? 127 : c)) & 0xffu;
+}
+
+// Quantise eight elements (part `part` of a row: elements 8*part .. 8*part+7) of token slot t of
+// block blk, K (kv = 0) or V (kv = 1) of head h, with scale s: x / s as an IEEE fp32 division, then
+// E4M3 round-to-nearest-even with saturation (or the int8 code), stored in the pool's layout.
+template <int D, bool I8>
+__device__ __forceinline__ void quant_store(uint8_t* __restrict__ pool, uint4 v, float s, int64_t blk, int t, int kv,
+                                            int h, int part, int Hkv, int bs) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t codes[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const float x0 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e]), s), x1 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e]), s);
+        const float x2 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e + 1]), s),
+                    x3 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e + 1]), s);
+        if constexpr (I8)
+            codes[e] = int8_code(x0) | (int8_code(x1) << 8) | (int8_code(x2) << 16) | (int8_code(x3) << 24);
+        else
+            codes[e] = ptx::f32x2_to_e4m3x2(x0, x1) | (ptx::f32x2_to_e4m3x2(x2, x3) << 16);
+    }
+    uint8_t* tile = pool + tile_elem(blk, kv, h, Hkv, bs, D);
+    if (kv == 0) {
+        *reinterpret_cast<uint2*>(tile + (int64_t)t * D + part * 8) = make_uint2(codes[0], codes[1]);
+    } else {
+        uint8_t* panel = tile + (int64_t)(t >> 4) * D * 16 + fp8_v_pos(t & 15);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) panel[(int64_t)(part * 8 + e) * 16] = (uint8_t)(codes[e >> 2] >> (8 * (e & 3)));
+    }
 }
 
 template <int D, bool I8>
@@ -151,26 +187,7 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_quant_kernel(uint8_t* __re
         s = *sp;
     }
     const uint4 v = __ldg(reinterpret_cast<const uint4*>((r.kv ? v_new : k_new) + (r.i * Hkv + r.h) * D + part * 8));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t codes[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const float x0 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e]), s), x1 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e]), s);
-        const float x2 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e + 1]), s),
-                    x3 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e + 1]), s);
-        if constexpr (I8)
-            codes[e] = int8_code(x0) | (int8_code(x1) << 8) | (int8_code(x2) << 16) | (int8_code(x3) << 24);
-        else
-            codes[e] = ptx::f32x2_to_e4m3x2(x0, x1) | (ptx::f32x2_to_e4m3x2(x2, x3) << 16);
-    }
-    uint8_t* tile = pool + tile_elem(blk, r.kv, r.h, Hkv, bs, D);
-    if (r.kv == 0) {
-        *reinterpret_cast<uint2*>(tile + (int64_t)t * D + part * 8) = make_uint2(codes[0], codes[1]);
-    } else {
-        uint8_t* panel = tile + (int64_t)(t >> 4) * D * 16 + fp8_v_pos(t & 15);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) panel[(int64_t)(part * 8 + e) * 16] = (uint8_t)(codes[e >> 2] >> (8 * (e & 3)));
-    }
+    quant_store<D, I8>(pool, v, s, blk, t, r.kv, r.h, part, Hkv, bs);
 }
 
 template <int D>
@@ -189,6 +206,87 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_reset_kernel(const int64_t
     const int64_t blk = slot / bs;
     amax[(blk * Hkv + r.h) * 2 + r.kv] = 0u;
     if (r.kv == 0 && r.h == 0) fresh[blk] = 0;
+}
+
+// One-pass quantising append for calls of up to kSmallAppendTokens tokens (a decode step appends
+// one token per sequence): the same stored bytes and scales as the three passes above, in one
+// launch.  One warp per token.  Every warp first scans the call's slots (staged in shared memory)
+// for the other tokens landing in its block: if the call writes the block's offset 0 ("fresh"),
+// the scale of each (K|V, head) row is amax/448 (amax/127 for int8) over the row and the same rows
+// of those other tokens, which every token of the block computes alike; otherwise the stored scale
+// is read (no token of this call writes it).  The usual decode step has no such other token, so a
+// fresh block's scale comes from the token's own row.
+constexpr int kSmallAppendTokens = 1024;
+
+template <int D, bool I8>
+__global__ void __launch_bounds__(kAppendThreads) quant_append_small_kernel(uint8_t* __restrict__ pool,
+                                                                             float* __restrict__ scales,
+                                                                             const uint16_t* __restrict__ k_new,
+                                                                             const uint16_t* __restrict__ v_new,
+                                                                             const int64_t* __restrict__ slots, int N,
+                                                                             int Hkv, int bs, int num_blocks, int* err) {
+    ptx::grid_launch_dependents();  // a following decode step may begin its set-up
+    constexpr int TPR = D / 8;        // lanes per row (8 elements each)
+    constexpr int RPI = 32 / TPR;     // rows per warp iteration
+    __shared__ int64_t s_slot[kSmallAppendTokens];
+    for (int j = threadIdx.x; j < N; j += blockDim.x) s_slot[j] = __ldg(slots + j);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5);  // this warp's token
+    if (i >= N) return;
+    const int64_t cap = (int64_t)num_blocks * bs;
+    const int64_t slot = s_slot[i];
+    if (slot < 0) return;
+    if (slot >= cap) {
+        if (lane == 0) atomicOr(err, kErrBounds);
+        return;
+    }
+    const int64_t blk = slot / bs;
+    const int t = (int)(slot - blk * bs);
+    // other tokens of the call in this block, and whether the call writes the block's offset 0
+    bool mates = false, fresh = t == 0;
+    for (int j0 = 0; j0 < N; j0 += 32) {
+        const int j = j0 + lane;
+        bool same = false, zero = false;
+        if (j < N && j != i) {
+            const int64_t sj = s_slot[j];
+            if (sj >= 0 && sj < cap && sj / bs == blk) {
+                same = true;
+                zero = sj - blk * bs == 0;
+            }
+        }
+        mates |= __any_sync(0xffffffffu, same);
+        fresh |= __any_sync(0xffffffffu, zero);
+    }
+    const int part = lane % TPR;
+    for (int r0 = 0; r0 < 2 * Hkv; r0 += RPI) {  // same trip count for every lane of the warp
+        const int r = r0 + lane / TPR;
+        const bool act = r < 2 * Hkv;
+        const int kv = act ? r / Hkv : 0, h = act ? r - kv * Hkv : 0;
+        const uint16_t* src = kv ? v_new : k_new;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (act) v = __ldg(reinterpret_cast<const uint4*>(src + ((int64_t)i * Hkv + h) * D + part * 8));
+        float s = 1.0f;
+        if (fresh) {
+            uint32_t m = act ? amax_bits(v) : 0u;
+            if (mates && act) {  // rare: several tokens of the call share the block
+                for (int j = 0; j < N; ++j) {
+                    const int64_t sj = s_slot[j];
+                    if (j == i || sj < 0 || sj >= cap || sj / bs != blk) continue;
+                    m = max(m, amax_bits(__ldg(reinterpret_cast<const uint4*>(src + ((int64_t)j * Hkv + h) * D +
+                                                                                 part * 8))));
+                }
+            }
+#pragma unroll
+            for (int o = TPR / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float a = __uint_as_float(m);
+            s = a > 0.0f ? __fdiv_rn(a, I8 ? 127.0f : 448.0f) : 1.0f;
+            if (act && t == 0 && part == 0) scales[(blk * Hkv + h) * 4 + kv] = s;
+        } else if (act) {
+            s = scales[(blk * Hkv + h) * 4 + kv];
+        }
+        if (act) quant_store<D, I8>(pool, v, s, blk, t, kv, h, part, Hkv, bs);
+    }
 }
 
 // ------------------------------------------------------------------ RoPE fused into the append
@@ -367,6 +465,18 @@ pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, cons
     if (p->dtype == PKV_KV_BF16) {
         append_bf16_kernel<D><<<grid, kAppendThreads, 0, st>>>(static_cast<uint16_t*>(p->kv), k, v, slots, N,
                                                                p->n_kv_heads, p->block_size, p->num_blocks, p->err);
+    } else if (N <= kSmallAppendTokens) {
+        // one pass: a warp per token
+        const dim3 g1((unsigned)((N + kAppendThreads / 32 - 1) / (kAppendThreads / 32)));
+        uint8_t* const kv8 = static_cast<uint8_t*>(p->kv);
+        if (p->dtype == PKV_KV_INT8)
+            quant_append_small_kernel<D, true><<<g1, kAppendThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
+                                                                            p->n_kv_heads, p->block_size,
+                                                                            p->num_blocks, p->err);
+        else
+            quant_append_small_kernel<D, false><<<g1, kAppendThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
+                                                                             p->n_kv_heads, p->block_size,
+                                                                             p->num_blocks, p->err);
     } else {
         // three kernels in a chain of programmatic dependents: the amax kernel waits for the
         // stream as usual; the quantising kernel and the reset are scheduled while their

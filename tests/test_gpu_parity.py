@@ -453,3 +453,43 @@ def test_queries_across_the_bf16_range(pkv, dtype, D):
     assert err.max() <= tol, f"max |err| {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
     assert err.mean() <= TOL_MEAN, f"mean |err| {err.mean():.3e}"
     step.close()
+
+
+@pytest.mark.parametrize("dtype", ["fp8_e4m3", "int8"])
+@pytest.mark.parametrize("bs", [16, 64])
+def test_small_appends_with_several_tokens_per_block(pkv, dtype, bs):
+    """Appends of up to 1024 tokens (a decode step appends one per sequence) quantise in one
+    pass, each token finding the call's other tokens in its block.  Calls whose tokens share
+    blocks in shuffled order (blocks the call opens, blocks continued from earlier calls), with a
+    padding slot, must store the oracle's codes and scales bit for bit after every call; so must
+    a call of 1025 tokens (three passes)."""
+    import torch
+    D, Hkv = 128, 2
+    nb = 6400 // bs
+    handle = pkv.pkv_pool_create(nb, bs, Hkv, D, pkv.KV_DTYPES[dtype])
+    ref = oracle.Pool(nb, bs, Hkv, D, odrive.KV_CODE[dtype])
+    rng = np.random.default_rng(bs + (7 if dtype == "int8" else 0))
+    fill = np.zeros(nb, dtype=np.int64)
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(handle)
+    for n in (1, 7, 33, 200, 1024, 1025, 3):
+        slots = []
+        while len(slots) < n - 1:
+            b = int(rng.choice(np.flatnonzero(fill < bs)))
+            run = int(min(n - 1 - len(slots), rng.integers(1, bs - fill[b] + 1)))
+            slots += [b * bs + int(fill[b]) + u for u in range(run)]
+            fill[b] += run
+        slots.insert(int(rng.integers(0, len(slots) + 1)), -1)  # a padding token
+        slots = np.array(slots, dtype=np.int64)
+        rng.shuffle(slots)
+        x = rng.standard_normal((2, n, Hkv, D)) * np.exp2(rng.integers(-3, 4, size=(2, n, 1, 1)))
+        bits = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        dk = torch.from_numpy(bits[0].view(np.int16)).view(torch.bfloat16).cuda()
+        dv = torch.from_numpy(bits[1].view(np.int16)).view(torch.bfloat16).cuda()
+        pkv.pkv_append(handle, dk, dv, torch.from_numpy(slots).cuda())
+        assert ref.append(bits[0], bits[1], slots) == 0
+        torch.cuda.synchronize()
+        assert pkv.pkv_check_device_error(handle) == pkv.PKV_OK
+        assert np.array_equal(_wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32), ref.scales), n
+        assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), ref.data), n
+    pkv.pkv_pool_destroy(handle)
