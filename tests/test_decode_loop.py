@@ -36,8 +36,12 @@ def test_loop_schedule_fits_its_pool_and_conserves_blocks():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("kv_dtype,bs,graphs", [("bf16", 16, True), ("bf16", 64, False), ("fp8_e4m3", 16, True)])
-def test_decode_loop_matches_oracle_every_step(kv_dtype, bs, graphs):
+@pytest.mark.parametrize("kv_dtype,bs,graphs,device_inputs", [("bf16", 16, True, False), ("bf16", 64, False, False),
+                                                              ("fp8_e4m3", 16, True, False), ("bf16", 16, True, True),
+                                                              ("int8", 64, False, True)])
+def test_decode_loop_matches_oracle_every_step(kv_dtype, bs, graphs, device_inputs):
+    """device_inputs: each step's q / new K / new V are written on the device into the loop's
+    input region (as a QKV projection would) instead of being staged from the host."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -48,9 +52,14 @@ def test_decode_loop_matches_oracle_every_step(kv_dtype, bs, graphs):
     sc = W.make_loop_script(index=41 if kv_dtype == "bf16" else 42, n_steps=24, block_size=bs, kv_dtype=kv_dtype)
     ref, pool = odrive.run_loop(sc)
     loop = DecodeLoop(sc, graphs=graphs)
-    tol = 3e-2 if kv_dtype == "fp8_e4m3" else 1e-2
+    tol = 3e-2 if kv_dtype != "bf16" else 1e-2
     for t in range(len(sc.steps)):
-        run, out = loop.step()
+        if device_inputs:
+            k, v, q = sc.step_inputs(t, ref[t][0])
+            _, qd, kd, vd = loop.device_input_region(len(ref[t][0]))
+            for dst, src in ((qd, q), (kd, k), (vd, v)):
+                dst.copy_(torch.from_numpy(src.view(np.int16)).view(torch.bfloat16))
+        run, out = loop.step(device_inputs=device_inputs)
         assert run == ref[t][0]
         err = np.abs(oracle.bf16_bits_to_f64(out) - ref[t][1])
         assert err.max() <= tol and err.mean() <= TOL_MEAN, (t, err.max(), err.mean())
