@@ -12,7 +12,7 @@
 // (block, K|V, head).  A block's scales are derived by the call
 // that writes its offset 0, as amax/448 over that call's tokens in the block (1 when the
 // amax is 0); later calls reuse them and saturate.  Calls of up to 1024 tokens (decode steps)
-// do this in one kernel, a warp per token that finds the call's other tokens in its block by
+// do this in one kernel, a CTA per token that finds the call's other tokens in its block by
 // scanning the call's slots (quant_append_small_kernel).  Larger calls take three short passes,
 // with no grid-wide synchronisation inside a kernel:
 //   1. amax: per row |x| max, atomicMax into a per-(block, K|V, head) scratch word, and a
@@ -210,12 +210,13 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_reset_kernel(const int64_t
 
 // One-pass quantising append for calls of up to kSmallAppendTokens tokens (a decode step appends
 // one token per sequence): the same stored bytes and scales as the three passes above, in one
-// launch.  One warp per token.  Every warp first scans the call's slots (staged in shared memory)
-// for the other tokens landing in its block: if the call writes the block's offset 0 ("fresh"),
-// the scale of each (K|V, head) row is amax/448 (amax/127 for int8) over the row and the same rows
-// of those other tokens, which every token of the block computes alike; otherwise the stored scale
-// is read (no token of this call writes it).  The usual decode step has no such other token, so a
-// fresh block's scale comes from the token's own row.
+// launch.  One CTA per token, one thread per 8 elements of its K and V rows.  Every warp scans
+// the call's slots (staged in shared memory) for the other tokens landing in the token's block:
+// if the call writes the block's offset 0 ("fresh"), the scale of each (K|V, head) row is
+// amax/448 (amax/127 for int8) over the row and the same rows of those other tokens, which every
+// token of the block computes alike; otherwise the stored scale is read (no token of this call
+// writes it).  The usual decode step has no such other token, so a fresh block's scale comes
+// from the token's own row.
 constexpr int kSmallAppendTokens = 1024;
 
 template <int D, bool I8>
@@ -226,19 +227,30 @@ __global__ void __launch_bounds__(kAppendThreads) quant_append_small_kernel(uint
                                                                              const int64_t* __restrict__ slots, int N,
                                                                              int Hkv, int bs, int num_blocks, int* err) {
     ptx::grid_launch_dependents();  // a following decode step may begin its set-up
-    constexpr int TPR = D / 8;        // lanes per row (8 elements each)
-    constexpr int RPI = 32 / TPR;     // rows per warp iteration
+    constexpr int TPR = D / 8;                     // threads per row (8 elements each)
+    constexpr int RPC = kAppendThreads / TPR;      // rows per CTA pass
     __shared__ int64_t s_slot[kSmallAppendTokens];
-    for (int j = threadIdx.x; j < N; j += blockDim.x) s_slot[j] = __ldg(slots + j);
+    const int i = blockIdx.x;  // this CTA's token
+    const int tid = threadIdx.x, lane = tid & 31, part = tid % TPR;
+    // the token's rows: loads issued before the slot scan, which they do not depend on
+    constexpr int kMaxPasses = 4;  // rows = 2 * Hkv <= kMaxPasses * RPC (checked on the host)
+    uint4 v[kMaxPasses];
+#pragma unroll
+    for (int ps = 0; ps < kMaxPasses; ++ps) {
+        const int r = ps * RPC + tid / TPR;
+        v[ps] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < 2 * Hkv) {
+            const int kv = r / Hkv, h = r - kv * Hkv;
+            v[ps] = __ldg(reinterpret_cast<const uint4*>((kv ? v_new : k_new) + ((int64_t)i * Hkv + h) * D + part * 8));
+        }
+    }
+    for (int j = tid; j < N; j += kAppendThreads) s_slot[j] = __ldg(slots + j);
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int i = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5);  // this warp's token
-    if (i >= N) return;
     const int64_t cap = (int64_t)num_blocks * bs;
     const int64_t slot = s_slot[i];
     if (slot < 0) return;
     if (slot >= cap) {
-        if (lane == 0) atomicOr(err, kErrBounds);
+        if (tid == 0) atomicOr(err, kErrBounds);
         return;
     }
     const int64_t blk = slot / bs;
@@ -258,18 +270,17 @@ __global__ void __launch_bounds__(kAppendThreads) quant_append_small_kernel(uint
         mates |= __any_sync(0xffffffffu, same);
         fresh |= __any_sync(0xffffffffu, zero);
     }
-    const int part = lane % TPR;
-    for (int r0 = 0; r0 < 2 * Hkv; r0 += RPI) {  // same trip count for every lane of the warp
-        const int r = r0 + lane / TPR;
+#pragma unroll
+    for (int ps = 0; ps < kMaxPasses; ++ps) {
+        if (ps * RPC >= 2 * Hkv) break;  // CTA-uniform
+        const int r = ps * RPC + tid / TPR;
         const bool act = r < 2 * Hkv;
         const int kv = act ? r / Hkv : 0, h = act ? r - kv * Hkv : 0;
-        const uint16_t* src = kv ? v_new : k_new;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (act) v = __ldg(reinterpret_cast<const uint4*>(src + ((int64_t)i * Hkv + h) * D + part * 8));
         float s = 1.0f;
         if (fresh) {
-            uint32_t m = act ? amax_bits(v) : 0u;
+            uint32_t m = act ? amax_bits(v[ps]) : 0u;
             if (mates && act) {  // rare: several tokens of the call share the block
+                const uint16_t* src = kv ? v_new : k_new;
                 for (int j = 0; j < N; ++j) {
                     const int64_t sj = s_slot[j];
                     if (j == i || sj < 0 || sj >= cap || sj / bs != blk) continue;
@@ -285,7 +296,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_append_small_kernel(uint
         } else if (act) {
             s = scales[(blk * Hkv + h) * 4 + kv];
         }
-        if (act) quant_store<D, I8>(pool, v, s, blk, t, kv, h, part, Hkv, bs);
+        if (act) quant_store<D, I8>(pool, v[ps], s, blk, t, kv, h, part, Hkv, bs);
     }
 }
 
@@ -465,9 +476,9 @@ pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, cons
     if (p->dtype == PKV_KV_BF16) {
         append_bf16_kernel<D><<<grid, kAppendThreads, 0, st>>>(static_cast<uint16_t*>(p->kv), k, v, slots, N,
                                                                p->n_kv_heads, p->block_size, p->num_blocks, p->err);
-    } else if (N <= kSmallAppendTokens) {
-        // one pass: a warp per token
-        const dim3 g1((unsigned)((N + kAppendThreads / 32 - 1) / (kAppendThreads / 32)));
+    } else if (N <= kSmallAppendTokens && 2 * p->n_kv_heads * (D / 8) <= 4 * kAppendThreads) {
+        // one pass: a CTA per token
+        const dim3 g1((unsigned)N);
         uint8_t* const kv8 = static_cast<uint8_t*>(p->kv);
         if (p->dtype == PKV_KV_INT8)
             quant_append_small_kernel<D, true><<<g1, kAppendThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
