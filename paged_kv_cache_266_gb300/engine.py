@@ -179,7 +179,7 @@ class DecodeLoop:
         the sequence decodes from the step after its last chunk.
 
         system_seq: the sequence id under which a script's shared system prompt is cached (any id
-        no request uses; needed when the script has a system prompt and reuses it)."""
+        no request uses; needed when the script has a system prompt)."""
         import torch
         self.prompts = prompts or {}
         self.torch, self.script, self.graphs, self.device = torch, script, graphs, device
@@ -196,11 +196,12 @@ class DecodeLoop:
         self.scheduler = (ChunkedContextScheduler(script.chunk, script.system, script.reuse) if script.chunk
                           else None)
         self.system_seq = system_seq
-        if script.chunk and script.system and script.reuse:
+        if script.chunk and script.system:
             # prefix caching ("TensorRT-LLM 推理加速实战" §8, KV cache reuse): the shared system
-            # prompt is cached once under its own sequence; joiners fork it
+            # prompt is cached once under its own sequence and, with reuse, joiners fork it
+            # (without reuse it stays cached, unused, so both schedules hold the same pool)
             if system_seq is None:
-                raise ValueError("a script with a cached system prompt needs system_seq")
+                raise ValueError("a script with a system prompt needs system_seq")
             k, v = script.system_kv()
             pkv_seq_reserve(self.alloc, system_seq, script.system)
             slots = pkv_slot_mapping(self.alloc, [system_seq] * script.system, np.arange(script.system))
