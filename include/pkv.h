@@ -342,7 +342,7 @@ pkv_status pkv_prefill_step(pkv_pool* pool, const void* k_new_dev, const void* v
  *   - The looked-up address is kept for the life of the process.  cudaDeviceReset (or anything
  *     else that destroys the device's primary context) invalidates it: do not use this call on
  *     a device after resetting it. */
-#define PKV_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+#define PKV_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
 pkv_status pkv_decode_attention_static(const pkv_pool* pool, const void* q_dev, const int32_t* block_tables_dev,
                                        int max_blocks, const int32_t* context_lens_dev, int B, int n_q_heads,
                                        float scale, void* out_dev, pkv_stream_t stream);

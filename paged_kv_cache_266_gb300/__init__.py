@@ -30,7 +30,7 @@ __all__ = [
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OOM, PKV_ERR_NO_SEQ, PKV_ERR_BOUNDS, PKV_ERR_CUDA, PKV_ERR_TIMEOUT = range(7)
 PKV_KV_BF16, PKV_KV_FP8_E4M3, PKV_KV_INT8 = 0, 1, 2
 KV_DTYPES = {"bf16": PKV_KV_BF16, "fp8_e4m3": PKV_KV_FP8_E4M3, "int8": PKV_KV_INT8}
-PKV_STATIC_WORKSPACE_BYTES = 32 << 20  # include/pkv.h
+PKV_STATIC_WORKSPACE_BYTES = 8 << 20  # include/pkv.h
 
 _lib = None
 

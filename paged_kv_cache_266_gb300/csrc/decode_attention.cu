@@ -5,13 +5,10 @@
 //     out[b][j] = sum_t softmax_t(scale * q[b][j] . K_b[t]) V_b[t].
 //
 // Work decomposition (GB300: 152 SMs, HBM-bound):
-//  * Every (sequence, KV head) pair's context is cut into 64-token groups.  A pair's first
-//    groups are static: those of all pairs, laid end to end (pairs in (b, h) order), are split
-//    into gridDim.x contiguous, equal ranges, one per CTA.  Its last few groups (about 15%, at
-//    most 4) are dynamic: a CTA whose range is done claims them one at a time from a counter,
-//    so the CTAs, whose streaming rates differ by about +-10% from run to run, finish together.
-//    The grid is sized to the resident CTA count, so one wave streams the whole pool at an
-//    even rate whatever the context-length mix.
+//  * Every (sequence, KV head) pair's context is cut into 64-token groups; the groups of all
+//    pairs, laid end to end (pairs in (b, h) order), are split into gridDim.x contiguous,
+//    equal ranges, one per CTA.  The grid is sized to the resident CTA count, so one wave
+//    streams the whole pool at an even rate whatever the context-length mix.
 //  * A CTA is one producer warp and four consumer warps.  The producer walks its range and,
 //    per group, issues TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzled rows) of the
 //    K and V rows of that group's pages into a ring of shared-memory stages, completion
@@ -29,11 +26,10 @@
 //    head by a power of two into f16's range before their conversion, which keeps it exact
 //    for any bf16 query; the inverse power of two joins the head's score scale.
 //  * When a pair ends inside the CTA the four warps' (max, sum, O) states are merged through
-//    shared memory and the result is written as bf16.  A pair cut into several parts (its
-//    static groups cut between CTAs, each dynamic group a part of its own) leaves one partial
-//    state per part in a fixed workspace slot; the last part to finish (atomic ticket, no
-//    waiting) merges them with the log-sum-exp rule in a fixed order, so results do not
-//    depend on timing or on which CTA took which group.
+//    shared memory and the result is written as bf16.  A pair cut between CTAs leaves one
+//    partial state per CTA in the workspace; the last CTA to finish (atomic ticket, no
+//    waiting) merges them with the log-sum-exp rule in slot order, so results do not depend
+//    on timing.
 //
 // Every mbarrier wait is bounded (2 s of wall time); on expiry the kernel sets the pool's
 // error word and finishes without touching memory outside its buffers.
@@ -63,8 +59,7 @@ struct Params {
     uint16_t* out;
     const uint8_t* pool;
     const float* scales;
-    int* counters;    // merge tickets [B * Hkv]
-    int* claim;       // [0]: dynamic groups claimed so far, [1]: CTAs done claiming (zero between launches)
+    int* counters;
     float* partials;  // O of the partial states [slots][G][D]
     float* part_ml;   // their (max, sum) [slots][G][2]
     int* err;
@@ -75,7 +70,6 @@ struct Params {
     uint32_t stage_bytes, off_q, off_s;  // within a stage: page parts, query rows, fp8 scale pairs
     uint32_t off_bar, off_misc, off_cmb, off_lens;  // within the shared-memory block
     float scale_log2;
-    int dyn_permille, dyn_max;  // share of a pair's groups handed out dynamically, and their cap
     uint64_t wait_ns;   // bound of every mbarrier wait
     uint32_t stall_tx;  // test hook: bytes each stage expects beyond its copies (0 in normal use)
 };
@@ -83,10 +77,10 @@ struct Params {
 // misc words in shared memory
 constexpr int kMiscAbort = 0;
 constexpr int kMiscMergeParts = 1;
-constexpr int kQuickMergeParts = 8;  // merges of up to this many parts load everything at once
+constexpr int kQuickMergeParts = 4;  // merges of up to this many parts load everything at once
                                      // (bf16 only: the one-byte kernels are capped at 128 registers)
+constexpr int kMiscMergeFirst = 2;
 constexpr uint32_t kMiscQinvBytes = 32;  // after the misc words: [kConsumerWarps][kMaxG] floats
-constexpr int kMiscHeaderWords = (kMiscQinvBytes + kConsumerWarps * kMaxG * 4) / 4;  // then [kMaxStages] headers
 
 __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* misc, uint64_t limit_ns) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -105,84 +99,15 @@ __device__ __forceinline__ void flag_abort(const Params& p, volatile int* misc) 
     atomicOr(p.err, kErrTimeout);
 }
 
-// Largest b with Hkv * cum[b] <= e (pairs of sequences without such groups are skipped).
-__device__ __forceinline__ int find_seq(const int32_t* cum, int B, int Hkv, int64_t e) {
+// Largest b with Hkv * cumg[b] <= e (pairs of empty sequences have no groups and are skipped).
+__device__ __forceinline__ int find_seq(const int32_t* cumg, int B, int Hkv, int64_t e) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)Hkv * cum[mid] <= e) lo = mid;
+        if ((int64_t)Hkv * cumg[mid] <= e) lo = mid;
         else hi = mid - 1;
     }
     return lo;
-}
-
-// Groups of a pair with ng groups that are handed out dynamically (its last ones): none for
-// pairs of fewer than three groups, else ceil(ng * permille / 1000), at most dyn_max and at most
-// ng - 1 (a pair keeps a static part).
-__device__ __forceinline__ int dyn_groups(int ng, int permille, int dyn_max) {
-    if (ng < 3 || permille <= 0) return 0;
-    const int d = (ng * permille + 999) / 1000;
-    return min(min(d, dyn_max), ng - 1);
-}
-
-// The group layout every role derives from the context lengths (shared memory):
-//   lens[b]   context length (clamped to the table's capacity);
-//   cum_s[b]  static groups per pair of the sequences before b (static group index es: the pairs'
-//             first ng - d groups, pairs in (b, h) order, split into contiguous CTA ranges);
-//   cum_d[b]  dynamic groups per pair before b (dynamic index ed: the pairs' last d groups,
-//             claimed one at a time from a counter by CTAs whose static range is done).
-struct Layout {
-    const int32_t* lens;
-    const int32_t* cum_s;
-    const int32_t* cum_d;
-    int64_t Ns, Nd;  // static and dynamic groups
-    int64_t C;       // CTAs sharing the static groups
-};
-
-__device__ __forceinline__ int n_groups(const Layout& L, int b) { return (L.lens[b] + kGroup - 1) / kGroup; }
-
-// (b, h, g) of static group es / dynamic group ed
-__device__ __forceinline__ void locate_static(const Layout& L, const Params& p, int64_t es, int& b, int& h, int& g) {
-    b = find_seq(L.cum_s, p.B, p.Hkv, es);
-    const int sg = L.cum_s[b + 1] - L.cum_s[b];
-    const int r = (int)(es - (int64_t)p.Hkv * L.cum_s[b]);  // < Hkv * sg
-    h = r / sg;
-    g = r - h * sg;
-}
-__device__ __forceinline__ void locate_dynamic(const Layout& L, const Params& p, int64_t ed, int& b, int& h, int& g) {
-    b = find_seq(L.cum_d, p.B, p.Hkv, ed);
-    const int d = L.cum_d[b + 1] - L.cum_d[b];
-    const int r = (int)(ed - (int64_t)p.Hkv * L.cum_d[b]);  // < Hkv * d
-    h = r / d;
-    g = (L.cum_s[b + 1] - L.cum_s[b]) + (r - h * d);
-}
-
-// The parts pair (b, h) is cut into, in merge order: the static parts of the CTAs c1 .. c1+ns-1
-// whose ranges cover its static groups (slots pair + c), then one part per dynamic group (slots
-// dyn_base + ed0 + j).  A pair of one part writes its output directly.
-struct PairParts {
-    int ns, nd;   // static parts, dynamic parts
-    int c1;       // first CTA of the static parts
-    int64_t ed0;  // dynamic index of the pair's first dynamic group
-};
-
-__device__ __forceinline__ PairParts pair_parts(const Layout& L, const Params& p, int b, int h) {
-    PairParts pp;
-    const int sg = L.cum_s[b + 1] - L.cum_s[b];
-    pp.nd = L.cum_d[b + 1] - L.cum_d[b];
-    pp.ed0 = (int64_t)p.Hkv * L.cum_d[b] + (int64_t)h * pp.nd;
-    pp.ns = 0;
-    pp.c1 = 0;
-    if (sg > 0) {
-        const int64_t e_first = (int64_t)p.Hkv * L.cum_s[b] + (int64_t)h * sg, e_last = e_first + sg - 1;
-        pp.c1 = (int)(((e_first + 1) * L.C - 1) / L.Ns);
-        pp.ns = (int)(((e_last + 1) * L.C - 1) / L.Ns) - pp.c1 + 1;
-    }
-    return pp;
-}
-
-__device__ __forceinline__ int64_t part_slot(const PairParts& pp, int u, int pair, int64_t dyn_base) {
-    return u < pp.ns ? (int64_t)pair + pp.c1 + u : dyn_base + pp.ed0 + (u - pp.ns);
 }
 
 // ------------------------------------------------------------------ producer warp
@@ -192,29 +117,28 @@ struct GroupDesc {
     float sk[4], sv[4];  // fp8 scales of the group's pages (loaded one batch after the ids)
 };
 
-// Stage header words (shared memory, one per stage): the dynamic group index a stage holds, or -1
-// when the producer has no more work (written before the stage's full barrier is arrived on).
 template <bool FP8, int D>
-__device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, const Params& p, const Layout& L,
+__device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, const Params& p, const int32_t* cumg, const int32_t* lens_s,
                          int64_t R0, int64_t R1, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
-                         volatile int* misc, volatile int* hdr) {
+                         volatile int* misc) {
     constexpr int kEsz = FP8 ? 1 : 2;
     const int lane = threadIdx.x & 31;
 
-    // the block ids of group (b, h, g)'s page parts
-    auto lookup = [&](GroupDesc& d) {
-        const int npages = (L.lens[d.b] + p.bs - 1) / p.bs;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k = p.ppg > 1 ? d.g * p.ppg + i : (d.g * kGroup) / p.bs;
-            d.id[i] = (i < p.ppg && k < npages) ? __ldg(p.tables + (int64_t)d.b * p.max_blocks + k) : -1;
-        }
-    };
     auto describe = [&](int64_t e, GroupDesc& d) {
         d.b = -1;
         if (e >= R1) return;
-        locate_static(L, p, e, d.b, d.h, d.g);
-        lookup(d);
+        const int b = find_seq(cumg, p.B, p.Hkv, e);
+        const int ng = cumg[b + 1] - cumg[b];
+        const int r = (int)(e - (int64_t)p.Hkv * cumg[b]);  // < Hkv * ng
+        d.b = b;
+        d.h = r / ng;
+        d.g = r - d.h * ng;
+        const int npages = (lens_s[b] + p.bs - 1) / p.bs;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = p.ppg > 1 ? d.g * p.ppg + i : (d.g * kGroup) / p.bs;
+            d.id[i] = (i < p.ppg && k < npages) ? __ldg(p.tables + (int64_t)b * p.max_blocks + k) : -1;
+        }
     };
     // fp8: the pages' scale pairs, once their block ids have arrived (out-of-range ids read 0)
     auto fetch_scales = [&](GroupDesc& d) {
@@ -230,101 +154,16 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
         }
     };
 
+    // Three batches of 32 group descriptors in flight: ids of batch +2 and scales of batch +1
+    // load while batch 0 is issued.
+    GroupDesc cur, nxt, nxt2;
+    describe(R0 + lane, cur);
+    describe(R0 + 32 + lane, nxt);
     int s = 0;
     uint32_t round = 0;
     int64_t issued = 0;
     bool ok = true;
     const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * kEsz;  // K rows + V rows of one page part
-
-    // Wait for stage s to be free (lane 0), warp-uniform result.
-    auto acquire = [&]() -> bool {
-        if (lane == 0) {
-            ok = !misc[kMiscAbort] && ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, p.wait_ns);
-            if (!ok) flag_abort(p, misc);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        return ok;
-    };
-    auto advance = [&]() {
-        ++issued;
-        if (++s == p.stages) {
-            s = 0;
-            ++round;
-        }
-    };
-    // Copies of group (b, h, g) with block ids id0..id3 and scales (held by lane `src` of the
-    // descriptors) into stage s; `first`: the stage also brings the pair's query rows.
-    auto issue = [&](int b, int h, int g, int id0, int id1, int id2, int id3, const GroupDesc& d, int src,
-                     bool first, int64_t header) {
-        int nparts = 1;
-        if (p.ppg > 1) nparts = min(p.ppg, (L.lens[b] + p.bs - 1) / p.bs - g * p.ppg);
-        // rows of the last part that hold tokens; a partly filled last part is copied in
-        // 16-row boxes up to its last token
-        const int tail_rows = min(p.box_rows, L.lens[b] - g * kGroup - (nparts - 1) * p.box_rows);
-        const int tail16 = (tail_rows + 15) >> 4;
-        const bool tail_short = p.box_rows > 16 && tail_rows <= p.box_rows - 16;  // saves a 16-row box
-        const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
-        const uint32_t fb = bar_full + 8 * s;
-        const int part = lane & 3;
-        int blk = part == 0 ? id0 : part == 1 ? id1 : part == 2 ? id2 : id3;
-        if (FP8) {  // scale pairs into the (now free) stage before it is published
-            const float sk0 = __shfl_sync(0xffffffffu, d.sk[0], src), sv0 = __shfl_sync(0xffffffffu, d.sv[0], src);
-            const float sk1 = __shfl_sync(0xffffffffu, d.sk[1], src), sv1 = __shfl_sync(0xffffffffu, d.sv[1], src);
-            const float sk2 = __shfl_sync(0xffffffffu, d.sk[2], src), sv2 = __shfl_sync(0xffffffffu, d.sv[2], src);
-            const float sk3 = __shfl_sync(0xffffffffu, d.sk[3], src), sv3 = __shfl_sync(0xffffffffu, d.sv[3], src);
-            if (lane < nparts) {
-                const float sk = part == 0 ? sk0 : part == 1 ? sk1 : part == 2 ? sk2 : sk3;
-                const float sv = part == 0 ? sv0 : part == 1 ? sv1 : part == 2 ? sv2 : sv3;
-                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(st + p.off_s + 8 * lane), "f"(sk), "f"(sv)
-                             : "memory");
-            }
-            __syncwarp();
-        }
-        if (lane == 0) {
-            hdr[s] = (int)header;
-            ptx::mbar_arrive_expect_tx(fb, (uint32_t)(nparts - (tail_short ? 1 : 0)) * part_bytes +
-                                               (tail_short ? (uint32_t)tail16 * 32u * D * kEsz : 0u) +
-                                               (first ? (uint32_t)(p.G * D * 2) : 0u) + p.stall_tx);
-        }
-        __syncwarp();  // the expect-tx precedes every lane's copies
-        // Lanes 0..nparts-1 issue one page part each (K and V rows in one tensor copy) and
-        // lane 4 the query rows, so a stage's copies go out in parallel.
-        if (lane < nparts) {
-            if (blk < 0 || blk >= p.num_blocks) {  // keep the byte count exact, read block 0
-                atomicOr(p.err, kErrBounds);
-                blk = 0;
-            }
-            const int row_off = p.ppg > 1 ? 0 : (g * kGroup) & (p.bs - 1);
-            const int32_t rowK = (int32_t)(((int64_t)(2 * blk) * p.Hkv + h) * p.bs + row_off);
-            const uint32_t dst = st + (uint32_t)lane * part_bytes;
-            if (tail_short && lane == nparts - 1) {
-                constexpr int kPanels = FP8 ? 1 : D / 64;
-                constexpr uint32_t kPanelRowBytes = FP8 ? D : 128;
-                const int32_t rowV = rowK + p.Hkv * p.bs;
-                for (int t = 0; t < tail16; ++t)
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-                        for (int q = 0; q < kPanels; ++q)
-                            ptx::tma_load_2d(dst + (uint32_t)((kv * kPanels + q) * p.box_rows + 16 * t) * kPanelRowBytes,
-                                             tmap_tail, q * 64, (kv ? rowV : rowK) + 16 * t, fb);
-            } else if (!FP8 && D == 128) {
-                ptx::tma_load_4d(dst, tmap, 0, rowK, 0, 0, fb);
-            } else {
-                ptx::tma_load_3d(dst, tmap, 0, rowK, 0, fb);
-            }
-        } else if (lane == 4 && first) {
-            ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D, (uint32_t)(p.G * D * 2),
-                           fb);
-        }
-        advance();
-    };
-
-    // ---- static range: three batches of 32 group descriptors in flight (ids of batch +2 and
-    // scales of batch +1 load while batch 0 is issued)
-    GroupDesc cur, nxt, nxt2;
-    describe(R0 + lane, cur);
-    describe(R0 + 32 + lane, nxt);
     // When launched behind this step's append (programmatic dependent launch), the pool and its
     // block scales (which the append sets on a block's first write) are read only after that
     // kernel has finished; otherwise this returns at once.  Block tables and lengths are inputs
@@ -344,53 +183,80 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
             const int id2 = __shfl_sync(0xffffffffu, cur.id[2], j);
             const int id3 = __shfl_sync(0xffffffffu, cur.id[3], j);
             const int64_t e = e0 + j;
-            if (!acquire()) break;
-            issue(b, h, g, id0, id1, id2, id3, cur, j, (e == R0) || (g == 0), -1);
+            const bool first = (e == R0) || (g == 0);
+            int nparts = 1;
+            if (p.ppg > 1) nparts = min(p.ppg, (lens_s[b] + p.bs - 1) / p.bs - g * p.ppg);
+            // rows of the last part that hold tokens; a partly filled last part is copied in
+            // 16-row boxes up to its last token
+            const int tail_rows = min(p.box_rows, lens_s[b] - g * kGroup - (nparts - 1) * p.box_rows);
+            const int tail16 = (tail_rows + 15) >> 4;
+            const bool tail_short = p.box_rows > 16 && tail_rows <= p.box_rows - 16;  // saves a 16-row box
+            const uint32_t st = sbase + (uint32_t)s * p.stage_bytes;
+            const uint32_t fb = bar_full + 8 * s;
+            if (lane == 0) {
+                ok = !misc[kMiscAbort] && ptx::mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1, p.wait_ns);
+                if (!ok) flag_abort(p, misc);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const int part = lane & 3;
+            int blk = part == 0 ? id0 : part == 1 ? id1 : part == 2 ? id2 : id3;
+            if (FP8) {  // scale pairs into the (now free) stage before it is published
+                const float sk0 = __shfl_sync(0xffffffffu, cur.sk[0], j), sv0 = __shfl_sync(0xffffffffu, cur.sv[0], j);
+                const float sk1 = __shfl_sync(0xffffffffu, cur.sk[1], j), sv1 = __shfl_sync(0xffffffffu, cur.sv[1], j);
+                const float sk2 = __shfl_sync(0xffffffffu, cur.sk[2], j), sv2 = __shfl_sync(0xffffffffu, cur.sv[2], j);
+                const float sk3 = __shfl_sync(0xffffffffu, cur.sk[3], j), sv3 = __shfl_sync(0xffffffffu, cur.sv[3], j);
+                if (lane < nparts) {
+                    const float sk = part == 0 ? sk0 : part == 1 ? sk1 : part == 2 ? sk2 : sk3;
+                    const float sv = part == 0 ? sv0 : part == 1 ? sv1 : part == 2 ? sv2 : sv3;
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(st + p.off_s + 8 * lane), "f"(sk), "f"(sv)
+                                 : "memory");
+                }
+                __syncwarp();
+            }
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)(nparts - (tail_short ? 1 : 0)) * part_bytes +
+                                                   (tail_short ? (uint32_t)tail16 * 32u * D * kEsz : 0u) +
+                                                   (first ? (uint32_t)(p.G * D * 2) : 0u) + p.stall_tx);
+            __syncwarp();  // the expect-tx precedes every lane's copies
+            // Lanes 0..nparts-1 issue one page part each (K and V rows in one tensor copy) and
+            // lane 4 the query rows, so a stage's copies go out in parallel.
+            if (lane < nparts) {
+                if (blk < 0 || blk >= p.num_blocks) {  // keep the byte count exact, read block 0
+                    atomicOr(p.err, kErrBounds);
+                    blk = 0;
+                }
+                const int row_off = p.ppg > 1 ? 0 : (g * kGroup) & (p.bs - 1);
+                const int32_t rowK = (int32_t)(((int64_t)(2 * blk) * p.Hkv + h) * p.bs + row_off);
+                const uint32_t dst = st + (uint32_t)lane * part_bytes;
+                if (tail_short && lane == nparts - 1) {
+                    constexpr int kPanels = FP8 ? 1 : D / 64;
+                    constexpr uint32_t kPanelRowBytes = FP8 ? D : 128;
+                    const int32_t rowV = rowK + p.Hkv * p.bs;
+                    for (int t = 0; t < tail16; ++t)
+#pragma unroll
+                        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+                            for (int q = 0; q < kPanels; ++q)
+                                ptx::tma_load_2d(dst + (uint32_t)((kv * kPanels + q) * p.box_rows + 16 * t) * kPanelRowBytes,
+                                                 tmap_tail, q * 64, (kv ? rowV : rowK) + 16 * t, fb);
+                } else if (!FP8 && D == 128) {
+                    ptx::tma_load_4d(dst, tmap, 0, rowK, 0, 0, fb);
+                } else {
+                    ptx::tma_load_3d(dst, tmap, 0, rowK, 0, fb);
+                }
+            } else if (lane == 4 && first) {
+                ptx::bulk_load(st + p.off_q, p.q + ((int64_t)b * p.Hq + (int64_t)h * p.G) * D, (uint32_t)(p.G * D * 2),
+                               fb);
+            }
+            ++issued;
+            if (++s == p.stages) {
+                s = 0;
+                ++round;
+            }
         }
         cur = nxt;
         nxt = nxt2;
-    }
-
-    // ---- dynamic groups: claimed one at a time (the next claim and its look-ups are in flight
-    // while the current group waits for a free stage), each a part of its own with the pair's
-    // query rows; then a stage with header -1 tells the consumers there is no more work
-    if (L.Nd > 0 && ok) {
-        auto claim = [&](GroupDesc& d) -> int64_t {
-            int64_t ed = 0;
-            if (lane == 0) ed = (int64_t)atomicAdd(p.claim, 1);
-            ed = __shfl_sync(0xffffffffu, ed, 0);
-            d.b = -1;
-            if (ed < L.Nd && lane == 0) {
-                locate_dynamic(L, p, ed, d.b, d.h, d.g);
-                lookup(d);
-            }
-            return ed;
-        };
-        GroupDesc dn;
-        int64_t ed_n = claim(dn);
-        while (ed_n < L.Nd) {
-            GroupDesc dc = dn;
-            const int64_t ed = ed_n;
-            ed_n = claim(dn);
-            fetch_scales(dc);
-            if (!acquire()) break;
-            issue(__shfl_sync(0xffffffffu, dc.b, 0), __shfl_sync(0xffffffffu, dc.h, 0),
-                  __shfl_sync(0xffffffffu, dc.g, 0), __shfl_sync(0xffffffffu, dc.id[0], 0),
-                  __shfl_sync(0xffffffffu, dc.id[1], 0), __shfl_sync(0xffffffffu, dc.id[2], 0),
-                  __shfl_sync(0xffffffffu, dc.id[3], 0), dc, 0, true, ed);
-        }
-        if (ok && acquire()) {  // end of work
-            if (lane == 0) {
-                hdr[s] = -1;
-                ptx::mbar_arrive(bar_full + 8 * s);
-            }
-            advance();
-        }
-        // the last CTA out returns the claim counter to zero for the next launch
-        if (lane == 0 && atomicAdd(p.claim + 1, 1) == (int)gridDim.x - 1) {
-            p.claim[0] = 0;
-            p.claim[1] = 0;
-        }
     }
     // Do not leave while copies into this CTA's shared memory may still be landing.
     if (lane == 0) {
@@ -668,9 +534,8 @@ __device__ __forceinline__ void load_q_f16(uint32_t (&qf)[D / 16][2], const uint
 // [slot][G][2]; slot = pair + CTA index.
 template <int D, int QUICK>
 __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const SoftmaxState& st, float osc, int b,
-                            int h, int64_t slot, const PairParts& pp, int64_t dyn_base, uint8_t* smem,
+                            int h, bool complete, int64_t Ng, int64_t C, const int32_t* cumg, uint8_t* smem,
                             volatile int* misc) {
-    const bool complete = pp.ns + pp.nd == 1;
     constexpr int kCT = kConsumerWarps * 32;
     constexpr int kStride = D + 4;  // keeps rows 16-byte aligned and spreads the fragment stores over banks
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, c4 = lane & 3;
@@ -728,6 +593,7 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
     ptx::named_barrier_sync(kCombineBar, kCT);
     const int pair = b * p.Hkv + h;
     uint16_t* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
+    const int64_t slot = (int64_t)pair + blockIdx.x;
     float* part_o = p.partials + slot * G * D;
     for (int e = tid; e < G * (D / 4); e += kCT) {
         const int j = e / (D / 4), d = (e % (D / 4)) * 4;
@@ -756,9 +622,15 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
         // acquire lets the last of the parts read all the others' after the next barrier.
         ptx::named_barrier_sync(kCombineBar, kCT);
         if (tid == 0) {
-            const int n = pp.ns + pp.nd;
+            const int ng = cumg[b + 1] - cumg[b];
+            const int64_t e_first = (int64_t)p.Hkv * cumg[b] + (int64_t)h * ng;
+            const int64_t e_last = e_first + ng - 1;
+            const int c1 = (int)(((e_first + 1) * C - 1) / Ng);
+            const int c2 = (int)(((e_last + 1) * C - 1) / Ng);
             const int ticket = ptx::atomic_add_acq_rel_gpu(p.counters + pair, 1);
-            misc[kMiscMergeParts] = ticket == n - 1 ? n : 0;  // the last part to arrive merges
+            const bool last_part = ticket == c2 - c1;
+            misc[kMiscMergeParts] = last_part ? c2 - c1 + 1 : 0;
+            misc[kMiscMergeFirst] = c1;
         }
         ptx::named_barrier_sync(kCombineBar, kCT);
         const int nparts = misc[kMiscMergeParts];
@@ -768,6 +640,7 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
                 // CTA reaching the pair last merges as its final work): every thread loads the parts'
                 // (m, l) and its slice of their O at once -- one round trip -- and forms the maximum,
                 // the sum and the weighted O itself, in part order.
+                const int64_t s0 = (int64_t)pair + misc[kMiscMergeFirst];
                 for (int e = tid; e < G * (D / 4); e += kCT) {
                     const int j = e / (D / 4), d = (e % (D / 4)) * 4;
                     float2 ml[QUICK];
@@ -775,9 +648,8 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
 #pragma unroll
                     for (int u = 0; u < QUICK; ++u) {
                         if (u < nparts) {
-                            const int64_t su = part_slot(pp, u, pair, dyn_base);
-                            ml[u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (su * G + j) * 2));
-                            v[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + (su * G + j) * D + d));
+                            ml[u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((s0 + u) * G + j) * 2));
+                            v[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + ((s0 + u) * G + j) * D + d));
                         }
                     }
                     float M = -INFINITY;
@@ -804,20 +676,19 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
                 if (tid == 0) p.counters[pair] = 0;
             }
         } else if (nparts) {
+            const int64_t s0 = (int64_t)pair + misc[kMiscMergeFirst];
             // per head: max and sum over the parts, 16 threads per head
             {
                 const int j = tid >> 4, sl = tid & 15;
                 float M = -INFINITY, L = 0.f;
                 if (j < G) {
-                    for (int s = sl; s < nparts; s += 16)
-                        M = fmaxf(M, __ldcg(p.part_ml + (part_slot(pp, s, pair, dyn_base) * G + j) * 2));
+                    for (int s = sl; s < nparts; s += 16) M = fmaxf(M, __ldcg(p.part_ml + ((s0 + s) * G + j) * 2));
                 }
 #pragma unroll
                 for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
                 if (j < G) {
                     for (int s = sl; s < nparts; s += 16) {
-                        const float2 ml = __ldcg(
-                            reinterpret_cast<const float2*>(p.part_ml + (part_slot(pp, s, pair, dyn_base) * G + j) * 2));
+                        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((s0 + s) * G + j) * 2));
                         L += ptx::exp2_approx(ml.x - M) * ml.y;
                     }
                 }
@@ -839,9 +710,8 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
                     float4 v[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int64_t su = part_slot(pp, s + u, pair, dyn_base);
-                        f[u] = __ldcg(p.part_ml + (su * G + j) * 2);
-                        v[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + (su * G + j) * D + d));
+                        f[u] = __ldcg(p.part_ml + ((s0 + s + u) * G + j) * 2);
+                        v[u] = __ldcg(reinterpret_cast<const float4*>(p.partials + ((s0 + s + u) * G + j) * D + d));
                     }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -853,9 +723,8 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
                     }
                 }
                 for (; s < nparts; ++s) {
-                    const int64_t su = part_slot(pp, s, pair, dyn_base);
-                    const float w = ptx::exp2_approx(__ldcg(p.part_ml + (su * G + j) * 2) - M);
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.partials + (su * G + j) * D + d));
+                    const float w = ptx::exp2_approx(__ldcg(p.part_ml + ((s0 + s) * G + j) * 2) - M);
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.partials + ((s0 + s) * G + j) * D + d));
                     acc.x += w * v.x;
                     acc.y += w * v.y;
                     acc.z += w * v.z;
@@ -872,10 +741,10 @@ __device__ void finish_pair(const Params& p, const float (&o)[D / 16][4], const 
 }
 
 template <bool FP8, int D, bool I8>
-__device__ void consumer(const Params& p, const Layout& L, int64_t R0, int64_t R1, uint8_t* smem, uint32_t sbase,
-                         uint32_t bar_full, uint32_t bar_empty, volatile int* misc, const volatile int* hdr) {
+__device__ void consumer(const Params& p, const int32_t* cumg, const int32_t* lens_s, int64_t R0, int64_t R1,
+                         int64_t Ng, int64_t C, uint8_t* smem, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
+                         volatile int* misc) {
     constexpr int KS = D / 16;
-    constexpr int kCT = kConsumerWarps * 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t qf[KS][2];
     float o[KS][4];
@@ -883,18 +752,26 @@ __device__ void consumer(const Params& p, const Layout& L, int64_t R0, int64_t R
     float sv_prev = 1.f;
     // one-byte KV: this warp's per-head undo of the query scaling (kMaxG floats)
     float* qinv = reinterpret_cast<float*>(smem + p.off_misc + kMiscQinvBytes) + warp * kMaxG;
-    const int64_t dyn_base = (int64_t)p.B * p.Hkv + gridDim.x;  // slots of the dynamic parts
+    int b = find_seq(cumg, p.B, p.Hkv, R0);
+    int ng = cumg[b + 1] - cumg[b];
+    const int r = (int)(R0 - (int64_t)p.Hkv * cumg[b]);
+    int h = r / ng;
+    int g = r - h * ng;
+    int g_first = g;
     int s = 0;
     uint32_t round = 0;
     bool alive = true;
     const int pidx = (16 * warp) / p.box_rows;  // page part holding this warp's tokens
     const int prow = (16 * warp) % p.box_rows;  // the warp's first row inside that part
     const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * (FP8 ? 1 : 2);
-
-    // Stage s holds group g of pair (b, h), whose stage has landed (or this warp gave up): a part
-    // starts here (first) and/or ends here (last, its partial state going to `slot`).
-    auto process = [&](int b, int h, int g, bool first, bool last, int64_t slot) {
+    for (int64_t e = R0; e < R1; ++e) {
+        const bool first = (e == R0) || (g == 0);
+        const bool last = (e == R1 - 1) || (g == ng - 1);
         const uint32_t st_addr = sbase + (uint32_t)s * p.stage_bytes;
+        if (alive && !wait_full(bar_full + 8 * s, round & 1, misc, p.wait_ns)) {
+            alive = false;
+            flag_abort(p, misc);
+        }
         if (first) {
             if constexpr (FP8)
                 load_q_f16<D>(qf, smem + (st_addr - sbase) + p.off_q, p.G, lane, qinv);
@@ -905,8 +782,9 @@ __device__ void consumer(const Params& p, const Layout& L, int64_t R0, int64_t R
             st.m[0] = st.m[1] = -INFINITY;
             st.l[0] = st.l[1] = 0.f;
             sv_prev = 1.f;
+            g_first = g;
         }
-        const int nvalid = min(16, L.lens[b] - g * kGroup - 16 * warp);
+        const int nvalid = min(16, lens_s[b] - g * kGroup - 16 * warp);
         if (alive && nvalid > 0) {
             const uint32_t kst = st_addr + (uint32_t)pidx * part_bytes;  // the warp's page part: K rows, then V rows
             const uint32_t vst = kst + part_bytes / 2;
@@ -921,54 +799,21 @@ __device__ void consumer(const Params& p, const Layout& L, int64_t R0, int64_t R
         // A warp that gave up waiting no longer releases stages: the stage's phase is unknown, so
         // the producer must not reuse it (its own bounded wait then runs out).
         if (lane == 0 && alive) ptx::mbar_arrive(bar_empty + 8 * s);
-        if (last)
-            finish_pair<D, FP8 ? 0 : kQuickMergeParts>(p, o, st, FP8 ? sv_prev : 1.f, b, h, slot,
-                                                       pair_parts(L, p, b, h), dyn_base, smem, misc);
+        if (last) finish_pair<D, FP8 ? 0 : kQuickMergeParts>(p, o, st, FP8 ? sv_prev : 1.f, b, h, g_first == 0 && g == ng - 1, Ng, C, cumg, smem,
+                                 misc);
         if (++s == p.stages) {
             s = 0;
             ++round;
         }
-    };
-
-    // ---- the static range: the same walk as the producer's
-    if (R0 < R1) {
-        int b, h, g;
-        locate_static(L, p, R0, b, h, g);
-        int sg = L.cum_s[b + 1] - L.cum_s[b];
-        for (int64_t e = R0; e < R1; ++e) {
-            if (alive && !wait_full(bar_full + 8 * s, round & 1, misc, p.wait_ns)) {
-                alive = false;
-                flag_abort(p, misc);
+        if (++g == ng) {
+            g = 0;
+            if (++h == p.Hkv) {
+                h = 0;
+                do {
+                    ++b;
+                } while (b < p.B && cumg[b + 1] == cumg[b]);
+                if (b < p.B) ng = cumg[b + 1] - cumg[b];
             }
-            process(b, h, g, (e == R0) || (g == 0), (e == R1 - 1) || (g == sg - 1),
-                    (int64_t)b * p.Hkv + h + blockIdx.x);
-            if (++g == sg) {
-                g = 0;
-                if (++h == p.Hkv) {
-                    h = 0;
-                    do {
-                        ++b;
-                    } while (b < p.B && L.cum_s[b + 1] == L.cum_s[b]);
-                    if (b < p.B) sg = L.cum_s[b + 1] - L.cum_s[b];
-                }
-            }
-        }
-    }
-    // ---- dynamic groups, as the stage headers name them, until the end marker.  The four warps
-    // decide together whether to go on (a warp whose wait ran out cannot read the header, and
-    // every part's merge synchronises all four).
-    if (L.Nd > 0) {
-        for (;;) {
-            if (alive && !wait_full(bar_full + 8 * s, round & 1, misc, p.wait_ns)) {
-                alive = false;
-                flag_abort(p, misc);
-            }
-            if (ptx::named_barrier_or(kCombineBar, kCT, !alive || misc[kMiscAbort] != 0)) break;
-            const int ed = hdr[s];
-            if (ed < 0) break;
-            int b, h, g;
-            locate_dynamic(L, p, ed, b, h, g);
-            process(b, h, g, true, true, dyn_base + ed);
         }
     }
 }
@@ -981,53 +826,39 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int32_t* lens_s = reinterpret_cast<int32_t*>(smem + p.off_lens);
-    int32_t* cum_s = lens_s + p.B;
-    int32_t* cum_d = cum_s + p.B + 1;
+    int32_t* cumg = reinterpret_cast<int32_t*>(smem + p.off_lens);
+    int32_t* lens_s = cumg + p.B + 1;
     volatile int* misc = reinterpret_cast<volatile int*>(smem + p.off_misc);
-    volatile int* hdr = misc + kMiscHeaderWords;
     const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * p.stages;
 
-    // Context lengths (clamped to the table's capacity) and the prefix sums of the static and the
-    // dynamic groups per pair.
+    // Context lengths (clamped to the table's capacity) and per-sequence group prefix sums.
     if (warp == 0) {
         const int cap = p.max_blocks * p.bs;
         const int per = (p.B + 31) >> 5;
         const int b0 = min(p.B, lane * per), b1 = min(p.B, b0 + per);
-        int sum_s = 0, sum_d = 0;
+        int sum = 0;
         bool bad = false;
         for (int bb = b0; bb < b1; ++bb) {
-            int Lb = __ldg(p.lens + bb);
-            if (Lb < 0 || Lb > cap) {
+            int L = __ldg(p.lens + bb);
+            if (L < 0 || L > cap) {
                 bad = true;
-                Lb = min(max(Lb, 0), cap);
+                L = min(max(L, 0), cap);
             }
-            lens_s[bb] = Lb;
-            const int ng = (Lb + kGroup - 1) / kGroup, d = dyn_groups(ng, p.dyn_permille, p.dyn_max);
-            sum_s += ng - d;
-            sum_d += d;
+            lens_s[bb] = L;
+            sum += (L + kGroup - 1) / kGroup;
         }
-        int inc_s = sum_s, inc_d = sum_d;
+        int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int ts = __shfl_up_sync(0xffffffffu, inc_s, o), td = __shfl_up_sync(0xffffffffu, inc_d, o);
-            if (lane >= o) {
-                inc_s += ts;
-                inc_d += td;
-            }
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
         }
-        int run_s = inc_s - sum_s, run_d = inc_d - sum_d;
+        int run = incl - sum;
         for (int bb = b0; bb < b1; ++bb) {
-            cum_s[bb] = run_s;
-            cum_d[bb] = run_d;
-            const int ng = (lens_s[bb] + kGroup - 1) / kGroup, d = dyn_groups(ng, p.dyn_permille, p.dyn_max);
-            run_s += ng - d;
-            run_d += d;
+            cumg[bb] = run;
+            run += (lens_s[bb] + kGroup - 1) / kGroup;
         }
-        if (lane == 31) {
-            cum_s[p.B] = inc_s;
-            cum_d[p.B] = inc_d;
-        }
+        if (lane == 31) cumg[p.B] = incl;
         if (bad && blockIdx.x == 0) atomicOr(p.err, kErrBounds);
         if (lane == 0) {
             misc[kMiscAbort] = 0;
@@ -1047,24 +878,18 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
     }
     __syncthreads();
 
-    // Static groups are split over C = min(grid, static groups) CTAs, so every participating CTA
-    // owns at least one and a pair's static groups cut between CTAs have one part per CTA in
-    // between; the dynamic groups go to whichever CTAs ask first.
-    Layout L;
-    L.lens = lens_s;
-    L.cum_s = cum_s;
-    L.cum_d = cum_d;
-    L.Ns = (int64_t)p.Hkv * cum_s[p.B];
-    L.Nd = (int64_t)p.Hkv * cum_d[p.B];
-    L.C = L.Ns < (int64_t)gridDim.x ? L.Ns : (int64_t)gridDim.x;
+    // Groups are split over C = min(grid, groups) CTAs, so every participating CTA owns at
+    // least one group and a pair cut between CTAs has exactly one part per CTA in between.
+    const int64_t Ng = (int64_t)p.Hkv * cumg[p.B];
+    const int64_t C = Ng < (int64_t)gridDim.x ? Ng : (int64_t)gridDim.x;
     int64_t R0 = 0, R1 = 0;
-    if ((int64_t)blockIdx.x < L.C) {
-        R0 = (int64_t)blockIdx.x * L.Ns / L.C;
-        R1 = ((int64_t)blockIdx.x + 1) * L.Ns / L.C;
+    if ((int64_t)blockIdx.x < C) {
+        R0 = (int64_t)blockIdx.x * Ng / C;
+        R1 = ((int64_t)blockIdx.x + 1) * Ng / C;
     }
 
     if (warp == kConsumerWarps) {
-        if (R0 < R1 || L.Nd > 0) producer<FP8, D>(&tmap, &tmap_tail, p, L, R0, R1, sbase, bar_full, bar_empty, misc, hdr);
+        if (R0 < R1) producer<FP8, D>(&tmap, &tmap_tail, p, cumg, lens_s, R0, R1, sbase, bar_full, bar_empty, misc);
         return;
     }
     // Sequences with an empty context get zeros (no group covers them).
@@ -1073,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
         uint4* row = reinterpret_cast<uint4*>(p.out + (int64_t)bb * p.Hq * D);
         for (int i = tid; i < p.Hq * D / 8; i += kConsumerWarps * 32) row[i] = make_uint4(0, 0, 0, 0);
     }
-    if (R0 < R1 || L.Nd > 0) consumer<FP8, D, I8>(p, L, R0, R1, smem, sbase, bar_full, bar_empty, misc, hdr);
+    if (R0 < R1) consumer<FP8, D, I8>(p, cumg, lens_s, R0, R1, Ng, C, smem, sbase, bar_full, bar_empty, misc);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1096,29 +921,17 @@ const void* kernel_for(const pkv_pool* pool) {
               : fp8 ? (const void*)decode_kernel<true, 64> : (const void*)decode_kernel<false, 64>;
 }
 
-bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, int dyn_max, Plan& pl);
-
-// Dynamic share of the work (see dyn_groups): the last ceil(15%) of a pair's groups, at most 4,
-// unless the settings say otherwise (a negative share turns it off).
-constexpr int kDynPermille = 150, kDynMax = 4;
-inline int dyn_permille_setting() {
-    const int v = settings().attn_dyn_permille;
-    return v < 0 ? 0 : (v > 0 ? std::min(v, 900) : kDynPermille);
-}
-inline int dyn_max_setting() {
-    const int v = settings().attn_dyn_max;
-    return dyn_permille_setting() == 0 ? 0 : (v > 0 ? std::min(v, 64) : kDynMax);
-}
+bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, Plan& pl);
 
 // The launch plan depends only on these values (not on the pool's address or contents), so the
 // plans of recent shapes are kept per host thread: a decode loop pays the shared-memory layout
 // and the occupancy query once per batch shape instead of once per step.
 struct PlanKey {
-    int B, G, Hkv, dtype, D, bs, sm_count, smem_block, smem_sm, device, pref, max_stages, dyn_max;
+    int B, G, Hkv, dtype, D, bs, sm_count, smem_block, smem_sm, device, pref, max_stages;
     bool operator==(const PlanKey& o) const {
         return B == o.B && G == o.G && Hkv == o.Hkv && dtype == o.dtype && D == o.D && bs == o.bs &&
                sm_count == o.sm_count && smem_block == o.smem_block && smem_sm == o.smem_sm && device == o.device &&
-               pref == o.pref && max_stages == o.max_stages && dyn_max == o.dyn_max;
+               pref == o.pref && max_stages == o.max_stages;
     }
 };
 
@@ -1127,9 +940,8 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     const Settings& cfg = settings();
     const int pref = cfg.attn_ctas_per_sm > 0 ? cfg.attn_ctas_per_sm : (q8 ? 3 : 2);
     const int max_stages = cfg.attn_max_stages > 0 ? cfg.attn_max_stages : kMaxStages;
-    const int dyn_max = dyn_max_setting();
     const PlanKey key{B, G, pool->n_kv_heads, (int)pool->dtype, pool->head_dim, pool->block_size, pool->sm_count,
-                      pool->max_smem_per_block, pool->max_smem_per_sm, pool->device, pref, max_stages, dyn_max};
+                      pool->max_smem_per_block, pool->max_smem_per_sm, pool->device, pref, max_stages};
     constexpr int kSlots = 8;
     thread_local PlanKey keys[kSlots];
     thread_local Plan plans[kSlots];
@@ -1139,7 +951,7 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
             pl = plans[i];
             return true;
         }
-    if (!compute_plan(pool, B, G, pref, max_stages, dyn_max, pl)) return false;
+    if (!compute_plan(pool, B, G, pref, max_stages, pl)) return false;
     keys[next] = key;
     plans[next] = pl;
     next = (next + 1) % kSlots;
@@ -1147,7 +959,7 @@ bool make_plan(const pkv_pool* pool, int B, int G, Plan& pl) {
     return true;
 }
 
-bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, int dyn_max, Plan& pl) {
+bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_stages_env, Plan& pl) {
     const bool fp8 = pool->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     const uint32_t D = (uint32_t)pool->head_dim, esz = fp8 ? 1 : 2;
     const uint32_t region = kGroup * D * esz;
@@ -1155,8 +967,8 @@ bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_sta
     pl.off_s = pl.off_q + align_up((uint32_t)G * D * 2, 128);
     pl.stage_bytes = align_up(pl.off_s + (fp8 ? 8u * 4 : 0u), 1024);
     const uint32_t cmb = align_up((kConsumerWarps * G * (D + 4) + 3 * kConsumerWarps * G + 2 * G) * 4, 16);
-    const uint32_t lens = align_up((3u * B + 2) * 4, 16);  // lengths, static and dynamic prefix sums
-    const uint32_t misc = 4u * (kMiscHeaderWords + kMaxStages);  // misc words, query factors, stage headers
+    const uint32_t lens = align_up((2u * B + 1) * 4, 16);
+    const uint32_t misc = kMiscQinvBytes + kConsumerWarps * kMaxG * 4;  // misc words, query factors
     const uint32_t fixed = 1024 + misc + cmb + lens;
     // fp8 tiles carry half the bytes of bf16 ones, so fp8 runs three CTAs per SM (its kernel is
     // compiled for that register budget) to keep enough tiles in flight
@@ -1187,9 +999,8 @@ bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_sta
     pl.ctas_per_sm = std::min(pl.ctas_per_sm, occ);
     pl.grid = pl.ctas_per_sm * pool->sm_count;
     const size_t pairs = (size_t)B * pool->n_kv_heads;
-    pl.counters_bytes = ((pairs + 2) * sizeof(int) + 255) / 256 * 256;  // tickets, claim and done counters
-    // a static part per pair and per CTA boundary, one part per dynamic group (at most dyn_max a pair)
-    pl.slots = pairs + (size_t)pl.grid + pairs * (size_t)dyn_max;
+    pl.counters_bytes = (pairs * sizeof(int) + 255) / 256 * 256;
+    pl.slots = pairs + (size_t)pl.grid;
     pl.ws_bytes = pl.counters_bytes + pl.slots * G * (D + 2) * sizeof(float);
     return true;
 }
@@ -1216,7 +1027,6 @@ pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tab
     p.pool = static_cast<const uint8_t*>(pool->kv);
     p.scales = pool->scales;
     p.counters = static_cast<int*>(workspace);
-    p.claim = p.counters + (size_t)B * pool->n_kv_heads;
     p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
     p.part_ml = p.partials + pl.slots * G * pool->head_dim;
     p.err = pool->err;
@@ -1238,8 +1048,6 @@ pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tab
     p.off_cmb = pl.off_cmb;
     p.off_lens = pl.off_lens;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.dyn_permille = dyn_permille_setting();
-    p.dyn_max = dyn_max_setting();
     // Test hooks for the bounded waits (failure detection is tested without a GPU fault): a
     // shorter wait limit, and stages that expect 16 bytes no copy delivers, so the waits run out
     // and the call reports PKV_ERR_TIMEOUT (both off unless set, see Settings).
@@ -1395,8 +1203,8 @@ extern "C" pkv_status pkv_decode_attention_static(const pkv_pool* pool, const vo
     void* ws = nullptr;
     const pkv_status ws_st = pkv::attn::static_workspace(cur, &ws);
     if (ws_st != PKV_OK) return ws_st;
-    // the merge tickets and the claim counters at the front of the workspace must start at zero
-    if (cudaMemsetAsync(ws, 0, ((size_t)B * pool->n_kv_heads + 2) * sizeof(int), reinterpret_cast<cudaStream_t>(stream)) !=
+    // the merge tickets at the front of the workspace must start at zero
+    if (cudaMemsetAsync(ws, 0, (size_t)B * pool->n_kv_heads * sizeof(int), reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
     return pkv_decode_attention(pool, q, block_tables, max_blocks, context_lens, B, n_q_heads, scale, out, ws,

@@ -30,17 +30,12 @@ void allocator_delete(pkv_allocator* a);
 //   PKV_TEST_STALL_COPIES   != 0: every pipeline stage expects 16 bytes no copy delivers, so the
 //                           bounded waits run out (failure detection tested without a fault);
 //   PKV_ATTN_CTAS_PER_SM    decode attention CTAs per SM (0: the kernel's default);
-//   PKV_ATTN_MAX_STAGES     decode attention pipeline stages at most (0: default);
-//   PKV_ATTN_DYN_PERMILLE   decode attention: share of a pair's groups handed out dynamically, in
-//                           thousandths (0: default, negative: none);
-//   PKV_ATTN_DYN_MAX        decode attention: at most this many dynamic groups a pair (0: default).
+//   PKV_ATTN_MAX_STAGES     decode attention pipeline stages at most (0: default).
 struct Settings {
     int wait_limit_ms;
     int stall_copies;
     int attn_ctas_per_sm;
     int attn_max_stages;
-    int attn_dyn_permille;
-    int attn_dyn_max;
 };
 const Settings& settings();
 

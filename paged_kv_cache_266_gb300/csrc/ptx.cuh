@@ -418,20 +418,5 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Named barrier that also ORs a predicate over the participating threads: every thread gets the
-// same result.
-__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "barrier.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
 }  // namespace ptx
 }  // namespace pkv
