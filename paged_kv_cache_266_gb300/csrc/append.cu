@@ -211,79 +211,90 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_reset_kernel(const int64_t
 // One-pass quantising append for calls of up to kSmallAppendTokens tokens (a decode step appends
 // one token per sequence): the same stored bytes and scales as the three passes above, in one
 // launch.  One CTA per token, one thread per 8 elements of its K and V rows.  Every warp scans
-// the call's slots (staged in shared memory) for the other tokens landing in the token's block:
-// if the call writes the block's offset 0 ("fresh"), the scale of each (K|V, head) row is
-// amax/448 (amax/127 for int8) over the row and the same rows of those other tokens, which every
-// token of the block computes alike; otherwise the stored scale is read (no token of this call
-// writes it).  The usual decode step has no such other token, so a fresh block's scale comes
-// from the token's own row.
+// the call's slots for the other tokens landing in the token's block: if the call writes the
+// block's offset 0 ("fresh"), the scale of each (K|V, head) row is amax/448 (amax/127 for int8)
+// over the row and the same rows of those other tokens, which every token of the block computes
+// alike; otherwise the stored scale is read (no token of this call writes it).  The usual decode
+// step has no such other token, so a fresh block's scale comes from the token's own row.
+// No shared memory; the slots are scanned with every thread's loads in flight at once.
 constexpr int kSmallAppendTokens = 1024;
+constexpr int kSmallThreads = 256;
 
 template <int D, bool I8>
-__global__ void __launch_bounds__(kAppendThreads) quant_append_small_kernel(uint8_t* __restrict__ pool,
-                                                                             float* __restrict__ scales,
-                                                                             const uint16_t* __restrict__ k_new,
-                                                                             const uint16_t* __restrict__ v_new,
-                                                                             const int64_t* __restrict__ slots, int N,
-                                                                             int Hkv, int bs, int num_blocks, int* err) {
+__global__ void __launch_bounds__(kSmallThreads, 4) quant_append_small_kernel(uint8_t* __restrict__ pool,
+                                                                                float* __restrict__ scales,
+                                                                                const uint16_t* __restrict__ k_new,
+                                                                                const uint16_t* __restrict__ v_new,
+                                                                                const int64_t* __restrict__ slots,
+                                                                                int N, int Hkv, int bs, int num_blocks,
+                                                                                int* err) {
     ptx::grid_launch_dependents();  // a following decode step may begin its set-up
-    constexpr int TPR = D / 8;                     // threads per row (8 elements each)
-    constexpr int RPC = kAppendThreads / TPR;      // rows per CTA pass
-    __shared__ int64_t s_slot[kSmallAppendTokens];
+    constexpr int TPR = D / 8;                 // threads per row (8 elements each)
+    constexpr int RPC = kSmallThreads / TPR;   // rows per CTA pass
+    constexpr int kPre = 2;                    // passes whose rows load before the slot scan
     const int i = blockIdx.x;  // this CTA's token
-    const int tid = threadIdx.x, lane = tid & 31, part = tid % TPR;
-    // the token's rows: loads issued before the slot scan, which they do not depend on
-    constexpr int kMaxPasses = 4;  // rows = 2 * Hkv <= kMaxPasses * RPC (checked on the host)
-    uint4 v[kMaxPasses];
+    const int tid = threadIdx.x, part = tid % TPR;
+    const int rows = 2 * Hkv;
+    auto row_src = [&](int r) {
+        const int kv = r / Hkv, h = r - kv * Hkv;
+        return reinterpret_cast<const uint4*>((kv ? v_new : k_new) + ((int64_t)i * Hkv + h) * D + part * 8);
+    };
+    uint4 pre[kPre];
 #pragma unroll
-    for (int ps = 0; ps < kMaxPasses; ++ps) {
+    for (int ps = 0; ps < kPre; ++ps) {
         const int r = ps * RPC + tid / TPR;
-        v[ps] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < 2 * Hkv) {
-            const int kv = r / Hkv, h = r - kv * Hkv;
-            v[ps] = __ldg(reinterpret_cast<const uint4*>((kv ? v_new : k_new) + ((int64_t)i * Hkv + h) * D + part * 8));
-        }
+        pre[ps] = r < rows ? __ldg(row_src(r)) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int j = tid; j < N; j += kAppendThreads) s_slot[j] = __ldg(slots + j);
-    __syncthreads();
     const int64_t cap = (int64_t)num_blocks * bs;
-    const int64_t slot = s_slot[i];
+    const int bs_shift = __ffs(bs) - 1;  // block sizes are powers of two
+    const int64_t slot = __ldg(slots + i);
     if (slot < 0) return;
     if (slot >= cap) {
         if (tid == 0) atomicOr(err, kErrBounds);
         return;
     }
-    const int64_t blk = slot / bs;
-    const int t = (int)(slot - blk * bs);
-    // other tokens of the call in this block, and whether the call writes the block's offset 0
-    bool mates = false, fresh = t == 0;
-    for (int j0 = 0; j0 < N; j0 += 32) {
-        const int j = j0 + lane;
-        bool same = false, zero = false;
-        if (j < N && j != i) {
-            const int64_t sj = s_slot[j];
-            if (sj >= 0 && sj < cap && sj / bs == blk) {
+    const int64_t blk = slot >> bs_shift;
+    const int t = (int)(slot & (bs - 1));
+    // other tokens of the call in this block, and whether the call writes the block's offset 0:
+    // every thread checks slots tid, tid + kSmallThreads, ... (four loads in flight at a time)
+    bool same = false, zero = false;
+    for (int j0 = tid; j0 < N; j0 += 4 * kSmallThreads) {
+        int64_t sj[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * kSmallThreads;
+            sj[u] = (j < N && j != i) ? __ldg(slots + j) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (sj[u] >= 0 && sj[u] < cap && (sj[u] >> bs_shift) == blk) {
                 same = true;
-                zero = sj - blk * bs == 0;
+                zero |= (sj[u] & (bs - 1)) == 0;
             }
         }
-        mates |= __any_sync(0xffffffffu, same);
-        fresh |= __any_sync(0xffffffffu, zero);
     }
-#pragma unroll
-    for (int ps = 0; ps < kMaxPasses; ++ps) {
-        if (ps * RPC >= 2 * Hkv) break;  // CTA-uniform
+    const bool mates = __syncthreads_or(same) != 0;
+    const bool fresh = t == 0 || __syncthreads_or(zero) != 0;
+    for (int ps = 0; ps * RPC < rows; ++ps) {  // CTA-uniform trip count
         const int r = ps * RPC + tid / TPR;
-        const bool act = r < 2 * Hkv;
+        const bool act = r < rows;
         const int kv = act ? r / Hkv : 0, h = act ? r - kv * Hkv : 0;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ps < kPre) {
+#pragma unroll
+            for (int q = 0; q < kPre; ++q)
+                if (q == ps) v = pre[q];
+        } else if (act) {
+            v = __ldg(row_src(r));
+        }
         float s = 1.0f;
         if (fresh) {
-            uint32_t m = act ? amax_bits(v[ps]) : 0u;
+            uint32_t m = act ? amax_bits(v) : 0u;
             if (mates && act) {  // rare: several tokens of the call share the block
                 const uint16_t* src = kv ? v_new : k_new;
                 for (int j = 0; j < N; ++j) {
-                    const int64_t sj = s_slot[j];
-                    if (j == i || sj < 0 || sj >= cap || sj / bs != blk) continue;
+                    const int64_t sj = __ldg(slots + j);
+                    if (j == i || sj < 0 || sj >= cap || (sj >> bs_shift) != blk) continue;
                     m = max(m, amax_bits(__ldg(reinterpret_cast<const uint4*>(src + ((int64_t)j * Hkv + h) * D +
                                                                                  part * 8))));
                 }
@@ -296,7 +307,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_append_small_kernel(uint
         } else if (act) {
             s = scales[(blk * Hkv + h) * 4 + kv];
         }
-        if (act) quant_store<D, I8>(pool, v[ps], s, blk, t, kv, h, part, Hkv, bs);
+        if (act) quant_store<D, I8>(pool, v, s, blk, t, kv, h, part, Hkv, bs);
     }
 }
 
@@ -476,18 +487,18 @@ pkv_status launch_append(pkv_pool* p, const uint16_t* k, const uint16_t* v, cons
     if (p->dtype == PKV_KV_BF16) {
         append_bf16_kernel<D><<<grid, kAppendThreads, 0, st>>>(static_cast<uint16_t*>(p->kv), k, v, slots, N,
                                                                p->n_kv_heads, p->block_size, p->num_blocks, p->err);
-    } else if (N <= kSmallAppendTokens && 2 * p->n_kv_heads * (D / 8) <= 4 * kAppendThreads) {
+    } else if (N <= kSmallAppendTokens) {
         // one pass: a CTA per token
         const dim3 g1((unsigned)N);
         uint8_t* const kv8 = static_cast<uint8_t*>(p->kv);
         if (p->dtype == PKV_KV_INT8)
-            quant_append_small_kernel<D, true><<<g1, kAppendThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
+            quant_append_small_kernel<D, true><<<g1, kSmallThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
+                                                                           p->n_kv_heads, p->block_size,
+                                                                           p->num_blocks, p->err);
+        else
+            quant_append_small_kernel<D, false><<<g1, kSmallThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
                                                                             p->n_kv_heads, p->block_size,
                                                                             p->num_blocks, p->err);
-        else
-            quant_append_small_kernel<D, false><<<g1, kAppendThreads, 0, st>>>(kv8, p->scales, k, v, slots, (int)N,
-                                                                             p->n_kv_heads, p->block_size,
-                                                                             p->num_blocks, p->err);
     } else {
         // three kernels in a chain of programmatic dependents: the amax kernel waits for the
         // stream as usual; the quantising kernel and the reset are scheduled while their
