@@ -295,12 +295,12 @@ pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes
  * context_lens[b] - n_b + i and attends causally to the cached tokens 0 .. that position:
  *     out[row][j] = sum_{t <= pos} softmax_t(scale * q[row][j] . K_b[t]) V_b[t],
  * query head j reading KV head j / (n_q_heads / n_kv_heads).
- *   q_dev, out_dev: bf16 [cu_q_lens[B]][n_q_heads][128], 16-byte aligned (rows of all chunks
+ *   q_dev, out_dev: bf16 [cu_q_lens[B]][n_q_heads][head_dim], 16-byte aligned (rows of all chunks
  *     packed back to back); fp32 accumulation, output rounded to bf16 (RNE).
  *   cu_q_lens_dev: int32 [B+1], non-decreasing, cu_q_lens[0] = 0.
  *   max_q_len: host int >= every n_b (sizes the grid; 0 launches nothing).
  *   block_tables_dev: int32 [B][max_blocks]; context_lens_dev: int32 [B].
- * Supported: bf16 pools with head_dim 128; n_q_heads / n_kv_heads a power of two <= 128;
+ * Supported: bf16 pools with head_dim 64 or 128; n_q_heads / n_kv_heads a power of two <= 128;
  * B * n_kv_heads * ceil(max_q_len * n_q_heads / n_kv_heads / 256) < 2^31; scale positive and
  * finite.  Otherwise PKV_ERR_INVALID_ARG (nothing launched).  A chunk longer than its
  * context or a context longer than max_blocks*block_size is skipped and a block id outside the

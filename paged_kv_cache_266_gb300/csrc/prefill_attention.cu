@@ -48,7 +48,6 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int kD = 128;
 constexpr int kRows = 128;   // query rows per tile
 constexpr int kTiles = 2;    // query tiles per CTA
 constexpr int kKeys = 128;   // keys per KV tile
@@ -59,15 +58,20 @@ constexpr int kThreads = 128 + kTiles * 128;  // control warpgroup + one softmax
 // i.e. 64512 for the block; control 128 x 48 + softmax 256 x 224 = 63488 fits.
 constexpr uint32_t kRegsControl = 48, kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + kTiles * 128 * kRegsSoftmax <= kThreads * 168, "register split");
-constexpr uint32_t kPanelBytes = 128u * 128u;      // 128 rows x 128 bytes
-constexpr uint32_t kQBytes = 2 * kPanelBytes;      // one Q tile: two 64-element panels
-constexpr uint32_t kHalfBytes = 2 * kPanelBytes;   // K (or V) of one KV tile: two panels
+constexpr uint32_t kPanelBytes = 128u * 128u;      // 128 rows x 128 bytes (64 bf16 of a row)
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTiles * kQBytes;
-constexpr uint32_t kOffV = kOffK + kKStages * kHalfBytes;
-constexpr uint32_t kOffBar = kOffV + kVStages * kHalfBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// Shared-memory layout for head_dim D (64 or 128): a row of Q, K or V is D / 64 panels.
+template <int D>
+struct Layout {
+    static constexpr int kPanels = D / 64;
+    static constexpr uint32_t kQBytes = kPanels * kPanelBytes;     // one Q tile
+    static constexpr uint32_t kHalfBytes = kPanels * kPanelBytes;  // K (or V) of one KV tile
+    static constexpr uint32_t kOffK = kOffQ + kTiles * kQBytes;
+    static constexpr uint32_t kOffV = kOffK + kKStages * kHalfBytes;
+    static constexpr uint32_t kOffBar = kOffV + kVStages * kHalfBytes;
+    static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (P stays <= 2^8)
@@ -75,7 +79,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kEndBar = 1;      // named barrier: every role done before TMEM is released
 constexpr int kMaxRankedSeqs = 512;  // above this the sequences are dispatched in index order
 constexpr int kSmallRankedSeqs = 64;  // up to this the ranking reads the inputs directly
-static_assert(kMaxRankedSeqs * sizeof(int64_t) <= kTiles * kQBytes, "dispatch ranking fits the Q tiles' space");
+static_assert(kMaxRankedSeqs * sizeof(int64_t) <= kTiles * Layout<64>::kQBytes, "dispatch ranking fits the Q tiles' space");
 
 // mbarrier slots
 constexpr int kBarQ = 0;                          // Q rows of both tiles written (8 warps arrive)
@@ -104,14 +108,37 @@ struct Params {
     uint32_t stall_tx;  // test hook: extra bytes every K/V stage expects and no copy delivers
 };
 
+// S = Q K^T over K = 64 (head_dim 64): four K=16 MMAs within one 128-byte panel of A and of B
+// (descriptor start addresses advance by 32 bytes a step), the first one overwriting D.
+__device__ __forceinline__ void umma_ss_k64_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                               uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 al, bl;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 pf, %1, %1;\n\tsetp.eq.b32 pt, %1, %1;\n\t"
+        "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pf;\n\t"
+        "add.u32 al, %1, 2;\n\tadd.u32 bl, %2, 2;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 4;\n\tadd.u32 bl, %2, 4;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t"
+        "add.u32 al, %1, 6;\n\tadd.u32 bl, %2, 6;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc));
+}
+
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
 }
 
-template <int PART>
+template <int PART, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
     static_assert(PART == 16 || PART == 32 || PART == 64, "page part of 16, 32 or 64 rows");
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    using LY = Layout<D>;
+    constexpr uint32_t kQBytes = LY::kQBytes, kHalfBytes = LY::kHalfBytes;
+    constexpr uint32_t kOffK = LY::kOffK, kOffV = LY::kOffV, kOffBar = LY::kOffBar;
+    constexpr int kPanels = LY::kPanels;
     constexpr int kParts = kKeys / PART;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_s;
@@ -241,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__shfl_sync(0xffffffffu, abort_s, 0)) break;  // warp-uniform
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar(full + s), kHalfBytes + p.stall_tx);
             __syncwarp();
-            if (lane < 2 * kParts) {
-                const int pi = lane >> 1, q = lane & 1;
+            if (lane < kPanels * kParts) {
+                const int pi = lane / kPanels, q = lane % kPanels;
                 const int tok = j * kKeys + pi * PART;  // first key of this page part
                 int32_t row = p.oob_row;
                 if (tok < L) {
@@ -263,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // descriptors are built once; the start-address field counts 16-byte units, so moving
             // an operand by X bytes adds X >> 4 (addresses stay below 256 KB: no carry out)
             constexpr uint32_t idS = ptx::umma_idesc_bf16(128, kKeys, 0, 0);
-            constexpr uint32_t idO = ptx::umma_idesc_bf16(128, kD, 0, 1);
+            constexpr uint32_t idO = ptx::umma_idesc_bf16(128, D, 0, 1);
             // a descriptor's high half (stride, version, swizzle) is the same for Q and K; V's
             // differs only in the low half (its panel stride)
             const uint64_t dQ0 = ptx::umma_sdesc_sw128(base + kOffQ, 16, 1024);
@@ -292,8 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // issued as one asm block: the issuing thread cannot run ahead of the tensor pipe, so
             // any arithmetic between two MMAs would be exposed.
             auto issue_s = [&](int t, int j) {
-                ptx::umma_ss_k128_x8(tmem + (uint32_t)(t * kKeys), q_lo + (uint32_t)t * (kQBytes >> 4),
-                                     k_lo + (uint32_t)(j % kKStages) * (kHalfBytes >> 4), hi, idS);
+                if constexpr (D == 128)
+                    ptx::umma_ss_k128_x8(tmem + (uint32_t)(t * kKeys), q_lo + (uint32_t)t * (kQBytes >> 4),
+                                         k_lo + (uint32_t)(j % kKStages) * (kHalfBytes >> 4), hi, idS);
+                else
+                    umma_ss_k64_x4(tmem + (uint32_t)(t * kKeys), q_lo + (uint32_t)t * (kQBytes >> 4),
+                                        k_lo + (uint32_t)(j % kKStages) * (kHalfBytes >> 4), hi, idS);
                 ptx::umma_commit(bar(kBarS + t));
                 // the last tile's S releases the K tile, if a later tile reuses its slot
                 if (t == last_tile && j + kKStages < n_kv) ptx::umma_commit(bar(kBarKEmpty + j % kKStages));
@@ -301,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_t += P_t(j) V_j: 16 keys per MMA, A from TMEM; on the first KV tile also the lo part
             auto issue_pv = [&](int t, int j) {
                 const uint32_t dv = v_lo + (uint32_t)(j % kVStages) * (kHalfBytes >> 4);
-                const uint32_t tP = tmem + (uint32_t)(t * kKeys), tO = tmem + kColO + (uint32_t)(t * kD);
+                const uint32_t tP = tmem + (uint32_t)(t * kKeys), tO = tmem + kColO + (uint32_t)(t * D);
                 const int left = L - j * kKeys;  // keys of this tile inside the context (> 0)
                 const int nk = left >= kKeys ? kKeys / 16 : (left + 15) / 16;
                 ptx::umma_ts_x8(tO, tP, dv, hi, idO, j > 0 ? 1u : 0u, nk);
@@ -352,15 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = qw * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
         const uint32_t tS = tmem + (uint32_t)(t * kKeys) + lane_off;
-        const uint32_t tO = tmem + kColO + (uint32_t)(t * kD) + lane_off;
+        const uint32_t tO = tmem + kColO + (uint32_t)(t * D) + lane_off;
         const int tok = t0 + t * T + r / p.G, g = r % p.G;
         const bool valid = tok < n;
         const int qlim = min(L - n + tok, L - 1);  // last key this row may see
         {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * kD);
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * D);
             uint8_t* qt = sm + kOffQ + (uint32_t)t * kQBytes;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < D / 8; ++c) {
                 const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4*>(qt + (uint32_t)(c >> 3) * kPanelBytes + swz128(r, c & 7)) = v;
             }
@@ -402,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = (grow && j > 0) ? ptx::exp2_approx(m - mt) : 1.f;
                 l *= alpha;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld32(tO + 32u * c, v);
                     ptx::tmem_wait_ld();
@@ -466,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 ptx::tc_fence_after();
                 const float inv = 1.f / l;
-                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * kD);
+                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * D);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld32(tO + 32u * c, v);
                     ptx::tmem_wait_ld();
@@ -499,12 +530,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 void prefill_configure(pkv_pool* pool) {
     (void)pool;
-    cudaFuncSetAttribute(prefill::prefill_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)prefill::kSmemBytes);
-    cudaFuncSetAttribute(prefill::prefill_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)prefill::kSmemBytes);
-    cudaFuncSetAttribute(prefill::prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)prefill::kSmemBytes);
+    using namespace prefill;
+    cudaFuncSetAttribute(prefill_kernel<16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<128>::kSmemBytes);
+    cudaFuncSetAttribute(prefill_kernel<32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<128>::kSmemBytes);
+    cudaFuncSetAttribute(prefill_kernel<64, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<128>::kSmemBytes);
+    cudaFuncSetAttribute(prefill_kernel<16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<64>::kSmemBytes);
+    cudaFuncSetAttribute(prefill_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<64>::kSmemBytes);
+    cudaFuncSetAttribute(prefill_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<64>::kSmemBytes);
 }
 
 // Argument checks shared by the prefill entry points; fills the kernel parameters and grid.
@@ -514,7 +546,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     using namespace prefill;
     if (!pool || B < 0 || max_q_len < 0 || Hq < 1) return PKV_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;  // masking relies on scale > 0
-    if (pool->dtype != PKV_KV_BF16 || pool->head_dim != kD) return PKV_ERR_INVALID_ARG;
+    if (pool->dtype != PKV_KV_BF16 || (pool->head_dim != 64 && pool->head_dim != 128)) return PKV_ERR_INVALID_ARG;
     if (Hq % pool->n_kv_heads) return PKV_ERR_INVALID_ARG;
     const int G = Hq / pool->n_kv_heads;
     if (G > kRows || (G & (G - 1))) return PKV_ERR_INVALID_ARG;
@@ -560,18 +592,28 @@ pkv_status prefill_launch(const pkv_pool* pool, const prefill::Params& p, dim3 g
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(prefill::kThreads);
-    cfg.dynamicSmemBytes = prefill::kSmemBytes;
+    const bool d64 = pool->head_dim == 64;
+    cfg.dynamicSmemBytes = d64 ? prefill::Layout<64>::kSmemBytes : prefill::Layout<128>::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    using prefill::prefill_kernel;
     cudaError_t e;
-    switch (p.part) {
-        case 16: e = cudaLaunchKernelEx(&cfg, prefill::prefill_kernel<16>, pool->tmap_panel, p); break;
-        case 32: e = cudaLaunchKernelEx(&cfg, prefill::prefill_kernel<32>, pool->tmap_panel, p); break;
-        default: e = cudaLaunchKernelEx(&cfg, prefill::prefill_kernel<64>, pool->tmap_panel, p); break;
+    if (d64) {
+        switch (p.part) {
+            case 16: e = cudaLaunchKernelEx(&cfg, prefill_kernel<16, 64>, pool->tmap_panel, p); break;
+            case 32: e = cudaLaunchKernelEx(&cfg, prefill_kernel<32, 64>, pool->tmap_panel, p); break;
+            default: e = cudaLaunchKernelEx(&cfg, prefill_kernel<64, 64>, pool->tmap_panel, p); break;
+        }
+    } else {
+        switch (p.part) {
+            case 16: e = cudaLaunchKernelEx(&cfg, prefill_kernel<16, 128>, pool->tmap_panel, p); break;
+            case 32: e = cudaLaunchKernelEx(&cfg, prefill_kernel<32, 128>, pool->tmap_panel, p); break;
+            default: e = cudaLaunchKernelEx(&cfg, prefill_kernel<64, 128>, pool->tmap_panel, p); break;
+        }
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

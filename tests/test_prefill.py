@@ -164,14 +164,17 @@ def _check_close(got_bits, ref):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("bs,G", [(16, 4), (64, 4), (64, 1), (16, 8), (128, 2), (32, 16)])
-def test_prefill_matches_oracle(bs, G):
+@pytest.mark.parametrize("bs,G,D", [(16, 4, 128), (64, 4, 128), (64, 1, 128), (16, 8, 128), (128, 2, 128),
+                                    (32, 16, 128), (16, 4, 64), (64, 1, 64), (64, 8, 64), (32, 16, 64),
+                                    (128, 2, 64)])
+def test_prefill_matches_oracle(bs, G, D):
     """Chunks at the start of a prompt, of one token, ending on a block boundary, spanning
-    several KV tiles and query tiles with ragged ends; pool bytes bit-exact after the append."""
+    several KV tiles and query tiles with ragged ends; pool bytes bit-exact after the append.
+    Head dims 128 and 64 (7B/8B/70B layers use 128; 64 is the other size the pool supports)."""
     torch, pkv = _gpu()
     import pkv_workloads as W
     from paged_kv_cache_266_gb300.runner import PrefillStep, _wrap_device
-    sc = W.make_prefill_script(71 + bs + G, Hq=2 * G, Hkv=2, D=128, block_size=bs,
+    sc = W.make_prefill_script(71 + bs + G + D, Hq=2 * G, Hkv=2, D=D, block_size=bs,
                                past=[0, 5, 64, 100, 250, 31, 0], chunk=[37, 1, 64, 150, 3, 200, 129])
     st = PrefillStep(sc)
     st.step()
