@@ -480,7 +480,7 @@ def run_loop(args, world, rank, local):
         lib.pkv_stage_copy(*copy_args[t])  # the projection's output, already on the device
         run, _ = loop.step(device_inputs=True)
         tokens += len(run)
-        kv_bytes += sum(loop.lens[s] for s in run) * sc.Hkv * 2 * sc.D * 2
+        kv_bytes += loop.attended_tokens * sc.Hkv * 2 * sc.D * 2
     dt = dist_max(time.perf_counter() - t0, world)
     if pkv_check_device_error(loop.pool.handle) != 0:
         raise RuntimeError("device error flag set in the decode loop")

@@ -118,6 +118,7 @@ class _Bucket:
         self.v = self.Dv["v"].view(torch.bfloat16)
         self.out = torch.zeros(Bp, sc.Hq, sc.D, dtype=torch.bfloat16, device=device)
         self.out_host = torch.empty(Bp, sc.Hq, sc.D, dtype=torch.int16).pin_memory()
+        self.out_np = self.out_host.numpy().view(np.uint16)  # the step's output as the caller sees it
         ws = pkv_decode_workspace_bytes(loop.pool.handle, Bp, sc.Hq, loop.max_blocks)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
         self.graphs = {}  # one captured graph per input mode (q/K/V staged on the host or on the device)
@@ -189,8 +190,10 @@ class DecodeLoop:
         self.scale = 1.0 / math.sqrt(script.D)
         self.buckets = sorted(buckets)
         self._bk = {}
-        self.lens: dict[int, int] = {}
-        self.running: list[int] = []
+        # decoding sequences in admission order and the tokens each holds before this step's token
+        self._ids = np.zeros(0, dtype=np.int64)
+        self._pos = np.zeros(0, dtype=np.int64)
+        self.attended_tokens = 0  # context tokens the last step's decode attention read (all sequences)
         self.t = 0
         self.timing = {"admit_s": 0.0, "prepare_s": 0.0, "device_s": 0.0}  # host wall time per phase
         self.scheduler = (ChunkedContextScheduler(script.chunk, script.system, script.reuse) if script.chunk
@@ -210,6 +213,15 @@ class DecodeLoop:
         self.last_prefill = ([], None)  # chunked context: (chunks [(seq, p0, p1)], output bits)
         self._pf = None  # chunked context: staging of the prefill call's small inputs
         self._adm = None  # staging of the joiners' prompt slots
+
+    @property
+    def running(self) -> list:
+        return self._ids.tolist()
+
+    @property
+    def lens(self) -> dict:
+        """Tokens each decoding sequence holds before its next step's token."""
+        return dict(zip(self._ids.tolist(), self._pos.tolist()))
 
     def _bucket(self, B: int) -> _Bucket:
         Bp = next((b for b in self.buckets if b >= B), None)
@@ -251,8 +263,8 @@ class DecodeLoop:
                     dv = torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).to(self.device)
                 pkv_append(self.pool.handle, dk, dv, S.D["slots"][off:off + m])
                 off += m
-            self.lens[seq] = m
-            self.running.append(seq)
+        self._ids = np.concatenate([self._ids, np.array([q for q, _ in joined], dtype=np.int64)])
+        self._pos = np.concatenate([self._pos, np.array([m for _, m in joined], dtype=np.int64)])
 
     def _prefill_chunks(self, prefill):
         """One chunked-context prefill call for all of this step's prompt chunks: the chunks'
@@ -303,7 +315,8 @@ class DecodeLoop:
         return bk.dbuf[:bk.qkv_bytes], bk.q[:B], bk.k[:B], bk.v[:B]
 
     def step(self, inputs=None, device_inputs: bool = False):
-        """Run the next scheduled step; returns (decoding sequence ids, output [B][Hq][D] bf16 bits).
+        """Run the next scheduled step; returns (decoding sequence ids, output [B][Hq][D] bf16 bits: a
+        view of the batch bucket's pinned output buffer, valid until that bucket's next step).
         inputs: optional host (k_new, v_new, q) for the decoding sequences (else drawn from the
         script).  device_inputs: the step's q/K/V are already on the device, in the region
         device_input_region() names (written there before this call, on the current stream).
@@ -316,9 +329,9 @@ class DecodeLoop:
             pkv_seq_release(self.alloc, s)
             if sc.chunk:
                 self.scheduler.finish(s)
-                continue
-            self.running.remove(s)
-            del self.lens[s]
+        if finished and not sc.chunk:
+            keep = ~np.isin(self._ids, np.asarray(finished, dtype=np.int64))
+            self._ids, self._pos = self._ids[keep], self._pos[keep]
         if sc.chunk:
             for s, m in joined:
                 if sc.system and sc.reuse:  # the joiner forks the cached system prompt (partial block copied)
@@ -328,22 +341,22 @@ class DecodeLoop:
                 self.scheduler.admit(s, m)
             prefill, decode = self.scheduler.plan()
             pre_out = self._prefill_chunks(prefill) if prefill else None
-            self.running = decode
-            self.lens = {s: self.scheduler.cached(s) for s in decode}
+            self._ids = np.array(decode, dtype=np.int64)
+            self._pos = np.array([self.scheduler.cached(s) for s in decode], dtype=np.int64)
             self.scheduler.mark_decoded(decode)
             self.last_prefill = (prefill, pre_out)
         elif joined:
             self._admit(joined)
         t1 = time.perf_counter()
-        run = list(self.running)
-        if not run:
+        B = len(self._ids)
+        if not B:
             self.t += 1
+            self.attended_tokens = 0
             if sc.chunk and self.last_prefill[1] is not None:
                 torch.cuda.current_stream().synchronize()
-            return run, np.zeros((0, sc.Hq, sc.D), dtype=np.uint16)
-        B = len(run)
-        ids = np.array(run, dtype=np.int64)
-        pos = np.array([self.lens[s] for s in run], dtype=np.int64)
+            return [], np.zeros((0, sc.Hq, sc.D), dtype=np.uint16)
+        ids, pos = self._ids, self._pos
+        run = ids.tolist()
         bk = self._bucket(B)
         # room for this step's token, then tables, slots and lengths (padding rows included)
         _check(_L().pkv_stage_decode(self.alloc, ids.ctypes.data, pos.ctypes.data, B, bk.Bp, self.max_blocks,
@@ -379,11 +392,11 @@ class DecodeLoop:
         self.timing["admit_s"] += t1 - t0
         self.timing["prepare_s"] += t2 - t1
         self.timing["device_s"] += t3 - t2
+        self.attended_tokens = int(pos.sum()) + B
         if not sc.chunk:
-            for s in run:
-                self.lens[s] += 1
+            self._pos = pos + 1
         self.t += 1
-        return run, bk.out_host.numpy()[:B].view(np.uint16).copy()
+        return run, bk.out_np[:B]
 
     def close(self):
         self.pool.close()
