@@ -588,7 +588,7 @@ def run_prefill(args, world, rank, local):
     from paged_kv_cache_266_gb300.runner import PrefillStep
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    sc = W.make_prefill_script()
+    sc = W.make_prefill_script(kv_dtype=args.kv or "bf16")
     st = PrefillStep(sc, device=dev)
     flops = sc.flops()
     tokens = int(sc.cu_q[-1])
@@ -637,10 +637,14 @@ def run_prefill(args, world, rank, local):
             "metric": "chunked prefill attention over the paged pool: causal attention TFLOP/s, prompt tokens/s",
             "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 MMA, f32 accumulate", "data": "synthetic",
-            "config": {"workload": sc.name, "description": "8 sequences at seeded points of 32K prompts, one 512-token "
+            "vs_baseline": None,
+            "dtype": "bf16 MMA, f32 accumulate" if sc.kv_dtype == "bf16" else
+                     f"{sc.kv_dtype} pool widened on chip to f16, f16 MMA, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": sc.name if sc.kv_dtype == "bf16" else f"{sc.name}-{sc.kv_dtype}",
+                       "description": "8 sequences at seeded points of 32K prompts, one 512-token "
                        "chunk each (4096 tokens per step), Llama-3-8B layer shapes (32 q / 8 kv heads, head_dim 128), "
-                       "block 64", "batch": sc.B, "chunk_tokens": tokens, "past_tokens": [int(x) for x in sc.past],
+                       f"block 64, {sc.kv_dtype} pool", "kv_dtype": sc.kv_dtype, "batch": sc.B, "chunk_tokens": tokens, "past_tokens": [int(x) for x in sc.past],
                        "causal_flops_per_step": flops, "l2": "flushed before every timed launch"},
             "tokens_per_s": round(world * tokens / (ms * 1e-3), 1),
             "kernel_us": {"step": round(ms * 1e3, 2), "attention": round(attn * 1e3, 2),
@@ -763,8 +767,8 @@ def run_chunk_loop(args, world, rank, local):
     torch.cuda.set_device(local)
     n = args.warmup + args.steps
     sc = W.make_chunked_loop_script(index=55, n_steps=n, max_batch=args.loop_batch, Hq=32, Hkv=8, D=128,
-                                    block_size=64, kv_dtype="bf16", prompt_lo=256, prompt_hi=4096, p_finish=0.02,
-                                    chunk=args.chunk, system=args.system, reuse=not args.no_reuse)
+                                    block_size=64, kv_dtype=args.kv or "bf16", prompt_lo=256, prompt_hi=4096,
+                                    p_finish=0.02, chunk=args.chunk, system=args.system, reuse=not args.no_reuse)
     dev = f"cuda:{local}"
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     prompts = {}
@@ -811,8 +815,11 @@ def run_chunk_loop(args, world, rank, local):
             "metric": "in-flight loop with chunked context (one layer): prompt + decode tokens/s",
             "value": round(world * (pre_tok + dec_tok) / dt, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 KV; bf16 MMA / f32 accumulate", "data": "synthetic",
-            "config": {"workload": sc.name, "batch": sc.max_batch, "q_heads": sc.Hq, "kv_heads": sc.Hkv,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 KV; bf16 MMA / f32 accumulate" if sc.kv_dtype == "bf16" else
+                     f"{sc.kv_dtype} KV; f16 MMA / f32 accumulate", "data": "synthetic",
+            "config": {"workload": sc.name if sc.kv_dtype == "bf16" else f"{sc.name}-{sc.kv_dtype}",
+                       "kv_dtype": sc.kv_dtype, "batch": sc.max_batch, "q_heads": sc.Hq, "kv_heads": sc.Hkv,
                        "head_dim": sc.D, "block_size": sc.block_size, "chunk": sc.chunk, "prompts": "U[256,4096]",
                        "finish_prob_per_step": 0.02, "graphs": "decode: one per batch bucket"},
             "prompt_tokens_per_s": round(world * pre_tok / dt, 1), "decode_tokens_per_s": round(world * dec_tok / dt, 1),

@@ -51,26 +51,33 @@ namespace prefill {
 constexpr int kRows = 128;   // query rows per tile
 constexpr int kTiles = 2;    // query tiles per CTA
 constexpr int kKeys = 128;   // keys per KV tile
-constexpr int kKStages = 3;  // K ring: a K tile is free once both tiles' S MMAs have read it
+constexpr int kKStages = 3;  // K ring slots (barriers); a K tile is free once both tiles' S MMAs have read it
 constexpr int kVStages = 2;  // V ring: a V tile is free once both tiles' PV MMAs have read it
 constexpr int kThreads = 128 + kTiles * 128;  // control warpgroup + one softmax warpgroup per tile
 // register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded down to 8),
-// i.e. 64512 for the block; control 128 x 48 + softmax 256 x 224 = 63488 fits.
-constexpr uint32_t kRegsControl = 48, kRegsSoftmax = 224;
+// i.e. 64512 for the block; control 128 x 56 + softmax 256 x 224 = 64512 fits exactly.
+constexpr uint32_t kRegsControl = 56, kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + kTiles * 128 * kRegsSoftmax <= kThreads * 168, "register split");
 constexpr uint32_t kPanelBytes = 128u * 128u;      // 128 rows x 128 bytes (64 bf16 of a row)
 constexpr uint32_t kOffQ = 0;
-// Shared-memory layout for head_dim D (64 or 128): a row of Q, K or V is D / 64 panels.
-template <int D>
+// Shared-memory layout for head_dim D (64 or 128): a row of Q, K or V is D / 64 panels of 16-bit
+// elements.  One-byte pools (ONE) also stage one K and one V tile of codes (D bytes a row) for
+// the widening warps, and keep two K stages instead of three.
+template <int D, bool ONE>
 struct Layout {
     static constexpr int kPanels = D / 64;
+    static constexpr int kKSt = ONE ? 2 : kKStages;                // K ring stages in use
     static constexpr uint32_t kQBytes = kPanels * kPanelBytes;     // one Q tile
     static constexpr uint32_t kHalfBytes = kPanels * kPanelBytes;  // K (or V) of one KV tile
+    static constexpr uint32_t kCodeRow = D;                        // bytes of one row of codes
+    static constexpr uint32_t kCodeBytes = ONE ? kKeys * kCodeRow : 0u;  // codes of one K (or V) tile
     static constexpr uint32_t kOffK = kOffQ + kTiles * kQBytes;
-    static constexpr uint32_t kOffV = kOffK + kKStages * kHalfBytes;
-    static constexpr uint32_t kOffBar = kOffV + kVStages * kHalfBytes;
+    static constexpr uint32_t kOffV = kOffK + kKSt * kHalfBytes;
+    static constexpr uint32_t kOffCode = kOffV + kVStages * kHalfBytes;  // [K | V] code stage
+    static constexpr uint32_t kOffBar = kOffCode + 2 * kCodeBytes;
     static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(kOffCode % 1024 == 0, "code stage on a swizzle-pattern boundary");
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -79,7 +86,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kEndBar = 1;      // named barrier: every role done before TMEM is released
 constexpr int kMaxRankedSeqs = 512;  // above this the sequences are dispatched in index order
 constexpr int kSmallRankedSeqs = 64;  // up to this the ranking reads the inputs directly
-static_assert(kMaxRankedSeqs * sizeof(int64_t) <= kTiles * Layout<64>::kQBytes, "dispatch ranking fits the Q tiles' space");
+static_assert(kMaxRankedSeqs * sizeof(int64_t) <= kTiles * Layout<64, false>::kQBytes, "dispatch ranking fits the Q tiles' space");
 
 // mbarrier slots
 constexpr int kBarQ = 0;                          // Q rows of both tiles written (8 warps arrive)
@@ -90,7 +97,8 @@ constexpr int kBarVEmpty = kBarVFull + kVStages;  // [kVStages] last PV MMA read
 constexpr int kBarS = kBarVEmpty + kVStages;      // [kTiles] S_t(j) ready (commit)
 constexpr int kBarP = kBarS + kTiles;             // [kTiles] P_t(j) in TMEM (4 warps arrive)
 constexpr int kBarO = kBarP + kTiles;             // [kTiles] last PV_t done (commit)
-constexpr int kBarDrain = kBarO + kTiles;         // MMAs in flight done (error path)
+constexpr int kBarCode = kBarO + kTiles;          // [2] K / V code stage landed (one-byte pools; tx bytes)
+constexpr int kBarDrain = kBarCode + 2;           // MMAs in flight done (error path)
 constexpr int kNumBars = kBarDrain + 1;
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -100,6 +108,7 @@ struct Params {
     const int32_t* cu_q;
     const int32_t* tables;
     const int32_t* ctx;
+    const float* scales;  // one-byte pools: [num_blocks][Hkv][4] (K scale, V scale, unused, unused)
     int* err;
     int B, Hq, Hkv, G, max_blocks, bs, part, num_blocks, tiles;
     int32_t oob_row;  // a row coordinate past the pool: the copy fills the box with zeros
@@ -126,16 +135,114 @@ __device__ __forceinline__ void umma_ss_k64_x4(uint32_t d_tmem, uint32_t a_lo, u
         "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc));
 }
 
+// 2^e as two normal fp32 factors (x * a * b scales x exactly while the result stays normal);
+// e is clamped to [-252, 252], beyond which no finite product of such factors is normal anyway.
+__device__ __forceinline__ void pow2_pair(int e, float& a, float& b) {
+    e = max(-252, min(252, e));
+    const int ea = e / 2, eb = e - ea;
+    a = __int_as_float((127 + ea) << 23);
+    b = __int_as_float((127 + eb) << 23);
+}
+
+// Exponent of the leading bit of a positive finite fp32 given by its bits (subnormals included).
+__device__ __forceinline__ int lead_exp(uint32_t bits) {
+    const int E = (int)(bits >> 23);
+    return E ? E - 127 : (31 - __clz((int)bits)) - 149;
+}
+
+// Four one-byte codes (byte 0 first) -> two f16x2 holding the codes' values exactly: E4M3 by
+// the hardware conversion (every E4M3 value is an f16); INT8 in [-127, 127] by writing code + 128
+// into the low mantissa bits of 1024.0 (f16 0x6400) and subtracting 1152, both exact.
+template <int KV>
+__device__ __forceinline__ void widen4(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    if constexpr (KV == 2) {
+        const uint32_t x = four ^ 0x80808080u;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(__byte_perm(x, 0x64u, 0x4140)), "r"(0x64806480u));
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(__byte_perm(x, 0x64u, 0x4342)), "r"(0x64806480u));
+    } else {
+        lo = ptx::e4m3x2_to_f16x2(four);
+        hi = ptx::e4m3x2_to_f16x2(four >> 16);
+    }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// code x (s_hi + s_lo) for a pair of widened codes, rounded once to f16: s_hi = f16(s) and
+// s_lo = f16(s - s_hi) carry the fp32 scale to 22 bits, the small product c s_lo is rounded
+// first (its error is below 2^-11 of c s_lo) and the fma adds c s_hi with one rounding.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t c, uint32_t s_hi, uint32_t s_lo) {
+    uint32_t d;
+    asm("{\n\t.reg .b32 t;\n\tmul.rn.f16x2 t, %1, %3;\n\tfma.rn.f16x2 %0, %1, %2, t;\n\t}"
+        : "=r"(d) : "r"(c), "r"(s_hi), "r"(s_lo));
+    return d;
+}
+
+// the scale of a page part as the (hi, lo) f16x2 pair scale_f16x2 takes
+__device__ __forceinline__ void split_scale(float v, uint32_t& s_hi, uint32_t& s_lo) {
+    s_hi = ptx::pack_f16x2(v, v);
+    const float r = v - ptx::f16x2_to_f32x2(s_hi).x;
+    s_lo = ptx::pack_f16x2(r, r);
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator, A and B both f16 (F16) or both bf16.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int a_mn, int b_mn, bool f16) {
+    return f16 ? (ptx::umma_idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10)))
+               : ptx::umma_idesc_bf16(M, N, a_mn, b_mn);
+}
+
+// Eight steps of D += A B with A (P) in tensor memory, 8 columns (16 keys) per step, and B = V^T
+// K-major (one 128-byte swizzled line of 64 keys per d): a step advances B by 32 bytes (+2 in
+// the start field), keys 64-127 sit one panel of D lines further (+PANEL).  Step kk runs only if
+// kk < nk; step 0 accumulates only if acc0 != 0.
+template <uint32_t PANEL>
+__device__ __forceinline__ void umma_ts_kmajor_x8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                  uint32_t idesc, uint32_t acc0, int nk) {
+    asm volatile(
+        "{\n\t.reg .pred pa, pt, g1, g2, g3, g4, g5, g6, g7;\n\t.reg .b32 ta, bl;\n\t.reg .b64 b;\n\t"
+        "setp.ne.b32 pa, %5, 0;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+        "setp.gt.s32 g1, %6, 1;\n\tsetp.gt.s32 g2, %6, 2;\n\tsetp.gt.s32 g3, %6, 3;\n\t"
+        "setp.gt.s32 g4, %6, 4;\n\tsetp.gt.s32 g5, %6, 5;\n\tsetp.gt.s32 g6, %6, 6;\n\t"
+        "setp.gt.s32 g7, %6, 7;\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, pa;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.u32 bl, %2, 2;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g1 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.u32 bl, %2, 4;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g2 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.u32 bl, %2, 6;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g3 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 32;\n\tadd.u32 bl, %2, %7;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g4 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 40;\n\tadd.u32 bl, %2, %8;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g5 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 48;\n\tadd.u32 bl, %2, %9;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g6 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+        "add.u32 ta, %1, 56;\n\tadd.u32 bl, %2, %10;\n\tmov.b64 b, {bl, %3};\n\t"
+        "@g7 tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc0), "r"(nk), "n"(PANEL), "n"(PANEL + 2), "n"(PANEL + 4),
+        "n"(PANEL + 6));
+}
+
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
 }
 
-template <int PART, int D>
+// KV: 0 bf16 pool, 1 FP8-E4M3 pool, 2 INT8 pool.
+template <int PART, int D, int KV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
     static_assert(PART == 16 || PART == 32 || PART == 64, "page part of 16, 32 or 64 rows");
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-    using LY = Layout<D>;
+    constexpr bool ONE = KV != 0;  // one-byte codes with per-(block, head) scales
+    using LY = Layout<D, ONE>;
+    constexpr int KS = LY::kKSt;
     constexpr uint32_t kQBytes = LY::kQBytes, kHalfBytes = LY::kHalfBytes;
     constexpr uint32_t kOffK = LY::kOffK, kOffV = LY::kOffV, kOffBar = LY::kOffBar;
     constexpr int kPanels = LY::kPanels;
@@ -226,6 +333,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_tile = nkv[1] > 0 ? 1 : 0;
     const int n_kv = nkv[last_tile];  // the last active tile sees the most keys
 
+    // One-byte pools: the largest K scale and V scale over this sequence's blocks for head h
+    // (per warp here, combined after the barrier below).  They fix the powers of two 2^-eK, 2^-eV
+    // that bring code x scale into f16 range (largest |value| below 2^16) for the widened tiles.
+    __shared__ uint32_t scale_max_s[kThreads / 32][2];
+    if constexpr (ONE) {
+        const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
+        const int nb = (L + p.bs - 1) / p.bs;
+        uint32_t mk = 0, mv = 0;  // fp32 bits: non-negative scales order like their bits
+        for (int i = threadIdx.x; i < nb; i += kThreads) {
+            const int blk = tb[i];
+            if (blk >= 0 && blk < p.num_blocks) {
+                const float2 sc = *reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + h) * 4);
+                mk = max(mk, __float_as_uint(sc.x));
+                mv = max(mv, __float_as_uint(sc.y));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+            mv = max(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+        }
+        if (lane == 0) {
+            scale_max_s[warp][0] = mk;
+            scale_max_s[warp][1] = mv;
+        }
+    }
+    // e such that the largest scale times 2^-e lies in [64, 128): codes up to 448 (E4M3) or 127
+    // (INT8) then give |value| < 2^16 in f16.  0 for a sequence whose scales are all zero.
+    auto scale_exp = [&](int kv) -> int {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) m = max(m, scale_max_s[w][kv]);
+        return m ? lead_exp(m) - 6 : 0;
+    };
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool wg_arrive = i == kBarQ || (i >= kBarP && i < kBarP + kTiles);
@@ -242,12 +384,165 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
       ptx::regs_dec<kRegsControl>();  // the whole control warpgroup, one instruction
-      if (warp == 0 || warp == 2) {
+      if (ONE && (warp == 0 || warp == 2)) {
+        // ---------------------------------------------------------------- one-byte K / V streams
+        // warp 0 K, warp 2 V.  Per KV tile: one 2-D copy of PART code rows per page part into
+        // the code stage (rows past the context read zeros), then the warp widens the codes into
+        // the f16 ring in the panel layout the MMA reads (128-byte swizzled lines): value =
+        // code x (scale x 2^-e), the scale that of the row's (block, head), rounded once to f16.
+        // The next tile's copy goes out as soon as the codes have been read.
+        const int kv = warp == 0 ? 0 : 1;
+        const int stages = kv ? kVStages : KS;
+        const uint32_t ring = kv ? sV : sK;
+        const uint32_t code = base + LY::kOffCode + (uint32_t)kv * LY::kCodeBytes;
+        const int full = kv ? kBarVFull : kBarKFull, empty = kv ? kBarVEmpty : kBarKEmpty;
+        const uint32_t cbar = bar(kBarCode + kv);
+        const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
+        float fa, fb;  // 2^-e
+        pow2_pair(-scale_exp(kv), fa, fb);
+        // the copies of tile j's page parts; lane pi < kParts returns part pi's scale
+        auto issue = [&](int j) -> float {
+            if (lane == 0) ptx::mbar_arrive_expect_tx(cbar, LY::kCodeBytes + p.stall_tx);
+            __syncwarp();
+            float sc = 0.f;
+            if (lane < kParts) {
+                const int tok = j * kKeys + lane * PART;
+                int32_t row = p.oob_row;
+                if (tok < L) {
+                    const int blk = tb[tok / p.bs];
+                    if (blk >= 0 && blk < p.num_blocks) {
+                        row = (int32_t)((((int64_t)2 * blk + kv) * p.Hkv + h) * p.bs + (tok % p.bs));
+                        sc = p.scales[((int64_t)blk * p.Hkv + h) * 4 + kv];
+                    } else if (kv == 0) {
+                        atomicOr(p.err, kErrBounds);
+                    }
+                }
+                ptx::tma_load_2d(code + (uint32_t)(lane * PART) * LY::kCodeRow, &tmap, 0, row, cbar);
+            }
+            return sc;
+        };
+        float sc_next = issue(0);
+        int issued = 1, landed = 0;  // code copies issued / seen complete (lane 0)
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const int slot = j % stages;
+            if (lane == 0) {
+                ok = ptx::mbar_wait(cbar, j & 1, p.wait_ns);
+                if (ok) landed = j + 1;
+                if (ok && j >= stages) ok = ptx::mbar_wait(bar(empty + slot), ((j / stages) - 1) & 1, p.wait_ns);
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            if (__shfl_sync(0xffffffffu, abort_s, 0)) break;  // warp-uniform
+            const float sc_cur = sc_next;
+            const uint32_t dst0 = ring + (uint32_t)slot * kHalfBytes;
+            if (kv == 1) {
+                // V codes: the pool keeps a V page as 16-token panels [d][16 codes], the tokens in the
+                // pair order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 (the decode MMA's fragment); one
+                // 16-byte chunk is the 16 tokens of one d.  Widened into V^T, K-major for the P.V MMA:
+                // [64-key panel][d line][128 bytes: 64 keys], 128-byte swizzled -- no transpose, four
+                // byte permutes restore the token order.  The code stage holds the panels as the copy
+                // wrote them: line = 16 group + 16 d / D of D bytes, in the copy's swizzle.
+                constexpr uint32_t kVtPanel = (uint32_t)D * 128u;
+#pragma unroll 1
+                for (int G = 0; G < kKeys / 16; ++G) {
+                    uint32_t s_hi, s_lo;
+                    split_scale(__shfl_sync(0xffffffffu, sc_cur, (16 * G) / PART) * fa * fb, s_hi, s_lo);
+#pragma unroll 2
+                    for (int qd = 0; qd < D / 32; ++qd) {
+                        const int d = 32 * qd + lane;
+                        uint32_t src;
+                        if constexpr (D == 128)
+                            src = code + (uint32_t)(16 * G + (d >> 3)) * 128u + ((uint32_t)((d & 7) ^ ((d >> 3) & 7)) << 4);
+                        else
+                            src = code + (uint32_t)(16 * G + (d >> 2)) * 64u + ((uint32_t)((d & 3) ^ ((d >> 3) & 3)) << 4);
+                        const uint4 w = lds128(src);
+                        uint32_t o[8];
+                        widen4<KV>(__byte_perm(w.x, w.y, 0x5410), o[0], o[1]);  // tokens 0-3
+                        widen4<KV>(__byte_perm(w.z, w.w, 0x5410), o[2], o[3]);  // tokens 4-7
+                        widen4<KV>(__byte_perm(w.x, w.y, 0x7632), o[4], o[5]);  // tokens 8-11
+                        widen4<KV>(__byte_perm(w.z, w.w, 0x7632), o[6], o[7]);  // tokens 12-15
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = scale_f16x2(o[e], s_hi, s_lo);
+                        const uint32_t dst = dst0 + (uint32_t)(G >> 2) * kVtPanel + (uint32_t)d * 128u;
+                        const int cc = (G & 3) * 2;
+                        sts128(dst + ((uint32_t)(cc ^ (d & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        sts128(dst + ((uint32_t)((cc + 1) ^ (d & 7)) << 4), o[4], o[5], o[6], o[7]);
+                    }
+                }
+            } else if constexpr (D == 128) {
+                // 4 rows a pass, 8 lanes a row, 16 codes a lane -> 32 bytes of f16 (two 16-byte
+                // chunks of one panel)
+                const int rs = lane >> 3, c = lane & 7;
+#pragma unroll 1
+                for (int pi = 0; pi < kParts; ++pi) {
+                    uint32_t s_hi, s_lo;
+                    split_scale(__shfl_sync(0xffffffffu, sc_cur, pi) * fa * fb, s_hi, s_lo);
+#pragma unroll 2
+                    for (int it = 0; it < PART / 4; ++it) {
+                        const int r = pi * PART + it * 4 + rs;
+                        const uint4 w = lds128(code + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4));
+                        uint32_t o[8];
+                        widen4<KV>(w.x, o[0], o[1]);
+                        widen4<KV>(w.y, o[2], o[3]);
+                        widen4<KV>(w.z, o[4], o[5]);
+                        widen4<KV>(w.w, o[6], o[7]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = scale_f16x2(o[e], s_hi, s_lo);
+                        const uint32_t dst = dst0 + (uint32_t)(c >> 2) * kPanelBytes;
+                        const int cc = (c & 3) * 2;
+                        sts128(dst + swz128(r, cc), o[0], o[1], o[2], o[3]);
+                        sts128(dst + swz128(r, cc + 1), o[4], o[5], o[6], o[7]);
+                    }
+                }
+            } else {
+                // 64-byte code rows (64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)):
+                // 8 rows a pass, 4 lanes a row
+                const int rs = lane >> 2, c = lane & 3;
+#pragma unroll 1
+                for (int pi = 0; pi < kParts; ++pi) {
+                    uint32_t s_hi, s_lo;
+                    split_scale(__shfl_sync(0xffffffffu, sc_cur, pi) * fa * fb, s_hi, s_lo);
+#pragma unroll 2
+                    for (int it = 0; it < PART / 8; ++it) {
+                        const int r = pi * PART + it * 8 + rs;
+                        const uint4 w = lds128(code + (uint32_t)r * 64u + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4));
+                        uint32_t o[8];
+                        widen4<KV>(w.x, o[0], o[1]);
+                        widen4<KV>(w.y, o[2], o[3]);
+                        widen4<KV>(w.z, o[4], o[5]);
+                        widen4<KV>(w.w, o[6], o[7]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = scale_f16x2(o[e], s_hi, s_lo);
+                        sts128(dst0 + swz128(r, 2 * c), o[0], o[1], o[2], o[3]);
+                        sts128(dst0 + swz128(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
+                    }
+                }
+            }
+            // widened rows visible to the MMAs (async proxy), and the code reads ordered before
+            // the next copy overwrites the stage
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(full + slot));
+            if (j + 1 < n_kv) {
+                sc_next = issue(j + 1);
+                issued = j + 2;
+            }
+        }
+        if (!ok && lane == 0) {
+            atomicOr(p.err, kErrTimeout);
+            abort_s = 1;
+        }
+        // a copy still in flight lands before the CTA can leave (bounded like every wait)
+        if (issued > landed && lane == 0) ptx::mbar_wait(cbar, (issued - 1) & 1, p.wait_ns);
+        __syncwarp();
+        ptx::named_barrier_sync(kEndBar, kThreads);
+      } else if (warp == 0 || warp == 2) {
         // ---------------------------------------------------------------- producers
         // warp 0 fills the K ring, warp 2 the V ring; each KV tile is two 128-row panels (the
         // 64-element halves), one 2-D copy of PART rows per (page part, half)
         const int kv = warp == 0 ? 0 : 1;
-        const int stages = kv ? kVStages : kKStages;
+        const int stages = kv ? kVStages : KS;
         const uint32_t ring = kv ? sV : sK;
         const int full = kv ? kBarVFull : kBarKFull, empty = kv ? kBarVEmpty : kBarKEmpty;
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
@@ -289,13 +584,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // descriptors are built once; the start-address field counts 16-byte units, so moving
             // an operand by X bytes adds X >> 4 (addresses stay below 256 KB: no carry out)
-            constexpr uint32_t idS = ptx::umma_idesc_bf16(128, kKeys, 0, 0);
-            constexpr uint32_t idO = ptx::umma_idesc_bf16(128, D, 0, 1);
+            // operands f16 for one-byte pools (widened K/V, rescaled Q, P), bf16 otherwise
+            constexpr uint32_t idS = idesc_f16kind(128, kKeys, 0, 0, ONE);
+            constexpr uint32_t idO = idesc_f16kind(128, D, 0, ONE ? 0 : 1, ONE);  // one-byte: V^T K-major
             // a descriptor's high half (stride, version, swizzle) is the same for Q and K; V's
             // differs only in the low half (its panel stride)
             const uint64_t dQ0 = ptx::umma_sdesc_sw128(base + kOffQ, 16, 1024);
             const uint64_t dK0 = ptx::umma_sdesc_sw128(sK, 16, 1024);
-            const uint64_t dV0 = ptx::umma_sdesc_sw128(sV, kPanelBytes, 1024);
+            const uint64_t dV0 = ONE ? ptx::umma_sdesc_sw128(sV, 16, 1024) : ptx::umma_sdesc_sw128(sV, kPanelBytes, 1024);
             const uint32_t hi = (uint32_t)(dQ0 >> 32);
             const uint32_t q_lo = (uint32_t)dQ0, k_lo = (uint32_t)dK0, v_lo = (uint32_t)dV0;
             int k_ready = 0, v_ready = 0;  // K / V tiles whose copies this thread has waited for
@@ -303,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             auto wait_k = [&](int j) -> bool {
                 if (j < k_ready) return true;
-                if (!ptx::mbar_wait(bar(kBarKFull + j % kKStages), (j / kKStages) & 1, p.wait_ns)) return false;
+                if (!ptx::mbar_wait(bar(kBarKFull + j % KS), (j / KS) & 1, p.wait_ns)) return false;
                 ptx::tc_fence_after();
                 k_ready = j + 1;
                 return true;
@@ -321,13 +617,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s = [&](int t, int j) {
                 if constexpr (D == 128)
                     ptx::umma_ss_k128_x8(tmem + (uint32_t)(t * kKeys), q_lo + (uint32_t)t * (kQBytes >> 4),
-                                         k_lo + (uint32_t)(j % kKStages) * (kHalfBytes >> 4), hi, idS);
+                                         k_lo + (uint32_t)(j % KS) * (kHalfBytes >> 4), hi, idS);
                 else
                     umma_ss_k64_x4(tmem + (uint32_t)(t * kKeys), q_lo + (uint32_t)t * (kQBytes >> 4),
-                                        k_lo + (uint32_t)(j % kKStages) * (kHalfBytes >> 4), hi, idS);
+                                        k_lo + (uint32_t)(j % KS) * (kHalfBytes >> 4), hi, idS);
                 ptx::umma_commit(bar(kBarS + t));
                 // the last tile's S releases the K tile, if a later tile reuses its slot
-                if (t == last_tile && j + kKStages < n_kv) ptx::umma_commit(bar(kBarKEmpty + j % kKStages));
+                if (t == last_tile && j + KS < n_kv) ptx::umma_commit(bar(kBarKEmpty + j % KS));
             };
             // O_t += P_t(j) V_j: 16 keys per MMA, A from TMEM; on the first KV tile also the lo part
             auto issue_pv = [&](int t, int j) {
@@ -335,8 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tP = tmem + (uint32_t)(t * kKeys), tO = tmem + kColO + (uint32_t)(t * D);
                 const int left = L - j * kKeys;  // keys of this tile inside the context (> 0)
                 const int nk = left >= kKeys ? kKeys / 16 : (left + 15) / 16;
-                ptx::umma_ts_x8(tO, tP, dv, hi, idO, j > 0 ? 1u : 0u, nk);
-                if (j == 0) ptx::umma_ts_x8(tO, tP + 64u, dv, hi, idO, 1u, nk);
+                if constexpr (ONE) {  // B = V^T, K-major lines of 64 keys, panels of D lines
+                    umma_ts_kmajor_x8<(uint32_t)D * 8u>(tO, tP, dv, hi, idO, j > 0 ? 1u : 0u, nk);
+                    if (j == 0) umma_ts_kmajor_x8<(uint32_t)D * 8u>(tO, tP + 64u, dv, hi, idO, 1u, nk);
+                } else {
+                    ptx::umma_ts_x8(tO, tP, dv, hi, idO, j > 0 ? 1u : 0u, nk);
+                    if (j == 0) ptx::umma_ts_x8(tO, tP + 64u, dv, hi, idO, 1u, nk);
+                }
             };
             if (ok) ok = wait_k(0);
             if (ok)
@@ -387,20 +688,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok = t0 + t * T + r / p.G, g = r % p.G;
         const bool valid = tok < n;
         const int qlim = min(L - n + tok, L - 1);  // last key this row may see
+        int eq = 0;  // one-byte pools: the row is staged as q x 2^eq in f16
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * D);
             uint8_t* qt = sm + kOffQ + (uint32_t)t * kQBytes;
+            if constexpr (ONE) {
+                // the MMA takes f16 with the widened K/V: scale the row by the power of two that
+                // puts its largest |q| in [2^15, 2^16), then convert -- exact for every element
+                // down to 2^-24 below that maximum (2^-31 of the row's largest term), so the
+                // products are those of the bf16 q; the power of two leaves with the score scale
+                uint4 v[D / 8];
+                uint32_t mx = 0;  // largest bf16 magnitude bits of the row (they order like the values)
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(qt + (uint32_t)(c >> 3) * kPanelBytes + swz128(r, c & 7)) = v;
+                for (int c = 0; c < D / 8; ++c) {
+                    v[c] = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    mx = max(mx, max(max(v[c].x & 0x7fffu, (v[c].x >> 16) & 0x7fffu),
+                                     max(v[c].y & 0x7fffu, (v[c].y >> 16) & 0x7fffu)));
+                    mx = max(mx, max(max(v[c].z & 0x7fffu, (v[c].z >> 16) & 0x7fffu),
+                                     max(v[c].w & 0x7fffu, (v[c].w >> 16) & 0x7fffu)));
+                }
+                if (mx) eq = 15 - lead_exp(mx << 16);
+                float fa, fb;
+                pow2_pair(eq, fa, fb);
+                auto cv = [&](uint32_t x) {
+                    return ptx::pack_f16x2(ptx::bf16lo_to_f32(x) * fa * fb, ptx::bf16hi_to_f32(x) * fa * fb);
+                };
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c)
+                    *reinterpret_cast<uint4*>(qt + (uint32_t)(c >> 3) * kPanelBytes + swz128(r, c & 7)) =
+                        make_uint4(cv(v[c].x), cv(v[c].y), cv(v[c].z), cv(v[c].w));
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(qt + (uint32_t)(c >> 3) * kPanelBytes + swz128(r, c & 7)) = v;
+                }
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarQ));
         }
         const int my_nkv = nkv[t];
-        const float c2 = p.scale_log2;
+        // scores in base 2: S x scale x log2(e); one-byte pools compute S' = (q 2^eq).(K 2^-eK)
+        float c2 = p.scale_log2;
+        if constexpr (ONE) {
+            float fa, fb;
+            pow2_pair(scale_exp(0) - eq, fa, fb);
+            c2 = c2 * fa * fb;
+        }
+        // P into tensor memory: f16 beside f16 V (one-byte pools), bf16 otherwise
+        auto packP = [](float lo, float hi) { return ONE ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi); };
         float m = -INFINITY, l = 0.f;  // running maximum (scaled, base 2) and sum
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
@@ -459,8 +796,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
                             c2x2, nmx2));
                         const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
-                        hi[e] = ptx::pack_bf16x2(p0, p1);
-                        lo[e] = ptx::pack_bf16x2(p0 - ptx::bf16lo_to_f32(hi[e]), p1 - ptx::bf16hi_to_f32(hi[e]));
+                        hi[e] = packP(p0, p1);
+                        if constexpr (ONE) {
+                            const float2 hv = ptx::f16x2_to_f32x2(hi[e]);
+                            lo[e] = packP(p0 - hv.x, p1 - hv.y);
+                        } else {
+                            lo[e] = packP(p0 - ptx::bf16lo_to_f32(hi[e]), p1 - ptx::bf16hi_to_f32(hi[e]));
+                        }
                         l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
@@ -476,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
                             c2x2, nmx2));
                         const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
-                        hi[e] = ptx::pack_bf16x2(p0, p1);
+                        hi[e] = packP(p0, p1);
                         l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
@@ -496,7 +838,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarO + t), 0, p.wait_ns));
             if (ok) {
                 ptx::tc_fence_after();
-                const float inv = 1.f / l;
+                float inv = 1.f / l;
+                if constexpr (ONE) {  // O was accumulated over V x 2^-eV
+                    float fa, fb;
+                    pow2_pair(scale_exp(1), fa, fb);
+                    inv = inv * fa * fb;
+                }
                 uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * D);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -528,15 +875,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace prefill
 
+namespace {
+
+template <int KV>
+void configure_kv() {
+    using namespace prefill;
+    constexpr int s128 = (int)Layout<128, KV != 0>::kSmemBytes, s64 = (int)Layout<64, KV != 0>::kSmemBytes;
+    cudaFuncSetAttribute(prefill_kernel<16, 128, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, s128);
+    cudaFuncSetAttribute(prefill_kernel<32, 128, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, s128);
+    cudaFuncSetAttribute(prefill_kernel<64, 128, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, s128);
+    cudaFuncSetAttribute(prefill_kernel<16, 64, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64);
+    cudaFuncSetAttribute(prefill_kernel<32, 64, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64);
+    cudaFuncSetAttribute(prefill_kernel<64, 64, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, s64);
+}
+
+// the instance for (page part, head_dim, KV type)
+template <int KV>
+const void* kernel_for(int part, bool d64) {
+    using prefill::prefill_kernel;
+    if (d64) {
+        switch (part) {
+            case 16: return (const void*)prefill_kernel<16, 64, KV>;
+            case 32: return (const void*)prefill_kernel<32, 64, KV>;
+            default: return (const void*)prefill_kernel<64, 64, KV>;
+        }
+    }
+    switch (part) {
+        case 16: return (const void*)prefill_kernel<16, 128, KV>;
+        case 32: return (const void*)prefill_kernel<32, 128, KV>;
+        default: return (const void*)prefill_kernel<64, 128, KV>;
+    }
+}
+
+}  // namespace
+
 void prefill_configure(pkv_pool* pool) {
     (void)pool;
-    using namespace prefill;
-    cudaFuncSetAttribute(prefill_kernel<16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<128>::kSmemBytes);
-    cudaFuncSetAttribute(prefill_kernel<32, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<128>::kSmemBytes);
-    cudaFuncSetAttribute(prefill_kernel<64, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<128>::kSmemBytes);
-    cudaFuncSetAttribute(prefill_kernel<16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<64>::kSmemBytes);
-    cudaFuncSetAttribute(prefill_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<64>::kSmemBytes);
-    cudaFuncSetAttribute(prefill_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<64>::kSmemBytes);
+    configure_kv<0>();
+    configure_kv<1>();
+    configure_kv<2>();
 }
 
 // Argument checks shared by the prefill entry points; fills the kernel parameters and grid.
@@ -546,7 +923,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     using namespace prefill;
     if (!pool || B < 0 || max_q_len < 0 || Hq < 1) return PKV_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;  // masking relies on scale > 0
-    if (pool->dtype != PKV_KV_BF16 || (pool->head_dim != 64 && pool->head_dim != 128)) return PKV_ERR_INVALID_ARG;
+    if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_INVALID_ARG;
     if (Hq % pool->n_kv_heads) return PKV_ERR_INVALID_ARG;
     const int G = Hq / pool->n_kv_heads;
     if (G > kRows || (G & (G - 1))) return PKV_ERR_INVALID_ARG;
@@ -564,6 +941,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
     p.cu_q = cu_q;
     p.tables = tables;
     p.ctx = ctx;
+    p.scales = pool->scales;
     p.err = pool->err;
     p.Hq = Hq;
     p.Hkv = pool->n_kv_heads;
@@ -593,28 +971,20 @@ pkv_status prefill_launch(const pkv_pool* pool, const prefill::Params& p, dim3 g
     cfg.gridDim = grid;
     cfg.blockDim = dim3(prefill::kThreads);
     const bool d64 = pool->head_dim == 64;
-    cfg.dynamicSmemBytes = d64 ? prefill::Layout<64>::kSmemBytes : prefill::Layout<128>::kSmemBytes;
+    const bool one = pool->dtype != PKV_KV_BF16;
+    cfg.dynamicSmemBytes = d64 ? (one ? prefill::Layout<64, true>::kSmemBytes : prefill::Layout<64, false>::kSmemBytes)
+                               : (one ? prefill::Layout<128, true>::kSmemBytes : prefill::Layout<128, false>::kSmemBytes);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    using prefill::prefill_kernel;
-    cudaError_t e;
-    if (d64) {
-        switch (p.part) {
-            case 16: e = cudaLaunchKernelEx(&cfg, prefill_kernel<16, 64>, pool->tmap_panel, p); break;
-            case 32: e = cudaLaunchKernelEx(&cfg, prefill_kernel<32, 64>, pool->tmap_panel, p); break;
-            default: e = cudaLaunchKernelEx(&cfg, prefill_kernel<64, 64>, pool->tmap_panel, p); break;
-        }
-    } else {
-        switch (p.part) {
-            case 16: e = cudaLaunchKernelEx(&cfg, prefill_kernel<16, 128>, pool->tmap_panel, p); break;
-            case 32: e = cudaLaunchKernelEx(&cfg, prefill_kernel<32, 128>, pool->tmap_panel, p); break;
-            default: e = cudaLaunchKernelEx(&cfg, prefill_kernel<64, 128>, pool->tmap_panel, p); break;
-        }
-    }
+    const void* fn = pool->dtype == PKV_KV_FP8_E4M3 ? kernel_for<1>(p.part, d64)
+                     : pool->dtype == PKV_KV_INT8   ? kernel_for<2>(p.part, d64)
+                                                    : kernel_for<0>(p.part, d64);
+    void* args[] = {const_cast<CUtensorMap*>(&pool->tmap_panel), const_cast<prefill::Params*>(&p)};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -160,10 +160,13 @@ def test_chunk_plans_cover_every_prompt_once():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("bs,graphs", [(16, True), (64, False)])
-def test_chunked_context_loop_matches_oracle_every_step(bs, graphs):
-    """Chunked context in the in-flight loop: every step's prefill-chunk outputs and decode
-    outputs against the oracle's replay, and the final pool bytes bit-exact."""
+@pytest.mark.parametrize("bs,graphs,kv_dtype", [(16, True, "bf16"), (64, False, "bf16"), (16, True, "fp8_e4m3"),
+                                                (64, False, "int8")])
+def test_chunked_context_loop_matches_oracle_every_step(bs, graphs, kv_dtype):
+    """Chunked context in the in-flight loop, on bf16 pools and on FP8 / INT8 pools (the chunks'
+    K/V quantised by the append, the prefill widening the codes on chip): every step's
+    prefill-chunk outputs and decode outputs against the oracle's replay, and the final pool bytes
+    bit-exact."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -171,15 +174,16 @@ def test_chunked_context_loop_matches_oracle_every_step(bs, graphs):
     build.build()
     import paged_kv_cache_266_gb300 as pkv
     from paged_kv_cache_266_gb300.engine import DecodeLoop
-    sc = W.make_chunked_loop_script(index=47, n_steps=20, block_size=bs, chunk=48)
+    sc = W.make_chunked_loop_script(index=47, n_steps=20, block_size=bs, chunk=48, kv_dtype=kv_dtype)
     ref, pool = odrive.run_chunked_loop(sc)
     loop = DecodeLoop(sc, graphs=graphs)
+    tol = 3e-2 if kv_dtype != "bf16" else 1e-2  # the decode bound of each pool type
     for t in range(len(sc.steps)):
         run, out = loop.step()
         assert run == ref[t][0]
         if run:
             err = np.abs(oracle.bf16_bits_to_f64(out) - ref[t][1])
-            assert err.max() <= 1e-2 and err.mean() <= TOL_MEAN, ("decode", t, err.max(), err.mean())
+            assert err.max() <= tol and err.mean() <= TOL_MEAN, ("decode", t, err.max(), err.mean())
         chunks, pre = loop.last_prefill
         assert chunks == ref[t][2]
         if chunks:
@@ -187,9 +191,11 @@ def test_chunked_context_loop_matches_oracle_every_step(bs, graphs):
             err = np.abs(got - ref[t][3])
             assert err.max() <= 1e-2 and err.mean() <= TOL_MEAN, ("prefill", t, err.max(), err.mean())
     assert pkv.pkv_check_device_error(loop.pool.handle) == pkv.PKV_OK
-    kv, kv_bytes, _, _ = pkv.pkv_pool_raw(loop.pool.handle)
+    kv, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(loop.pool.handle)
     from paged_kv_cache_266_gb300.runner import _wrap_device
     assert np.array_equal(_wrap_device(kv, kv_bytes).cpu().numpy(), pool.data)
+    if kv_dtype != "bf16":
+        assert np.array_equal(_wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32), pool.scales)
     loop.close()
 
 

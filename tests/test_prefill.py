@@ -8,6 +8,9 @@ import pytest
 import oracle
 
 
+KV_CODE = {"bf16": 0, "fp8_e4m3": 1, "int8": 2}  # the oracle pool's element code
+
+
 def _bf16_bits(x):
     import torch
     return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
@@ -118,6 +121,23 @@ def test_prefill_rows_equal_decode_and_chunks_compose():
         assert np.array_equal(part, whole[c0:c1])
 
 
+@pytest.mark.parametrize("code", [1, 2])
+def test_prefill_rows_equal_decode_on_one_byte_pools(code):
+    """On FP8 and INT8 pools too, a prefill row is the decode definition over the context ending
+    at its position: the same dequantised K/V (code x the (block, head) scale) and the same
+    softmax, so the two oracle paths give identical values."""
+    rng = np.random.default_rng(40 + code)
+    bs, Hkv, G, D, L = 16, 2, 4, 64, 70
+    Hq = Hkv * G
+    a, pool, tables, _, _ = _build(rng, [L], bs, Hkv, D, fp8=code)
+    assert np.any(pool.scales != 0) and np.any(pool.scales != 1)
+    q = _bf16_bits(rng.standard_normal((L, Hq, D)))
+    whole = pool.prefill_attention(q, np.array([0, L], np.int32), tables, np.array([L], np.int32), Hq, 0.125)
+    for i in (0, 15, 16, 47, 69):
+        dec = pool.attention(q[i:i + 1], tables, np.array([i + 1], np.int32), Hq, 0.125)
+        assert np.array_equal(dec[0], whole[i])
+
+
 def test_prefill_rejects_chunk_longer_than_context():
     rng = np.random.default_rng(5)
     a, pool, tables, _, _ = _build(rng, [10], 16, 1, 64)
@@ -141,7 +161,7 @@ def _oracle_replay(sc, threads=8):
     """The oracle's pool after the same appends, the tables, and the prefill outputs."""
     a = oracle.Allocator(sc.num_blocks, sc.block_size)
     a.set_free_order(sc.free_order)
-    pool = oracle.Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, sc.kv_dtype == "fp8_e4m3")
+    pool = oracle.Pool(sc.num_blocks, sc.block_size, sc.Hkv, sc.D, KV_CODE[sc.kv_dtype])
     for b in range(sc.B):
         assert a.reserve(b, int(sc.ctx[b])) == 0
     for b in range(sc.B):
@@ -160,6 +180,19 @@ def _check_close(got_bits, ref):
     got = oracle.bf16_bits_to_f64(got_bits)
     err = np.abs(got - ref)
     assert err.max() <= 1e-2, err.max()
+    assert err.mean() <= 1e-3, err.mean()
+
+
+def _check_close_one_byte(got_bits, ref):
+    """One-byte pools: a row led by one key returns code x scale, generally not a bf16 value, so
+    the output's own rounding (half a bf16 ulp, <= 2^-8 relative) is part of the bound; the
+    arithmetic adds the widened K/V and P, each rounded once to f16 (<= 2^-12 relative), which
+    for these values (|V| < 5) stays below 4e-3."""
+    got = oracle.bf16_bits_to_f64(got_bits)
+    err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 4e-3
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (float(err[worst]), float(ref[worst]), float(got[worst]))
     assert err.mean() <= 1e-3, err.mean()
 
 
@@ -186,6 +219,88 @@ def test_prefill_matches_oracle(bs, G, D):
     assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), opool.data)
     _check_close(st.out_host(), ref)
     st.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "int8"])
+@pytest.mark.parametrize("bs,G,D", [(16, 4, 128), (64, 4, 128), (128, 1, 128), (32, 16, 128), (16, 8, 64),
+                                    (64, 2, 64)])
+def test_prefill_one_byte_pools_match_oracle(kv, bs, G, D):
+    """FP8 and INT8 pools: the codes are widened on chip (code x scale, to f16 with a power of two
+    per sequence and head), q goes to f16 exactly and P is f16.  Pool bytes and scales bit-exact
+    after the append; outputs within the one-byte bound of the oracle's exact dequantisation."""
+    torch, pkv = _gpu()
+    import pkv_workloads as W
+    from paged_kv_cache_266_gb300.runner import PrefillStep, _wrap_device
+    sc = W.make_prefill_script(171 + bs + G + D, Hq=2 * G, Hkv=2, D=D, block_size=bs, kv_dtype=kv,
+                               past=[0, 5, 64, 100, 250, 31, 0], chunk=[37, 1, 64, 150, 3, 200, 129])
+    st = PrefillStep(sc)
+    st.step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(st.pool.handle) == pkv.PKV_OK
+    opool, tables, ref = _oracle_replay(sc)
+    assert np.array_equal(st.tables_host, tables)
+    kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(st.pool.handle)
+    assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), opool.data)
+    assert np.array_equal(_wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32), opool.scales)
+    _check_close_one_byte(st.out_host(), ref)
+    st.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "int8"])
+def test_prefill_one_byte_pools_wide_range(kv):
+    """Blocks whose K reach 2^17 and V 2^18 (past the f16 range, so the widened tiles must be
+    rescaled by the sequence's power of two) beside blocks at 2^-10, with queries at 2^-17 (so q
+    itself needs its own power of two to reach the f16 range): every output within 1e-2 (max)
+    and 1e-3 (mean) of the largest |V| of its head, against the oracle."""
+    torch, pkv = _gpu()
+    rng = np.random.default_rng(7 if kv == "int8" else 8)
+    bs, Hkv, G, D = 16, 2, 4, 128
+    Hq = Hkv * G
+    lens, chunk = [150, 61], [40, 61]
+    nb = sum(-(-L // bs) for L in lens) + 2
+    code = KV_CODE[kv]
+    pool = pkv.KVPool(nb, bs, Hkv, D, {1: pkv.PKV_KV_FP8_E4M3, 2: pkv.PKV_KV_INT8}[code])
+    a = pool.allocator
+    order = rng.permutation(nb).astype(np.int32)
+    pkv.pkv_allocator_set_free_order(a, order)
+    oa, op = oracle.Allocator(nb, bs), oracle.Pool(nb, bs, Hkv, D, code)
+    oa.set_free_order(order)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    vmax = np.zeros((len(lens), Hkv))
+    for b, L in enumerate(lens):
+        pkv.pkv_seq_reserve(a, b, L)
+        oa.reserve(b, L)
+        kexp = rng.choice([-10, 0, 17], size=-(-L // bs))
+        vexp = rng.choice([-10, 0, 18], size=-(-L // bs))
+        tok_blk = np.arange(L) // bs
+        kf = rng.standard_normal((L, Hkv, D)) * np.exp2(kexp[tok_blk])[:, None, None]
+        vf = rng.standard_normal((L, Hkv, D)) * np.exp2(vexp[tok_blk])[:, None, None]
+        k, v = _bf16_bits(kf), _bf16_bits(vf)
+        vmax[b] = np.abs(oracle.bf16_bits_to_f64(v)).max(axis=(0, 2))
+        slots = pkv.pkv_slot_mapping(a, [b] * L, np.arange(L))
+        pkv.pkv_append(pool.handle, dev(k), dev(v), torch.from_numpy(slots).cuda())
+        op.append(k, v, slots)
+    cu = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    q = _bf16_bits(rng.standard_normal((int(cu[-1]), Hq, D)) * 2.0 ** -17)
+    mb = max(-(-L // bs) for L in lens)
+    tables = pkv.pkv_get_block_tables(a, np.arange(len(lens)), mb)
+    out = torch.zeros(int(cu[-1]), Hq, D, dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_prefill_attention(pool.handle, dev(q), torch.from_numpy(cu).cuda(), max(chunk),
+                              torch.from_numpy(tables).cuda(), torch.tensor(lens, dtype=torch.int32).cuda(),
+                              1 / math.sqrt(D), out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_OK
+    ref = op.prefill_attention(q, cu, oa.block_tables(list(range(len(lens))), mb), np.array(lens, np.int32), Hq,
+                               1 / math.sqrt(D))
+    got = oracle.bf16_bits_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert np.all(np.isfinite(got))
+    for b in range(len(lens)):
+        for h in range(Hkv):
+            err = np.abs(got[cu[b]:cu[b + 1], h * G:(h + 1) * G] - ref[cu[b]:cu[b + 1], h * G:(h + 1) * G])
+            assert err.max() <= 1e-2 * vmax[b, h] and err.mean() <= 1e-3 * vmax[b, h], (b, h, err.max(), vmax[b, h])
+    pool.close()
 
 
 @pytest.mark.gpu
@@ -270,10 +385,6 @@ def test_prefill_rejects_unsupported_and_flags_bounds():
     cu = torch.tensor([0, 4], dtype=torch.int32, device=dev)
     tables = torch.zeros(1, 1, dtype=torch.int32, device=dev)
     ctx = torch.tensor([4], dtype=torch.int32, device=dev)
-    fp8 = pkv.KVPool(4, 16, 2, 128, pkv.PKV_KV_FP8_E4M3)
-    with pytest.raises(pkv.PKVError):  # fp8 pools have no prefill kernel
-        pkv.pkv_prefill_attention(fp8.handle, q, cu, 4, tables, ctx, 0.1, out)
-    fp8.close()
     pool = pkv.KVPool(4, 16, 2, 128, pkv.PKV_KV_BF16)
     with pytest.raises(pkv.PKVError):  # 6 query heads over 2 KV heads: 3 per group
         pkv.pkv_prefill_attention(pool.handle, q, cu, 4, tables, ctx, 0.1, out)
@@ -293,6 +404,11 @@ def test_prefill_rejects_unsupported_and_flags_bounds():
     assert pkv.pkv_check_device_error(pool.handle) == pkv.PKV_ERR_BOUNDS
     pkv.pkv_prefill_attention(pool.handle, q8, cu, 0, tables, ctx, 0.1, out8)  # max_q_len 0: nothing launched
     pool.close()
+    fp8 = pkv.KVPool(4, 16, 2, 128, pkv.PKV_KV_FP8_E4M3)  # the one-byte path flags a bad block id too
+    pkv.pkv_prefill_attention(fp8.handle, q8, cu, 4, bad_tab, ctx, 0.1, out8)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(fp8.handle) == pkv.PKV_ERR_BOUNDS
+    fp8.close()
 
 
 @pytest.mark.gpu
@@ -344,15 +460,17 @@ def test_chunked_prefill_with_rope_matches_oracle():
 
 
 @pytest.mark.gpu
-def test_prefill_bounded_waits_report_timeout_and_leave_the_context_usable(stall_hooks):
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "int8"])
+def test_prefill_bounded_waits_report_timeout_and_leave_the_context_usable(stall_hooks, kv):
     """Every mbarrier wait in the prefill kernel is bounded. With the test hooks each K/V stage
-    expects bytes no copy delivers and the waits give up after 20 ms: the call reports
-    PKV_ERR_TIMEOUT without a fault, tensor memory is released, and the next normal call gives the
-    same bits as before."""
+    (each code stage on one-byte pools) expects bytes no copy delivers and the waits give up after
+    20 ms: the call reports PKV_ERR_TIMEOUT without a fault, tensor memory is released, and the next
+    normal call gives the same bits as before."""
     torch, pkv = _gpu()
     import pkv_workloads as W
     from paged_kv_cache_266_gb300.runner import PrefillStep
-    sc = W.make_prefill_script(91, B=3, Hq=8, Hkv=2, block_size=64, past=[300, 0, 40], chunk=[200, 90, 17])
+    sc = W.make_prefill_script(91, B=3, Hq=8, Hkv=2, block_size=64, past=[300, 0, 40], chunk=[200, 90, 17],
+                               kv_dtype=kv)
     st = PrefillStep(sc)
     st.step()
     torch.cuda.synchronize()
