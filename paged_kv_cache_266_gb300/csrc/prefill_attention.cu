@@ -53,16 +53,25 @@ constexpr int kTiles = 2;    // query tiles per CTA
 constexpr int kKeys = 128;   // keys per KV tile
 constexpr int kKStages = 3;  // K ring slots (barriers); a K tile is free once both tiles' S MMAs have read it
 constexpr int kVStages = 2;  // V ring: a V tile is free once both tiles' PV MMAs have read it
-constexpr int kThreads = 128 + kTiles * 128;  // control warpgroup + one softmax warpgroup per tile
-// register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded down to 8),
-// i.e. 64512 for the block; control 128 x 56 + softmax 256 x 224 = 64512 fits exactly.
+constexpr int kThreads = 128 + kTiles * 128;  // bf16 pools: control warpgroup + one softmax warpgroup per tile
+constexpr int kThreadsOne = kThreads + 128;    // one-byte pools: + a widening warpgroup
+constexpr int kConverters = 6;                 // one-byte pools: widening warps 2, 3 (control) and 4-7
+// register splits (setmaxnreg).  bf16: launched at 168 per thread (65536 / 384, rounded down to
+// 8), i.e. 64512 for the block; control 128 x 56 + softmax 256 x 224 = 64512 fits exactly.
+// One-byte: launched at 128 (65536 / 512); control and widening 256 x 48 + softmax 256 x 208 =
+// 65536 fits exactly.
 constexpr uint32_t kRegsControl = 56, kRegsSoftmax = 224;
+constexpr uint32_t kRegsControlOne = 48, kRegsSoftmaxOne = 208;
 static_assert(128 * kRegsControl + kTiles * 128 * kRegsSoftmax <= kThreads * 168, "register split");
+static_assert(256 * kRegsControlOne + kTiles * 128 * kRegsSoftmaxOne <= kThreadsOne * 128, "register split");
 constexpr uint32_t kPanelBytes = 128u * 128u;      // 128 rows x 128 bytes (64 bf16 of a row)
 constexpr uint32_t kOffQ = 0;
 // Shared-memory layout for head_dim D (64 or 128): a row of Q, K or V is D / 64 panels of 16-bit
-// elements.  One-byte pools (ONE) also stage one K and one V tile of codes (D bytes a row) for
-// the widening warps, and keep two K stages instead of three.
+// elements.  One-byte pools (ONE) keep two K stages and stage the codes (D bytes a row) for the
+// widening warps, two tiles deep: with D = 128 a K tile's codes land in the upper half of its
+// own ring slot and are widened in place (a code row is overwritten only by the panel-1 row of
+// the same key, written after the whole row was read), V's in two stages of their own; with
+// D = 64 both K and V have two code stages.
 template <int D, bool ONE>
 struct Layout {
     static constexpr int kPanels = D / 64;
@@ -71,13 +80,16 @@ struct Layout {
     static constexpr uint32_t kHalfBytes = kPanels * kPanelBytes;  // K (or V) of one KV tile
     static constexpr uint32_t kCodeRow = D;                        // bytes of one row of codes
     static constexpr uint32_t kCodeBytes = ONE ? kKeys * kCodeRow : 0u;  // codes of one K (or V) tile
+    static constexpr bool kInPlaceK = ONE && D == 128;
     static constexpr uint32_t kOffK = kOffQ + kTiles * kQBytes;
     static constexpr uint32_t kOffV = kOffK + kKSt * kHalfBytes;
-    static constexpr uint32_t kOffCode = kOffV + kVStages * kHalfBytes;  // [K | V] code stage
-    static constexpr uint32_t kOffBar = kOffCode + 2 * kCodeBytes;
+    static constexpr uint32_t kOffCodeK = kOffV + kVStages * kHalfBytes;  // [2] K code stages (D = 64)
+    static constexpr uint32_t kOffCodeV = kOffCodeK + (ONE && !kInPlaceK ? 2 * kCodeBytes : 0u);  // [2] V
+    static constexpr uint32_t kOffBar = kOffCodeV + (ONE ? 2 * kCodeBytes : 0u);
     static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static_assert(kOffCode % 1024 == 0, "code stage on a swizzle-pattern boundary");
+    static_assert(kOffCodeK % 1024 == 0 && kOffCodeV % 1024 == 0, "code stages on a swizzle-pattern boundary");
+    static_assert(!kInPlaceK || kCodeBytes * 2 == kHalfBytes, "K codes fill the upper half of their slot");
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -97,8 +109,8 @@ constexpr int kBarVEmpty = kBarVFull + kVStages;  // [kVStages] last PV MMA read
 constexpr int kBarS = kBarVEmpty + kVStages;      // [kTiles] S_t(j) ready (commit)
 constexpr int kBarP = kBarS + kTiles;             // [kTiles] P_t(j) in TMEM (4 warps arrive)
 constexpr int kBarO = kBarP + kTiles;             // [kTiles] last PV_t done (commit)
-constexpr int kBarCode = kBarO + kTiles;          // [2] K / V code stage landed (one-byte pools; tx bytes)
-constexpr int kBarDrain = kBarCode + 2;           // MMAs in flight done (error path)
+constexpr int kBarCode = kBarO + kTiles;          // [2 K, 2 V] code stages landed (one-byte pools; tx bytes)
+constexpr int kBarDrain = kBarCode + 4;           // MMAs in flight done (error path)
 constexpr int kNumBars = kBarDrain + 1;
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -174,21 +186,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// code x (s_hi + s_lo) for a pair of widened codes, rounded once to f16: s_hi = f16(s) and
-// s_lo = f16(s - s_hi) carry the fp32 scale to 22 bits, the small product c s_lo is rounded
-// first (its error is below 2^-11 of c s_lo) and the fma adds c s_hi with one rounding.
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t c, uint32_t s_hi, uint32_t s_lo) {
+// a pair of widened codes times the part's scale (an f16 pair), rounded to f16
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
     uint32_t d;
-    asm("{\n\t.reg .b32 t;\n\tmul.rn.f16x2 t, %1, %3;\n\tfma.rn.f16x2 %0, %1, %2, t;\n\t}"
-        : "=r"(d) : "r"(c), "r"(s_hi), "r"(s_lo));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
-}
-
-// the scale of a page part as the (hi, lo) f16x2 pair scale_f16x2 takes
-__device__ __forceinline__ void split_scale(float v, uint32_t& s_hi, uint32_t& s_lo) {
-    s_hi = ptx::pack_f16x2(v, v);
-    const float r = v - ptx::f16x2_to_f32x2(s_hi).x;
-    s_lo = ptx::pack_f16x2(r, r);
 }
 
 // kind::f16 instruction descriptor: fp32 accumulator, A and B both f16 (F16) or both bf16.
@@ -236,13 +238,15 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 
 // KV: 0 bf16 pool, 1 FP8-E4M3 pool, 2 INT8 pool.
 template <int PART, int D, int KV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap, const Params p) {
     static_assert(PART == 16 || PART == 32 || PART == 64, "page part of 16, 32 or 64 rows");
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     constexpr bool ONE = KV != 0;  // one-byte codes with per-(block, head) scales
     using LY = Layout<D, ONE>;
     constexpr int KS = LY::kKSt;
+    constexpr int kThr = ONE ? kThreadsOne : kThreads;
+    constexpr int kSmWarp0 = ONE ? 8 : 4;  // first softmax warp
     constexpr uint32_t kQBytes = LY::kQBytes, kHalfBytes = LY::kHalfBytes;
     constexpr uint32_t kOffK = LY::kOffK, kOffV = LY::kOffV, kOffBar = LY::kOffBar;
     constexpr int kPanels = LY::kPanels;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t nn = p.cu_q[i + 1] - p.cu_q[i], ll = p.ctx[i];
             return nn * (2 * ll - nn);
         };
-        for (int i = threadIdx.x; i < p.B; i += kThreads) {
+        for (int i = threadIdx.x; i < p.B; i += kThr) {
             const int64_t wi = work(i);
             int r = 0;
             for (int k = 0; k < p.B; ++k) {
@@ -294,13 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // against all of them from shared memory (B^2 comparisons per CTA)
         __shared__ int seq_of_rank;
         int64_t* work_s = reinterpret_cast<int64_t*>(sm + kOffQ);
-        for (int i = threadIdx.x; i < p.B; i += kThreads) {
+        for (int i = threadIdx.x; i < p.B; i += kThr) {
             const int64_t nn = p.cu_q[i + 1] - p.cu_q[i], ll = p.ctx[i];
             work_s[i] = nn * (2 * ll - nn);
         }
         if (threadIdx.x == 0) seq_of_rank = -1;
         __syncthreads();
-        for (int i = threadIdx.x; i < p.B; i += kThreads) {
+        for (int i = threadIdx.x; i < p.B; i += kThr) {
             const int64_t wi = work_s[i];
             int r = 0;
             for (int k = 0; k < p.B; ++k) {
@@ -336,12 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One-byte pools: the largest K scale and V scale over this sequence's blocks for head h
     // (per warp here, combined after the barrier below).  They fix the powers of two 2^-eK, 2^-eV
     // that bring code x scale into f16 range (largest |value| below 2^16) for the widened tiles.
-    __shared__ uint32_t scale_max_s[kThreads / 32][2];
+    __shared__ uint32_t scale_max_s[kThreadsOne / 32][2];
     if constexpr (ONE) {
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
         const int nb = (L + p.bs - 1) / p.bs;
         uint32_t mk = 0, mv = 0;  // fp32 bits: non-negative scales order like their bits
-        for (int i = threadIdx.x; i < nb; i += kThreads) {
+        for (int i = threadIdx.x; i < nb; i += kThr) {
             const int blk = tb[i];
             if (blk >= 0 && blk < p.num_blocks) {
                 const float2 sc = *reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + h) * 4);
@@ -364,14 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto scale_exp = [&](int kv) -> int {
         uint32_t m = 0;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) m = max(m, scale_max_s[w][kv]);
+        for (int w = 0; w < kThr / 32; ++w) m = max(m, scale_max_s[w][kv]);
         return m ? lead_exp(m) - 6 : 0;
     };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool wg_arrive = i == kBarQ || (i >= kBarP && i < kBarP + kTiles);
-            ptx::mbar_init(bar(i), i == kBarQ ? 8u : (wg_arrive ? 4u : 1u));
+            // one-byte pools: a K / V ring slot is full once every widening warp has written its share
+            const bool widened = ONE && ((i >= kBarKFull && i < kBarKFull + kKStages) ||
+                                         (i >= kBarVFull && i < kBarVFull + kVStages));
+            ptx::mbar_init(bar(i), i == kBarQ ? 8u : (wg_arrive ? 4u : (widened ? (uint32_t)kConverters : 1u)));
         }
         abort_s = 0;
         ptx::fence_barrier_init();
@@ -382,163 +389,201 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    if (warp < 4) {
-      ptx::regs_dec<kRegsControl>();  // the whole control warpgroup, one instruction
-      if (ONE && (warp == 0 || warp == 2)) {
-        // ---------------------------------------------------------------- one-byte K / V streams
-        // warp 0 K, warp 2 V.  Per KV tile: one 2-D copy of PART code rows per page part into
-        // the code stage (rows past the context read zeros), then the warp widens the codes into
-        // the f16 ring in the panel layout the MMA reads (128-byte swizzled lines): value =
-        // code x (scale x 2^-e), the scale that of the row's (block, head), rounded once to f16.
-        // The next tile's copy goes out as soon as the codes have been read.
-        const int kv = warp == 0 ? 0 : 1;
-        const int stages = kv ? kVStages : KS;
-        const uint32_t ring = kv ? sV : sK;
-        const uint32_t code = base + LY::kOffCode + (uint32_t)kv * LY::kCodeBytes;
-        const int full = kv ? kBarVFull : kBarKFull, empty = kv ? kBarVEmpty : kBarKEmpty;
-        const uint32_t cbar = bar(kBarCode + kv);
+    if (warp < kSmWarp0) {
+      ptx::regs_dec<ONE ? kRegsControlOne : kRegsControl>();  // whole warpgroups, one instruction each
+      if (ONE && warp == 0) {
+        // ---------------------------------------------------------------- one-byte code copies
+        // Two code stages per stream: tile j's copies go out once its stage is free -- a K slot
+        // holding its own codes once the S MMAs of tile j-2 have read it, a separate stage once
+        // the widening warps are done with tile j-2.  One 2-D copy of PART code rows per page
+        // part (rows past the context read zeros).
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
-        float fa, fb;  // 2^-e
-        pow2_pair(-scale_exp(kv), fa, fb);
-        // the copies of tile j's page parts; lane pi < kParts returns part pi's scale
-        auto issue = [&](int j) -> float {
+        auto issue = [&](int kv, int j) {
+            const uint32_t cbar = bar(kBarCode + 2 * kv + (j & 1));
+            const uint32_t dst = kv ? base + LY::kOffCodeV + (uint32_t)(j & 1) * LY::kCodeBytes
+                                 : LY::kInPlaceK ? sK + (uint32_t)(j & 1) * kHalfBytes + LY::kCodeBytes
+                                                 : base + LY::kOffCodeK + (uint32_t)(j & 1) * LY::kCodeBytes;
             if (lane == 0) ptx::mbar_arrive_expect_tx(cbar, LY::kCodeBytes + p.stall_tx);
             __syncwarp();
-            float sc = 0.f;
             if (lane < kParts) {
                 const int tok = j * kKeys + lane * PART;
                 int32_t row = p.oob_row;
                 if (tok < L) {
                     const int blk = tb[tok / p.bs];
-                    if (blk >= 0 && blk < p.num_blocks) {
+                    if (blk >= 0 && blk < p.num_blocks)
                         row = (int32_t)((((int64_t)2 * blk + kv) * p.Hkv + h) * p.bs + (tok % p.bs));
-                        sc = p.scales[((int64_t)blk * p.Hkv + h) * 4 + kv];
-                    } else if (kv == 0) {
+                    else if (kv == 0)
                         atomicOr(p.err, kErrBounds);
+                }
+                ptx::tma_load_2d(dst + (uint32_t)(lane * PART) * LY::kCodeRow, &tmap, 0, row, cbar);
+            }
+        };
+        bool ok = true;
+        for (int j = 0; j < n_kv && ok; ++j) {
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                if (j >= 2) {
+                    // the stage of tile j-2: the K slot read by its S MMAs (in place), else widened
+                    const int free_bar = kv ? kBarVFull : LY::kInPlaceK ? kBarKEmpty : kBarKFull;
+                    if (lane == 0) ok = ptx::mbar_wait(bar(free_bar + (j & 1)), ((j >> 1) - 1) & 1, p.wait_ns);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok || __shfl_sync(0xffffffffu, abort_s, 0)) {
+                        ok = false;
+                        break;
                     }
                 }
-                ptx::tma_load_2d(code + (uint32_t)(lane * PART) * LY::kCodeRow, &tmap, 0, row, cbar);
+                issue(kv, j);
             }
-            return sc;
+        }
+        if (lane == 0 && !ok) {
+            if (!abort_s) atomicOr(p.err, kErrTimeout);
+            abort_s = 1;
+        }
+        __syncwarp();
+        ptx::named_barrier_sync(kEndBar, kThr);
+      } else if (ONE && warp >= 2) {
+        // ---------------------------------------------------------------- one-byte widening
+        // Six warps (2, 3, 4-7) widen each tile: value = code x (scale x 2^-e), the scale that of
+        // the code's (block, head), rounded once to f16.  K rows go to the K ring as the 128-byte
+        // swizzled panels the S MMA reads; V, which the pool keeps as 16-token panels [d][16
+        // codes] in the pair order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 (one 16-byte chunk = the
+        // 16 tokens of one d), goes to the V ring as V^T, K-major for the P.V MMA: [64-key
+        // panel][d line][128 bytes: 64 keys] -- no transpose, four byte permutes restore the
+        // token order.  The passes of a tile (4 K rows or 32 d of one 16-key group each with
+        // D = 128; 8 rows or 32 d with D = 64) are dealt round-robin to the warps.
+        const int cw = warp - 2;  // 0..5
+        const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
+        float fak, fbk, fav, fbv;  // 2^-eK, 2^-eV
+        pow2_pair(-scale_exp(0), fak, fbk);
+        pow2_pair(-scale_exp(1), fav, fbv);
+        constexpr int kPassK = D == 128 ? 32 : 16;  // passes per tile: K
+        constexpr int kPassV = D / 4;               // passes per tile: V (8 groups x D / 32)
+        constexpr uint32_t kVtPanel = (uint32_t)D * 128u;
+
+        // lane pi < kParts: part pi's K and V scales of tile j (0 past the context)
+        auto load_scales = [&](int j, float& sk, float& sv) {
+            sk = sv = 0.f;
+            if (lane < kParts) {
+                const int tok = j * kKeys + lane * PART;
+                if (tok < L) {
+                    const int blk = tb[tok / p.bs];
+                    if (blk >= 0 && blk < p.num_blocks) {
+                        const float2 v = *reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + h) * 4);
+                        sk = v.x;
+                        sv = v.y;
+                    }
+                }
+            }
         };
-        float sc_next = issue(0);
-        int issued = 1, landed = 0;  // code copies issued / seen complete (lane 0)
+        // Every lane waits (bounded) for the codes of tile j (stage j & 1): a copy's bytes are
+        // visible to the threads that observe its phase complete, and every lane reads them.
+        // Unless the codes sit in the slot itself, lane 0 then waits for the ring slot (the MMAs
+        // of tile j-2 done with it) and the warp follows.
+        auto wait2 = [&](int kv, int j, bool slot_wait) -> bool {
+            bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarCode + 2 * kv + (j & 1)), (j >> 1) & 1, p.wait_ns));
+            if (ok && slot_wait && j >= 2) {
+                const int emptyb = kv ? kBarVEmpty : kBarKEmpty;
+                if (lane == 0) ok = ptx::mbar_wait(bar(emptyb + (j & 1)), ((j >> 1) - 1) & 1, p.wait_ns);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            }
+            return ok;
+        };
+        float skn, svn;
+        load_scales(0, skn, svn);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            const int slot = j % stages;
-            if (lane == 0) {
-                ok = ptx::mbar_wait(cbar, j & 1, p.wait_ns);
-                if (ok) landed = j + 1;
-                if (ok && j >= stages) ok = ptx::mbar_wait(bar(empty + slot), ((j / stages) - 1) & 1, p.wait_ns);
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            if (__shfl_sync(0xffffffffu, abort_s, 0)) break;  // warp-uniform
-            const float sc_cur = sc_next;
-            const uint32_t dst0 = ring + (uint32_t)slot * kHalfBytes;
-            if (kv == 1) {
-                // V codes: the pool keeps a V page as 16-token panels [d][16 codes], the tokens in the
-                // pair order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 (the decode MMA's fragment); one
-                // 16-byte chunk is the 16 tokens of one d.  Widened into V^T, K-major for the P.V MMA:
-                // [64-key panel][d line][128 bytes: 64 keys], 128-byte swizzled -- no transpose, four
-                // byte permutes restore the token order.  The code stage holds the panels as the copy
-                // wrote them: line = 16 group + 16 d / D of D bytes, in the copy's swizzle.
-                constexpr uint32_t kVtPanel = (uint32_t)D * 128u;
+            const float skc = skn, svc = svn;
+            if (j + 1 < n_kv) load_scales(j + 1, skn, svn);  // in flight while this tile is widened
+            // ---- K
+            ok = wait2(0, j, !LY::kInPlaceK);
+            if (!ok || __shfl_sync(0xffffffffu, abort_s, 0)) break;
+            {
+                const uint32_t dst0 = sK + (uint32_t)(j % KS) * kHalfBytes;
+                // in place: the codes fill the slot's upper half (panel 1), code row r under the
+                // panel-1 row of key r, which this pass writes only after reading the whole row
+                const uint32_t codeK = LY::kInPlaceK ? dst0 + LY::kCodeBytes
+                                                     : base + LY::kOffCodeK + (uint32_t)(j & 1) * LY::kCodeBytes;
 #pragma unroll 1
-                for (int G = 0; G < kKeys / 16; ++G) {
-                    uint32_t s_hi, s_lo;
-                    split_scale(__shfl_sync(0xffffffffu, sc_cur, (16 * G) / PART) * fa * fb, s_hi, s_lo);
-#pragma unroll 2
-                    for (int qd = 0; qd < D / 32; ++qd) {
-                        const int d = 32 * qd + lane;
-                        uint32_t src;
-                        if constexpr (D == 128)
-                            src = code + (uint32_t)(16 * G + (d >> 3)) * 128u + ((uint32_t)((d & 7) ^ ((d >> 3) & 7)) << 4);
-                        else
-                            src = code + (uint32_t)(16 * G + (d >> 2)) * 64u + ((uint32_t)((d & 3) ^ ((d >> 3) & 3)) << 4);
-                        const uint4 w = lds128(src);
-                        uint32_t o[8];
-                        widen4<KV>(__byte_perm(w.x, w.y, 0x5410), o[0], o[1]);  // tokens 0-3
-                        widen4<KV>(__byte_perm(w.z, w.w, 0x5410), o[2], o[3]);  // tokens 4-7
-                        widen4<KV>(__byte_perm(w.x, w.y, 0x7632), o[4], o[5]);  // tokens 8-11
-                        widen4<KV>(__byte_perm(w.z, w.w, 0x7632), o[6], o[7]);  // tokens 12-15
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = scale_f16x2(o[e], s_hi, s_lo);
-                        const uint32_t dst = dst0 + (uint32_t)(G >> 2) * kVtPanel + (uint32_t)d * 128u;
-                        const int cc = (G & 3) * 2;
-                        sts128(dst + ((uint32_t)(cc ^ (d & 7)) << 4), o[0], o[1], o[2], o[3]);
-                        sts128(dst + ((uint32_t)((cc + 1) ^ (d & 7)) << 4), o[4], o[5], o[6], o[7]);
-                    }
-                }
-            } else if constexpr (D == 128) {
-                // 4 rows a pass, 8 lanes a row, 16 codes a lane -> 32 bytes of f16 (two 16-byte
-                // chunks of one panel)
-                const int rs = lane >> 3, c = lane & 7;
-#pragma unroll 1
-                for (int pi = 0; pi < kParts; ++pi) {
-                    uint32_t s_hi, s_lo;
-                    split_scale(__shfl_sync(0xffffffffu, sc_cur, pi) * fa * fb, s_hi, s_lo);
-#pragma unroll 2
-                    for (int it = 0; it < PART / 4; ++it) {
-                        const int r = pi * PART + it * 4 + rs;
-                        const uint4 w = lds128(code + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4));
+                for (int i = cw; i < kPassK; i += kConverters) {
+                    if constexpr (D == 128) {
+                        const int rs = lane >> 3, c = lane & 7, r = 4 * i + rs;
+                        const float v = __shfl_sync(0xffffffffu, skc, (4 * i) / PART) * fak * fbk;
+                        const uint32_t s2 = ptx::pack_f16x2(v, v);
+                        const uint4 w = lds128(codeK + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4));
                         uint32_t o[8];
                         widen4<KV>(w.x, o[0], o[1]);
                         widen4<KV>(w.y, o[2], o[3]);
                         widen4<KV>(w.z, o[4], o[5]);
                         widen4<KV>(w.w, o[6], o[7]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = scale_f16x2(o[e], s_hi, s_lo);
+                        for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
                         const uint32_t dst = dst0 + (uint32_t)(c >> 2) * kPanelBytes;
                         const int cc = (c & 3) * 2;
                         sts128(dst + swz128(r, cc), o[0], o[1], o[2], o[3]);
                         sts128(dst + swz128(r, cc + 1), o[4], o[5], o[6], o[7]);
-                    }
-                }
-            } else {
-                // 64-byte code rows (64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)):
-                // 8 rows a pass, 4 lanes a row
-                const int rs = lane >> 2, c = lane & 3;
-#pragma unroll 1
-                for (int pi = 0; pi < kParts; ++pi) {
-                    uint32_t s_hi, s_lo;
-                    split_scale(__shfl_sync(0xffffffffu, sc_cur, pi) * fa * fb, s_hi, s_lo);
-#pragma unroll 2
-                    for (int it = 0; it < PART / 8; ++it) {
-                        const int r = pi * PART + it * 8 + rs;
-                        const uint4 w = lds128(code + (uint32_t)r * 64u + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4));
+                    } else {
+                        // 64-byte code rows, 64-byte swizzle: chunk c of row r at c ^ ((r >> 1) & 3)
+                        const int rs = lane >> 2, c = lane & 3, r = 8 * i + rs;
+                        const float v = __shfl_sync(0xffffffffu, skc, (8 * i) / PART) * fak * fbk;
+                        const uint32_t s2 = ptx::pack_f16x2(v, v);
+                        const uint4 w = lds128(codeK + (uint32_t)r * 64u + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4));
                         uint32_t o[8];
                         widen4<KV>(w.x, o[0], o[1]);
                         widen4<KV>(w.y, o[2], o[3]);
                         widen4<KV>(w.z, o[4], o[5]);
                         widen4<KV>(w.w, o[6], o[7]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = scale_f16x2(o[e], s_hi, s_lo);
+                        for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
                         sts128(dst0 + swz128(r, 2 * c), o[0], o[1], o[2], o[3]);
                         sts128(dst0 + swz128(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
                     }
                 }
             }
-            // widened rows visible to the MMAs (async proxy), and the code reads ordered before
-            // the next copy overwrites the stage
-            ptx::fence_proxy_async_smem();
+            ptx::fence_proxy_async_smem();  // the S MMAs (async proxy) read what was written
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(full + slot));
-            if (j + 1 < n_kv) {
-                sc_next = issue(j + 1);
-                issued = j + 2;
+            if (lane == 0) ptx::mbar_arrive(bar(kBarKFull + j % KS));
+            // ---- V
+            ok = wait2(1, j, true);
+            if (!ok || __shfl_sync(0xffffffffu, abort_s, 0)) break;
+            {
+                const uint32_t dst0 = sV + (uint32_t)(j % kVStages) * kHalfBytes;
+                const uint32_t codeV = base + LY::kOffCodeV + (uint32_t)(j & 1) * LY::kCodeBytes;
+#pragma unroll 1
+                for (int i = cw; i < kPassV; i += kConverters) {
+                    const int G = i / (D / 32), d = 32 * (i % (D / 32)) + lane;
+                    const float v = __shfl_sync(0xffffffffu, svc, (16 * G) / PART) * fav * fbv;
+                    const uint32_t s2 = ptx::pack_f16x2(v, v);
+                    uint32_t src;
+                    if constexpr (D == 128)
+                        src = codeV + (uint32_t)(16 * G + (d >> 3)) * 128u + ((uint32_t)((d & 7) ^ ((d >> 3) & 7)) << 4);
+                    else
+                        src = codeV + (uint32_t)(16 * G + (d >> 2)) * 64u + ((uint32_t)((d & 3) ^ ((d >> 3) & 3)) << 4);
+                    const uint4 w = lds128(src);
+                    uint32_t o[8];
+                    widen4<KV>(__byte_perm(w.x, w.y, 0x5410), o[0], o[1]);  // tokens 0-3
+                    widen4<KV>(__byte_perm(w.z, w.w, 0x5410), o[2], o[3]);  // tokens 4-7
+                    widen4<KV>(__byte_perm(w.x, w.y, 0x7632), o[4], o[5]);  // tokens 8-11
+                    widen4<KV>(__byte_perm(w.z, w.w, 0x7632), o[6], o[7]);  // tokens 12-15
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
+                    const uint32_t dst = dst0 + (uint32_t)(G >> 2) * kVtPanel + (uint32_t)d * 128u;
+                    const int cc = (G & 3) * 2;
+                    sts128(dst + ((uint32_t)(cc ^ (d & 7)) << 4), o[0], o[1], o[2], o[3]);
+                    sts128(dst + ((uint32_t)((cc + 1) ^ (d & 7)) << 4), o[4], o[5], o[6], o[7]);
+                }
             }
+            ptx::fence_proxy_async_smem();  // the P.V MMAs read what was written
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarVFull + j % kVStages));
         }
         if (!ok && lane == 0) {
             atomicOr(p.err, kErrTimeout);
             abort_s = 1;
         }
-        // a copy still in flight lands before the CTA can leave (bounded like every wait)
-        if (issued > landed && lane == 0) ptx::mbar_wait(cbar, (issued - 1) & 1, p.wait_ns);
         __syncwarp();
-        ptx::named_barrier_sync(kEndBar, kThreads);
-      } else if (warp == 0 || warp == 2) {
-        // ---------------------------------------------------------------- producers
+        ptx::named_barrier_sync(kEndBar, kThr);
+      } else if (!ONE && (warp == 0 || warp == 2)) {
+        // ---------------------------------------------------------------- producers (bf16 pools)
         // warp 0 fills the K ring, warp 2 the V ring; each KV tile is two 128-row panels (the
         // 64-element halves), one 2-D copy of PART rows per (page part, half)
         const int kv = warp == 0 ? 0 : 1;
@@ -578,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  &tmap, q * 64, row, bar(full + s));
             }
         }
-        ptx::named_barrier_sync(kEndBar, kThreads);
+        ptx::named_barrier_sync(kEndBar, kThr);
       } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -670,16 +715,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // every role has finished with tensor memory: release it
-        ptx::named_barrier_sync(kEndBar, kThreads);
+        ptx::named_barrier_sync(kEndBar, kThr);
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
       } else {
-        ptx::named_barrier_sync(kEndBar, kThreads);  // warp 3: idle member of the control warpgroup
+        ptx::named_barrier_sync(kEndBar, kThr);  // warp 3: idle member of the control warpgroup
       }
     } else {
-        ptx::regs_inc<kRegsSoftmax>();
+        ptx::regs_inc<ONE ? kRegsSoftmaxOne : kRegsSoftmax>();
         // ---------------------------------------------------------------- softmax / epilogue
-        const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+        const int t = (warp - kSmWarp0) >> 2;  // query tile of this warpgroup
         const int qw = warp & 3;        // TMEM lane quarter this warp may access
         const int r = qw * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
@@ -869,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             abort_s = 1;
         }
         ptx::tc_fence_before();
-        ptx::named_barrier_sync(kEndBar, kThreads);
+        ptx::named_barrier_sync(kEndBar, kThr);
     }
 }
 
@@ -969,7 +1014,7 @@ pkv_status prefill_prepare(const pkv_pool* pool, const void* q, const int32_t* c
 pkv_status prefill_launch(const pkv_pool* pool, const prefill::Params& p, dim3 grid, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(prefill::kThreads);
+    cfg.blockDim = dim3(pool->dtype != PKV_KV_BF16 ? prefill::kThreadsOne : prefill::kThreads);
     const bool d64 = pool->head_dim == 64;
     const bool one = pool->dtype != PKV_KV_BF16;
     cfg.dynamicSmemBytes = d64 ? (one ? prefill::Layout<64, true>::kSmemBytes : prefill::Layout<64, false>::kSmemBytes)
