@@ -475,10 +475,12 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                 }
             }
         };
-        // Every lane waits (bounded) for the codes of tile j (stage j & 1): a copy's bytes are
-        // visible to the threads that observe its phase complete, and every lane reads them.
-        // Unless the codes sit in the slot itself, lane 0 then waits for the ring slot (the MMAs
-        // of tile j-2 done with it) and the warp follows.
+        // Every lane waits (bounded) for the codes of tile j (stage j & 1) itself, as the decode
+        // kernel's consumers do: a copy's bytes are visible to the threads that observe its phase
+        // complete, and every lane reads them (one spinning lane followed by a single poll of the
+        // others failed the one-byte parity tests).  Unless the codes sit in the slot itself,
+        // lane 0 then waits for the ring slot (the MMAs of tile j-2 done with it) and the warp
+        // follows.
         auto wait2 = [&](int kv, int j, bool slot_wait) -> bool {
             bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarCode + 2 * kv + (j & 1)), (j >> 1) & 1, p.wait_ns));
             if (ok && slot_wait && j >= 2) {
