@@ -25,8 +25,8 @@
 //                                       P_t(j): the tensor pipe runs one thread's MMAs in
 //                                       issue order
 //              with descriptors built once and advanced by constant offsets (issuing must
-//              stay faster than the ~65 cycles an M=128 N=128 K=16 MMA takes).
-//              so one tile's MMAs run while the other tile's softmax works.
+//              stay faster than the ~65 cycles an M=128 N=128 K=16 MMA takes), so one
+//              tile's MMAs run while the other tile's softmax works.
 //   warp 3     idle (it completes the control warpgroup, which gives registers away)
 //   warps 4-7, 8-11  one softmax warpgroup per query tile, one row per thread (TMEM lane =
 //              row): the Q row into shared memory, then per KV tile the S row out of TMEM,
@@ -37,6 +37,16 @@
 //              (hi + lo, two MMAs): short contexts have all their weight there, and a single
 //              bf16 P would add its rounding to the output's.  Finally O / l as bf16.
 // TMEM: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t (bf16 pairs) lives in S_t's columns.
+//
+// FP8-E4M3 and INT8 pools (KV != 0): the tensor cores take one 16-bit type for both operands,
+// so the codes are widened on chip to f16 -- K' = code x f16(scale x 2^-eK), V' likewise, with
+// a power of two per (sequence, KV head) that keeps the values in f16's range; q goes to f16
+// exactly with a power of two per row; P is f16; the powers of two return in the score scale
+// and the epilogue.  512 threads: warp 0 issues the code copies (two tiles deep: at head_dim 128
+// a K tile's codes land in the upper half of its own ring slot and are widened in place), warp 1
+// the MMAs, warps 2-7 widen (K rows into the K ring; V, kept by the pool as 16-token panels
+// [d][16 codes], into V^T, which the P.V MMA reads K-major), warps 8-15 run the softmax.
+//
 // Every mbarrier wait is bounded; on expiry the kernel sets the pool's error word, every role
 // stops, and tensor memory is released.
 #include <cmath>
@@ -179,7 +189,10 @@ __device__ __forceinline__ void widen4(uint32_t four, uint32_t& lo, uint32_t& hi
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
