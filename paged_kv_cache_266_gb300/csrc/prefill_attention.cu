@@ -39,8 +39,9 @@
 // TMEM: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t (bf16 pairs) lives in S_t's columns.
 //
 // FP8-E4M3 and INT8 pools (KV != 0): the tensor cores take one 16-bit type for both operands,
-// so the codes are widened on chip to f16 -- K' = code x f16(scale x 2^-eK), V' likewise, with
-// a power of two per (sequence, KV head) that keeps the values in f16's range; q goes to f16
+// so the codes are widened on chip to f16 -- K' = the codes themselves (exact), whose scale, one
+// per page part, multiplies the score in the softmax; V' = code x f16(scale x 2^-eV), with a
+// power of two per (sequence, KV head) that keeps the values in f16's range; q goes to f16
 // exactly with a power of two per row; P is f16; the powers of two return in the score scale
 // and the epilogue.  512 threads: warp 0 issues the code copies (two tiles deep: at head_dim 128
 // a K tile's codes land in the upper half of its own ring slot and are widened in place), warp 1
@@ -68,10 +69,10 @@ constexpr int kThreadsOne = kThreads + 128;    // one-byte pools: + a widening w
 constexpr int kConverters = 6;                 // one-byte pools: widening warps 2, 3 (control) and 4-7
 // register splits (setmaxnreg).  bf16: launched at 168 per thread (65536 / 384, rounded down to
 // 8), i.e. 64512 for the block; control 128 x 56 + softmax 256 x 224 = 64512 fits exactly.
-// One-byte: launched at 128 (65536 / 512); control and widening 256 x 48 + softmax 256 x 208 =
+// One-byte: launched at 128 (65536 / 512); control and widening 256 x 40 + softmax 256 x 216 =
 // 65536 fits exactly.
 constexpr uint32_t kRegsControl = 56, kRegsSoftmax = 224;
-constexpr uint32_t kRegsControlOne = 48, kRegsSoftmaxOne = 208;
+constexpr uint32_t kRegsControlOne = 40, kRegsSoftmaxOne = 216;
 static_assert(128 * kRegsControl + kTiles * 128 * kRegsSoftmax <= kThreads * 168, "register split");
 static_assert(256 * kRegsControlOne + kTiles * 128 * kRegsSoftmaxOne <= kThreadsOne * 128, "register split");
 constexpr uint32_t kPanelBytes = 128u * 128u;      // 128 rows x 128 bytes (64 bf16 of a row)
@@ -350,38 +351,28 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
     const int last_tile = nkv[1] > 0 ? 1 : 0;
     const int n_kv = nkv[last_tile];  // the last active tile sees the most keys
 
-    // One-byte pools: the largest K scale and V scale over this sequence's blocks for head h
-    // (per warp here, combined after the barrier below).  They fix the powers of two 2^-eK, 2^-eV
-    // that bring code x scale into f16 range (largest |value| below 2^16) for the widened tiles.
-    __shared__ uint32_t scale_max_s[kThreadsOne / 32][2];
+    // One-byte pools: the largest V scale over this sequence's blocks for head h (per warp here,
+    // combined after the barrier below).  It fixes the power of two 2^-eV that brings
+    // code x scale into f16 range (largest |value| below 2^16) for the widened V tiles.
+    __shared__ uint32_t scale_max_s[kThreadsOne / 32];
     if constexpr (ONE) {
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
         const int nb = (L + p.bs - 1) / p.bs;
-        uint32_t mk = 0, mv = 0;  // fp32 bits: non-negative scales order like their bits
+        uint32_t mv = 0;  // fp32 bits: non-negative scales order like their bits
         for (int i = threadIdx.x; i < nb; i += kThr) {
             const int blk = tb[i];
-            if (blk >= 0 && blk < p.num_blocks) {
-                const float2 sc = *reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + h) * 4);
-                mk = max(mk, __float_as_uint(sc.x));
-                mv = max(mv, __float_as_uint(sc.y));
-            }
+            if (blk >= 0 && blk < p.num_blocks) mv = max(mv, __float_as_uint(p.scales[((int64_t)blk * p.Hkv + h) * 4 + 1]));
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o));
-            mv = max(mv, __shfl_xor_sync(0xffffffffu, mv, o));
-        }
-        if (lane == 0) {
-            scale_max_s[warp][0] = mk;
-            scale_max_s[warp][1] = mv;
-        }
+        for (int o = 16; o > 0; o >>= 1) mv = max(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+        if (lane == 0) scale_max_s[warp] = mv;
     }
-    // e such that the largest scale times 2^-e lies in [64, 128): codes up to 448 (E4M3) or 127
-    // (INT8) then give |value| < 2^16 in f16.  0 for a sequence whose scales are all zero.
-    auto scale_exp = [&](int kv) -> int {
+    // eV such that the largest V scale times 2^-eV lies in [64, 128): codes up to 448 (E4M3) or
+    // 127 (INT8) then give |value| < 2^16 in f16.  0 for a sequence whose scales are all zero.
+    auto scale_exp_v = [&]() -> int {
         uint32_t m = 0;
 #pragma unroll
-        for (int w = 0; w < kThr / 32; ++w) m = max(m, scale_max_s[w][kv]);
+        for (int w = 0; w < kThr / 32; ++w) m = max(m, scale_max_s[w]);
         return m ? lead_exp(m) - 6 : 0;
     };
 
@@ -456,9 +447,10 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
         ptx::named_barrier_sync(kEndBar, kThr);
       } else if (ONE && warp >= 2) {
         // ---------------------------------------------------------------- one-byte widening
-        // Six warps (2, 3, 4-7) widen each tile: value = code x (scale x 2^-e), the scale that of
-        // the code's (block, head), rounded once to f16.  K rows go to the K ring as the 128-byte
-        // swizzled panels the S MMA reads; V, which the pool keeps as 16-token panels [d][16
+        // Six warps (2, 3, 4-7) widen each tile.  K rows go to the K ring as the 128-byte swizzled
+        // panels the S MMA reads, the codes' values exactly (their scale joins the score in the
+        // softmax); V becomes code x (scale x 2^-eV), the scale that of the code's (block, head),
+        // rounded once to f16.  V, which the pool keeps as 16-token panels [d][16
         // codes] in the pair order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 (one 16-byte chunk = the
         // 16 tokens of one d), goes to the V ring as V^T, K-major for the P.V MMA: [64-key
         // panel][d line][128 bytes: 64 keys] -- no transpose, four byte permutes restore the
@@ -466,25 +458,21 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
         // D = 128; 8 rows or 32 d with D = 64) are dealt round-robin to the warps.
         const int cw = warp - 2;  // 0..5
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
-        float fak, fbk, fav, fbv;  // 2^-eK, 2^-eV
-        pow2_pair(-scale_exp(0), fak, fbk);
-        pow2_pair(-scale_exp(1), fav, fbv);
+        float fav, fbv;  // 2^-eV
+        pow2_pair(-scale_exp_v(), fav, fbv);
         constexpr int kPassK = D == 128 ? 32 : 16;  // passes per tile: K
         constexpr int kPassV = D / 4;               // passes per tile: V (8 groups x D / 32)
         constexpr uint32_t kVtPanel = (uint32_t)D * 128u;
 
-        // lane pi < kParts: part pi's K and V scales of tile j (0 past the context)
-        auto load_scales = [&](int j, float& sk, float& sv) {
-            sk = sv = 0.f;
+        // lane pi < kParts: part pi's V scale of tile j (0 past the context; K codes are widened
+        // exactly and their scale joins the score in the softmax)
+        auto load_scales = [&](int j, float& sv) {
+            sv = 0.f;
             if (lane < kParts) {
                 const int tok = j * kKeys + lane * PART;
                 if (tok < L) {
                     const int blk = tb[tok / p.bs];
-                    if (blk >= 0 && blk < p.num_blocks) {
-                        const float2 v = *reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + h) * 4);
-                        sk = v.x;
-                        sv = v.y;
-                    }
+                    if (blk >= 0 && blk < p.num_blocks) sv = p.scales[((int64_t)blk * p.Hkv + h) * 4 + 1];
                 }
             }
         };
@@ -503,12 +491,12 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
             }
             return ok;
         };
-        float skn, svn;
-        load_scales(0, skn, svn);
+        float svn;
+        load_scales(0, svn);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            const float skc = skn, svc = svn;
-            if (j + 1 < n_kv) load_scales(j + 1, skn, svn);  // in flight while this tile is widened
+            const float svc = svn;
+            if (j + 1 < n_kv) load_scales(j + 1, svn);  // in flight while this tile is widened
             // ---- K
             ok = wait2(0, j, !LY::kInPlaceK);
             if (!ok || __shfl_sync(0xffffffffu, abort_s, 0)) break;
@@ -522,16 +510,12 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                 for (int i = cw; i < kPassK; i += kConverters) {
                     if constexpr (D == 128) {
                         const int rs = lane >> 3, c = lane & 7, r = 4 * i + rs;
-                        const float v = __shfl_sync(0xffffffffu, skc, (4 * i) / PART) * fak * fbk;
-                        const uint32_t s2 = ptx::pack_f16x2(v, v);
                         const uint4 w = lds128(codeK + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4));
                         uint32_t o[8];
                         widen4<KV>(w.x, o[0], o[1]);
                         widen4<KV>(w.y, o[2], o[3]);
                         widen4<KV>(w.z, o[4], o[5]);
                         widen4<KV>(w.w, o[6], o[7]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
                         const uint32_t dst = dst0 + (uint32_t)(c >> 2) * kPanelBytes;
                         const int cc = (c & 3) * 2;
                         sts128(dst + swz128(r, cc), o[0], o[1], o[2], o[3]);
@@ -539,16 +523,12 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                     } else {
                         // 64-byte code rows, 64-byte swizzle: chunk c of row r at c ^ ((r >> 1) & 3)
                         const int rs = lane >> 2, c = lane & 3, r = 8 * i + rs;
-                        const float v = __shfl_sync(0xffffffffu, skc, (8 * i) / PART) * fak * fbk;
-                        const uint32_t s2 = ptx::pack_f16x2(v, v);
                         const uint4 w = lds128(codeK + (uint32_t)r * 64u + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4));
                         uint32_t o[8];
                         widen4<KV>(w.x, o[0], o[1]);
                         widen4<KV>(w.y, o[2], o[3]);
                         widen4<KV>(w.z, o[4], o[5]);
                         widen4<KV>(w.w, o[6], o[7]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
                         sts128(dst0 + swz128(r, 2 * c), o[0], o[1], o[2], o[3]);
                         sts128(dst0 + swz128(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
                     }
@@ -789,18 +769,41 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(bar(kBarQ));
         }
         const int my_nkv = nkv[t];
-        // scores in base 2: S x scale x log2(e); one-byte pools compute S' = (q 2^eq).(K 2^-eK)
+        // scores in base 2: S x scale x log2(e).  One-byte pools compute S' = (q 2^eq).code: the
+        // key's scale (that of its page part) multiplies the score here, per part of PART keys
         float c2 = p.scale_log2;
+        float kmul[kParts];  // one-byte: c2 x 2^-eq x the part's K scale, this tile
+        float knext = 1.f;   // lane q < kParts: part q's K scale of the next tile
+        const int32_t* tbs = p.tables + (int64_t)b * p.max_blocks;
+        // part `lane`'s K scale of tile j (1 past the context: a multiplier > 0 keeps masked
+        // -inf scores -inf)
+        auto load_kscale = [&](int j) -> float {
+            float v = 1.f;
+            if (lane < kParts) {
+                const int tok = j * kKeys + lane * PART;
+                if (tok < L) {
+                    const int blk = tbs[tok / p.bs];
+                    if (blk >= 0 && blk < p.num_blocks) v = p.scales[((int64_t)blk * p.Hkv + h) * 4];
+                }
+            }
+            return v;
+        };
         if constexpr (ONE) {
             float fa, fb;
-            pow2_pair(scale_exp(0) - eq, fa, fb);
+            pow2_pair(-eq, fa, fb);
             c2 = c2 * fa * fb;
+            knext = load_kscale(0);
         }
         // P into tensor memory: f16 beside f16 V (one-byte pools), bf16 otherwise
         auto packP = [](float lo, float hi) { return ONE ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi); };
         float m = -INFINITY, l = 0.f;  // running maximum (scaled, base 2) and sum
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
+            if constexpr (ONE) {
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) kmul[q] = c2 * __shfl_sync(0xffffffffu, knext, q);
+                if (j + 1 < my_nkv) knext = load_kscale(j + 1);  // in flight while this tile waits
+            }
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS + t), j & 1, p.wait_ns));
             if (!ok) break;
             ptx::tc_fence_after();
@@ -816,14 +819,29 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
             }
             // row maximum: three-input max into 4 independent accumulators (64 instructions,
             // no serial chain of 128 dependent ones)
-            float mx4[4];
+            float mt;  // this tile's maximum, scaled (finite: key kbase <= qlim)
+            if constexpr (ONE) {
+                // per page part: its maximum times its multiplier (both > 0 scales), then across parts
+                mt = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
+                for (int q = 0; q < kParts; ++q) {
+                    float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kKeys; c += 2)
-                mx4[(c >> 1) & 3] = ptx::max3(mx4[(c >> 1) & 3], __uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1]));
-            const float smax = ptx::max3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
-            const float mt = smax * c2;  // this tile's maximum, scaled (finite: key kbase <= qlim)
+                    for (int c = q * PART; c < (q + 1) * PART; c += 4) {
+                        a0 = ptx::max3(a0, __uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1]));
+                        a1 = ptx::max3(a1, __uint_as_float(sraw[c + 2]), __uint_as_float(sraw[c + 3]));
+                    }
+                    mt = fmaxf(mt, fmaxf(a0, a1) * kmul[q]);
+                }
+            } else {
+                float mx4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKeys; c += 2)
+                    mx4[(c >> 1) & 3] = ptx::max3(mx4[(c >> 1) & 3], __uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1]));
+                mt = ptx::max3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * c2;
+            }
             // lazy rescale: keep the running maximum unless this tile exceeds it by 2^8
             const bool grow = mt > m + kRescaleLog2;
             if (__any_sync(0xffffffffu, grow && j > 0)) {
@@ -852,9 +870,10 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                     uint32_t hi[32], lo[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
+                        const float mul = ONE ? kmul[(64 * c + 2 * e) / PART] : c2;
                         const float2 x = ptx::f32x2_split(ptx::fma_f32x2(
                             ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
-                            c2x2, nmx2));
+                            ONE ? ptx::f32x2(mul, mul) : c2x2, nmx2));
                         const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
                         hi[e] = packP(p0, p1);
                         if constexpr (ONE) {
@@ -874,9 +893,10 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                     uint32_t hi[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
+                        const float mul = ONE ? kmul[(64 * c + 2 * e) / PART] : c2;
                         const float2 x = ptx::f32x2_split(ptx::fma_f32x2(
                             ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
-                            c2x2, nmx2));
+                            ONE ? ptx::f32x2(mul, mul) : c2x2, nmx2));
                         const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
                         hi[e] = packP(p0, p1);
                         l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
@@ -901,7 +921,7 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                 float inv = 1.f / l;
                 if constexpr (ONE) {  // O was accumulated over V x 2^-eV
                     float fa, fb;
-                    pow2_pair(scale_exp(1), fa, fb);
+                    pow2_pair(scale_exp_v(), fa, fb);
                     inv = inv * fa * fb;
                 }
                 uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + tok) * p.Hq + h * p.G + g) * D);
