@@ -300,12 +300,13 @@ pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes
  *   cu_q_lens_dev: int32 [B+1], non-decreasing, cu_q_lens[0] = 0.
  *   max_q_len: host int >= every n_b (sizes the grid; 0 launches nothing).
  *   block_tables_dev: int32 [B][max_blocks]; context_lens_dev: int32 [B].
- * Pools: bf16, FP8-E4M3 or INT8.  On a one-byte pool the kernel dequantises K and V on chip
- * (code x the (block, head) scale, times a power of two per sequence and KV head that keeps the
- * values inside f16's range) and rounds each element once to f16 for the tensor-core products;
- * q is converted to f16 exactly (a power of two per row), the probabilities are f16 and fp32
- * accumulates.  Against the exact definition over code x scale the output is then within half
- * a bf16 ulp plus about 2^-11 of the largest |V| the row attends to.
+ * Pools: bf16, FP8-E4M3 or INT8.  On a one-byte pool the tensor-core products run in f16: K's
+ * codes exactly (their (block, head) scale multiplies the fp32 scores), V as code x the scale
+ * times a power of two per sequence and KV head that keeps the values inside f16's range,
+ * rounded once to f16; q is converted to f16 exactly (a power of two per row), the
+ * probabilities are f16 and fp32 accumulates.  Against the exact definition over code x scale
+ * the output is then within half a bf16 ulp plus about 2^-11 of the largest |V| the row
+ * attends to.
  * Supported: head_dim 64 or 128; n_q_heads / n_kv_heads a power of two <= 128;
  * B * n_kv_heads * ceil(max_q_len * n_q_heads / n_kv_heads / 256) < 2^31; scale positive and
  * finite.  Otherwise PKV_ERR_INVALID_ARG (nothing launched).  A chunk longer than its
