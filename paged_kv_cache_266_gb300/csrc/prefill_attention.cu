@@ -261,6 +261,9 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
     constexpr int KS = LY::kKSt;
     constexpr int kThr = ONE ? kThreadsOne : kThreads;
     constexpr int kSmWarp0 = ONE ? 8 : 4;  // first softmax warp
+    // one-byte pools with page parts of 32 or more keys take V's scale in the softmax exponent
+    // (V widened exactly); with parts of 16 (eight scales a tile) the widening applies it
+    constexpr bool VS = ONE && PART >= 32;
     constexpr uint32_t kQBytes = LY::kQBytes, kHalfBytes = LY::kHalfBytes;
     constexpr uint32_t kOffK = LY::kOffK, kOffV = LY::kOffV, kOffBar = LY::kOffBar;
     constexpr int kPanels = LY::kPanels;
@@ -458,8 +461,8 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
         // D = 128; 8 rows or 32 d with D = 64) are dealt round-robin to the warps.
         const int cw = warp - 2;  // 0..5
         const int32_t* tb = p.tables + (int64_t)b * p.max_blocks;
-        float fav, fbv;  // 2^-eV
-        pow2_pair(-scale_exp_v(), fav, fbv);
+        float fav = 1.f, fbv = 1.f;  // 2^-eV (parts of 16: the widening applies V's scale)
+        if constexpr (!VS) pow2_pair(-scale_exp_v(), fav, fbv);
         constexpr int kPassK = D == 128 ? 32 : 16;  // passes per tile: K
         constexpr int kPassV = D / 4;               // passes per tile: V (8 groups x D / 32)
         constexpr uint32_t kVtPanel = (uint32_t)D * 128u;
@@ -491,12 +494,14 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
             }
             return ok;
         };
-        float svn;
-        load_scales(0, svn);
+        float svn = 0.f;
+        if constexpr (!VS) load_scales(0, svn);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const float svc = svn;
-            if (j + 1 < n_kv) load_scales(j + 1, svn);  // in flight while this tile is widened
+            if constexpr (!VS) {
+                if (j + 1 < n_kv) load_scales(j + 1, svn);  // in flight while this tile is widened
+            }
             // ---- K
             ok = wait2(0, j, !LY::kInPlaceK);
             if (!ok || __shfl_sync(0xffffffffu, abort_s, 0)) break;
@@ -546,8 +551,11 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
 #pragma unroll 1
                 for (int i = cw; i < kPassV; i += kConverters) {
                     const int G = i / (D / 32), d = 32 * (i % (D / 32)) + lane;
-                    const float v = __shfl_sync(0xffffffffu, svc, (16 * G) / PART) * fav * fbv;
-                    const uint32_t s2 = ptx::pack_f16x2(v, v);
+                    uint32_t s2 = 0u;
+                    if constexpr (!VS) {
+                        const float v = __shfl_sync(0xffffffffu, svc, (16 * G) / PART) * fav * fbv;
+                        s2 = ptx::pack_f16x2(v, v);
+                    }
                     uint32_t src;
                     if constexpr (D == 128)
                         src = codeV + (uint32_t)(16 * G + (d >> 3)) * 128u + ((uint32_t)((d & 7) ^ ((d >> 3) & 7)) << 4);
@@ -559,8 +567,10 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                     widen4<KV>(__byte_perm(w.z, w.w, 0x5410), o[2], o[3]);  // tokens 4-7
                     widen4<KV>(__byte_perm(w.x, w.y, 0x7632), o[4], o[5]);  // tokens 8-11
                     widen4<KV>(__byte_perm(w.z, w.w, 0x7632), o[6], o[7]);  // tokens 12-15
+                    if constexpr (!VS) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
+                        for (int e = 0; e < 8; ++e) o[e] = mul_f16x2(o[e], s2);
+                    }
                     const uint32_t dst = dst0 + (uint32_t)(G >> 2) * kVtPanel + (uint32_t)d * 128u;
                     const int cc = (G & 3) * 2;
                     sts128(dst + ((uint32_t)(cc ^ (d & 7)) << 4), o[0], o[1], o[2], o[3]);
@@ -772,27 +782,34 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
         // scores in base 2: S x scale x log2(e).  One-byte pools compute S' = (q 2^eq).code: the
         // key's scale (that of its page part) multiplies the score here, per part of PART keys
         float c2 = p.scale_log2;
-        float kmul[kParts];  // one-byte: c2 x 2^-eq x the part's K scale, this tile
-        float knext = 1.f;   // lane q < kParts: part q's K scale of the next tile
+        // One-byte pools: per page part q of the tile, kmul[q] = c2 x 2^-eq x the part's K scale
+        // multiplies the scores; with parts of 32 or more keys lgv[q] = log2(the part's V scale x
+        // 2^-eV) also joins the exponent, so P' = p x V scale x 2^-eV comes out of the same ex2
+        // and V is widened exactly, the row sum taking P' x 2^-lgv[q] (the p the definition sums).
+        float kmul[kParts], lgv[kParts];
+        float2 snext = make_float2(1.f, 1.f);  // lane q < kParts: part q's (K, V) scales of the next tile
         const int32_t* tbs = p.tables + (int64_t)b * p.max_blocks;
-        // part `lane`'s K scale of tile j (1 past the context: a multiplier > 0 keeps masked
-        // -inf scores -inf)
-        auto load_kscale = [&](int j) -> float {
-            float v = 1.f;
+        // part `lane`'s scales of tile j (1 past the context: a multiplier > 0 keeps masked -inf
+        // scores -inf)
+        auto load_scales2 = [&](int j) -> float2 {
+            float2 v = make_float2(1.f, 1.f);
             if (lane < kParts) {
                 const int tok = j * kKeys + lane * PART;
                 if (tok < L) {
                     const int blk = tbs[tok / p.bs];
-                    if (blk >= 0 && blk < p.num_blocks) v = p.scales[((int64_t)blk * p.Hkv + h) * 4];
+                    if (blk >= 0 && blk < p.num_blocks)
+                        v = *reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + h) * 4);
                 }
             }
             return v;
         };
+        float vfa = 1.f, vfb = 1.f;  // 2^-eV
         if constexpr (ONE) {
             float fa, fb;
             pow2_pair(-eq, fa, fb);
             c2 = c2 * fa * fb;
-            knext = load_kscale(0);
+            pow2_pair(-scale_exp_v(), vfa, vfb);
+            snext = load_scales2(0);
         }
         // P into tensor memory: f16 beside f16 V (one-byte pools), bf16 otherwise
         auto packP = [](float lo, float hi) { return ONE ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi); };
@@ -801,8 +818,11 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
         for (int j = 0; j < my_nkv; ++j) {
             if constexpr (ONE) {
 #pragma unroll
-                for (int q = 0; q < kParts; ++q) kmul[q] = c2 * __shfl_sync(0xffffffffu, knext, q);
-                if (j + 1 < my_nkv) knext = load_kscale(j + 1);  // in flight while this tile waits
+                for (int q = 0; q < kParts; ++q) {
+                    kmul[q] = c2 * __shfl_sync(0xffffffffu, snext.x, q);
+                    if constexpr (VS) lgv[q] = __log2f(__shfl_sync(0xffffffffu, snext.y, q) * vfa * vfb);
+                }
+                if (j + 1 < my_nkv) snext = load_scales2(j + 1);  // in flight while this tile waits
             }
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS + t), j & 1, p.wait_ns));
             if (!ok) break;
@@ -870,10 +890,11 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                     uint32_t hi[32], lo[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float mul = ONE ? kmul[(64 * c + 2 * e) / PART] : c2;
+                        const int q = (64 * c + 2 * e) / PART;  // page part of this pair (unrolled)
+                        const float mul = ONE ? kmul[q] : c2, nm = VS ? lgv[q] - m : -m;
                         const float2 x = ptx::f32x2_split(ptx::fma_f32x2(
                             ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
-                            ONE ? ptx::f32x2(mul, mul) : c2x2, nmx2));
+                            ONE ? ptx::f32x2(mul, mul) : c2x2, VS ? ptx::f32x2(nm, nm) : nmx2));
                         const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
                         hi[e] = packP(p0, p1);
                         if constexpr (ONE) {
@@ -882,7 +903,12 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                         } else {
                             lo[e] = packP(p0 - ptx::bf16lo_to_f32(hi[e]), p1 - ptx::bf16hi_to_f32(hi[e]));
                         }
-                        l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
+                        if constexpr (VS) {
+                            const float iv = ptx::exp2_approx(-lgv[q]);
+                            l4[e & 3] = ptx::fma_f32x2(ptx::f32x2(p0, p1), ptx::f32x2(iv, iv), l4[e & 3]);
+                        } else {
+                            l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
+                        }
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
                     ptx::tmem_st32(tS + 64u + 32u * c, lo);
@@ -893,13 +919,19 @@ __global__ void __launch_bounds__(KV != 0 ? kThreadsOne : kThreads, 1)
                     uint32_t hi[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float mul = ONE ? kmul[(64 * c + 2 * e) / PART] : c2;
+                        const int q = (64 * c + 2 * e) / PART;  // page part of this pair (unrolled)
+                        const float mul = ONE ? kmul[q] : c2, nm = VS ? lgv[q] - m : -m;
                         const float2 x = ptx::f32x2_split(ptx::fma_f32x2(
                             ptx::f32x2(__uint_as_float(sraw[64 * c + 2 * e]), __uint_as_float(sraw[64 * c + 2 * e + 1])),
-                            ONE ? ptx::f32x2(mul, mul) : c2x2, nmx2));
+                            ONE ? ptx::f32x2(mul, mul) : c2x2, VS ? ptx::f32x2(nm, nm) : nmx2));
                         const float p0 = ptx::exp2_approx(x.x), p1 = ptx::exp2_approx(x.y);
                         hi[e] = packP(p0, p1);
-                        l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
+                        if constexpr (VS) {
+                            const float iv = ptx::exp2_approx(-lgv[q]);
+                            l4[e & 3] = ptx::fma_f32x2(ptx::f32x2(p0, p1), ptx::f32x2(iv, iv), l4[e & 3]);
+                        } else {
+                            l4[e & 3] = ptx::add_f32x2(l4[e & 3], ptx::f32x2(p0, p1));
+                        }
                     }
                     ptx::tmem_st32(tS + 32u * c, hi);
                 }
