@@ -301,9 +301,10 @@ pkv_status pkv_decode_workspace_init(void* workspace_dev, size_t workspace_bytes
  *   max_q_len: host int >= every n_b (sizes the grid; 0 launches nothing).
  *   block_tables_dev: int32 [B][max_blocks]; context_lens_dev: int32 [B].
  * Pools: bf16, FP8-E4M3 or INT8.  On a one-byte pool the tensor-core products run in f16: K's
- * codes exactly (their (block, head) scale multiplies the fp32 scores), V as code x the scale
- * times a power of two per sequence and KV head that keeps the values inside f16's range,
- * rounded once to f16; q is converted to f16 exactly (a power of two per row), the
+ * codes exactly (their (block, head) scale multiplies the fp32 scores); V's codes exactly with
+ * their scale carried by the probabilities (block_size >= 32), or as code x the scale rounded
+ * once to f16 (block_size 16), times a power of two per sequence and KV head that keeps the
+ * values inside f16's range; q is converted to f16 exactly (a power of two per row), the
  * probabilities are f16 and fp32 accumulates.  Against the exact definition over code x scale
  * the output is then within half a bf16 ulp plus about 2^-11 of the largest |V| the row
  * attends to.
