@@ -258,11 +258,17 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q_dev, const i
  * running batch appends one token per sequence and runs one forward pass): pkv_append of the
  * step's new K/V followed by pkv_decode_attention over the grown contexts.  Same arguments,
  * layouts, results and errors as those two calls made in sequence; all arguments are checked
- * before anything is launched.  The attention kernel is launched as a programmatic dependent
- * of the append, so its set-up (context lengths, block tables, query rows) overlaps the append
- * and its first pool read waits for the append to finish — the per-step launch overhead the
- * pages counter with CUDA graphs ("TensorRT-LLM 推理加速实战", §7.1).  The append must not write
- * q, block_tables or context_lens (it only writes the pool). */
+ * before anything is launched.  On a bf16 pool (and for more than 1024 new tokens) the
+ * attention kernel is launched as a programmatic dependent of the append, so its set-up
+ * (context lengths, block tables, query rows) overlaps the append and its first pool read waits
+ * for the append to finish — the per-step launch overhead the pages counter with CUDA graphs
+ * ("TensorRT-LLM 推理加速实战", §7.1).  On an FP8 or INT8 pool with 1 to 1024 new tokens one
+ * kernel does both: its warps quantise the new rows (the same codes and scales as pkv_append)
+ * while its set-up runs, and every page and scale is read after all rows are in.  That launch is
+ * cooperative (all its CTAs resident at once, which a GPU busy with other work can delay) and
+ * uses two words of the workspace, which return to zero like the merge tickets; its wait is
+ * bounded like the others.  The append must not write q, block_tables or context_lens (it only
+ * writes the pool). */
 pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new_dev, const void* v_new_dev,
                            const int64_t* slot_mapping_dev, int64_t N, const void* q_dev,
                            const int32_t* block_tables_dev, int max_blocks, const int32_t* context_lens_dev, int B,

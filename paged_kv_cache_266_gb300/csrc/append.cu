@@ -23,11 +23,17 @@
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace pkv {
 namespace {
 
 constexpr int kAppendThreads = 256;
+
+using quant::amax_bits;
+using quant::fp8_v_pos;
+using quant::quant_store;
+using quant::tile_elem;
 
 struct RowIndex {
     int64_t i;  // token
@@ -43,13 +49,6 @@ __device__ __forceinline__ RowIndex row_index(int64_t row, int Hkv) {
     r.h = rem - r.kv * Hkv;
     return r;
 }
-
-__device__ __forceinline__ int64_t tile_elem(int64_t blk, int kv, int h, int Hkv, int bs, int D) {
-    return ((blk * 2 + kv) * Hkv + h) * (int64_t)bs * D;
-}
-
-// Position of token u (0..15) inside a 16-byte fp8 V panel row (pair order of the MMA).
-__device__ __forceinline__ int fp8_v_pos(int u) { return u < 8 ? 4 * (u >> 1) + (u & 1) : 4 * ((u - 8) >> 1) + 2 + (u & 1); }
 
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) append_bf16_kernel(uint16_t* __restrict__ pool,
@@ -75,18 +74,6 @@ __global__ void __launch_bounds__(kAppendThreads) append_bf16_kernel(uint16_t* _
     const uint16_t* src = (r.kv ? v_new : k_new) + (r.i * Hkv + r.h) * D + part * 8;
     uint16_t* dst = pool + tile_elem(blk, r.kv, r.h, Hkv, bs, D) + (int64_t)t * D + part * 8;
     *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
-}
-
-// max |x| over eight bf16 elements, as fp32 bits (non-negative floats order like their bits)
-__device__ __forceinline__ uint32_t amax_bits(uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t m = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = (w[e] << 16) & 0x7fffffffu, hi = w[e] & 0x7fff0000u;
-        m = max(m, max(lo, hi));
-    }
-    return m;
 }
 
 template <int D>
@@ -119,41 +106,6 @@ __global__ void __launch_bounds__(kAppendThreads) fp8_amax_kernel(const uint16_t
     const int64_t blk = slot / bs;
     atomicMax(amax + (blk * Hkv + r.h) * 2 + r.kv, m);
     if (slot - blk * bs == 0 && r.kv == 0 && r.h == 0) fresh[blk] = 1;
-}
-
-// INT8 code of a quotient x / scale: nearest integer, ties to even (cvt.rni), clamped to
-// [-127, 127] (symmetric: -128 is never produced); the byte in the low 8 bits.
-__device__ __forceinline__ uint32_t int8_code(float q) {
-    const int c = __float2int_rn(q);
-    return (uint32_t)(c < -127 ? -127 : (c > 127 ? 127 : c)) & 0xffu;
-}
-
-// Quantise eight elements (part `part` of a row: elements 8*part .. 8*part+7) of token slot t of
-// block blk, K (kv = 0) or V (kv = 1) of head h, with scale s: x / s as an IEEE fp32 division, then
-// E4M3 round-to-nearest-even with saturation (or the int8 code), stored in the pool's layout.
-template <int D, bool I8>
-__device__ __forceinline__ void quant_store(uint8_t* __restrict__ pool, uint4 v, float s, int64_t blk, int t, int kv,
-                                            int h, int part, int Hkv, int bs) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t codes[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const float x0 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e]), s), x1 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e]), s);
-        const float x2 = __fdiv_rn(ptx::bf16lo_to_f32(w[2 * e + 1]), s),
-                    x3 = __fdiv_rn(ptx::bf16hi_to_f32(w[2 * e + 1]), s);
-        if constexpr (I8)
-            codes[e] = int8_code(x0) | (int8_code(x1) << 8) | (int8_code(x2) << 16) | (int8_code(x3) << 24);
-        else
-            codes[e] = ptx::f32x2_to_e4m3x2(x0, x1) | (ptx::f32x2_to_e4m3x2(x2, x3) << 16);
-    }
-    uint8_t* tile = pool + tile_elem(blk, kv, h, Hkv, bs, D);
-    if (kv == 0) {
-        *reinterpret_cast<uint2*>(tile + (int64_t)t * D + part * 8) = make_uint2(codes[0], codes[1]);
-    } else {
-        uint8_t* panel = tile + (int64_t)(t >> 4) * D * 16 + fp8_v_pos(t & 15);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) panel[(int64_t)(part * 8 + e) * 16] = (uint8_t)(codes[e >> 2] >> (8 * (e & 3)));
-    }
 }
 
 template <int D, bool I8>

@@ -30,6 +30,12 @@
 //    partial state per CTA in the workspace; the last CTA to finish (atomic ticket, no
 //    waiting) merges them with the log-sum-exp rule in slot order, so results do not depend
 //    on timing.
+//  * pkv_decode_step on a one-byte pool appends inside this kernel: while the producers look up
+//    their first block ids, the consumer warps of all CTAs quantise the step's new K/V rows into
+//    the pool, one warp per row pair, and count them in the workspace; every producer waits for
+//    the count before it reads a page or a scale.  The launch is cooperative (every CTA resident
+//    at once), as CTAs wait on rows other CTAs write.  A separate append kernel would take the
+//    registers the third one-byte CTA of each SM needs, so that CTA could start only after it.
 //
 // Every mbarrier wait is bounded (2 s of wall time); on expiry the kernel sets the pool's
 // error word and finishes without touching memory outside its buffers.
@@ -39,6 +45,7 @@
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace pkv {
 namespace attn {
@@ -50,6 +57,13 @@ constexpr int kMaxG = 8;
 constexpr int kMaxStages = 8;
 constexpr int kMaxBatch = 4096;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kFusedAppendMax = 1024;  // pkv_decode_step quantises up to this many tokens in-kernel
+// The step's own append counts its items in kAppCounters words kAppStride ints apart (separate
+// 128-byte lines, so the items' atomics and the producers' polls spread over the L2), followed by
+// the word that counts CTAs done with the pool.
+constexpr int kAppCounters = 32;
+constexpr int kAppStride = 32;
+constexpr int kAppWords = kAppCounters * kAppStride + 1;
 constexpr uint32_t kCombineBar = 1;  // named barrier of the consumer warps
 
 struct Params {
@@ -72,6 +86,15 @@ struct Params {
     float scale_log2;
     uint64_t wait_ns;   // bound of every mbarrier wait
     uint32_t stall_tx;  // test hook: bytes each stage expects beyond its copies (0 in normal use)
+    // pkv_decode_step on a one-byte pool: its n_new tokens' K and V rows ([n_new][Hkv][D] bf16)
+    // and slots, quantised into the pool by this kernel (n_new = 0: nothing to append); app:
+    // kAppWords workspace words (item counters, CTAs done), zero between calls.
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    const int64_t* slots;
+    int* app;
+    int n_new;
+    int app_extra;  // test hook: row pairs the wait expects beyond those quantised (0 in normal use)
 };
 
 // misc words in shared memory
@@ -110,6 +133,125 @@ __device__ __forceinline__ int find_seq(const int32_t* cumg, int B, int Hkv, int
     return lo;
 }
 
+// ------------------------------------------------------------------ the step's own append
+// Items: the RPP rows of one token that one warp covers (D/8 lanes of 8 elements per row), items
+// of token i numbered i * nrp ... i * nrp + nrp - 1.
+template <int D>
+__device__ __forceinline__ int append_items(const Params& p) {
+    constexpr int RPP = 32 / (D / 8);
+    return p.n_new * ((2 * p.Hkv + RPP - 1) / RPP);
+}
+
+// Consumer warp `warp` quantises items warp * gridDim.x + blockIdx.x, ... into the pool, with the
+// codes and scales of the appends (quant.cuh): a token opening its block (offset 0, or another
+// token of the call at offset 0 of the same block) sets the scale of each (K|V, head) row to the
+// row's amax over the call's tokens in that block / 448 (int8: / 127); any other token uses the
+// stored scale, which no token of the call writes.  Each item is counted in one of the
+// kAppCounters words once its stores are visible at GPU scope and to TMA reads.
+template <int D, bool I8>
+__device__ void append_rows(const Params& p, int warp) {
+    constexpr int TPR = D / 8, RPP = 32 / TPR;
+    const int lane = threadIdx.x & 31, part = lane % TPR, rsub = lane / TPR;
+    const int rows = 2 * p.Hkv, nrp = (rows + RPP - 1) / RPP, items = append_items<D>(p);
+    const int64_t cap = (int64_t)p.num_blocks * p.bs;
+    const int bs_shift = __ffs(p.bs) - 1;  // block sizes are powers of two
+    uint8_t* pool = const_cast<uint8_t*>(p.pool);
+    float* scales = const_cast<float*>(p.scales);
+    for (int it = warp * (int)gridDim.x + (int)blockIdx.x; it < items; it += kConsumerWarps * (int)gridDim.x) {
+        const int i = it / nrp, r = (it - i * nrp) * RPP + rsub;
+        const bool act = r < rows;
+        const int kv = act ? r / p.Hkv : 0, h = act ? r - kv * p.Hkv : 0;
+        const int64_t slot = __ldg(p.slots + i);
+        const uint4 v = act ? __ldg(reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) +
+                                                                   ((int64_t)i * p.Hkv + h) * D + part * 8))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        if (slot >= cap && lane == 0 && it == i * nrp) atomicOr(p.err, kErrBounds);
+        if (slot >= 0 && slot < cap) {  // one token per item: the same branch for the whole warp
+            const int64_t blk = slot >> bs_shift;
+            const int t = (int)(slot & (p.bs - 1));
+            float* sp = scales + (blk * p.Hkv + h) * 4 + kv;
+            const float stored = act ? __ldcg(sp) : 1.0f;  // used only if the block is not fresh
+            // the call's other tokens in this block, and whether one of them writes offset 0
+            bool same = false, zero = false;
+            for (int j0 = lane; j0 < p.n_new; j0 += 4 * 32) {
+                int64_t sj[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = j0 + 32 * u;
+                    sj[u] = (j < p.n_new && j != i) ? __ldg(p.slots + j) : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (sj[u] >= 0 && sj[u] < cap && (sj[u] >> bs_shift) == blk) {
+                        same = true;
+                        zero |= (sj[u] & (p.bs - 1)) == 0;
+                    }
+                }
+            }
+            const bool mates = __any_sync(0xffffffffu, same);
+            const bool fresh = t == 0 || __any_sync(0xffffffffu, zero);
+            float sc = stored;
+            if (fresh) {
+                uint32_t m = act ? quant::amax_bits(v) : 0u;
+                if (mates && act) {  // rare: several tokens of the call share the block
+                    const uint16_t* src = kv ? p.v_new : p.k_new;
+                    for (int j = 0; j < p.n_new; ++j) {
+                        const int64_t sj = __ldg(p.slots + j);
+                        if (j == i || sj < 0 || sj >= cap || (sj >> bs_shift) != blk) continue;
+                        m = max(m, quant::amax_bits(__ldg(
+                                       reinterpret_cast<const uint4*>(src + ((int64_t)j * p.Hkv + h) * D + part * 8))));
+                    }
+                }
+#pragma unroll
+                for (int o = TPR / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const float a = __uint_as_float(m);
+                sc = a > 0.0f ? __fdiv_rn(a, I8 ? 127.0f : 448.0f) : 1.0f;
+                if (act && t == 0 && part == 0) *sp = sc;
+            }
+            if (act) quant::quant_store<D, I8>(pool, v, sc, blk, t, kv, h, part, p.Hkv, p.bs);
+        }
+        ptx::fence_proxy_async_global();
+        __threadfence();  // with the atomic below: a release of every lane's stores
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.app + (it % kAppCounters) * kAppStride, 1);
+    }
+}
+
+// Producer warp: wait (bounded) until every item of the step's append is counted (lane k reads
+// counter k with acquire ordering, the warp sums them); then the pool's pages (TMA) and scales
+// read by this warp include the new rows.  Returns false if the wait ran out.
+template <int D>
+__device__ bool wait_appends(const Params& p) {
+    static_assert(kAppCounters == 32, "one counter per lane");
+    const int lane = threadIdx.x & 31;
+    const int need = append_items<D>(p) + p.app_extra;
+    const int* ctr = p.app + lane * kAppStride;
+    bool ok = true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {  // every exit is taken by the whole warp at once
+        if (__reduce_add_sync(0xffffffffu, (unsigned)ptx::ld_acquire_gpu(ctr)) >= (unsigned)need) break;
+        if ((i & 63u) == 0 && __any_sync(0xffffffffu, ptx::globaltimer_ns() - t0 > p.wait_ns)) {
+            ok = false;
+            break;
+        }
+    }
+    ptx::fence_proxy_async_global();
+    return ok;
+}
+
+// Producer warp, once this CTA reads nothing more of the pool: count the CTA done; the last CTA
+// returns every counter to zero for the next call.  Only after a wait that succeeded (otherwise
+// the words are left as they are and the workspace must be initialised again).
+__device__ void appends_done(const Params& p) {
+    const int lane = threadIdx.x & 31;
+    int last = 0;
+    if (lane == 0) last = ptx::atomic_add_acq_rel_gpu(p.app + kAppCounters * kAppStride, 1) == (int)gridDim.x - 1;
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+        atomicExch(p.app + lane * kAppStride, 0);
+        if (lane == 0) atomicExch(p.app + kAppCounters * kAppStride, 0);
+    }
+}
+
 // ------------------------------------------------------------------ producer warp
 struct GroupDesc {
     int b, h, g;
@@ -117,8 +259,9 @@ struct GroupDesc {
     float sk[4], sv[4];  // fp8 scales of the group's pages (loaded one batch after the ids)
 };
 
+// Returns false if the wait for the step's own append ran out.
 template <bool FP8, int D>
-__device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, const Params& p, const int32_t* cumg, const int32_t* lens_s,
+__device__ bool producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, const Params& p, const int32_t* cumg, const int32_t* lens_s,
                          int64_t R0, int64_t R1, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
                          volatile int* misc) {
     constexpr int kEsz = FP8 ? 1 : 2;
@@ -140,14 +283,15 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
             d.id[i] = (i < p.ppg && k < npages) ? __ldg(p.tables + (int64_t)b * p.max_blocks + k) : -1;
         }
     };
-    // fp8: the pages' scale pairs, once their block ids have arrived (out-of-range ids read 0)
+    // fp8: the pages' scale pairs, once their block ids have arrived (out-of-range ids read 0);
+    // coherent loads, as this kernel's own append may have written them
     auto fetch_scales = [&](GroupDesc& d) {
         if constexpr (FP8) {
             if (d.b < 0) return;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int blk = (d.id[i] >= 0 && d.id[i] < p.num_blocks) ? d.id[i] : 0;
-                const float2 v = __ldg(reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + d.h) * 4));
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(p.scales + ((int64_t)blk * p.Hkv + d.h) * 4));
                 d.sk[i] = v.x;
                 d.sv[i] = v.y;
             }
@@ -166,9 +310,15 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
     const uint32_t part_bytes = 2u * (uint32_t)p.box_rows * D * kEsz;  // K rows + V rows of one page part
     // When launched behind this step's append (programmatic dependent launch), the pool and its
     // block scales (which the append sets on a block's first write) are read only after that
-    // kernel has finished; otherwise this returns at once.  Block tables and lengths are inputs
-    // the append does not write, so their look-ups above overlap it.
+    // kernel has finished; otherwise this returns at once.  When this kernel appends the step's
+    // tokens itself, they are read only after every row is in.  Block tables and lengths are
+    // inputs the append does not write, so their look-ups above overlap it.
     ptx::grid_dependency_wait();
+    const bool appended = !(FP8 && p.n_new > 0) || wait_appends<D>(p);
+    if (!appended) {
+        if (lane == 0) flag_abort(p, misc);
+        ok = false;
+    }
     fetch_scales(cur);
     for (int64_t e0 = R0; e0 < R1 && ok; e0 += 32) {
         describe(e0 + 64 + lane, nxt2);
@@ -268,6 +418,7 @@ __device__ void producer(const CUtensorMap* tmap, const CUtensorMap* tmap_tail, 
             }
     }
     __syncwarp();
+    return appended;
 }
 
 // ------------------------------------------------------------------ consumer math
@@ -889,8 +1040,18 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
     }
 
     if (warp == kConsumerWarps) {
-        if (R0 < R1) producer<FP8, D>(&tmap, &tmap_tail, p, cumg, lens_s, R0, R1, sbase, bar_full, bar_empty, misc);
+        bool appended = true;
+        if (R0 < R1) {
+            appended = producer<FP8, D>(&tmap, &tmap_tail, p, cumg, lens_s, R0, R1, sbase, bar_full, bar_empty, misc);
+        } else if (FP8 && p.n_new > 0) {  // no groups here, but every CTA takes part in the count
+            appended = wait_appends<D>(p);
+            if (!appended && lane == 0) atomicOr(p.err, kErrTimeout);
+        }
+        if (FP8 && p.n_new > 0 && appended) appends_done(p);
         return;
+    }
+    if constexpr (FP8) {
+        if (p.n_new > 0) append_rows<D, I8>(p, warp);
     }
     // Sequences with an empty context get zeros (no group covers them).
     for (int bb = blockIdx.x; bb < p.B; bb += gridDim.x) {
@@ -999,7 +1160,9 @@ bool compute_plan(const pkv_pool* pool, int B, int G, int pref_ctas, int max_sta
     pl.ctas_per_sm = std::min(pl.ctas_per_sm, occ);
     pl.grid = pl.ctas_per_sm * pool->sm_count;
     const size_t pairs = (size_t)B * pool->n_kv_heads;
-    pl.counters_bytes = (pairs * sizeof(int) + 255) / 256 * 256;
+    // merge tickets [pairs], then (from a 128-byte boundary) the words of the step's own append
+    pl.counters_bytes = ((pairs + kAppStride - 1) / kAppStride * kAppStride + kAppWords) * sizeof(int);
+    pl.counters_bytes = (pl.counters_bytes + 255) / 256 * 256;
     pl.slots = pairs + (size_t)pl.grid;
     pl.ws_bytes = pl.counters_bytes + pl.slots * G * (D + 2) * sizeof(float);
     return true;
@@ -1027,6 +1190,11 @@ pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tab
     p.pool = static_cast<const uint8_t*>(pool->kv);
     p.scales = pool->scales;
     p.counters = static_cast<int*>(workspace);
+    p.app = p.counters + ((size_t)B * pool->n_kv_heads + kAppStride - 1) / kAppStride * kAppStride;
+    p.k_new = p.v_new = nullptr;
+    p.slots = nullptr;
+    p.n_new = 0;
+    p.app_extra = 0;
     p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
     p.part_ml = p.partials + pl.slots * G * pool->head_dim;
     p.err = pool->err;
@@ -1059,7 +1227,9 @@ pkv_status prepare(const pkv_pool* pool, const void* q, const int32_t* block_tab
 
 // Launch on `st`.  With `pdl` the kernel may start while the preceding kernel on the stream
 // (an append of this step) is still running: it prepares everything that does not read the
-// pool and waits (griddepcontrol.wait) before its first page copy.
+// pool and waits (griddepcontrol.wait) before its first page copy.  A kernel that appends the
+// step's tokens itself (p.n_new > 0) is launched cooperatively: its CTAs wait on rows other CTAs
+// write, so all of them must be resident at once (the grid is the SMs' resident capacity).
 pkv_status launch(const pkv_pool* pool, const Plan& pl, const Params& p, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
@@ -1067,10 +1237,15 @@ pkv_status launch(const pkv_pool* pool, const Plan& pl, const Params& p, cudaStr
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (p.n_new > 0) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = (pdl || p.n_new > 0) ? 1 : 0;
     const bool i8 = pool->dtype == PKV_KV_INT8;
     const bool fp8 = pool->dtype != PKV_KV_BF16;  // one-byte codes (fp8 or int8)
     cudaError_t e;
@@ -1130,6 +1305,15 @@ pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new, const void* v_new,
     st = pkv::attn::prepare(pool, q, block_tables, max_blocks, context_lens, B, n_q_heads, scale, out, workspace,
                             workspace_bytes, pl, p);
     if (st != PKV_OK) return st;
+    if (pool->dtype != PKV_KV_BF16 && B > 0 && N > 0 && N <= pkv::attn::kFusedAppendMax) {
+        // one-byte pool: the attention kernel quantises the new tokens itself
+        p.k_new = static_cast<const uint16_t*>(k_new);
+        p.v_new = static_cast<const uint16_t*>(v_new);
+        p.slots = slot_mapping;
+        p.n_new = (int)N;
+        p.app_extra = pkv::settings().stall_appends ? 1 : 0;
+        return pkv::attn::launch(pool, pl, p, reinterpret_cast<cudaStream_t>(stream), false);
+    }
     st = pkv_append(pool, k_new, v_new, slot_mapping, N, stream);
     if (st != PKV_OK || B == 0) return st;
     return pkv::attn::launch(pool, pl, p, reinterpret_cast<cudaStream_t>(stream), N > 0);

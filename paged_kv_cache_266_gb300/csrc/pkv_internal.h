@@ -29,11 +29,14 @@ void allocator_delete(pkv_allocator* a);
 //   PKV_TEST_WAIT_LIMIT_MS  > 0: bound of every kernel wait in ms (default 2 s);
 //   PKV_TEST_STALL_COPIES   != 0: every pipeline stage expects 16 bytes no copy delivers, so the
 //                           bounded waits run out (failure detection tested without a fault);
+//   PKV_TEST_STALL_APPENDS  != 0: the decode step's wait for its own append expects one row more
+//                           than the kernel quantises, so that bounded wait runs out;
 //   PKV_ATTN_CTAS_PER_SM    decode attention CTAs per SM (0: the kernel's default);
 //   PKV_ATTN_MAX_STAGES     decode attention pipeline stages at most (0: default).
 struct Settings {
     int wait_limit_ms;
     int stall_copies;
+    int stall_appends;
     int attn_ctas_per_sm;
     int attn_max_stages;
 };

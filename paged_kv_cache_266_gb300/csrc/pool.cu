@@ -24,7 +24,8 @@ int env_int(const char* name) {
 
 Settings read_settings() {
     return Settings{env_int("PKV_TEST_WAIT_LIMIT_MS"), env_int("PKV_TEST_STALL_COPIES"),
-                    env_int("PKV_ATTN_CTAS_PER_SM"), env_int("PKV_ATTN_MAX_STAGES")};
+                    env_int("PKV_TEST_STALL_APPENDS"), env_int("PKV_ATTN_CTAS_PER_SM"),
+                    env_int("PKV_ATTN_MAX_STAGES")};
 }
 
 Settings g_settings = read_settings();

@@ -193,6 +193,17 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
     return old;
 }
 
+// Load at GPU scope with acquire ordering: reads ordered after it (the caller's, and after a
+// barrier its warp's or CTA's) see every write ordered before the release that produced the value.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Generic-proxy accesses to global memory ordered with this thread's async-proxy ones (TMA).
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // 2^x with the hardware approximation (flushes denormal results; 2^-inf = +0).
 __device__ __forceinline__ float exp2_approx(float x) {
     float y;

@@ -99,15 +99,27 @@ def test_shapes(pkv, dtype, D, bs):
         step.close()
 
 
-@pytest.mark.parametrize("name", ["c0", "c2", "c4"])
+@pytest.mark.parametrize("name", ["c0", "c2", "c4", "c4-int8"])
 def test_fused_step_equals_separate_calls(pkv, name):
-    """pkv_decode_step (append, then attention as a programmatic dependent launch) gives the
-    same pool bytes and outputs, bit for bit, as pkv_append followed by pkv_decode_attention."""
+    """pkv_decode_step gives the same pool bytes and outputs, bit for bit, as pkv_append followed
+    by pkv_decode_attention: on bf16 pools the append kernel with the attention as a programmatic
+    dependent launch, on one-byte pools (c4) the attention kernel quantising the tokens itself.
+    Three steps in a row: the step's workspace words (tickets and the append's counters) are back
+    at zero after each."""
+    import dataclasses
     import torch
     from paged_kv_cache_266_gb300.runner import DecodeStep
-    w = W.make_workload(name)
+    w = W.make_workload(name.split("-")[0])
+    if name.endswith("int8"):
+        w = dataclasses.replace(w, kv_dtype="int8")
     a, b = DecodeStep(w), DecodeStep(w)
-    a.step(fused=True)
+    # merge tickets [B * Hkv], then from the next multiple of 32 ints the append's 32 counters
+    # (32 ints apart) and its CTA count
+    words = -(-w.B * w.Hkv // 32) * 32 + 32 * 32 + 1
+    for _ in range(3):
+        a.step(fused=True)
+        torch.cuda.synchronize()
+        assert not a.workspace[: words * 4].any(), "workspace words must return to zero"
     b.step(fused=False)
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_error(a.pool.handle) == pkv.PKV_OK
@@ -321,6 +333,35 @@ def test_bounded_waits_report_timeout_and_leave_the_context_usable(pkv, stall_ho
     step.close()
 
 
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int8"])
+def test_step_append_wait_is_bounded(pkv, monkeypatch, kv_dtype):
+    """On a one-byte pool pkv_decode_step quantises its new tokens inside the attention kernel,
+    whose producers wait until every row is in.  With the test hook that wait expects one row
+    pair more than the kernel writes and gives up after 20 ms: the call reports PKV_ERR_TIMEOUT,
+    no fault, and once the workspace is initialised again the next step stores the oracle's
+    codes and scales and gives its outputs (the append is idempotent: same rows, same slots)."""
+    import torch
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    w = W.custom_workload(307, 3, 8, 2, 128, 16, [300, 70, 900], append=True, kv_dtype=kv_dtype)
+    step = DecodeStep(w)
+    monkeypatch.setenv("PKV_TEST_STALL_APPENDS", "1")
+    monkeypatch.setenv("PKV_TEST_WAIT_LIMIT_MS", "20")
+    pkv.pkv_debug_reload_env()
+    try:
+        step.step()
+        torch.cuda.synchronize()
+        assert pkv.pkv_check_device_error(step.pool.handle) == pkv.PKV_ERR_TIMEOUT
+    finally:
+        monkeypatch.delenv("PKV_TEST_STALL_APPENDS", raising=False)
+        monkeypatch.delenv("PKV_TEST_WAIT_LIMIT_MS", raising=False)
+        pkv.pkv_debug_reload_env()
+    pkv.pkv_decode_workspace_init(step.workspace)  # the wait's counters may have been left mid-count
+    step.step()
+    torch.cuda.synchronize()
+    _check_against_oracle(pkv, w, step)
+    step.close()
+
+
 def test_context_longer_than_table_is_clamped_and_flagged(pkv):
     import torch
     w = W.custom_workload(303, 2, 4, 1, 64, 16, [30, 20], append=False)
@@ -410,6 +451,82 @@ def test_fp8_encode_matches_oracle_on_ties_and_subnormals(pkv):
     pkv.pkv_pool_destroy(handle)
 
 
+def _near_boundary_rows(int8: bool, n_tok: int, D: int, seed: int) -> np.ndarray:
+    """Token rows (one KV head) for quantisation at rounding boundaries.  Element 0 of a row is
+    its amax, so a token opening its own block gets the scale s = amax/448 (amax/127 for int8);
+    the other elements are bf16 values x whose fp32 quotient x / s lies within 16 fp32 steps of
+    a code's rounding boundary (the midpoint of two adjacent E4M3 values; a half-integer for
+    int8), found by trying every positive bf16 value up to amax, with random signs, and random
+    bf16 values below amax where too few are that close.  The amax values: random ones, powers
+    of two times the code's largest value (s a power of two: the boundaries are hit exactly) and
+    the same times 1.125, 1.25 or 1.375 (exact boundary hits at a scale whose reciprocal is
+    inexact)."""
+    import torch
+    rng = np.random.default_rng(seed)
+    cmax = 127.0 if int8 else 448.0
+    if int8:
+        bounds = np.arange(0.5, 127.0, 1.0)
+    else:
+        vals = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+        bounds = (vals[:-1] + vals[1:]) / 2
+    bounds = bounds.astype(np.float32)
+    bound_bits = bounds.view(np.int32).astype(np.int64)
+    pos_bits = np.arange(1, 0x7F80, dtype=np.uint32)
+    allx = (pos_bits << 16).view(np.float32)
+
+    def to_bf16(a):
+        return torch.tensor(np.asarray(a, np.float32)).to(torch.bfloat16).float().numpy()
+
+    rows = np.zeros((n_tok, 1, D), dtype=np.uint16)
+    for t in range(n_tok):
+        kind = t % 3
+        if kind == 0:
+            amax = to_bf16(rng.uniform(1.0, 2.0) * 2.0 ** rng.integers(-8, 9))
+        else:
+            f = 1.0 if kind == 1 else float(rng.choice([1.125, 1.25, 1.375]))
+            amax = to_bf16(cmax * f * 2.0 ** rng.integers(-8, 9))
+        amax = np.float32(amax)
+        sc = np.float32(amax / np.float32(cmax))
+        xs = allx[allx <= amax]
+        q = (xs / sc).astype(np.float32)
+        i = np.clip(np.searchsorted(bounds, q), 1, len(bounds) - 1)
+        qb = q.view(np.int32).astype(np.int64)
+        steps = np.minimum(np.abs(qb - bound_bits[i - 1]), np.abs(qb - bound_bits[i]))
+        near = xs[steps <= 16]
+        pick = rng.choice(near, size=min(len(near), D - 1), replace=False) if len(near) else near
+        fill = rng.choice(xs, size=D - 1 - len(pick))
+        x = np.concatenate([pick, fill]).astype(np.float32) * rng.choice([-1.0, 1.0], size=D - 1)
+        row = np.concatenate([[amax], x]).astype(np.float32)
+        rows[t, 0] = torch.tensor(row).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return rows
+
+
+@pytest.mark.parametrize("dtype", ["fp8_e4m3", "int8"])
+def test_one_byte_encode_at_rounding_boundaries(pkv, dtype):
+    """Quantisation where x / s falls on or within a few fp32 steps of a code's rounding boundary,
+    at power-of-two and other scales: the stored codes and scales match the oracle bit for bit,
+    through the one-pass append (700 tokens) and the three-pass one (1100 tokens)."""
+    import torch
+    from paged_kv_cache_266_gb300 import pkv_append
+    from paged_kv_cache_266_gb300.runner import _wrap_device
+    D, n1, n2 = 128, 700, 1100
+    rows = _near_boundary_rows(dtype == "int8", n1 + n2, D, seed=11 if dtype == "int8" else 12)
+    nb = n1 + n2
+    handle = pkv.pkv_pool_create(nb, 16, 1, D, pkv.KV_DTYPES[dtype])
+    ref = oracle.Pool(nb, 16, 1, D, odrive.KV_CODE[dtype])
+    slots = np.arange(nb, dtype=np.int64) * 16  # each token opens its own block
+    for a, b in ((0, n1), (n1, nb)):
+        dk = torch.from_numpy(rows[a:b].view(np.int16)).view(torch.bfloat16).cuda()
+        pkv_append(handle, dk, dk, torch.from_numpy(slots[a:b]).cuda())
+        assert ref.append(rows[a:b], rows[a:b], slots[a:b]) == 0
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(handle) == pkv.PKV_OK
+    kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(handle)
+    assert np.array_equal(_wrap_device(sc_ptr, sc_bytes).cpu().numpy().view(np.float32), ref.scales)
+    assert np.array_equal(_wrap_device(kv_ptr, kv_bytes).cpu().numpy(), ref.data)
+    pkv.pkv_pool_destroy(handle)
+
+
 def _wide_range_queries(q_bits: np.ndarray, seed: int) -> np.ndarray:
     """bf16 query rows whose magnitudes span 2^-30 .. 2^40 (the f16 range is about 2^-24 ..
     65504): each row is the drawn N(0,1) row times 2^u for its own u, and a few rows mix
@@ -458,18 +575,20 @@ def test_queries_across_the_bf16_range(pkv, dtype, D):
 
 @pytest.mark.parametrize("dtype", ["fp8_e4m3", "int8"])
 @pytest.mark.parametrize("bs", [16, 64])
-def test_small_appends_with_several_tokens_per_block(pkv, dtype, bs):
+@pytest.mark.parametrize("D,Hkv", [(128, 2), (128, 12), (64, 20)])
+def test_small_appends_with_several_tokens_per_block(pkv, dtype, bs, D, Hkv):
     """Appends of up to 1024 tokens (a decode step appends one per sequence) quantise in one
     pass, each token finding the call's other tokens in its block.  Calls whose tokens share
     blocks in shuffled order (blocks the call opens, blocks continued from earlier calls), with a
     padding slot, must store the oracle's codes and scales bit for bit after every call; so must
-    a call of 1025 tokens (three passes)."""
+    a call of 1025 tokens (three passes).  Head counts: all of a token's 2 * Hkv rows loaded up
+    front (Hkv 2), rows loaded after the slot scan (Hkv 12 at D 128), and rows past the 32nd,
+    whose stored scale is read on its own (Hkv 20)."""
     import torch
-    D, Hkv = 128, 2
     nb = 6400 // bs
     handle = pkv.pkv_pool_create(nb, bs, Hkv, D, pkv.KV_DTYPES[dtype])
     ref = oracle.Pool(nb, bs, Hkv, D, odrive.KV_CODE[dtype])
-    rng = np.random.default_rng(bs + (7 if dtype == "int8" else 0))
+    rng = np.random.default_rng(bs + (7 if dtype == "int8" else 0) + Hkv)
     fill = np.zeros(nb, dtype=np.int64)
     from paged_kv_cache_266_gb300.runner import _wrap_device
     kv_ptr, kv_bytes, sc_ptr, sc_bytes = pkv.pkv_pool_raw(handle)
