@@ -65,9 +65,11 @@ def measured_peaks():
 
 
 # The sources that determine the decode attention kernel's code and launch (its own file, the
-# PTX helpers, the pool's tensor maps and the shared declarations; not the ABI header's comments).
+# PTX helpers, the one-byte codes its step's append writes, the pool's tensor maps and the shared
+# declarations; not the ABI header's comments).
 DECODE_KERNEL_SOURCES = ("paged_kv_cache_266_gb300/csrc/decode_attention.cu", "paged_kv_cache_266_gb300/csrc/ptx.cuh",
-                         "paged_kv_cache_266_gb300/csrc/pkv_internal.h", "paged_kv_cache_266_gb300/csrc/pool.cu")
+                         "paged_kv_cache_266_gb300/csrc/quant.cuh", "paged_kv_cache_266_gb300/csrc/pkv_internal.h",
+                         "paged_kv_cache_266_gb300/csrc/pool.cu")
 
 
 def kernel_source_hash() -> str:

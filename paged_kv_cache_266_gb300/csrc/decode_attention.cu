@@ -148,8 +148,32 @@ __device__ __forceinline__ int append_items(const Params& p) {
 // row's amax over the call's tokens in that block / 448 (int8: / 127); any other token uses the
 // stored scale, which no token of the call writes.  Each item is counted in one of the
 // kAppCounters words once its stores are visible at GPU scope and to TMA reads.
+struct AppendPre {
+    int64_t slot;
+    uint4 v;
+};
+
+// The first item's slot and row, loaded before the kernel's set-up so that they arrive meanwhile.
+template <int D>
+__device__ __forceinline__ AppendPre append_preload(const Params& p, int warp) {
+    constexpr int TPR = D / 8, RPP = 32 / TPR;
+    const int lane = threadIdx.x & 31, part = lane % TPR, rsub = lane / TPR;
+    const int rows = 2 * p.Hkv, nrp = (rows + RPP - 1) / RPP;
+    const int it = warp * (int)gridDim.x + (int)blockIdx.x;
+    AppendPre pre{-1, make_uint4(0u, 0u, 0u, 0u)};
+    if (it < append_items<D>(p)) {
+        const int i = it / nrp, r = (it - i * nrp) * RPP + rsub;
+        pre.slot = __ldg(p.slots + i);
+        if (r < rows) {
+            const int kv = r / p.Hkv, h = r - kv * p.Hkv;
+            pre.v = __ldg(reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) + ((int64_t)i * p.Hkv + h) * D + part * 8));
+        }
+    }
+    return pre;
+}
+
 template <int D, bool I8>
-__device__ void append_rows(const Params& p, int warp) {
+__device__ void append_rows(const Params& p, int warp, const AppendPre& pre) {
     constexpr int TPR = D / 8, RPP = 32 / TPR;
     const int lane = threadIdx.x & 31, part = lane % TPR, rsub = lane / TPR;
     const int rows = 2 * p.Hkv, nrp = (rows + RPP - 1) / RPP, items = append_items<D>(p);
@@ -161,10 +185,12 @@ __device__ void append_rows(const Params& p, int warp) {
         const int i = it / nrp, r = (it - i * nrp) * RPP + rsub;
         const bool act = r < rows;
         const int kv = act ? r / p.Hkv : 0, h = act ? r - kv * p.Hkv : 0;
-        const int64_t slot = __ldg(p.slots + i);
-        const uint4 v = act ? __ldg(reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) +
-                                                                   ((int64_t)i * p.Hkv + h) * D + part * 8))
-                            : make_uint4(0u, 0u, 0u, 0u);
+        const bool first = it == warp * (int)gridDim.x + (int)blockIdx.x;
+        const int64_t slot = first ? pre.slot : __ldg(p.slots + i);
+        const uint4 v = first ? pre.v
+                        : act ? __ldg(reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) +
+                                                                     ((int64_t)i * p.Hkv + h) * D + part * 8))
+                              : make_uint4(0u, 0u, 0u, 0u);
         if (slot >= cap && lane == 0 && it == i * nrp) atomicOr(p.err, kErrBounds);
         if (slot >= 0 && slot < cap) {  // one token per item: the same branch for the whole warp
             const int64_t blk = slot >> bs_shift;
@@ -211,9 +237,8 @@ __device__ void append_rows(const Params& p, int warp) {
             if (act) quant::quant_store<D, I8>(pool, v, sc, blk, t, kv, h, part, p.Hkv, p.bs);
         }
         ptx::fence_proxy_async_global();
-        __threadfence();  // with the atomic below: a release of every lane's stores
-        __syncwarp();
-        if (lane == 0) atomicAdd(p.app + (it % kAppCounters) * kAppStride, 1);
+        __syncwarp();  // orders every lane's stores before lane 0's release, which covers them all
+        if (lane == 0) ptx::red_add_release_gpu(p.app + (it % kAppCounters) * kAppStride, 1);
     }
 }
 
@@ -977,6 +1002,10 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    AppendPre pre{-1, make_uint4(0u, 0u, 0u, 0u)};
+    if constexpr (FP8) {
+        if (p.n_new > 0 && warp < kConsumerWarps) pre = append_preload<D>(p, warp);
+    }
     int32_t* cumg = reinterpret_cast<int32_t*>(smem + p.off_lens);
     int32_t* lens_s = cumg + p.B + 1;
     volatile int* misc = reinterpret_cast<volatile int*>(smem + p.off_misc);
@@ -1051,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) decode_kernel(const __g
         return;
     }
     if constexpr (FP8) {
-        if (p.n_new > 0) append_rows<D, I8>(p, warp);
+        if (p.n_new > 0) append_rows<D, I8>(p, warp, pre);
     }
     // Sequences with an empty context get zeros (no group covers them).
     for (int bb = blockIdx.x; bb < p.B; bb += gridDim.x) {

@@ -201,6 +201,13 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     return v;
 }
 
+// Atomic add at GPU scope with release ordering, no result: writes ordered before it (the
+// caller's, and after a barrier its warp's or CTA's) are visible to a thread whose acquire reads
+// a value it produced.
+__device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Generic-proxy accesses to global memory ordered with this thread's async-proxy ones (TMA).
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
