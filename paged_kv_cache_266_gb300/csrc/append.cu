@@ -11,10 +11,12 @@
 // cache) and int8 pools (the same with amax/127 and symmetric int8 codes): one fp32 scale per
 // (block, K|V, head).  A block's scales are derived by the call
 // that writes its offset 0, as amax/448 over that call's tokens in the block (1 when the
-// amax is 0); later calls reuse them and saturate.  Calls of up to 1024 tokens (decode steps)
-// do this in one kernel, a CTA per token that finds the call's other tokens in its block by
-// scanning the call's slots (quant_append_small_kernel).  Larger calls take three short passes,
-// with no grid-wide synchronisation inside a kernel:
+// amax is 0); later calls reuse them and saturate.  Calls of up to 1024 tokens (a decode step's
+// size) do this in one kernel, a CTA per token that finds the call's other tokens in its block by
+// scanning the call's slots (quant_append_small_kernel); pkv_decode_step on a one-byte pool does
+// the same per row pair inside the attention kernel instead (decode_attention.cu), with the
+// element codes of quant.cuh.  Larger calls take three short passes, with no grid-wide
+// synchronisation inside a kernel:
 //   1. amax: per row |x| max, atomicMax into a per-(block, K|V, head) scratch word, and a
 //      per-block "offset 0 written" flag;
 //   2. quantise: derive/lookup the scale, x / scale (IEEE division), RNE-satfinite to E4M3;
