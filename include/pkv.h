@@ -266,7 +266,8 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, const void* q_dev, const i
  * kernel does both: its warps quantise the new rows (the same codes and scales as pkv_append)
  * while its set-up runs, and every page and scale is read after all rows are in.  That launch is
  * cooperative (all its CTAs resident at once, which a GPU busy with other work can delay) and
- * uses two words of the workspace, which return to zero like the merge tickets; its wait is
+ * uses 33 words of the workspace (32 item counters 128 bytes apart and a CTA count, about 4 KB,
+ * included in pkv_decode_workspace_bytes), which return to zero like the merge tickets; its wait is
  * bounded like the others.  The append must not write q, block_tables or context_lens (it only
  * writes the pool). */
 pkv_status pkv_decode_step(pkv_pool* pool, const void* k_new_dev, const void* v_new_dev,
@@ -285,7 +286,8 @@ pkv_status pkv_decode_step_rope(pkv_pool* pool, void* k_new_dev, const void* v_n
                                 const int32_t* context_lens_dev, int B, int n_q_heads, float scale, void* out_dev,
                                 void* workspace_dev, size_t workspace_bytes, pkv_stream_t stream);
 
-/* Workspace size for pkv_decode_attention with these B, n_q_heads and max_blocks. */
+/* Workspace size for pkv_decode_attention and pkv_decode_step with these B, n_q_heads and
+ * max_blocks. */
 pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int B, int n_q_heads, int max_blocks, size_t* out);
 
 /* cudaMemsetAsync(workspace, 0, bytes, stream): prepares a fresh workspace. */
