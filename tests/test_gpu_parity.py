@@ -362,6 +362,49 @@ def test_step_append_wait_is_bounded(pkv, monkeypatch, kv_dtype):
     step.close()
 
 
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int8"])
+def test_step_in_kernel_append_with_block_mates(pkv, kv_dtype):
+    """pkv_decode_step on a one-byte pool appends inside the attention kernel, each row pair
+    finding the call's other tokens in its block.  A call whose 40-odd tokens share six blocks in
+    shuffled order (runs from offset 0, which open their block and derive its scale from all of
+    the call's rows there, and runs from later offsets, which keep the stored scale), with a
+    padding slot, into blocks the attention reads: the pool bytes, scales and outputs equal,
+    bit for bit, those of pkv_append followed by pkv_decode_attention."""
+    import torch
+    from paged_kv_cache_266_gb300 import pkv_append, pkv_decode_attention, pkv_decode_step
+    from paged_kv_cache_266_gb300.runner import DecodeStep
+    w = W.custom_workload(308, 4, 8, 2, 128, 16, [200, 37, 500, 64], append=True, kv_dtype=kv_dtype)
+    a, b = DecodeStep(w), DecodeStep(w)
+    rng = np.random.default_rng(5 if kv_dtype == "int8" else 6)
+    used = np.unique(a.tables_host[a.tables_host >= 0])
+    blocks = rng.choice(used, size=6, replace=False)
+    slots = []
+    for j, blk in enumerate(blocks):
+        start = 0 if j % 2 == 0 else int(rng.integers(1, 8))
+        slots += [int(blk) * 16 + start + u for u in range(int(rng.integers(3, 9)))]
+    slots.append(-1)
+    slots = np.array(slots, dtype=np.int64)
+    rng.shuffle(slots)
+    N = len(slots)
+    gen = torch.Generator().manual_seed(7)
+    k = (torch.randn(N, w.Hkv, w.D, generator=gen) * 3).to(torch.bfloat16).cuda()
+    v = (torch.randn(N, w.Hkv, w.D, generator=gen) * 3).to(torch.bfloat16).cuda()
+    sd = torch.from_numpy(slots).cuda()
+    pkv_decode_step(a.pool.handle, k, v, sd, a.q, a.tables, a.lens, a.scale, a.out, a.workspace)
+    pkv_append(b.pool.handle, k, v, sd)
+    pkv_decode_attention(b.pool.handle, b.q, b.tables, b.lens, b.scale, b.out, b.workspace)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_error(a.pool.handle) == pkv.PKV_OK
+    assert pkv.pkv_check_device_error(b.pool.handle) == pkv.PKV_OK
+    ka, sa = a.pool_bytes_host()
+    kb, sb = b.pool_bytes_host()
+    assert np.array_equal(sa, sb), "block scales differ"
+    assert np.array_equal(ka, kb), "pool bytes differ"
+    assert np.array_equal(a.out_host(), b.out_host())
+    a.close()
+    b.close()
+
+
 def test_context_longer_than_table_is_clamped_and_flagged(pkv):
     import torch
     w = W.custom_workload(303, 2, 4, 1, 64, 16, [30, 20], append=False)
