@@ -10,7 +10,9 @@ import pytest
 import torch
 
 import oracle
+import oracle.drive as odrive
 import pkv_workloads as W
+from boundary_rows import near_boundary_rows
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -376,3 +378,35 @@ def test_fp8_quantisation_error_within_half_step():
         for d in range(0, 128, 7):
             back = oracle.e4m3_decode(int(pool.data[pool.elem_byte(0, 0, 0, t, d)])) * s
             assert abs(back - xf[t, d]) <= max(abs(xf[t, d]) * 2 ** -4, 2 ** -10 * s) + 1e-12
+
+
+@pytest.mark.parametrize("dtype", ["fp8_e4m3", "int8"])
+def test_oracle_quantisation_at_rounding_boundaries(dtype):
+    """CPU pin of the oracle's append quantisation on the rounding-boundary rows of the GPU test
+    below: every block's scale is numpy's IEEE fp32 amax / 448 (int8: / 127), and every stored K
+    code is torch's float8_e4m3fn conversion (round to nearest even; |q| < 464 here) of numpy's
+    fp32 quotient x / s, or for int8 its nearest-even integer clipped to +-127.  On the int8 rows
+    a quotient taken in fp64 instead of fp32 changes codes; on both, rounding ties away from zero
+    instead of to even does."""
+    import torch
+    D, n = 128, 300
+    i8 = dtype == "int8"
+    rows = near_boundary_rows(i8, n, D, seed=21 if i8 else 22)
+    pool = oracle.Pool(n, 16, 1, D, odrive.KV_CODE[dtype])
+    slots = np.arange(n, dtype=np.int64) * 16
+    assert pool.append(rows, rows, slots) == 0
+    x = (rows[:, 0, :].astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(x).max(axis=1)
+    sc = (amax / np.float32(127.0 if i8 else 448.0)).astype(np.float32)
+    assert np.array_equal(pool.scales.reshape(n, 1, 4)[:, 0, 0], sc)
+    assert np.array_equal(pool.scales.reshape(n, 1, 4)[:, 0, 1], sc)
+    q = (x / sc[:, None]).astype(np.float32)
+    if i8:
+        want = np.clip(np.rint(q.astype(np.float64)), -127, 127).astype(np.int8).view(np.uint8)
+    else:
+        # below 464, the midpoint above the largest code, nearest-even needs no saturation rule
+        # (the amax element's own quotient can exceed 448 by the rounding of s)
+        assert np.abs(q).max() < 464.0
+        want = torch.tensor(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    k_codes = pool.data.reshape(n, 2, 1, 16, D)[:, 0, 0, 0, :]  # K row of offset 0 of each block
+    assert np.array_equal(k_codes, want)
