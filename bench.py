@@ -104,6 +104,19 @@ def ncu_traffic(w):
     return None, None
 
 
+def append_launches(kv_dtype: str, n_tokens: int, in_step: bool = False) -> int:
+    """Kernels the library launches to append n_tokens tokens: a bf16 pool takes one; a one-byte
+    pool one up to 1024 tokens, three above; and none inside pkv_decode_step (in_step) on a
+    one-byte pool for 1..1024 tokens, where the attention kernel appends them itself."""
+    if n_tokens == 0:
+        return 0
+    if kv_dtype == "bf16":
+        return 1
+    if n_tokens <= 1024:
+        return 0 if in_step else 1
+    return 3
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
     FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -268,7 +281,7 @@ def measure_decode(w, args, world, local, stream):
         w = W.truncated(w, args.seqs)
     nbytes = algorithmic_bytes(w)
     # append kernels per step (bf16: one; one-byte KV: one up to 1024 tokens, else three) + attention
-    launches_per_step = (0 if not w.append else (1 if w.kv_dtype == "bf16" or w.B <= 1024 else 3)) + 1
+    launches_per_step = append_launches(w.kv_dtype, w.B if w.append else 0, in_step=True) + 1
 
     for _ in range(args.warmup):
         step.step()
@@ -655,7 +668,7 @@ def run_prefill(args, world, rank, local):
                          "frac": round(achieved / peak, 4), "traffic": None,
                          "peak_kind": "measured" if peaks else "fallback", "kernel": "prefill_kernel",
                          "algorithmic_flops_per_launch": flops},
-            "gpu_launches": 2 * K,
+            "gpu_launches": (append_launches(sc.kv_dtype, tokens) + 1) * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }), flush=True)

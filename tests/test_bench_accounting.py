@@ -57,3 +57,18 @@ def test_partial_captures_scale_by_algorithmic_bytes(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0ther")
     assert bench.ncu_traffic(w3) == (None, None)
     assert os.path.exists(prof / "ncu_traffic.txt")
+
+
+def test_append_launch_count_follows_the_library_paths():
+    """gpu_launches counts the library's kernels: a bf16 append is one launch; a one-byte append
+    one up to 1024 tokens and three above; a one-byte decode step of up to 1024 tokens appends
+    inside its attention kernel (no append launch)."""
+    import bench
+    assert bench.append_launches("bf16", 200, in_step=True) == 1
+    assert bench.append_launches("bf16", 4096) == 1
+    assert bench.append_launches("fp8_e4m3", 200, in_step=True) == 0
+    assert bench.append_launches("int8", 1024, in_step=True) == 0
+    assert bench.append_launches("fp8_e4m3", 200) == 1
+    assert bench.append_launches("int8", 1025, in_step=True) == 3
+    assert bench.append_launches("fp8_e4m3", 4096) == 3
+    assert bench.append_launches("fp8_e4m3", 0, in_step=True) == 0
